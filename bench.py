@@ -1,0 +1,443 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 Mamba-2 SSD chunked forward.
+
+One step = one SSD forward (all four chunk steps, or the fused kernel) over
+one batch of the workload, inputs already resident in HBM.  Metric: tokens/s
+(tokens = B*L) and ms per step at the large training shape
+[B,L,H,P,N,chunk,G] = [8,4096,256,64,64,64,64] (fp32 public tensors, bf16
+operands) unless --workload says otherwise.
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the float64 CPU
+oracle instead, on a bounded sample of the same workload.
+
+Multi-GPU (torchrun, one process per GPU): each rank runs its own replica of
+the workload on its own GPU (weak scaling; the path shards by batch and group
+with no exchange), timing is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import signal
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import ssd_inputs  # noqa: E402
+
+METRIC = "SSD fwd ms & tokens/s at [8,4096,256,64,64,64,64] on 1 GB300; % of roofline"
+# The reference project's own number for this exact shape (AscendC on Ascend
+# 910B3, 31.888 ms, README "Benchmark"): 8*4096 tokens / 31.888 ms.
+PUBLISHED_TOKENS_PER_S = {"large_training": 8 * 4096 / 31.888e-3}
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 2**20
+
+
+# ---- helpers ---------------------------------------------------------------------
+
+def rank_info():
+    r = int(os.environ.get("RANK", "0"))
+    w = int(os.environ.get("WORLD_SIZE", "1"))
+    lr = int(os.environ.get("LOCAL_RANK", "0"))
+    return r, w, lr
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def algorithmic_bytes(w) -> dict:
+    """Public I/O of one forward, each tensor read or written once."""
+    io = 4 if w.x_dtype == "f32" else 2
+    nx = w.B * w.L * w.H * w.P
+    nbc = w.B * w.L * w.G * w.N
+    nst = w.B * w.H * w.P * w.N
+    b = {
+        "x": nx * io, "y": nx * io, "B": nbc * io, "C": nbc * io, "dt": w.B * w.L * w.H * 4,
+        "params": w.H * 4 * (1 + (w.dt_bias_std is not None) + (w.D_std is not None)),
+        "z": nx * io if w.z else 0,
+        "h0": nst * 4 if w.h0_std is not None else 0,
+        "final_state": nst * 4 if w.return_final_state else 0,
+    }
+    b["total"] = sum(b.values())
+    return b
+
+
+def stage_bytes(w) -> dict:
+    """Compulsory bytes of each chunked-plan kernel (its own inputs read once,
+    its own outputs written once)."""
+    io = 4 if w.x_dtype == "f32" else 2
+    c = -(-w.L // w.chunk)
+    nx = w.B * w.L * w.H * w.P
+    nbc = w.B * w.L * w.G * w.N
+    vec = w.B * w.H * c * w.chunk * 4
+    st = w.B * c * w.H * w.P * w.N * 4
+    nst = w.B * w.H * w.P * w.N * 4
+    return {
+        "chunk_cumsum": w.B * w.L * w.H * 4 + 2 * vec,
+        "chunk_state": nx * io + nbc * io + 2 * vec + st,
+        "state_passing": 2 * st + vec // w.chunk + (nst if w.return_final_state else 0)
+        + (nst if w.h0_std is not None else 0),
+        "chunk_scan": nx * io * (2 if w.z else 1) + 2 * nbc * io + 2 * vec + st + nx * io,
+    }
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while active."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(prefix="ssd_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.idx), "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.send_signal(signal.SIGTERM)
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v == "Active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def traffic_for(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, when the kernel's
+    source is unchanged since the counters were taken (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        table = json.load(open(p))
+    except Exception:
+        return None
+    ent = table.get(kernel, {}).get(workload)
+    if not ent:
+        return None
+    src = os.path.join(ROOT, ent["source"])
+    try:
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except Exception:
+        return None
+    if sha != ent["source_sha"]:
+        return None
+    return float(ent["dram_bytes_per_launch"])
+
+
+# ---- the GPU arm ----------------------------------------------------------------------
+
+def run_gpu(args):
+    import mamba_ssd_chunked_fwd_gb300 as ssd
+    rank, world, lrank = rank_info()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist  # noqa: F811
+        torch.cuda.set_device(lrank)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", lrank if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    w = ssd_inputs.WORKLOADS[args.workload]
+    inp = ssd_inputs.make(w, seed=w.seed + 1000 * rank)
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    y = torch.empty_like(d["x"])
+    fin = torch.empty((w.B, w.H, w.P, w.N), device=dev) if w.return_final_state else None
+    a = ssd.make_args(d["x"], d["dt"], d["A"], d["B"], d["C"], w.chunk, y=y, final_state=fin,
+                      D=d["D"], z=d["z"], dt_bias=d["dt_bias"], initial_states=d["initial_states"],
+                      dt_softplus=w.dt_softplus, ops=args.ops or w.ops, plan=args.plan)
+    plan = ssd.ssd_fwd_resolve_plan(a)
+    nws = ssd.ssd_fwd_workspace_size(a)
+    ws = torch.zeros(max(nws, 256), dtype=torch.uint8, device=dev)
+    a.workspace, a.workspace_bytes = ws.data_ptr(), nws
+    stream = torch.cuda.current_stream(dev)
+    sh = ssd._stream_handle(dev)
+    ab = algorithmic_bytes(w)
+    in_bytes = ab["x"] + ab["B"] + ab["C"] + ab["dt"] + ab["z"]
+    flush = None
+    if in_bytes < 2 * L2_BYTES:
+        flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step():
+        ssd.ssd_fwd(a, sh)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(dev.index) as clk:
+        torch.cuda.synchronize(dev)
+        if dist:
+            dist.barrier()
+        for i in range(args.steps):
+            if flush is not None:
+                flush.fill_(float(i))
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+        if dist:
+            dist.barrier()
+        if args.steps * 0.002 < 1.0:  # keep the sampler alive for a few samples
+            extra_until = time.time() + 0.5
+            while time.time() < extra_until:
+                step()
+            torch.cuda.synchronize(dev)
+    clocks = clk.summary()
+    per_step = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = sum(per_step) / len(per_step)
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    tokens = w.tokens * world
+    value = tokens / (ms * 1e-3)
+
+    # dominant kernel: time it alone with events on the launching stream
+    hbm, peak_kind = peaks()
+    if plan == ssd.SSD_PLAN_FUSED:
+        kname, kbytes, kms = "ssd_fused_kernel", ab["total"], ms
+        launches_per_step = 1
+    else:
+        kname, kbytes, kms = stage_timing(ssd, a, w, dev, sh, stream, args)
+        launches_per_step = 4
+    achieved = kbytes / (kms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1), "peak": hbm,
+                "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                "traffic": traffic_for(kname, args.workload), "alg_bytes_per_launch": kbytes,
+                "launch_ms": round(kms, 5)}
+    path_roofline_ms = ab["total"] / (hbm * 1e9) * 1e3
+
+    e2e = e2e_timing(ssd, inp, w, dev, args) if not args.no_e2e else None
+
+    ops_name = {0: "f32", 1: "f16", 2: "bf16"}[a.ops]
+    line = {
+        "metric": METRIC if args.workload == "large_training" else f"SSD fwd tokens/s ({args.workload})",
+        "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": (round(value / PUBLISHED_TOKENS_PER_S[args.workload], 3)
+                        if args.workload in PUBLISHED_TOKENS_PER_S else None),
+        "dtype": ops_name if plan == ssd.SSD_PLAN_FUSED else "f32",
+        "data": "synthetic (seeded, pages' distributions)",
+        "config": {"workload": f"{args.workload} {w.shape_tuple()} [B,L,H,P,N,chunk,G]",
+                   "plan": {1: "chunked", 2: "fused"}[plan], "ops_requested": ops_name,
+                   "public_dtype": w.x_dtype, "tokens_per_step_per_gpu": w.tokens,
+                   "l2": ("flushed between steps (256 MiB write)" if flush is not None
+                          else f"inputs {in_bytes / 1e9:.2f} GB > 129 MB L2, no flush"),
+                   "path_roofline_ms": round(path_roofline_ms, 4),
+                   "path_frac_of_roofline": round(path_roofline_ms / ms, 4),
+                   "parallelism": f"replica x{world}" if world > 1 else "1 GPU"},
+        "roofline": roofline,
+        "clocks": clocks,
+        "gpu_launches": launches_per_step * args.steps,
+        "e2e": e2e,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, inp, args.cpu_seconds)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def stage_timing(ssd, a, w, dev, sh, stream, args):
+    """Time the four chunked-plan kernels one by one (events between launches)
+    and return the dominant one with its algorithmic bytes."""
+    c = -(-w.L // w.chunk)
+    dtp = torch.empty((w.B, w.H, c, w.chunk), device=dev)
+    cs = torch.empty_like(dtp)
+    states = torch.empty((w.B, c, w.H, w.P, w.N), device=dev)
+    names = ["chunk_cumsum", "chunk_state", "state_passing", "chunk_scan"]
+    calls = [lambda: ssd.ssd_chunk_cumsum(a, dtp, cs, sh),
+             lambda: ssd.ssd_chunk_state(a, dtp, cs, states, sh),
+             lambda: ssd.ssd_state_passing(a, cs, states, sh),
+             lambda: ssd.ssd_chunk_scan(a, dtp, cs, states, sh)]
+    for _ in range(2):
+        for f in calls:
+            f()
+    reps = max(3, min(args.steps, 10))
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(reps)]
+    torch.cuda.synchronize(dev)
+    for r in range(reps):
+        ev[r][0].record(stream)
+        for i, f in enumerate(calls):
+            f()
+            ev[r][i + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    t = [sum(ev[r][i].elapsed_time(ev[r][i + 1]) for r in range(reps)) / reps for i in range(4)]
+    sb = stage_bytes(w)
+    i = max(range(4), key=lambda j: t[j])
+    return names[i], sb[names[i]], t[i]
+
+
+def e2e_timing(ssd, inp, w, dev, args):
+    """Same metric through ssd_fwd_host: pinned host inputs copied in and y /
+    final_state copied out inside the timed region."""
+    h = {k: (v.contiguous().pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    y = torch.empty_like(h["x"]).pin_memory()
+    fin = torch.empty((w.B, w.H, w.P, w.N)).pin_memory() if w.return_final_state else None
+    a = ssd.make_args(h["x"], h["dt"], h["A"], h["B"], h["C"], w.chunk, y=y, final_state=fin,
+                      D=h["D"], z=h["z"], dt_bias=h["dt_bias"], initial_states=h["initial_states"],
+                      dt_softplus=w.dt_softplus, ops=args.ops or w.ops, plan=args.plan)
+    nws = ssd.ssd_fwd_host_workspace_size(a)
+    ws = torch.empty(nws, dtype=torch.uint8, device=dev)
+    a.workspace, a.workspace_bytes = ws.data_ptr(), nws
+    sh = ssd._stream_handle(dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(2):
+        ssd.ssd_fwd_host(a, sh)
+    torch.cuda.synchronize(dev)
+    steps = max(2, min(args.steps, 5))
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(steps):
+        ssd.ssd_fwd_host(a, sh)
+    e.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = s.elapsed_time(e) / steps
+    h2d = sum(v.numel() * v.element_size() for k, v in h.items()
+              if isinstance(v, torch.Tensor))
+    d2h = y.numel() * y.element_size() + (fin.numel() * 4 if fin is not None else 0)
+    return {"value": round(w.tokens / (ms * 1e-3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# ---- the CPU oracle (cpu_baseline and --impl reference) --------------------------------
+
+def oracle_sample(w, inp, seconds, *, nthreads=0):
+    """Time the float64 oracle on a bounded sample of the workload: whole
+    (batch, head) sequences over the full L, as many as fit in ~``seconds``."""
+    import oracle
+    oracle.build()
+    prob = oracle.Problem(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], D=inp["D"], z=inp["z"],
+                          dt_bias=inp["dt_bias"], initial_states=inp["initial_states"],
+                          dt_softplus=inp["dt_softplus"])
+    cores = nthreads or oracle.threads()
+    total = w.B * w.H
+    n = min(total, max(1, cores))
+    t0 = time.perf_counter()
+    oracle.recurrence(prob, [(i // w.H, i % w.H) for i in range(n)], nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    per_pair = dt / n
+    n2 = int(min(total, max(n, seconds / max(per_pair, 1e-9))))
+    if n2 > n:
+        pairs = [(i // w.H, i % w.H) for i in range(n2)]
+        t0 = time.perf_counter()
+        oracle.recurrence(prob, pairs, nthreads=nthreads)
+        dt = time.perf_counter() - t0
+        n = n2
+    frac = n / total
+    tok_s = w.tokens * frac / dt
+    return {"value": round(tok_s, 1), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} of {total} (batch, head) sequences over the full L={w.L} "
+                      f"({frac * 100:.2f}% of one step), {dt:.2f} s wall",
+            "seconds": round(dt, 3)}
+
+
+def cpu_baseline(w, inp, seconds):
+    return oracle_sample(w, inp, seconds)
+
+
+def run_reference(args):
+    rank, world, _ = rank_info()
+    if rank != 0:
+        return
+    w = ssd_inputs.WORKLOADS[args.workload]
+    inp = ssd_inputs.make(w)
+    per_step = max(1.0, args.cpu_seconds / max(1, args.steps))
+    samples = [oracle_sample(w, inp, per_step) for _ in range(args.warmup and 1 or 0)]
+    samples = [oracle_sample(w, inp, per_step) for _ in range(args.steps)]
+    value = statistics.median(s["value"] for s in samples)
+    ms = w.tokens / value * 1e3
+    line = {
+        "impl": "reference",
+        "metric": METRIC if args.workload == "large_training" else f"SSD fwd tokens/s ({args.workload})",
+        "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{args.workload} {w.shape_tuple()} [B,L,H,P,N,chunk,G]",
+                   "what": "float64 CPU oracle (token-by-token recurrence), bounded sample per step"},
+        "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": samples[0]["cores"],
+                         "kind": "oracle", "sample": samples[0]["sample"]},
+        "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(ssd_inputs.WORKLOADS), default="large_training")
+    ap.add_argument("--plan", choices=["auto", "chunked", "fused"], default="auto")
+    ap.add_argument("--ops", choices=["f32", "f16", "bf16"], default=None)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the reference arm runs with --impl reference)")
+    run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,187 @@
+/*
+ * ssd.h -- C ABI of the GB300 (sm_103a) Mamba-2 SSD chunked forward.
+ *
+ * The operation.  The public call of the "Mamba-2 SSD for Ascend NPU" README
+ * ("Usage", "Implementation": mamba2_ssd_fwd(x, dt, A, B, C, chunk_size,
+ * dt_softplus, return_final_state) with D, z, dt_bias, dt_limit and
+ * initial_states): for every batch b, head h and token t, with group
+ * g = h / (H/G),
+ *
+ *     d_t = clamp(softplus(dt[b,t,h] + dt_bias[h]))   bias / softplus / clamp optional
+ *     h_t = exp(d_t * A[h]) * h_{t-1} + d_t * x[b,t,h,:] (outer) B[b,t,g,:]
+ *     y[b,t,h,:] = (h_t . C[b,t,g,:] + D[h] * x[b,t,h,:]) * silu(z[b,t,h,:])
+ *
+ * with h_{-1} = initial_state[b,h] (or 0) and final_state[b,h] = h_{L-1}.
+ * It is computed chunk by chunk (ops-transformer MambaV2 article, section 2:
+ * chunk_cumsum -> chunk_state -> chunk_state_passing -> chunk_scan), which
+ * reorders floating-point sums but not the result.
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers (except ssd_fwd_host), dense and
+ *    contiguous in the stated layout (row-major, last index fastest).
+ *  - The caller owns every buffer, including the workspace.  The library
+ *    allocates no memory and never synchronises the stream except where an
+ *    entry point says so.
+ *  - Work is enqueued on `stream` (a cudaStream_t passed as void*; NULL is the
+ *    legacy default stream) and runs asynchronously.
+ *  - Arguments are validated on the host before anything is enqueued.  A bad
+ *    argument returns SSD_ERR_INVALID_ARG or SSD_ERR_UNSUPPORTED and enqueues
+ *    nothing; ssd_last_error_detail() then names the offending field.
+ *  - A CUDA launch error returns SSD_ERR_CUDA.  No kernel traps or asserts.
+ *  - Results are bitwise deterministic run to run (no floating atomics).
+ */
+#ifndef SSD_GB300_SSD_H
+#define SSD_GB300_SSD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SSD_ABI_VERSION 1
+
+/* Element types of the public tensors. */
+typedef enum { SSD_F32 = 0, SSD_F16 = 1, SSD_BF16 = 2 } ssd_dtype;
+
+/* Operand precision of the contractions (accumulation is always fp32).
+ * SSD_OPS_F32: every product in fp32 on the CUDA cores ("exact" path).
+ * SSD_OPS_F16 / SSD_OPS_BF16: x, B, C and the derived operands are rounded to
+ * fp16 / bf16 (round to nearest even) and multiplied on the tensor cores with
+ * fp32 accumulation; the cumulative decay, the exponentials and the
+ * inter-chunk recurrence stay fp32.  This is the README's "FP16 operands with
+ * FP32 accumulation" ("Benchmark" notes). */
+typedef enum { SSD_OPS_F32 = 0, SSD_OPS_F16 = 1, SSD_OPS_BF16 = 2 } ssd_operand_mode;
+
+/* Execution plan.  CHUNKED runs the four chunk steps as separate launches
+ * with the chunk states in the workspace; FUSED runs one persistent
+ * tensor-core kernel per call that keeps every state on chip.  AUTO picks the
+ * fastest plan the shape supports. */
+typedef enum { SSD_PLAN_AUTO = 0, SSD_PLAN_CHUNKED = 1, SSD_PLAN_FUSED = 2 } ssd_plan;
+
+typedef enum {
+    SSD_OK = 0,
+    SSD_ERR_INVALID_ARG = 1, /* null required pointer, dim <= 0, H % G != 0, ... */
+    SSD_ERR_UNSUPPORTED = 2, /* valid but outside what the kernels implement   */
+    SSD_ERR_WORKSPACE = 3,   /* workspace missing or smaller than required      */
+    SSD_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed            */
+    SSD_ERR_TIMEOUT = 5      /* a bounded device-side wait gave up              */
+} ssd_status;
+
+/*
+ * Arguments of one SSD forward.  Shapes (B batch, L tokens, H heads, P head
+ * dim, N state dim, G groups, chunk = chunk_size):
+ *   x              [B,L,H,P]  x_dtype                         required
+ *   dt             [B,L,H]    fp32                            required
+ *   A              [H]        fp32 (per-head decay rate)      required
+ *   Bm, Cm         [B,L,G,N]  bc_dtype                        required
+ *   D              [H]        fp32 (skip, per head)           optional (NULL)
+ *   z              [B,L,H,P]  z_dtype  (gate: y *= silu(z))   optional (NULL)
+ *   dt_bias        [H]        fp32                            optional (NULL)
+ *   initial_state  [B,H,P,N]  fp32                            optional (NULL = 0)
+ *   y              [B,L,H,P]  y_dtype                         required output
+ *   final_state    [B,H,P,N]  fp32                            optional output
+ *                  (NULL = return_final_state false)
+ * Constraints: all dims > 0, H % G == 0, 16 <= chunk <= 256 with chunk % 16
+ * == 0, P and N multiples of 16 no larger than 128.  x, B, C, z and y share
+ * one dtype.  L need not be a multiple of chunk: the ragged tail is computed
+ * as if padded with dt' = 0 and x = 0 (nothing is read or written past L).
+ * dt_min/dt_max: the clamp of d_t, applied only when (dt_min, dt_max) differs
+ * from the no-op default (0, +inf).
+ */
+typedef struct ssd_fwd_args {
+    int64_t B, L, H, P, N, G, chunk;
+    const void *x;
+    const float *dt;
+    const float *A;
+    const void *Bm;
+    const void *Cm;
+    const float *D;
+    const void *z;
+    const float *dt_bias;
+    const float *initial_state;
+    void *y;
+    float *final_state;
+    int32_t x_dtype, bc_dtype, z_dtype, y_dtype; /* ssd_dtype */
+    int32_t ops;                                  /* ssd_operand_mode */
+    int32_t plan;                                 /* ssd_plan */
+    int32_t dt_softplus;                          /* nonzero: softplus(dt + bias) */
+    float dt_min, dt_max;
+    void *workspace;                              /* device, 256-byte aligned */
+    size_t workspace_bytes;
+} ssd_fwd_args;
+
+/* ABI version of the loaded library (SSD_ABI_VERSION). */
+int32_t ssd_abi_version(void);
+
+/* Bytes of device workspace ssd_fwd needs for these arguments (pointers are
+ * not inspected).  Returns INVALID_ARG / UNSUPPORTED like ssd_fwd. */
+ssd_status ssd_fwd_workspace_size(const ssd_fwd_args *args, size_t *bytes);
+
+/* The plan ssd_fwd would run for these arguments (SSD_PLAN_CHUNKED or
+ * SSD_PLAN_FUSED), after resolving SSD_PLAN_AUTO. */
+ssd_status ssd_fwd_resolve_plan(const ssd_fwd_args *args, int32_t *plan);
+
+/* The whole forward: y (and final_state when non-NULL).  Enqueue only. */
+ssd_status ssd_fwd(const ssd_fwd_args *args, void *stream);
+
+/*
+ * The four chunk steps, callable one at a time (ops-transformer MambaV2
+ * article, sections 4.2-4.5).  c = ceil(L / chunk).  Intermediate layouts:
+ *   dtp, cs  [B,H,c,chunk] fp32   processed step d_t and the inclusive
+ *                                 within-chunk cumulative sum of d_t*A[h]
+ *                                 (past L: d = 0, cs holds its last value)
+ *   states   [B,c,H,P,N]   fp32
+ * These entry points need no workspace and ignore args->workspace.
+ */
+
+/* Step 1, chunk_cumsum (article section 4.2): writes dtp and cs. */
+ssd_status ssd_chunk_cumsum(const ssd_fwd_args *args, float *dtp, float *cs, void *stream);
+
+/* Step 2, chunk_state (article section 4.3): states[b,k,h] =
+ *   sum_{i in chunk k} exp(cs[k,last] - cs[k,i]) * dtp[k,i] * x_i (outer) B_i,
+ * the state chunk k produces from a zero start. */
+ssd_status ssd_chunk_state(const ssd_fwd_args *args, const float *dtp, const float *cs,
+                           float *states, void *stream);
+
+/* Step 3, chunk_state_passing (article section 4.4): in place, replaces each
+ * chunk's own state by the state ENTERING that chunk:
+ *   S_0 = initial_state (or 0),  S_{k+1} = exp(cs[k,last]) * S_k + states[k],
+ * and writes S_c to args->final_state when it is non-NULL. */
+ssd_status ssd_state_passing(const ssd_fwd_args *args, const float *cs, float *states,
+                             void *stream);
+
+/* Step 4, chunk_scan (article section 4.5): writes args->y from the entering
+ * states:  y_i = exp(cs_i) C_i . S_k + sum_{j<=i} (C_i . B_j) exp(cs_i - cs_j)
+ * dtp_j x_j, then + D x_i and * silu(z_i). */
+ssd_status ssd_chunk_scan(const ssd_fwd_args *args, const float *dtp, const float *cs,
+                          const float *states, void *stream);
+
+/*
+ * End-to-end call with HOST buffers: every tensor pointer in args is host
+ * memory (pinned for overlap; pageable works but serialises).  The library
+ * copies the inputs into the device workspace, runs ssd_fwd there and copies
+ * y and final_state back, all enqueued on `stream`; the host outputs are
+ * valid after the caller synchronises the stream.  The workspace (device)
+ * must hold ssd_fwd_host_workspace_size() bytes.
+ */
+ssd_status ssd_fwd_host_workspace_size(const ssd_fwd_args *args, size_t *bytes);
+ssd_status ssd_fwd_host(const ssd_fwd_args *args, void *stream);
+
+/* Synchronises `stream`, then reads the device error word the last ssd_fwd
+ * on this workspace left behind (bounded waits that gave up set it).
+ * Returns SSD_OK or SSD_ERR_TIMEOUT (or SSD_ERR_CUDA). */
+ssd_status ssd_check_device_error(const ssd_fwd_args *args, void *stream);
+
+/* Short static description of a status code. */
+const char *ssd_status_string(ssd_status status);
+
+/* Thread-local detail of the last failing call on this thread ("" if none). */
+const char *ssd_last_error_detail(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSD_GB300_SSD_H */

@@ -1,0 +1,253 @@
+"""GB300 (sm_103a) Mamba-2 SSD chunked forward: thin Python binding.
+
+Every step of the computation runs in the CUDA kernels of
+``libssd_gb300.so``; this module only marshals torch tensors (device memory
+and the current stream) into the C ABI of ``include/ssd.h``.  The binding
+functions carry the C names (``ssd_fwd``, ``ssd_chunk_cumsum``,
+``ssd_chunk_state``, ``ssd_state_passing``, ``ssd_chunk_scan``,
+``ssd_fwd_host`` ...).  ``mamba2_ssd_fwd`` mirrors the public call of the
+"Mamba-2 SSD for Ascend NPU" README ("Usage": mamba2_ssd_fwd(x, dt, A, B, C,
+chunk_size, dt_softplus, return_final_state) plus D, z, dt_bias, dt_limit and
+initial_states).
+
+There is no fallback: if the library cannot be built or loaded, every call
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import threading
+
+import torch
+
+from . import _build
+
+__all__ = [
+    "SSD_F32", "SSD_F16", "SSD_BF16", "SSD_OPS_F32", "SSD_OPS_F16", "SSD_OPS_BF16",
+    "SSD_PLAN_AUTO", "SSD_PLAN_CHUNKED", "SSD_PLAN_FUSED", "SsdError", "SsdFwdArgs",
+    "load_library", "library_path", "make_args", "ssd_fwd", "ssd_fwd_workspace_size",
+    "ssd_fwd_resolve_plan", "ssd_chunk_cumsum", "ssd_chunk_state", "ssd_state_passing",
+    "ssd_chunk_scan", "ssd_fwd_host", "ssd_fwd_host_workspace_size", "ssd_check_device_error",
+    "mamba2_ssd_fwd",
+]
+
+SSD_F32, SSD_F16, SSD_BF16 = 0, 1, 2
+SSD_OPS_F32, SSD_OPS_F16, SSD_OPS_BF16 = 0, 1, 2
+SSD_PLAN_AUTO, SSD_PLAN_CHUNKED, SSD_PLAN_FUSED = 0, 1, 2
+_PLAN_NAMES = {"auto": SSD_PLAN_AUTO, "chunked": SSD_PLAN_CHUNKED, "fused": SSD_PLAN_FUSED}
+_OPS_NAMES = {"f32": SSD_OPS_F32, "fp32": SSD_OPS_F32, "f16": SSD_OPS_F16, "fp16": SSD_OPS_F16,
+              "bf16": SSD_OPS_BF16}
+_DTYPE_CODES = {torch.float32: SSD_F32, torch.float16: SSD_F16, torch.bfloat16: SSD_BF16}
+_STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration",
+           3: "workspace missing or too small", 4: "CUDA error", 5: "device-side wait timed out"}
+
+
+class SsdError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str):
+        super().__init__(f"{where}: {_STATUS.get(status, status)} ({detail})")
+        self.status = status
+        self.detail = detail
+
+
+class SsdFwdArgs(ctypes.Structure):
+    """Mirror of ``ssd_fwd_args`` in include/ssd.h."""
+    _fields_ = [
+        ("B", ctypes.c_int64), ("L", ctypes.c_int64), ("H", ctypes.c_int64),
+        ("P", ctypes.c_int64), ("N", ctypes.c_int64), ("G", ctypes.c_int64),
+        ("chunk", ctypes.c_int64),
+        ("x", ctypes.c_void_p), ("dt", ctypes.c_void_p), ("A", ctypes.c_void_p),
+        ("Bm", ctypes.c_void_p), ("Cm", ctypes.c_void_p), ("D", ctypes.c_void_p),
+        ("z", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p), ("initial_state", ctypes.c_void_p),
+        ("y", ctypes.c_void_p), ("final_state", ctypes.c_void_p),
+        ("x_dtype", ctypes.c_int32), ("bc_dtype", ctypes.c_int32), ("z_dtype", ctypes.c_int32),
+        ("y_dtype", ctypes.c_int32), ("ops", ctypes.c_int32), ("plan", ctypes.c_int32),
+        ("dt_softplus", ctypes.c_int32), ("dt_min", ctypes.c_float), ("dt_max", ctypes.c_float),
+        ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+    ]
+
+
+_lock = threading.Lock()
+_lib = None
+
+# C entry points: name -> argument types (all return ssd_status / int32)
+_P = ctypes.POINTER(SsdFwdArgs)
+_SIGS = {
+    "ssd_fwd_workspace_size": [_P, ctypes.POINTER(ctypes.c_size_t)],
+    "ssd_fwd_resolve_plan": [_P, ctypes.POINTER(ctypes.c_int32)],
+    "ssd_fwd": [_P, ctypes.c_void_p],
+    "ssd_chunk_cumsum": [_P, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p],
+    "ssd_chunk_state": [_P, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p],
+    "ssd_state_passing": [_P, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p],
+    "ssd_chunk_scan": [_P, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p],
+    "ssd_fwd_host_workspace_size": [_P, ctypes.POINTER(ctypes.c_size_t)],
+    "ssd_fwd_host": [_P, ctypes.c_void_p],
+    "ssd_check_device_error": [_P, ctypes.c_void_p],
+}
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load_library(build: bool = True):
+    """Build (if stale) and load libssd_gb300.so.  Raises if that fails."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build() if build else _build.LIB
+            lib = ctypes.CDLL(path)
+            for name, argtypes in _SIGS.items():
+                fn = getattr(lib, name)
+                fn.argtypes = argtypes
+                fn.restype = ctypes.c_int32
+            lib.ssd_abi_version.restype = ctypes.c_int32
+            lib.ssd_abi_version.argtypes = []
+            lib.ssd_status_string.restype = ctypes.c_char_p
+            lib.ssd_status_string.argtypes = [ctypes.c_int32]
+            lib.ssd_last_error_detail.restype = ctypes.c_char_p
+            lib.ssd_last_error_detail.argtypes = []
+            _lib = lib
+    return _lib
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        detail = load_library().ssd_last_error_detail().decode(errors="replace")
+        raise SsdError(status, where, detail)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("every tensor passed to the SSD library must be contiguous")
+    return t.data_ptr()
+
+
+def _stream_handle(device=None):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def make_args(x, dt, A, B, C, chunk_size, *, y=None, final_state=None, D=None, z=None,
+              dt_bias=None, initial_states=None, dt_softplus=False,
+              dt_limit=(0.0, math.inf), ops=None, plan="auto", workspace=None) -> SsdFwdArgs:
+    """Fill an ``ssd_fwd_args`` from tensors (device or host; no copies)."""
+    Bb, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    io = _DTYPE_CODES.get(x.dtype)
+    if io is None:
+        raise ValueError(f"unsupported dtype {x.dtype}")
+    if ops is None:
+        ops = {SSD_F32: "f32", SSD_F16: "f16", SSD_BF16: "bf16"}[io]
+    a = SsdFwdArgs()
+    a.B, a.L, a.H, a.P, a.N, a.G, a.chunk = Bb, L, H, P, N, G, int(chunk_size)
+    a.x, a.dt, a.A, a.Bm, a.Cm = _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C)
+    a.D, a.z, a.dt_bias, a.initial_state = _ptr(D), _ptr(z), _ptr(dt_bias), _ptr(initial_states)
+    a.y, a.final_state = _ptr(y), _ptr(final_state)
+    a.x_dtype = io
+    a.bc_dtype = _DTYPE_CODES.get(B.dtype, -1)
+    a.z_dtype = _DTYPE_CODES.get(z.dtype, -1) if z is not None else io
+    a.y_dtype = _DTYPE_CODES.get(y.dtype, -1) if y is not None else io
+    a.ops = _OPS_NAMES[ops] if isinstance(ops, str) else int(ops)
+    a.plan = _PLAN_NAMES[plan] if isinstance(plan, str) else int(plan)
+    a.dt_softplus = 1 if dt_softplus else 0
+    a.dt_min, a.dt_max = float(dt_limit[0]), float(dt_limit[1])
+    if workspace is not None:
+        a.workspace, a.workspace_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
+    return a
+
+
+# ---- the C entry points, one Python function each ----------------------------
+
+def ssd_fwd_workspace_size(args: SsdFwdArgs) -> int:
+    out = ctypes.c_size_t(0)
+    _check(load_library().ssd_fwd_workspace_size(ctypes.byref(args), ctypes.byref(out)),
+           "ssd_fwd_workspace_size")
+    return int(out.value)
+
+
+def ssd_fwd_resolve_plan(args: SsdFwdArgs) -> int:
+    out = ctypes.c_int32(0)
+    _check(load_library().ssd_fwd_resolve_plan(ctypes.byref(args), ctypes.byref(out)),
+           "ssd_fwd_resolve_plan")
+    return int(out.value)
+
+
+def ssd_fwd(args: SsdFwdArgs, stream=None):
+    s = stream if stream is not None else _stream_handle()
+    _check(load_library().ssd_fwd(ctypes.byref(args), s), "ssd_fwd")
+
+
+def ssd_chunk_cumsum(args: SsdFwdArgs, dtp, cs, stream=None):
+    s = stream if stream is not None else _stream_handle()
+    _check(load_library().ssd_chunk_cumsum(ctypes.byref(args), _ptr(dtp), _ptr(cs), s),
+           "ssd_chunk_cumsum")
+
+
+def ssd_chunk_state(args: SsdFwdArgs, dtp, cs, states, stream=None):
+    s = stream if stream is not None else _stream_handle()
+    _check(load_library().ssd_chunk_state(ctypes.byref(args), _ptr(dtp), _ptr(cs), _ptr(states), s),
+           "ssd_chunk_state")
+
+
+def ssd_state_passing(args: SsdFwdArgs, cs, states, stream=None):
+    s = stream if stream is not None else _stream_handle()
+    _check(load_library().ssd_state_passing(ctypes.byref(args), _ptr(cs), _ptr(states), s),
+           "ssd_state_passing")
+
+
+def ssd_chunk_scan(args: SsdFwdArgs, dtp, cs, states, stream=None):
+    s = stream if stream is not None else _stream_handle()
+    _check(load_library().ssd_chunk_scan(ctypes.byref(args), _ptr(dtp), _ptr(cs), _ptr(states), s),
+           "ssd_chunk_scan")
+
+
+def ssd_fwd_host_workspace_size(args: SsdFwdArgs) -> int:
+    out = ctypes.c_size_t(0)
+    _check(load_library().ssd_fwd_host_workspace_size(ctypes.byref(args), ctypes.byref(out)),
+           "ssd_fwd_host_workspace_size")
+    return int(out.value)
+
+
+def ssd_fwd_host(args: SsdFwdArgs, stream=None):
+    s = stream if stream is not None else _stream_handle()
+    _check(load_library().ssd_fwd_host(ctypes.byref(args), s), "ssd_fwd_host")
+
+
+def ssd_check_device_error(args: SsdFwdArgs, stream=None):
+    s = stream if stream is not None else _stream_handle()
+    _check(load_library().ssd_check_device_error(ctypes.byref(args), s), "ssd_check_device_error")
+
+
+# ---- the README-style call ---------------------------------------------------
+
+def mamba2_ssd_fwd(x, dt, A, B, C, chunk_size, dt_softplus=False, return_final_state=False, *,
+                   D=None, z=None, dt_bias=None, dt_limit=(0.0, math.inf), initial_states=None,
+                   ops=None, plan="auto", workspace=None, out=None):
+    """SSD forward on the GPU.  Returns ``out`` or ``(out, final_state)``.
+
+    x [B,L,H,P], dt [B,L,H] fp32, A [H] fp32, B/C [B,L,G,N], D [H] fp32,
+    z [B,L,H,P], dt_bias [H] fp32, initial_states [B,H,P,N] fp32; x, B, C, z
+    share a dtype (fp32, fp16 or bf16) and the output takes it.  ``ops``
+    ("f32" | "f16" | "bf16") is the operand precision of the contractions
+    (default: that of x).  Allocation of out, final_state and the workspace is
+    done here with torch; all compute runs in libssd_gb300.so on the current
+    stream.
+    """
+    if not x.is_cuda:
+        raise ValueError("mamba2_ssd_fwd takes CUDA tensors; use ssd_fwd_host for host buffers")
+    y = out if out is not None else torch.empty_like(x)
+    fin = None
+    if return_final_state:
+        Bb, L, H, P = x.shape
+        fin = torch.empty((Bb, H, P, B.shape[3]), device=x.device, dtype=torch.float32)
+    args = make_args(x, dt, A, B, C, chunk_size, y=y, final_state=fin, D=D, z=z, dt_bias=dt_bias,
+                     initial_states=initial_states, dt_softplus=dt_softplus, dt_limit=dt_limit,
+                     ops=ops, plan=plan)
+    if workspace is None:
+        nbytes = ssd_fwd_workspace_size(args)
+        workspace = torch.empty(max(nbytes, 256), device=x.device, dtype=torch.uint8)
+    args.workspace, args.workspace_bytes = workspace.data_ptr(), workspace.numel()
+    ssd_fwd(args, _stream_handle(x.device))
+    return (y, fin) if return_final_state else y

@@ -1,0 +1,105 @@
+// chunk_state.cu -- step 2 of the chunked SSD forward (ops-transformer
+// MambaV2 article, section 4.3 "mamba2_chunk_state"): the state each chunk
+// produces from a zero start,
+//     states[b,k,h,p,n] = sum_i w_i x[b,kQ+i,h,p] B[b,kQ+i,g,n],
+//     w_i = exp(cs[k,Q-1] - cs[k,i]) * dtp[k,i]   (exponent <= 0: no overflow).
+//
+// CUDA-core fp32 version (the exact plan): one CTA per (chunk, batch*head),
+// 256 threads as a 16 x 16 grid over (p, n), each owning a strided
+// (P/16) x (N/16) block of the [P,N] output.  Tokens stream through shared
+// memory 32 at a time.  Grid: x = batch*head, y = chunk.
+#include "ssd_internal.cuh"
+
+namespace ssd {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kTok = 32;
+constexpr int kMaxDim = 128;
+
+template <int IO>
+__global__ void __launch_bounds__(kThreads)
+chunk_state_kernel(Params p, const float *__restrict__ dtp, const float *__restrict__ cs,
+                   float *__restrict__ states) {
+    __shared__ float xs[kTok][kMaxDim];
+    __shared__ float bs[kTok][kMaxDim];
+    __shared__ float w_s[kTok];
+    const int k = blockIdx.y;
+    const int bh = blockIdx.x;
+    const int b = bh / p.H, h = bh % p.H, g = h / p.hpg;
+    const int P = p.P, N = p.N, Q = p.Q, L = p.L;
+    const int PT = P >> 4, NT = N >> 4;
+    const int tn = threadIdx.x & 15, tp = threadIdx.x >> 4;
+    const size_t crow = (((size_t)b * p.H + h) * p.nchunks + k) * Q;
+    const float cs_last = __ldg(cs + crow + Q - 1);
+
+    float acc[8][8];
+#pragma unroll
+    for (int a = 0; a < 8; ++a)
+#pragma unroll
+        for (int c = 0; c < 8; ++c) acc[a][c] = 0.f;
+
+    for (int i0 = 0; i0 < Q; i0 += kTok) {
+        const int ntok = min(kTok, Q - i0);
+        if (threadIdx.x < kTok) {
+            const int i = i0 + threadIdx.x;
+            float w = 0.f;
+            if (threadIdx.x < ntok && k * Q + i < L)
+                w = expf(cs_last - __ldg(cs + crow + i)) * __ldg(dtp + crow + i);
+            w_s[threadIdx.x] = w;
+        }
+        __syncthreads();
+        for (int e = threadIdx.x; e < kTok * P; e += kThreads) {
+            const int i = e / P, pp = e % P;
+            const int t = k * Q + i0 + i;
+            float v = 0.f;
+            if (i < ntok && t < L) v = ld_io<IO>(p.x, (((size_t)b * L + t) * p.H + h) * P + pp) * w_s[i];
+            xs[i][pp] = v;
+        }
+        for (int e = threadIdx.x; e < kTok * N; e += kThreads) {
+            const int i = e / N, n = e % N;
+            const int t = k * Q + i0 + i;
+            float v = 0.f;
+            if (i < ntok && t < L) v = ld_io<IO>(p.Bm, (((size_t)b * L + t) * p.G + g) * N + n);
+            bs[i][n] = v;
+        }
+        __syncthreads();
+        for (int i = 0; i < ntok; ++i) {
+            float xv[8], bv[8];
+#pragma unroll
+            for (int a = 0; a < 8; ++a) xv[a] = (a < PT) ? xs[i][tp + 16 * a] : 0.f;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) bv[c] = (c < NT) ? bs[i][tn + 16 * c] : 0.f;
+#pragma unroll
+            for (int a = 0; a < 8; ++a)
+#pragma unroll
+                for (int c = 0; c < 8; ++c) acc[a][c] = fmaf(xv[a], bv[c], acc[a][c]);
+        }
+        __syncthreads();
+    }
+
+    float *out = states + ((((size_t)b * p.nchunks + k) * p.H + h) * P) * N;
+#pragma unroll
+    for (int a = 0; a < 8; ++a)
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            if (a < PT && c < NT) out[(size_t)(tp + 16 * a) * N + tn + 16 * c] = acc[a][c];
+}
+
+}  // namespace
+
+cudaError_t launch_chunk_state(const Params &p, int io, const float *dtp, const float *cs,
+                               float *states, cudaStream_t s) {
+    if (p.P > kMaxDim || p.N > kMaxDim || (p.P & 15) || (p.N & 15)) return cudaErrorInvalidValue;
+    dim3 grid(p.B * p.H, p.nchunks);
+    switch (io) {
+        case IO_F32: chunk_state_kernel<IO_F32><<<grid, kThreads, 0, s>>>(p, dtp, cs, states); break;
+        case IO_F16: chunk_state_kernel<IO_F16><<<grid, kThreads, 0, s>>>(p, dtp, cs, states); break;
+        case IO_BF16: chunk_state_kernel<IO_BF16><<<grid, kThreads, 0, s>>>(p, dtp, cs, states); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace ssd

@@ -1,0 +1,358 @@
+// ssd_api.cu -- the C ABI declared in include/ssd.h: argument validation,
+// plan choice, workspace layout and launches.  Everything here runs on the
+// host; nothing allocates device memory or synchronises a stream except
+// ssd_check_device_error.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "ssd_fused.cuh"
+#include "ssd_internal.cuh"
+
+namespace {
+
+thread_local char g_detail[512] = "";
+
+ssd_status fail(ssd_status st, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_detail, sizeof(g_detail), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+ssd_status ok() {
+    g_detail[0] = '\0';
+    return SSD_OK;
+}
+
+ssd_status cuda_fail(cudaError_t e, const char *where) {
+    return fail(SSD_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+size_t io_size(int32_t dt) { return dt == SSD_F32 ? 4 : 2; }
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Shape and dtype checks shared by every entry point (pointers excluded).
+ssd_status check_shape(const ssd_fwd_args *a) {
+    if (!a) return fail(SSD_ERR_INVALID_ARG, "args is NULL");
+    if (a->B <= 0 || a->L <= 0 || a->H <= 0 || a->P <= 0 || a->N <= 0 || a->G <= 0 || a->chunk <= 0)
+        return fail(SSD_ERR_INVALID_ARG, "every dim must be > 0 (B=%lld L=%lld H=%lld P=%lld N=%lld G=%lld chunk=%lld)",
+                    (long long)a->B, (long long)a->L, (long long)a->H, (long long)a->P,
+                    (long long)a->N, (long long)a->G, (long long)a->chunk);
+    if (a->H % a->G != 0)
+        return fail(SSD_ERR_INVALID_ARG, "H (%lld) must be a multiple of G (%lld)", (long long)a->H,
+                    (long long)a->G);
+    if (a->chunk < 16 || a->chunk > 256 || a->chunk % 16 != 0)
+        return fail(SSD_ERR_UNSUPPORTED, "chunk must be a multiple of 16 in [16, 256] (got %lld)",
+                    (long long)a->chunk);
+    if (a->P % 16 != 0 || a->P > 128 || a->N % 16 != 0 || a->N > 128)
+        return fail(SSD_ERR_UNSUPPORTED, "P and N must be multiples of 16 up to 128 (P=%lld N=%lld)",
+                    (long long)a->P, (long long)a->N);
+    const int64_t nchunks = (a->L + a->chunk - 1) / a->chunk;
+    if (a->B > 65535 || nchunks > 65535 || a->B * a->H > 0x7fffffffLL || a->L > 0x7fffffffLL)
+        return fail(SSD_ERR_UNSUPPORTED, "B <= 65535, ceil(L/chunk) <= 65535 and B*H, L < 2^31 required");
+    for (int32_t d : {a->x_dtype, a->bc_dtype, a->y_dtype})
+        if (d != SSD_F32 && d != SSD_F16 && d != SSD_BF16)
+            return fail(SSD_ERR_INVALID_ARG, "unknown dtype code %d", d);
+    if (a->bc_dtype != a->x_dtype || a->y_dtype != a->x_dtype)
+        return fail(SSD_ERR_UNSUPPORTED, "x, B, C and y must share one dtype");
+    if (a->z && a->z_dtype != a->x_dtype)
+        return fail(SSD_ERR_UNSUPPORTED, "z must have the dtype of x");
+    if (a->ops != SSD_OPS_F32 && a->ops != SSD_OPS_F16 && a->ops != SSD_OPS_BF16)
+        return fail(SSD_ERR_INVALID_ARG, "unknown operand mode %d", a->ops);
+    if (a->plan != SSD_PLAN_AUTO && a->plan != SSD_PLAN_CHUNKED && a->plan != SSD_PLAN_FUSED)
+        return fail(SSD_ERR_INVALID_ARG, "unknown plan %d", a->plan);
+    if (!(a->dt_min <= a->dt_max) || isnan(a->dt_min) || isnan(a->dt_max))
+        return fail(SSD_ERR_INVALID_ARG, "dt_limit must satisfy dt_min <= dt_max");
+    return SSD_OK;
+}
+
+ssd_status check_pointers(const ssd_fwd_args *a, bool need_y) {
+    if (!a->x || !a->dt || !a->A || !a->Bm || !a->Cm)
+        return fail(SSD_ERR_INVALID_ARG, "x, dt, A, B and C are required");
+    if (need_y && !a->y) return fail(SSD_ERR_INVALID_ARG, "y is required");
+    if (a->initial_state && !aligned(a->initial_state, 16))
+        return fail(SSD_ERR_INVALID_ARG, "initial_state must be 16-byte aligned");
+    if (a->final_state && !aligned(a->final_state, 16))
+        return fail(SSD_ERR_INVALID_ARG, "final_state must be 16-byte aligned");
+    return SSD_OK;
+}
+
+ssd::Params make_params(const ssd_fwd_args *a) {
+    ssd::Params p;
+    p.B = (int)a->B; p.L = (int)a->L; p.H = (int)a->H; p.P = (int)a->P; p.N = (int)a->N;
+    p.G = (int)a->G; p.Q = (int)a->chunk;
+    p.nchunks = (int)((a->L + a->chunk - 1) / a->chunk);
+    p.hpg = (int)(a->H / a->G);
+    p.x = a->x; p.dt = a->dt; p.A = a->A; p.Bm = a->Bm; p.Cm = a->Cm; p.D = a->D; p.z = a->z;
+    p.dt_bias = a->dt_bias; p.h0 = a->initial_state; p.y = a->y; p.final_state = a->final_state;
+    p.dt_softplus = a->dt_softplus ? 1 : 0;
+    p.has_limit = !(a->dt_min == 0.f && isinf(a->dt_max) && a->dt_max > 0.f);
+    p.dt_min = a->dt_min; p.dt_max = a->dt_max;
+    return p;
+}
+
+struct ChunkedLayout {
+    size_t err_off, dtp_off, cs_off, states_off, total;
+};
+
+ChunkedLayout chunked_layout(const ssd_fwd_args *a) {
+    const size_t nchunks = (size_t)((a->L + a->chunk - 1) / a->chunk);
+    const size_t vec = (size_t)a->B * a->H * nchunks * a->chunk * sizeof(float);
+    const size_t st = (size_t)a->B * nchunks * a->H * a->P * a->N * sizeof(float);
+    ChunkedLayout l;
+    l.err_off = 0;
+    l.dtp_off = kAlign;
+    l.cs_off = l.dtp_off + align_up(vec);
+    l.states_off = l.cs_off + align_up(vec);
+    l.total = l.states_off + align_up(st);
+    return l;
+}
+
+int32_t resolve_plan(const ssd_fwd_args *a) {
+    if (a->plan != SSD_PLAN_AUTO) return a->plan;
+    if (ssd::fused_supported(a) && ssd::fused_preferred(a)) return SSD_PLAN_FUSED;
+    return SSD_PLAN_CHUNKED;
+}
+
+size_t workspace_for(const ssd_fwd_args *a, int32_t plan) {
+    if (plan == SSD_PLAN_FUSED) return ssd::fused_workspace_size(a);
+    return chunked_layout(a).total;
+}
+
+ssd_status run_chunked(const ssd_fwd_args *a, cudaStream_t s) {
+    const ChunkedLayout l = chunked_layout(a);
+    char *ws = static_cast<char *>(a->workspace);
+    float *dtp = reinterpret_cast<float *>(ws + l.dtp_off);
+    float *cs = reinterpret_cast<float *>(ws + l.cs_off);
+    float *states = reinterpret_cast<float *>(ws + l.states_off);
+    const ssd::Params p = make_params(a);
+    // the chunked plan has no device-side waits; its error word is cleared so
+    // that ssd_check_device_error reads "no error" after it
+    cudaError_t e = cudaMemsetAsync(ws + l.err_off, 0, kAlign, s);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the error word");
+    if ((e = ssd::launch_chunk_cumsum(p, dtp, cs, s)) != cudaSuccess) return cuda_fail(e, "chunk_cumsum");
+    if ((e = ssd::launch_chunk_state(p, a->x_dtype, dtp, cs, states, s)) != cudaSuccess)
+        return cuda_fail(e, "chunk_state");
+    if ((e = ssd::launch_state_passing(p, cs, states, s)) != cudaSuccess) return cuda_fail(e, "state_passing");
+    if ((e = ssd::launch_chunk_scan(p, a->x_dtype, dtp, cs, states, s)) != cudaSuccess)
+        return cuda_fail(e, "chunk_scan");
+    return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t ssd_abi_version(void) { return SSD_ABI_VERSION; }
+
+const char *ssd_status_string(ssd_status st) {
+    switch (st) {
+        case SSD_OK: return "ok";
+        case SSD_ERR_INVALID_ARG: return "invalid argument";
+        case SSD_ERR_UNSUPPORTED: return "unsupported configuration";
+        case SSD_ERR_WORKSPACE: return "workspace missing or too small";
+        case SSD_ERR_CUDA: return "CUDA error";
+        case SSD_ERR_TIMEOUT: return "device-side wait timed out";
+    }
+    return "unknown status";
+}
+
+const char *ssd_last_error_detail(void) { return g_detail; }
+
+ssd_status ssd_fwd_resolve_plan(const ssd_fwd_args *a, int32_t *plan) {
+    ssd_status st = check_shape(a);
+    if (st != SSD_OK) return st;
+    if (!plan) return fail(SSD_ERR_INVALID_ARG, "plan is NULL");
+    const int32_t pl = resolve_plan(a);
+    if (pl == SSD_PLAN_FUSED && !ssd::fused_supported(a))
+        return fail(SSD_ERR_UNSUPPORTED, "the fused plan does not support this shape: %s",
+                    ssd::fused_unsupported_reason(a));
+    *plan = pl;
+    return ok();
+}
+
+ssd_status ssd_fwd_workspace_size(const ssd_fwd_args *a, size_t *bytes) {
+    int32_t plan = 0;
+    ssd_status st = ssd_fwd_resolve_plan(a, &plan);
+    if (st != SSD_OK) return st;
+    if (!bytes) return fail(SSD_ERR_INVALID_ARG, "bytes is NULL");
+    *bytes = workspace_for(a, plan);
+    return ok();
+}
+
+ssd_status ssd_fwd(const ssd_fwd_args *a, void *stream) {
+    int32_t plan = 0;
+    ssd_status st = ssd_fwd_resolve_plan(a, &plan);
+    if (st != SSD_OK) return st;
+    if ((st = check_pointers(a, true)) != SSD_OK) return st;
+    const size_t need = workspace_for(a, plan);
+    if (!a->workspace || a->workspace_bytes < need)
+        return fail(SSD_ERR_WORKSPACE, "workspace of %zu bytes required (%zu given)", need,
+                    a->workspace ? a->workspace_bytes : (size_t)0);
+    if (!aligned(a->workspace, kAlign)) return fail(SSD_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (plan == SSD_PLAN_FUSED) {
+        cudaError_t e = ssd::run_fused(a, s);
+        if (e != cudaSuccess) return cuda_fail(e, "fused kernel");
+        return ok();
+    }
+    return run_chunked(a, s);
+}
+
+ssd_status ssd_chunk_cumsum(const ssd_fwd_args *a, float *dtp, float *cs, void *stream) {
+    ssd_status st = check_shape(a);
+    if (st != SSD_OK) return st;
+    if (!a->dt || !a->A) return fail(SSD_ERR_INVALID_ARG, "dt and A are required");
+    if (!dtp || !cs) return fail(SSD_ERR_INVALID_ARG, "dtp and cs are required");
+    cudaError_t e = ssd::launch_chunk_cumsum(make_params(a), dtp, cs, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "chunk_cumsum");
+    return ok();
+}
+
+ssd_status ssd_chunk_state(const ssd_fwd_args *a, const float *dtp, const float *cs, float *states,
+                           void *stream) {
+    ssd_status st = check_shape(a);
+    if (st != SSD_OK) return st;
+    if ((st = check_pointers(a, false)) != SSD_OK) return st;
+    if (!dtp || !cs || !states) return fail(SSD_ERR_INVALID_ARG, "dtp, cs and states are required");
+    cudaError_t e = ssd::launch_chunk_state(make_params(a), a->x_dtype, dtp, cs, states,
+                                            static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "chunk_state");
+    return ok();
+}
+
+ssd_status ssd_state_passing(const ssd_fwd_args *a, const float *cs, float *states, void *stream) {
+    ssd_status st = check_shape(a);
+    if (st != SSD_OK) return st;
+    if (a->initial_state && !aligned(a->initial_state, 16))
+        return fail(SSD_ERR_INVALID_ARG, "initial_state must be 16-byte aligned");
+    if (a->final_state && !aligned(a->final_state, 16))
+        return fail(SSD_ERR_INVALID_ARG, "final_state must be 16-byte aligned");
+    if (!cs || !states) return fail(SSD_ERR_INVALID_ARG, "cs and states are required");
+    if (!aligned(states, 16)) return fail(SSD_ERR_INVALID_ARG, "states must be 16-byte aligned");
+    cudaError_t e = ssd::launch_state_passing(make_params(a), cs, states, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "state_passing");
+    return ok();
+}
+
+ssd_status ssd_chunk_scan(const ssd_fwd_args *a, const float *dtp, const float *cs, const float *states,
+                          void *stream) {
+    ssd_status st = check_shape(a);
+    if (st != SSD_OK) return st;
+    if ((st = check_pointers(a, true)) != SSD_OK) return st;
+    if (!dtp || !cs || !states) return fail(SSD_ERR_INVALID_ARG, "dtp, cs and states are required");
+    cudaError_t e = ssd::launch_chunk_scan(make_params(a), a->x_dtype, dtp, cs, states,
+                                           static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "chunk_scan");
+    return ok();
+}
+
+// ---- end-to-end entry with host buffers ----------------------------------
+
+namespace {
+
+struct HostLayout {
+    size_t fwd_ws, x, dt, A, Bm, Cm, D, z, dt_bias, h0, y, fin, total;
+};
+
+HostLayout host_layout(const ssd_fwd_args *a, int32_t plan) {
+    const size_t io = io_size(a->x_dtype);
+    const size_t nx = (size_t)a->B * a->L * a->H * a->P;
+    const size_t nbc = (size_t)a->B * a->L * a->G * a->N;
+    const size_t nst = (size_t)a->B * a->H * a->P * a->N;
+    HostLayout l;
+    size_t off = 0;
+    auto take = [&](size_t bytes) { size_t o = off; off += align_up(bytes); return o; };
+    l.fwd_ws = take(workspace_for(a, plan));
+    l.x = take(nx * io);
+    l.dt = take((size_t)a->B * a->L * a->H * 4);
+    l.A = take((size_t)a->H * 4);
+    l.Bm = take(nbc * io);
+    l.Cm = take(nbc * io);
+    l.D = take(a->D ? (size_t)a->H * 4 : 0);
+    l.z = take(a->z ? nx * io : 0);
+    l.dt_bias = take(a->dt_bias ? (size_t)a->H * 4 : 0);
+    l.h0 = take(a->initial_state ? nst * 4 : 0);
+    l.y = take(nx * io);
+    l.fin = take(a->final_state ? nst * 4 : 0);
+    l.total = off;
+    return l;
+}
+
+}  // namespace
+
+ssd_status ssd_fwd_host_workspace_size(const ssd_fwd_args *a, size_t *bytes) {
+    int32_t plan = 0;
+    ssd_status st = ssd_fwd_resolve_plan(a, &plan);
+    if (st != SSD_OK) return st;
+    if (!bytes) return fail(SSD_ERR_INVALID_ARG, "bytes is NULL");
+    *bytes = host_layout(a, plan).total;
+    return ok();
+}
+
+ssd_status ssd_fwd_host(const ssd_fwd_args *a, void *stream) {
+    int32_t plan = 0;
+    ssd_status st = ssd_fwd_resolve_plan(a, &plan);
+    if (st != SSD_OK) return st;
+    if ((st = check_pointers(a, true)) != SSD_OK) return st;
+    const HostLayout l = host_layout(a, plan);
+    if (!a->workspace || a->workspace_bytes < l.total)
+        return fail(SSD_ERR_WORKSPACE, "workspace of %zu bytes required (%zu given)", l.total,
+                    a->workspace ? a->workspace_bytes : (size_t)0);
+    if (!aligned(a->workspace, kAlign)) return fail(SSD_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char *ws = static_cast<char *>(a->workspace);
+    const size_t io = io_size(a->x_dtype);
+    const size_t nx = (size_t)a->B * a->L * a->H * a->P;
+    const size_t nbc = (size_t)a->B * a->L * a->G * a->N;
+    const size_t nst = (size_t)a->B * a->H * a->P * a->N;
+    ssd_fwd_args d = *a;
+    cudaError_t e = cudaSuccess;
+    auto h2d = [&](size_t off, const void *src, size_t bytes) -> void * {
+        if (!src || bytes == 0) return nullptr;
+        if (e == cudaSuccess) e = cudaMemcpyAsync(ws + off, src, bytes, cudaMemcpyHostToDevice, s);
+        return ws + off;
+    };
+    d.x = h2d(l.x, a->x, nx * io);
+    d.dt = static_cast<const float *>(h2d(l.dt, a->dt, (size_t)a->B * a->L * a->H * 4));
+    d.A = static_cast<const float *>(h2d(l.A, a->A, (size_t)a->H * 4));
+    d.Bm = h2d(l.Bm, a->Bm, nbc * io);
+    d.Cm = h2d(l.Cm, a->Cm, nbc * io);
+    d.D = static_cast<const float *>(h2d(l.D, a->D, (size_t)a->H * 4));
+    d.z = h2d(l.z, a->z, nx * io);
+    d.dt_bias = static_cast<const float *>(h2d(l.dt_bias, a->dt_bias, (size_t)a->H * 4));
+    d.initial_state = static_cast<const float *>(h2d(l.h0, a->initial_state, nst * 4));
+    if (e != cudaSuccess) return cuda_fail(e, "host-to-device copy");
+    d.y = ws + l.y;
+    d.final_state = a->final_state ? reinterpret_cast<float *>(ws + l.fin) : nullptr;
+    d.workspace = ws + l.fwd_ws;
+    d.workspace_bytes = workspace_for(a, plan);
+    d.plan = plan;
+    if ((st = ssd_fwd(&d, stream)) != SSD_OK) return st;
+    e = cudaMemcpyAsync(a->y, d.y, nx * io, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess && a->final_state)
+        e = cudaMemcpyAsync(a->final_state, d.final_state, nst * 4, cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return cuda_fail(e, "device-to-host copy");
+    return ok();
+}
+
+ssd_status ssd_check_device_error(const ssd_fwd_args *a, void *stream) {
+    if (!a || !a->workspace) return fail(SSD_ERR_INVALID_ARG, "args with a workspace required");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+    uint32_t word = 0;
+    e = cudaMemcpy(&word, a->workspace, sizeof(word), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the error word");
+    if (word != 0) return fail(SSD_ERR_TIMEOUT, "device error word 0x%08x", word);
+    return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,99 @@
+// ssd_internal.cuh -- shared device helpers and the kernel parameter block
+// of the GB300 SSD forward.  Not part of the public ABI (see include/ssd.h).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ssd.h"
+
+namespace ssd {
+
+// Everything a kernel needs to know about one call, in device-friendly form.
+struct Params {
+    int B, L, H, P, N, G, Q, nchunks, hpg;  // hpg = heads per group = H / G
+    const void *x;
+    const float *dt;
+    const float *A;
+    const void *Bm;
+    const void *Cm;
+    const float *D;
+    const void *z;
+    const float *dt_bias;
+    const float *h0;
+    void *y;
+    float *final_state;
+    int dt_softplus;
+    int has_limit;
+    float dt_min, dt_max;
+};
+
+enum IoType { IO_F32 = SSD_F32, IO_F16 = SSD_F16, IO_BF16 = SSD_BF16 };
+
+template <int IO> struct IoTraits;
+template <> struct IoTraits<IO_F32> {
+    using T = float;
+    static __device__ __forceinline__ float to_f(T v) { return v; }
+    static __device__ __forceinline__ T from_f(float v) { return v; }
+};
+template <> struct IoTraits<IO_F16> {
+    using T = __half;
+    static __device__ __forceinline__ float to_f(T v) { return __half2float(v); }
+    static __device__ __forceinline__ T from_f(float v) { return __float2half_rn(v); }
+};
+template <> struct IoTraits<IO_BF16> {
+    using T = __nv_bfloat16;
+    static __device__ __forceinline__ float to_f(T v) { return __bfloat162float(v); }
+    static __device__ __forceinline__ T from_f(float v) { return __float2bfloat16_rn(v); }
+};
+
+template <int IO>
+__device__ __forceinline__ float ld_io(const void *base, size_t i) {
+    using T = typename IoTraits<IO>::T;
+    return IoTraits<IO>::to_f(__ldg(reinterpret_cast<const T *>(base) + i));
+}
+template <>
+__device__ __forceinline__ float ld_io<IO_F16>(const void *base, size_t i) {
+    return __half2float(reinterpret_cast<const __half *>(base)[i]);
+}
+template <>
+__device__ __forceinline__ float ld_io<IO_BF16>(const void *base, size_t i) {
+    return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(base)[i]);
+}
+
+template <int IO>
+__device__ __forceinline__ void st_io(void *base, size_t i, float v) {
+    using T = typename IoTraits<IO>::T;
+    reinterpret_cast<T *>(base)[i] = IoTraits<IO>::from_f(v);
+}
+
+// softplus(u) = log(1 + e^u).  Above 20 it equals u to within 2e-9 relative,
+// far below fp32 resolution, so u is returned there.
+__device__ __forceinline__ float softplus_f(float u) {
+    return u > 20.f ? u : log1pf(expf(u));
+}
+
+// Processed step d_t: add the bias, then softplus, then clamp ("Preprocess:
+// softplus / clamp / decay", README "AscendC execution path").
+__device__ __forceinline__ float dt_processed(const Params &p, float raw, int h) {
+    float u = raw;
+    if (p.dt_bias) u += __ldg(p.dt_bias + h);
+    float d = p.dt_softplus ? softplus_f(u) : u;
+    if (p.has_limit) d = fminf(fmaxf(d, p.dt_min), p.dt_max);
+    return d;
+}
+
+__device__ __forceinline__ float silu_f(float v) { return v / (1.f + expf(-v)); }
+
+// Launchers of the chunked plan (CUDA-core fp32 kernels).
+cudaError_t launch_chunk_cumsum(const Params &p, float *dtp, float *cs, cudaStream_t s);
+cudaError_t launch_chunk_state(const Params &p, int io, const float *dtp, const float *cs,
+                               float *states, cudaStream_t s);
+cudaError_t launch_state_passing(const Params &p, const float *cs, float *states,
+                                 cudaStream_t s);
+cudaError_t launch_chunk_scan(const Params &p, int io, const float *dtp, const float *cs,
+                              const float *states, cudaStream_t s);
+
+}  // namespace ssd

@@ -1,0 +1,127 @@
+"""The C-ABI library builds, loads and exports every symbol include/ssd.h
+declares; host-side validation answers without a GPU (no compute calls)."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import mamba_ssd_chunked_fwd_gb300 as ssd
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "ssd.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ssd_[a-z_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ssd.load_library()
+    names = _declared_functions()
+    assert "ssd_fwd" in names and "ssd_chunk_scan" in names
+    for name in names:
+        assert hasattr(lib, name), f"missing export {name}"
+    assert lib.ssd_abi_version() == 1
+
+
+def test_status_strings():
+    lib = ssd.load_library()
+    for code in range(6):
+        assert lib.ssd_status_string(code)
+    assert lib.ssd_status_string(0) == b"ok"
+
+
+def _args(**over):
+    kw = dict(B=1, L=128, H=4, P=64, N=64, G=2)
+    kw.update({k: over.pop(k) for k in list(over) if k in kw})
+    x = torch.empty((kw["B"], kw["L"], kw["H"], kw["P"]))
+    dt = torch.empty((kw["B"], kw["L"], kw["H"]))
+    A = torch.empty((kw["H"],))
+    Bm = torch.empty((kw["B"], kw["L"], kw["G"], kw["N"]))
+    chunk = over.pop("chunk", 64)
+    a = ssd.make_args(x, dt, A, Bm, Bm, chunk, y=x, **over)
+    return a
+
+
+def _status(fn, a):
+    out = ctypes.c_size_t(0)
+    return fn(ctypes.byref(a), ctypes.byref(out)), out.value
+
+
+def test_workspace_size_for_valid_shape():
+    lib = ssd.load_library()
+    a = _args()
+    st, n = _status(lib.ssd_fwd_workspace_size, a)
+    assert st == 0
+    # chunked plan: error word + dtp + cs + states
+    c = 2
+    assert n >= 256 + 2 * 1 * 4 * c * 64 * 4 + 1 * c * 4 * 64 * 64 * 4
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("B", 0, 1), ("L", -3, 1), ("H", 0, 1), ("P", 0, 1), ("G", 3, 1),
+    ("chunk", 24, 2), ("chunk", 512, 2), ("P", 72, 2), ("N", 256, 2),
+    ("ops", 7, 1), ("plan", 9, 1), ("x_dtype", 5, 1), ("bc_dtype", 2, 2),
+])
+def test_validation_rejects(field, value, code):
+    lib = ssd.load_library()
+    a = _args()
+    setattr(a, field, value)
+    st, _ = _status(lib.ssd_fwd_workspace_size, a)
+    assert st == code, (field, value, st, lib.ssd_last_error_detail())
+    assert lib.ssd_last_error_detail()
+
+
+def test_dt_limit_must_be_ordered():
+    lib = ssd.load_library()
+    a = _args(dt_limit=(0.5, 0.1))
+    st, _ = _status(lib.ssd_fwd_workspace_size, a)
+    assert st == 1
+
+
+def test_missing_pointers_rejected_before_any_launch():
+    lib = ssd.load_library()
+    a = _args()
+    a.x = None
+    assert lib.ssd_fwd(ctypes.byref(a), None) == 1
+    a = _args()
+    a.y = None
+    assert lib.ssd_fwd(ctypes.byref(a), None) == 1
+    a = _args()
+    assert lib.ssd_chunk_cumsum(ctypes.byref(a), None, None, None) == 1
+
+
+def test_missing_workspace_rejected():
+    lib = ssd.load_library()
+    a = _args()
+    a.workspace = None
+    assert lib.ssd_fwd(ctypes.byref(a), None) == 3
+    assert b"workspace" in lib.ssd_last_error_detail()
+
+
+def test_misaligned_state_rejected():
+    lib = ssd.load_library()
+    a = _args()
+    a.final_state = 8  # not 16-byte aligned
+    assert lib.ssd_fwd(ctypes.byref(a), None) == 1
+
+
+def test_python_binding_raises_with_detail():
+    a = _args()
+    a.G = 3
+    with pytest.raises(ssd.SsdError) as ei:
+        ssd.ssd_fwd_workspace_size(a)
+    assert "G" in str(ei.value)
+
+
+def test_fused_plan_request_is_checked():
+    a = _args(plan="fused")
+    lib = ssd.load_library()
+    plan = ctypes.c_int32(-1)
+    st = lib.ssd_fwd_resolve_plan(ctypes.byref(a), ctypes.byref(plan))
+    assert st in (0, 2)
+    if st == 0:
+        assert plan.value == ssd.SSD_PLAN_FUSED

@@ -1,0 +1,267 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the float64
+oracle on the same seeded inputs.
+
+Small shapes are compared element by element in full (several chunks and a
+ragged tail); the five named workloads run at full size and are compared on
+sampled (batch, head) sequences the oracle recomputes one by one.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import ssd_inputs
+from _harness import (TOL, assert_close, gather_pairs, oracle_problem, pick_pairs, run_gpu,
+                      to_device, workload_inputs)
+
+pytestmark = pytest.mark.gpu
+
+
+def _mode(ops):
+    return {"f32": "f32", "f16": "f16", "bf16": "bf16"}[ops]
+
+
+def _full_compare(oracle_mod, inp, y, fin, mode, what):
+    prob = oracle_problem(oracle_mod, inp)
+    yr, fr = oracle_mod.forward(prob)
+    assert_close(oracle_mod, y.double().cpu().numpy(), yr, mode, what + " y")
+    if fin is not None:
+        assert_close(oracle_mod, fin.double().cpu().numpy(), fr, mode, what + " final_state")
+
+
+# ---- named workloads at full size ---------------------------------------------
+
+@pytest.mark.parametrize("name", ["tiny", "same_device", "large_training", "long_sequence",
+                                  "gated_prefill"])
+@pytest.mark.parametrize("plan", ["auto", "chunked"])
+def test_named_workload(oracle_mod, name, plan):
+    w, inp = workload_inputs(name)
+    y, fin = run_gpu(inp, ops=w.ops, plan=plan)
+    assert y.dtype == inp["x"].dtype
+    if name == "tiny":
+        _full_compare(oracle_mod, inp, y, fin, _mode(w.ops), name)
+        return
+    pairs = pick_pairs(w.B, w.H, 6, seed=w.seed)
+    prob = oracle_problem(oracle_mod, inp)
+    ref = oracle_mod.recurrence(prob, pairs, want_final=w.return_final_state)
+    ys, fs = gather_pairs(y, fin, pairs)
+    assert_close(oracle_mod, ys, ref["y"], _mode(w.ops), f"{name} y")
+    if w.return_final_state:
+        assert_close(oracle_mod, fs, ref["final_state"], _mode(w.ops), f"{name} final_state")
+    assert torch.isfinite(y.float()).all()
+
+
+# ---- small shapes, every feature, element by element ----------------------------
+
+SHAPES = [
+    # B, L, H, P, N, G, chunk
+    (1, 128, 2, 64, 128, 1, 128),
+    (2, 200, 4, 32, 64, 2, 64),      # ragged tail
+    (1, 77, 3, 16, 16, 1, 16),       # tiny dims, ragged
+    (2, 300, 8, 64, 64, 8, 64),      # G = H
+    (1, 513, 4, 64, 128, 1, 256),    # one token past a chunk boundary
+    (3, 96, 6, 48, 80, 3, 32),
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+@pytest.mark.parametrize("feat", ["plain", "all"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_small_shapes(oracle_mod, shape, feat, dtype):
+    B, L, H, P, N, G, Q = shape
+    f = dict(D=True, z=True, dt_bias=True, h0=True) if feat == "all" else {}
+    _, inp = ssd_inputs.custom(B, L, H, P, N, G, Q, seed=hash(shape) % 1000, x_dtype=dtype,
+                               ops=dtype, **f)
+    y, fin = run_gpu(inp, ops=dtype)
+    _full_compare(oracle_mod, inp, y, fin, dtype, f"{shape} {feat} {dtype}")
+
+
+@pytest.mark.parametrize("ops", ["f32", "f16", "bf16"])
+def test_operand_modes(oracle_mod, ops):
+    _, inp = ssd_inputs.custom(2, 256, 8, 64, 64, 2, 64, seed=21, ops=ops, h0=True, D=True)
+    y, fin = run_gpu(inp, ops=ops)
+    _full_compare(oracle_mod, inp, y, fin, ops, f"ops={ops}")
+
+
+def test_dt_limit_and_no_softplus(oracle_mod):
+    _, inp = ssd_inputs.custom(1, 160, 4, 32, 32, 2, 32, seed=22, dt_bias=True,
+                               dt_dist=("uniform", -0.5, 1.5), dt_softplus=False)
+    y, fin = run_gpu(inp, ops="f32", dt_limit=(0.05, 0.8))
+    prob = oracle_problem(oracle_mod, inp, dt_limit=(0.05, 0.8))
+    yr, fr = oracle_mod.forward(prob)
+    assert_close(oracle_mod, y.double().cpu().numpy(), yr, "f32", "dt_limit y")
+    assert_close(oracle_mod, fin.double().cpu().numpy(), fr, "f32", "dt_limit final")
+
+
+# ---- the four steps, one at a time -------------------------------------------------
+
+def _stage_setup(oracle_mod, shape=(2, 200, 4, 32, 64, 2, 64), dtype="f32", **feat):
+    import mamba_ssd_chunked_fwd_gb300 as ssd
+    B, L, H, P, N, G, Q = shape
+    _, inp = ssd_inputs.custom(B, L, H, P, N, G, Q, seed=31, x_dtype=dtype, **feat)
+    d = to_device(inp)
+    c = -(-L // Q)
+    y = torch.empty_like(d["x"])
+    fin = torch.empty((B, H, P, N), device="cuda")
+    args = ssd.make_args(d["x"], d["dt"], d["A"], d["B"], d["C"], Q, y=y, final_state=fin,
+                         D=d["D"], z=d["z"], dt_bias=d["dt_bias"],
+                         initial_states=d["initial_states"], dt_softplus=True)
+    prob = oracle_problem(oracle_mod, inp)
+    return ssd, inp, d, args, prob, (B, L, H, P, N, G, Q, c), y, fin
+
+
+def test_stage_chunk_cumsum(oracle_mod):
+    ssd, inp, d, args, prob, (B, L, H, P, N, G, Q, c), _, _ = _stage_setup(oracle_mod, dt_bias=True)
+    dtp = torch.full((B, H, c, Q), float("nan"), device="cuda")
+    cs = torch.full((B, H, c, Q), float("nan"), device="cuda")
+    ssd.ssd_chunk_cumsum(args, dtp, cs)
+    torch.cuda.synchronize()
+    rd, rc = oracle_mod.chunk_cumsum(prob, Q)
+    assert_close(oracle_mod, dtp.double().cpu().numpy(), rd, "f32", "dtp")
+    assert_close(oracle_mod, cs.double().cpu().numpy(), rc, "f32", "cs")
+    # past the ragged end: zero step, constant cumulative sum
+    tail = L - (c - 1) * Q
+    assert torch.all(dtp[:, :, -1, tail:] == 0)
+    assert torch.all(cs[:, :, -1, tail:] == cs[:, :, -1, tail - 1:tail])
+
+
+def test_stage_chunk_state(oracle_mod):
+    ssd, inp, d, args, prob, (B, L, H, P, N, G, Q, c), _, _ = _stage_setup(oracle_mod, dt_bias=True)
+    rd, rc = oracle_mod.chunk_cumsum(prob, Q)
+    dtp = torch.from_numpy(rd).float().cuda()
+    cs = torch.from_numpy(rc).float().cuda()
+    states = torch.full((B, c, H, P, N), float("nan"), device="cuda")
+    ssd.ssd_chunk_state(args, dtp, cs, states)
+    torch.cuda.synchronize()
+    ref = oracle_mod.chunk_local_states(prob, Q)              # [B*H, c, P, N]
+    got = states.permute(0, 2, 1, 3, 4).reshape(B * H, c, P, N)
+    assert_close(oracle_mod, got.double().cpu().numpy(), ref, "f32", "chunk states")
+
+
+def test_stage_state_passing(oracle_mod):
+    ssd, inp, d, args, prob, (B, L, H, P, N, G, Q, c), _, fin = _stage_setup(
+        oracle_mod, h0=True, dt_bias=True)
+    _, rc = oracle_mod.chunk_cumsum(prob, Q)
+    local = oracle_mod.chunk_local_states(prob, Q).reshape(B, H, c, P, N)
+    states = torch.from_numpy(local).float().permute(0, 2, 1, 3, 4).contiguous().cuda()
+    cs = torch.from_numpy(rc).float().cuda()
+    ssd.ssd_state_passing(args, cs, states)
+    torch.cuda.synchronize()
+    rec = oracle_mod.recurrence(prob, chunk=Q, want_y=False, want_chunk_states=True)
+    got = states.permute(0, 2, 1, 3, 4).reshape(B * H, c, P, N)
+    assert_close(oracle_mod, got.double().cpu().numpy(), rec["chunk_states"], "f32", "entering states")
+    assert_close(oracle_mod, fin.double().cpu().numpy().reshape(B * H, P, N), rec["final_state"],
+                 "f32", "final state")
+
+
+def test_stage_chunk_scan(oracle_mod):
+    ssd, inp, d, args, prob, (B, L, H, P, N, G, Q, c), y, _ = _stage_setup(
+        oracle_mod, h0=True, D=True, z=True, dt_bias=True)
+    rd, rc = oracle_mod.chunk_cumsum(prob, Q)
+    rec = oracle_mod.recurrence(prob, chunk=Q, want_chunk_states=True)
+    states = torch.from_numpy(rec["chunk_states"].reshape(B, H, c, P, N)).float()
+    states = states.permute(0, 2, 1, 3, 4).contiguous().cuda()
+    ssd.ssd_chunk_scan(args, torch.from_numpy(rd).float().cuda(), torch.from_numpy(rc).float().cuda(),
+                       states)
+    torch.cuda.synchronize()
+    got = y.permute(0, 2, 1, 3).reshape(B * H, L, P)
+    assert_close(oracle_mod, got.double().cpu().numpy(), rec["y"], "f32", "chunk scan y")
+
+
+# ---- properties ------------------------------------------------------------------
+
+def test_chunk_size_invariance(oracle_mod):
+    _, inp = ssd_inputs.custom(1, 512, 4, 64, 128, 1, 64, seed=41, h0=True, D=True)
+    outs = []
+    for Q in (64, 128, 256):
+        y, fin = run_gpu(inp, chunk=Q, ops="f32")
+        outs.append((y.double().cpu().numpy(), fin.double().cpu().numpy()))
+    yr, fr = oracle_mod.forward(oracle_problem(oracle_mod, inp))
+    for y, f in outs:
+        assert_close(oracle_mod, y, yr, "f32", "chunk invariance y")
+        assert_close(oracle_mod, f, fr, "f32", "chunk invariance final")
+    assert oracle_mod.compare(outs[0][0], outs[2][0])["rel_l2"] < 2e-6
+
+
+@pytest.mark.parametrize("L1", [128, 150])
+def test_split_consistency(oracle_mod, L1):
+    _, inp = ssd_inputs.custom(2, 320, 4, 64, 64, 2, 64, seed=42, h0=True, D=True)
+    y, fin = run_gpu(inp, ops="f32")
+    head = {k: (v[:, :L1].contiguous() if k in ("x", "dt", "B", "C") else v) for k, v in inp.items()}
+    _, fh = run_gpu(head, ops="f32")
+    tail = {k: (v[:, L1:].contiguous() if k in ("x", "dt", "B", "C") else v) for k, v in inp.items()}
+    tail["initial_states"] = fh.cpu()
+    yt, ft = run_gpu(tail, ops="f32")
+    m = oracle_mod.compare(yt.double().cpu().numpy(), y[:, L1:].double().cpu().numpy())
+    assert m["rel_l2"] < 1e-5
+    assert oracle_mod.compare(ft.double().cpu().numpy(), fin.double().cpu().numpy())["rel_l2"] < 1e-5
+
+
+@pytest.mark.parametrize("name,plan", [("tiny", "auto"), ("same_device", "auto"),
+                                       ("large_training", "auto"), ("gated_prefill", "auto")])
+def test_bitwise_determinism(name, plan):
+    w, inp = workload_inputs(name)
+    y1, f1 = run_gpu(inp, ops=w.ops, plan=plan)
+    y2, f2 = run_gpu(inp, ops=w.ops, plan=plan)
+    assert torch.equal(y1, y2)
+    if f1 is not None:
+        assert torch.equal(f1, f2)
+
+
+def test_outputs_stay_inside_their_buffers():
+    """Canary guard bands around y and final_state, NaN-poisoned workspace."""
+    import mamba_ssd_chunked_fwd_gb300 as ssd
+    _, inp = ssd_inputs.custom(2, 200, 4, 64, 64, 2, 64, seed=43, h0=True, D=True, z=True)
+    d = to_device(inp)
+    B, L, H, P = inp["x"].shape
+    N = inp["B"].shape[3]
+    pad = 4096
+    ybuf = torch.full((pad + B * L * H * P + pad,), 12345.0, device="cuda")
+    fbuf = torch.full((pad + B * H * P * N + pad,), -777.0, device="cuda")
+    y = ybuf[pad:pad + B * L * H * P].view(B, L, H, P)
+    fin = fbuf[pad:pad + B * H * P * N].view(B, H, P, N)
+    args = ssd.make_args(d["x"], d["dt"], d["A"], d["B"], d["C"], 64, y=y, final_state=fin,
+                         D=d["D"], z=d["z"], initial_states=d["initial_states"], dt_softplus=True)
+    nws = ssd.ssd_fwd_workspace_size(args)
+    ws = torch.full((nws // 4 + 1,), float("nan"), device="cuda")
+    args.workspace, args.workspace_bytes = ws.data_ptr(), nws
+    ssd.ssd_fwd(args)
+    torch.cuda.synchronize()
+    assert torch.all(ybuf[:pad] == 12345.0) and torch.all(ybuf[-pad:] == 12345.0)
+    assert torch.all(fbuf[:pad] == -777.0) and torch.all(fbuf[-pad:] == -777.0)
+    assert torch.isfinite(y).all() and torch.isfinite(fin).all()
+
+
+def test_host_buffer_entry_matches_device_entry():
+    import mamba_ssd_chunked_fwd_gb300 as ssd
+    _, inp = ssd_inputs.custom(2, 256, 4, 64, 64, 2, 64, seed=44, h0=True, D=True, z=True)
+    yd, fd = run_gpu(inp, ops="f32")
+    h = {k: (v.contiguous().pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    y = torch.empty_like(h["x"]).pin_memory()
+    B, L, H, P = h["x"].shape
+    fin = torch.empty((B, H, P, h["B"].shape[3])).pin_memory()
+    args = ssd.make_args(h["x"], h["dt"], h["A"], h["B"], h["C"], 64, y=y, final_state=fin,
+                         D=h["D"], z=h["z"], initial_states=h["initial_states"], dt_softplus=True)
+    nws = ssd.ssd_fwd_host_workspace_size(args)
+    ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
+    args.workspace, args.workspace_bytes = ws.data_ptr(), nws
+    ssd.ssd_fwd_host(args)
+    torch.cuda.synchronize()
+    assert torch.equal(y, yd.cpu()) and torch.equal(fin, fd.cpu())
+
+
+def test_small_workspace_is_an_error_not_a_fault():
+    import mamba_ssd_chunked_fwd_gb300 as ssd
+    _, inp = ssd_inputs.custom(1, 128, 2, 64, 64, 1, 64, seed=45)
+    d = to_device(inp)
+    y = torch.empty_like(d["x"])
+    args = ssd.make_args(d["x"], d["dt"], d["A"], d["B"], d["C"], 64, y=y, dt_softplus=True)
+    nws = ssd.ssd_fwd_workspace_size(args)
+    ws = torch.empty(nws - 256, dtype=torch.uint8, device="cuda")
+    args.workspace, args.workspace_bytes = ws.data_ptr(), nws - 256
+    with pytest.raises(ssd.SsdError) as ei:
+        ssd.ssd_fwd(args)
+    assert ei.value.status == 3
+    ssd.ssd_check_device_error(ssd.make_args(d["x"], d["dt"], d["A"], d["B"], d["C"], 64, y=y,
+                                             workspace=torch.zeros(256, dtype=torch.uint8, device="cuda")))
