@@ -2,6 +2,7 @@
 oracle on the same seeded inputs, and compare them."""
 from __future__ import annotations
 
+import functools
 import math
 
 import numpy as np
@@ -78,6 +79,8 @@ def assert_close(oracle, got, ref, mode, what=""):
     return m
 
 
+@functools.lru_cache(maxsize=2)
 def workload_inputs(name):
+    """Inputs of a named workload (cached: the large ones take seconds to draw)."""
     w = ssd_inputs.WORKLOADS[name]
     return w, ssd_inputs.make(w)

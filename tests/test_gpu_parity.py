@@ -265,3 +265,57 @@ def test_small_workspace_is_an_error_not_a_fault():
     assert ei.value.status == 3
     ssd.ssd_check_device_error(ssd.make_args(d["x"], d["dt"], d["A"], d["B"], d["C"], 64, y=y,
                                              workspace=torch.zeros(256, dtype=torch.uint8, device="cuda")))
+
+
+# ---- the fused tensor-core plan ---------------------------------------------------
+
+FUSED_SHAPES = [
+    # B, L, H, P, N, G, chunk  (P = N = chunk = 64, even heads per group)
+    (1, 64, 2, 64, 64, 1, 64),       # one chunk, one unit
+    (2, 256, 8, 64, 64, 2, 64),      # several chunks and units
+    (1, 200, 4, 64, 64, 1, 64),      # ragged tail
+    (3, 448, 12, 64, 64, 3, 64),     # 4 heads per group, 7 chunks
+]
+
+
+@pytest.mark.parametrize("shape", FUSED_SHAPES)
+@pytest.mark.parametrize("feat", ["plain", "all"])
+@pytest.mark.parametrize("io,ops", [("f32", "bf16"), ("f32", "f16"), ("bf16", "bf16")])
+def test_fused_plan(oracle_mod, shape, feat, io, ops):
+    B, L, H, P, N, G, Q = shape
+    f = dict(D=True, z=True, dt_bias=True, h0=True) if feat == "all" else {}
+    _, inp = ssd_inputs.custom(B, L, H, P, N, G, Q, seed=7 + L + H, x_dtype=io, ops=ops, **f)
+    y, fin = run_gpu(inp, ops=ops, plan="fused")
+    _full_compare(oracle_mod, inp, y, fin, ops, f"fused {shape} {feat} {io}/{ops}")
+
+
+def test_fused_plan_many_units(oracle_mod):
+    """More units than CTAs, so each CTA walks several units in turn."""
+    _, inp = ssd_inputs.custom(4, 128, 128, 64, 64, 32, 64, seed=77, ops="bf16", h0=True)
+    y, fin = run_gpu(inp, ops="bf16", plan="fused")
+    pairs = pick_pairs(4, 128, 12, seed=3)
+    ref = oracle_mod.recurrence(oracle_problem(oracle_mod, inp), pairs)
+    ys, fs = gather_pairs(y, fin, pairs)
+    assert_close(oracle_mod, ys, ref["y"], "bf16", "fused many units y")
+    assert_close(oracle_mod, fs, ref["final_state"], "bf16", "fused many units final")
+
+
+def test_fused_plan_reports_no_device_error():
+    import mamba_ssd_chunked_fwd_gb300 as ssd
+    _, inp = ssd_inputs.custom(2, 256, 8, 64, 64, 2, 64, seed=78, ops="bf16")
+    d = to_device(inp)
+    y = torch.empty_like(d["x"])
+    args = ssd.make_args(d["x"], d["dt"], d["A"], d["B"], d["C"], 64, y=y, dt_softplus=True,
+                         ops="bf16", plan="fused")
+    ws = torch.full((ssd.ssd_fwd_workspace_size(args),), 255, dtype=torch.uint8, device="cuda")
+    args.workspace, args.workspace_bytes = ws.data_ptr(), ws.numel()
+    ssd.ssd_fwd(args)
+    ssd.ssd_check_device_error(args)
+
+
+def test_fused_plan_rejects_unsupported_shape():
+    import mamba_ssd_chunked_fwd_gb300 as ssd
+    _, inp = ssd_inputs.custom(1, 128, 2, 64, 128, 1, 64, seed=79, ops="bf16")
+    with pytest.raises(ssd.SsdError) as ei:
+        run_gpu(inp, ops="bf16", plan="fused")
+    assert ei.value.status == 2
