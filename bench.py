@@ -104,12 +104,15 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, device_index: int):
+    def __init__(self, device_index: int, enabled: bool = True):
         self.idx = device_index
+        self.enabled = enabled
         self.proc = None
         self.path = None
 
     def __enter__(self):
+        if not self.enabled:
+            return self
         fd, self.path = tempfile.mkstemp(prefix="ssd_clocks_", suffix=".csv")
         os.close(fd)
         try:
@@ -185,6 +188,8 @@ def run_gpu(args):
     dev = torch.device("cuda", lrank if world > 1 else 0)
     torch.cuda.set_device(dev)
     w = ssd_inputs.WORKLOADS[args.workload]
+    if args.batch:
+        w = w.with_(B=args.batch)
     inp = ssd_inputs.make(w, seed=w.seed + 1000 * rank)
     d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
     y = torch.empty_like(d["x"])
@@ -214,7 +219,7 @@ def run_gpu(args):
         dist.barrier()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    with ClockSampler(dev.index) as clk:
+    with ClockSampler(dev.index, enabled=not args.no_clocks) as clk:
         torch.cuda.synchronize(dev)
         if dist:
             dist.barrier()
@@ -227,7 +232,7 @@ def run_gpu(args):
         torch.cuda.synchronize(dev)
         if dist:
             dist.barrier()
-        if args.steps * 0.002 < 1.0:  # keep the sampler alive for a few samples
+        if not args.no_clocks:  # keep the sampler alive for a few samples
             extra_until = time.time() + 0.5
             while time.time() < extra_until:
                 step()
@@ -269,7 +274,8 @@ def run_gpu(args):
                         if args.workload in PUBLISHED_TOKENS_PER_S else None),
         "dtype": ops_name if plan == ssd.SSD_PLAN_FUSED else "f32",
         "data": "synthetic (seeded, pages' distributions)",
-        "config": {"workload": f"{args.workload} {w.shape_tuple()} [B,L,H,P,N,chunk,G]",
+        "config": {"workload": f"{args.workload} {w.shape_tuple()} [B,L,H,P,N,chunk,G]"
+                               + (" (batch overridden)" if args.batch else ""),
                    "plan": {1: "chunked", 2: "fused"}[plan], "ops_requested": ops_name,
                    "public_dtype": w.x_dtype, "tokens_per_step_per_gpu": w.tokens,
                    "l2": ("flushed between steps (256 MiB write)" if flush is not None
@@ -428,6 +434,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true", help="skip the nvidia-smi clock sampler")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's batch size (a smaller case of the same shape)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)

@@ -5,9 +5,9 @@
 // of the "Mamba-2 SSD for Ascend NPU" README ("Limitations and roadmap"),
 // re-designed for tcgen05 tensor cores with TMEM accumulators.
 //
-// Work unit: (batch b, group g, head pair).  One CTA (256 threads, 8 warps)
-// walks the unit's chunks in order, carrying the fp32 [P,N] states of its two
-// heads in registers.  Per chunk of Q = 64 tokens (P = N = 64):
+// Work unit: (batch b, group g, head pair).  One CTA per SM walks units, and
+// each unit's chunks in order, carrying the fp32 [P,N] states of its two heads
+// in registers.  Per chunk of Q = 64 tokens (P = N = 64):
 //
 //   G     = C B^T                  [Q x Q]   rows duplicated to M = 128
 //   dS    = Xw^T B                 [2P x N]  Xw = exp(cs_last - cs_j) dt_j x_j
@@ -23,9 +23,28 @@
 // operands; the intra-chunk product reaches M = 128 with a zero block between
 // the heads' x tiles.  Operands are written into shared memory in the
 // no-swizzle block layout (see tc_ptx.cuh) straight from the natural
-// row-major global layout: x, B and C tiles are MN- or K-major as they come,
-// so no transposes are needed.  The next chunk's inputs are loaded into
-// registers while the current chunk computes.
+// row-major global layout (MN- or K-major as the tensors come), so nothing is
+// transposed.
+//
+// Warp roles (544 threads): warps 0-15 compute (thread = TMEM lane (head, p)
+// x 16 columns), warp 16 issues the MMAs from one thread.  They hand off
+// through mbarriers in both directions, so the compute warps never block on
+// MMA issue and the tensor core works on chunk k while the compute warps
+// finish chunk k-1:
+//
+//   compute, iteration k:  A_k  operands of chunk k -> smem        (arrive OPS_FULL)
+//                               prefetch chunk k+1 into registers
+//                          B_k  wait G_DONE;  G -> Mcat             (arrive MCAT_FULL)
+//                          C_k  wait DS_DONE; S <- a S + dS -> smem (arrive S_FULL)
+//                          D_k-1 wait Y_DONE; epilogue of chunk k-1 -> y
+//                          decay vectors of chunk k+1 (warps 14, 15)
+//   MMA warp, chunk k:     wait OPS_FULL -> G (commit G_DONE);
+//                          wait S_FULL -> dS, Yoff (commit DS_DONE);
+//                          wait MCAT_FULL -> Yint (commit Y_DONE[k%2])
+//
+// Xcat, Mcat and the Yoff / Yint TMEM accumulators are double-buffered, the
+// per-chunk decay vectors triple-buffered.  Every mbarrier wait gives up
+// after 2 s (recorded in the workspace error word) instead of hanging.
 #include <stdio.h>
 
 #include "ssd_fused.cuh"
@@ -37,29 +56,52 @@ namespace ssd {
 namespace {
 
 constexpr int kQ = 64, kN = 64, kP = 64;
-constexpr int kThreads = 256;
-constexpr uint64_t kWaitNs = 2000000000ull;  // an mbarrier wait gives up after 2 s
+constexpr int kComputeWarps = 16;
+constexpr int kComputeThreads = kComputeWarps * 32;
+constexpr int kMmaWarp = kComputeWarps;           // warp 16
+constexpr int kThreads = kComputeThreads + 32;    // 544
+constexpr int kCols = 16;                         // columns of each TMEM region per thread
+constexpr int kDecayWarp0 = 14;                   // warps 14, 15 compute the decay vectors
+constexpr uint64_t kWaitNs = 2000000000ull;       // an mbarrier wait gives up after 2 s
 
 // shared-memory layout, bytes from a 1024-aligned base
-constexpr uint32_t OFF_CB2 = 0;      // C twice (rows 0-63, 64-127), K-major, 16 KB
-constexpr uint32_t OFF_BB = 16384;   // B blocks (j, n), 8 KB: K-major for G, MN-major for dS
-constexpr uint32_t OFF_XT = 24576;   // Xw^T, MN-major, 128 (h,p) x 64 j, 16 KB
-constexpr uint32_t OFF_XC = 40960;   // [X_h0 | 0 | X_h1], MN-major, 192 rows x 64 j, 24 KB
-constexpr uint32_t OFF_MC = 65536;   // Mcat, K-major B operand, 64 i x 128 (h', j), 16 KB
-constexpr uint32_t OFF_S = 81920;    // S, K-major, 128 (h,p) x 64 n, 16 KB
-constexpr uint32_t OFF_VEC = 98304;  // per-chunk vectors
-constexpr uint32_t SMEM_BYTES = OFF_VEC + 4096 + 1024;  // + alignment slack
+constexpr uint32_t OFF_CB2 = 0;       // C twice (rows 0-63, 64-127), K-major, 16 KB
+constexpr uint32_t OFF_BB = 16384;    // B blocks (j, n), 8 KB: K-major for G, MN-major for dS
+constexpr uint32_t OFF_XT = 24576;    // Xw^T, MN-major, 128 (h,p) x 64 j, 16 KB
+constexpr uint32_t OFF_XC = 40960;    // 2 x [X_h0 | 0 | X_h1], MN-major, 192 rows x 64 j, 24 KB each
+constexpr uint32_t XC_BYTES = 24576;
+constexpr uint32_t OFF_MC = 90112;    // 2 x Mcat, K-major B operand, 64 i x 128 (h', j), 16 KB each
+constexpr uint32_t MC_BYTES = 16384;
+constexpr uint32_t OFF_S = 122880;    // S, K-major, 128 (h,p) x 64 n, 16 KB
+constexpr uint32_t OFF_VEC = 139264;  // 3 x ChunkVec
+constexpr uint32_t VEC_BYTES = 2560;
+constexpr uint32_t SMEM_BYTES = OFF_VEC + 3 * VEC_BYTES + 1024;  // + alignment slack
 
-// TMEM columns (256 allocated)
-constexpr uint32_t TM_G = 0, TM_DS = 64, TM_YOFF = 128, TM_YINT = 192, TM_COLS = 256;
+// TMEM columns (512 allocated)
+constexpr uint32_t TM_G = 0, TM_DS = 64, TM_COLS = 512;
+__device__ __forceinline__ uint32_t tm_yoff(int buf) { return 128u + 128u * buf; }
+__device__ __forceinline__ uint32_t tm_yint(int buf) { return 192u + 128u * buf; }
 
-struct ChunkVec {
+// mbarriers
+enum { BAR_OPS_FULL = 0, BAR_MCAT_FULL, BAR_S_FULL, BAR_G_DONE, BAR_DS_DONE, BAR_Y_DONE0, BAR_Y_DONE1, NBARS };
+
+// 16-byte aligned so that consecutive slots keep their float4 reads aligned
+struct alignas(16) ChunkVec {
     float d[2][kQ];    // processed step
-    float cs[2][kQ];   // within-chunk cumulative d*A
+    float cs2[2][kQ];  // within-chunk cumulative d*A, times log2(e)
     float ecs[2][kQ];  // exp(cs)
     float w[2][kQ];    // exp(cs_last - cs) * d
     float a[2];        // exp(cs_last)
 };
+static_assert(sizeof(ChunkVec) % 16 == 0 && 3 * sizeof(ChunkVec) <= 3 * VEC_BYTES, "ChunkVec slots");
+
+// 2^x on the MUFU unit (PTX ex2.approx, relative error ~2^-22, flushes below
+// 2^-126 to 0): used where the result is rounded to a 16-bit operand.
+__device__ __forceinline__ float ex2_approx(float x) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
 
 __device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
     if (bf16) {
@@ -70,9 +112,11 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// 16-byte shared store of an MMA operand.  No "memory" clobber: operand
+// memory is only read by the tensor core, and the fences / barriers that
+// publish it carry the ordering.
 __device__ __forceinline__ void st_shared_v4(uint32_t saddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(a), "r"(b), "r"(c), "r"(d)
-                 : "memory");
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(a), "r"(b), "r"(c), "r"(d));
 }
 
 __device__ __forceinline__ void store8(uint32_t saddr, const float (&v)[8], bool bf16) {
@@ -110,296 +154,398 @@ __device__ __forceinline__ void load8(const void *base, size_t off, bool valid, 
     }
 }
 
-// Registers holding one chunk of inputs for this thread.
+// Shapes of one call, held in registers by every thread.
+struct Dims {
+    int L, H, G, hpg, nchunks;
+};
+
+// Registers holding one chunk of inputs for one compute thread.
 struct ChunkRegs {
-    float x[4][8];   // 4 items of (token j, head h, 8 consecutive p)
-    float bm[2][8];  // 2 items of (token j, 8 consecutive n)
-    float cm[2][8];
-    float dt;        // threads < 128: (head, token)
+    float x[2][8];   // 2 items of (token j, head h, 8 consecutive p)
+    float bm[8];     // (token j, 8 consecutive n)
+    float cm[8];
+    float dt0, dt1;  // decay warps: raw dt of tokens lane and lane + 32
 };
 
 template <int IO>
-__device__ __forceinline__ void load_chunk(const Params &p, int b, int g, int h0, int k, int tid,
-                                           ChunkRegs &r) {
+__device__ __forceinline__ void load_chunk(const Params &p, const Dims &dm, int b, int g, int h0, int k,
+                                           int tid, int warp, int lane, ChunkRegs &r) {
     const int tok0 = k * kQ;
 #pragma unroll
-    for (int it = 0; it < 4; ++it) {
-        const int e = tid + kThreads * it;
+    for (int it = 0; it < 2; ++it) {
+        const int e = tid + kComputeThreads * it;
         const int jl = e & 7, c16 = (e >> 3) & 15, jg = e >> 7;
         const int h = c16 >> 3, po = c16 & 7, t = tok0 + jg * 8 + jl;
-        load8<IO>(p.x, (((size_t)b * p.L + t) * p.H + h0 + h) * kP + 8 * po, t < p.L, r.x[it]);
+        load8<IO>(p.x, (((size_t)b * dm.L + t) * dm.H + h0 + h) * kP + 8 * po, t < dm.L, r.x[it]);
     }
-#pragma unroll
-    for (int it = 0; it < 2; ++it) {
-        const int e = tid + kThreads * it;
+    {
+        const int e = tid;
         const int jl = e & 7, ng = (e >> 3) & 7, jg = e >> 6;
         const int t = tok0 + jg * 8 + jl;
-        const size_t off = (((size_t)b * p.L + t) * p.G + g) * kN + 8 * ng;
-        load8<IO>(p.Bm, off, t < p.L, r.bm[it]);
-        load8<IO>(p.Cm, off, t < p.L, r.cm[it]);
+        const size_t off = (((size_t)b * dm.L + t) * dm.G + g) * kN + 8 * ng;
+        load8<IO>(p.Bm, off, t < dm.L, r.bm);
+        load8<IO>(p.Cm, off, t < dm.L, r.cm);
     }
-    r.dt = 0.f;
-    if (tid < 2 * kQ) {
-        const int h = tid >> 6, i = tid & 63, t = tok0 + i;
-        if (t < p.L) r.dt = __ldg(p.dt + ((size_t)b * p.L + t) * p.H + h0 + h);
+    if (warp >= kDecayWarp0) {
+        const int h = h0 + warp - kDecayWarp0;
+        const int t0 = tok0 + lane, t1 = tok0 + lane + 32;
+        r.dt0 = t0 < dm.L ? __ldg(p.dt + ((size_t)b * dm.L + t0) * dm.H + h) : 0.f;
+        r.dt1 = t1 < dm.L ? __ldg(p.dt + ((size_t)b * dm.L + t1) * dm.H + h) : 0.f;
     }
+}
+
+// Decay vectors of one chunk for head hh (one warp): processed step, the
+// within-chunk inclusive cumulative sum of d*A (warp scan over 64 tokens)
+// and the exponentials the other phases need.
+__device__ __forceinline__ void decay_vectors(const Params &p, const Dims &dm, int h, int hh, int tok0,
+                                              int lane, float raw0, float raw1, ChunkVec &V) {
+    const float d0 = (tok0 + lane < dm.L) ? dt_processed(p, raw0, h) : 0.f;
+    const float d1 = (tok0 + lane + 32 < dm.L) ? dt_processed(p, raw1, h) : 0.f;
+    const float A = __ldg(p.A + h);
+    float v0 = d0 * A, v1 = d1 * A;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float o0 = __shfl_up_sync(0xffffffffu, v0, off);
+        const float o1 = __shfl_up_sync(0xffffffffu, v1, off);
+        if (lane >= off) { v0 += o0; v1 += o1; }
+    }
+    v1 += __shfl_sync(0xffffffffu, v0, 31);
+    const float last = __shfl_sync(0xffffffffu, v1, 31);
+    constexpr float kLog2e = 1.4426950408889634f;
+    V.d[hh][lane] = d0;
+    V.d[hh][lane + 32] = d1;
+    V.cs2[hh][lane] = v0 * kLog2e;
+    V.cs2[hh][lane + 32] = v1 * kLog2e;
+    V.ecs[hh][lane] = expf(v0);
+    V.ecs[hh][lane + 32] = expf(v1);
+    V.w[hh][lane] = expf(last - v0) * d0;
+    V.w[hh][lane + 32] = expf(last - v1) * d1;
+    if (lane == 0) V.a[hh] = expf(last);
+}
+
+// y for one (head, p) and 8 consecutive tokens from tok_base, read from the
+// TMEM accumulators of buffer bp.  Every shared-memory value is read before
+// the first global store.
+template <int IO>
+__device__ __forceinline__ void epilogue8(const Params &p, const Dims &dm, const ChunkVec &V, uint32_t tlane,
+                                          int bp, int col, int b, int h0, int my_h, int my_p, int tok_base) {
+    float yo[8], yi[8];
+    tc::tmem_ld8(tlane + tm_yoff(bp) + col, yo);
+    tc::tmem_ld8(tlane + tm_yint(bp) + col, yi);
+    tc::fence_before_sync();
+    const int i0 = tok_base % kQ;
+    const float4 e0 = *reinterpret_cast<const float4 *>(&V.ecs[my_h][i0]);
+    const float4 e1 = *reinterpret_cast<const float4 *>(&V.ecs[my_h][i0 + 4]);
+    const float ev[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
+    const int h = h0 + my_h;
+    const size_t step = (size_t)dm.H * kP;
+    const size_t off0 = (((size_t)b * dm.L + tok_base) * dm.H + h) * kP + my_p;
+    float v[8];
+#pragma unroll
+    for (int ii = 0; ii < 8; ++ii) v[ii] = fmaf(ev[ii], yo[ii], yi[ii]);
+    if (p.D) {
+        const float Dh = __ldg(p.D + h);
+        float xv[8];
+#pragma unroll
+        for (int ii = 0; ii < 8; ++ii)
+            xv[ii] = (tok_base + ii < dm.L) ? ld_io<IO>(p.x, off0 + ii * step) : 0.f;
+#pragma unroll
+        for (int ii = 0; ii < 8; ++ii) v[ii] = fmaf(Dh, xv[ii], v[ii]);
+    }
+    if (p.z) {
+        float zv[8];
+#pragma unroll
+        for (int ii = 0; ii < 8; ++ii)
+            zv[ii] = (tok_base + ii < dm.L) ? ld_io<IO>(p.z, off0 + ii * step) : 0.f;
+#pragma unroll
+        for (int ii = 0; ii < 8; ++ii) v[ii] *= silu_f(zv[ii]);
+    }
+#pragma unroll
+    for (int ii = 0; ii < 8; ++ii)
+        if (tok_base + ii < dm.L) st_io<IO>(p.y, off0 + ii * step, v[ii]);
 }
 
 template <int IO, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
-ssd_fused_kernel(Params p, int n_units, unsigned int *err) {
+ssd_fused_kernel(const __grid_constant__ Params p, int n_units, unsigned int *err) {
     extern __shared__ unsigned char smem_raw[];
-    __shared__ __align__(8) uint64_t bars[3];
+    __shared__ __align__(8) uint64_t bars[NBARS];
     __shared__ uint32_t tmem_slot;
     const uint32_t raw = tc::smem_addr(smem_raw);
     unsigned char *sm = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
     const uint32_t sbase = tc::smem_addr(sm);
-    ChunkVec &V = *reinterpret_cast<ChunkVec *>(sm + OFF_VEC);
+    ChunkVec *Vbuf = reinterpret_cast<ChunkVec *>(sm + OFF_VEC);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int wg = warp >> 2, quarter = warp & 3;
-    const int row = quarter * 32 + lane;  // TMEM lane owned by this thread
-    const int my_h = row >> 6, my_p = row & 63;
-    const int col0 = wg * 32;             // this thread's 32 columns of each 64-column region
-    const uint32_t bar_g = tc::smem_addr(&bars[0]);
-    const uint32_t bar_b = tc::smem_addr(&bars[1]);
-    const uint32_t bar_c = tc::smem_addr(&bars[2]);
+    const Dims dm{p.L, p.H, p.G, p.hpg, p.nchunks};
+    const uint32_t bar0 = tc::smem_addr(&bars[0]);
+    auto bar = [bar0](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
 
     if (tid == 0) {
-        tc::mbar_init(bar_g, 1);
-        tc::mbar_init(bar_b, 1);
-        tc::mbar_init(bar_c, 1);
+        tc::mbar_init(bar(BAR_OPS_FULL), kComputeWarps);
+        tc::mbar_init(bar(BAR_MCAT_FULL), kComputeWarps);
+        tc::mbar_init(bar(BAR_S_FULL), kComputeWarps);
+        tc::mbar_init(bar(BAR_G_DONE), 1);
+        tc::mbar_init(bar(BAR_DS_DONE), 1);
+        tc::mbar_init(bar(BAR_Y_DONE0), 1);
+        tc::mbar_init(bar(BAR_Y_DONE1), 1);
         tc::mbar_init_fence();
     }
-    if (warp == 0) {
+    if (warp == kMmaWarp) {
         tc::tmem_alloc(tc::smem_addr(&tmem_slot), TM_COLS);
         tc::tmem_relinquish();
     }
-    // the zero block between the two heads' x tiles (MN groups 8..15 of Xcat)
-    for (int e = tid; e < 8 * 8 * 8; e += kThreads) {  // 8 K groups x 8 MN groups x 8 rows of 16 B
-        const int jg = e >> 6, mg = 8 + ((e >> 3) & 7), rr = e & 7;
-        st_shared_v4(sbase + OFF_XC + (jg * 24 + mg) * 128 + rr * 16, 0u, 0u, 0u, 0u);
+    // the zero block between the two heads' x tiles (MN groups 8..15), both buffers
+    for (int e = tid; e < 2 * 8 * 8 * 8; e += kThreads) {
+        const int buf = e >> 9, jg = (e >> 6) & 7, mg = 8 + ((e >> 3) & 7), rr = e & 7;
+        st_shared_v4(sbase + OFF_XC + buf * XC_BYTES + (jg * 24 + mg) * 128 + rr * 16, 0u, 0u, 0u, 0u);
     }
     tc::fence_smem_to_async();
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = tmem_slot;
-    const uint32_t tlane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-
-    constexpr uint32_t ID_KK = tc::idesc_f16(128, 64, BF16, false, false);
-    constexpr uint32_t ID_MNMN = tc::idesc_f16(128, 64, BF16, true, true);
-    constexpr uint32_t ID_MNK = tc::idesc_f16(128, 64, BF16, true, false);
-
-    const int pairs = p.hpg >> 1;
-    const int nchunks = p.nchunks;
-    uint32_t parity = 0;
+    const int pairs = dm.hpg >> 1;
     bool timed_out = false;
 
-    for (int unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
-        const int pair = unit % pairs;
-        const int bg = unit / pairs;
-        const int g = bg % p.G, b = bg / p.G;
-        const int h0 = g * p.hpg + 2 * pair;
-
-        // state of (head my_h, row my_p), columns n = col0 .. col0+31
-        float S[32];
-        if (p.h0) {
-            const float4 *src = reinterpret_cast<const float4 *>(
-                p.h0 + (((size_t)b * p.H + h0 + my_h) * kP + my_p) * kN + col0);
+    if (warp == kMmaWarp) {
+        // ---------------- MMA issue (one thread) ----------------
+        if (lane == 0) {
+            constexpr uint32_t ID_KK = tc::idesc_f16(128, 64, BF16, false, false);
+            constexpr uint32_t ID_MNMN = tc::idesc_f16(128, 64, BF16, true, true);
+            constexpr uint32_t ID_MNK = tc::idesc_f16(128, 64, BF16, true, false);
+            uint32_t gk = 0;
+            for (int unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
+                for (int k = 0; k < dm.nchunks; ++k, ++gk) {
+                    const uint32_t ph = gk & 1u;
+                    const int buf = gk & 1;
+                    if (!timed_out && !tc::mbar_wait(bar(BAR_OPS_FULL), ph, kWaitNs)) timed_out = true;
+                    tc::fence_after_sync();
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const float4 v = __ldg(src + q);
-                S[4 * q] = v.x; S[4 * q + 1] = v.y; S[4 * q + 2] = v.z; S[4 * q + 3] = v.w;
-            }
-        } else {
+                    for (int ks = 0; ks < kN / 16; ++ks)  // G = C B^T, K = n
+                        tc::mma_f16(tmem + TM_G, tc::desc(sbase + OFF_CB2 + ks * 4096, 2048, 128),
+                                    tc::desc(sbase + OFF_BB + ks * 2048, 1024, 128), ID_KK, ks > 0);
+                    tc::commit(bar(BAR_G_DONE));
+                    if (!timed_out && !tc::mbar_wait(bar(BAR_S_FULL), ph, kWaitNs)) timed_out = true;
+                    tc::fence_after_sync();
 #pragma unroll
-            for (int n = 0; n < 32; ++n) S[n] = 0.f;
-        }
+                    for (int ks = 0; ks < kQ / 16; ++ks)  // dS = Xw^T B, K = j
+                        tc::mma_f16(tmem + TM_DS, tc::desc(sbase + OFF_XT + ks * 4096, 2048, 128),
+                                    tc::desc(sbase + OFF_BB + ks * 256, 128, 1024), ID_MNMN, ks > 0);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            float v[8];
+                    for (int ks = 0; ks < kN / 16; ++ks)  // Yoff = S C^T, K = n
+                        tc::mma_f16(tmem + tm_yoff(buf), tc::desc(sbase + OFF_S + ks * 4096, 2048, 128),
+                                    tc::desc(sbase + OFF_CB2 + ks * 4096, 2048, 128), ID_KK, ks > 0);
+                    tc::commit(bar(BAR_DS_DONE));
+                    if (!timed_out && !tc::mbar_wait(bar(BAR_MCAT_FULL), ph, kWaitNs)) timed_out = true;
+                    tc::fence_after_sync();
+                    const uint32_t xc = sbase + OFF_XC + buf * XC_BYTES, mc = sbase + OFF_MC + buf * MC_BYTES;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) v[e] = S[8 * q + e];
-            const int ng = (col0 >> 3) + q;
-            store8(sbase + OFF_S + (ng * 16 + (row >> 3)) * 128 + (row & 7) * 16, v, BF16);
-        }
-
-        ChunkRegs cur;
-        load_chunk<IO>(p, b, g, h0, 0, tid, cur);
-
-        for (int k = 0; k < nchunks; ++k) {
-            // ---- P1: processed step and within-chunk cumulative decay ----
-            if (tid < 2 * kQ) {
-                const int h = tid >> 6, i = tid & 63;
-                V.d[h][i] = (k * kQ + i < p.L) ? dt_processed(p, cur.dt, h0 + h) : 0.f;
-            }
-            __syncthreads();
-            if (warp < 2) {
-                const int h = warp;
-                const float A = __ldg(p.A + h0 + h);
-                float v0 = V.d[h][lane] * A, v1 = V.d[h][lane + 32] * A;
+                    for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
-                for (int off = 1; off < 32; off <<= 1) {
-                    const float o0 = __shfl_up_sync(0xffffffffu, v0, off);
-                    const float o1 = __shfl_up_sync(0xffffffffu, v1, off);
-                    if (lane >= off) { v0 += o0; v1 += o1; }
+                        for (int ks = 0; ks < kQ / 16; ++ks)
+                            tc::mma_f16(tmem + tm_yint(buf), tc::desc(xc + hh * 1024 + ks * 6144, 3072, 128),
+                                        tc::desc(mc + hh * 8192 + ks * 2048, 1024, 128), ID_MNK,
+                                        (hh | ks) != 0);
+                    tc::commit(bar(buf ? BAR_Y_DONE1 : BAR_Y_DONE0));
                 }
-                v1 += __shfl_sync(0xffffffffu, v0, 31);
-                V.cs[h][lane] = v0;
-                V.cs[h][lane + 32] = v1;
             }
-            __syncthreads();
-            if (tid < 2 * kQ) {
-                const int h = tid >> 6, i = tid & 63;
-                const float c = V.cs[h][i], last = V.cs[h][kQ - 1];
-                V.ecs[h][i] = expf(c);
-                V.w[h][i] = expf(last - c) * V.d[h][i];
-                if (i == 0) V.a[h] = expf(last);
-            }
-            __syncthreads();
+        }
+        __syncwarp();
+    } else {
+        // ---------------- compute warps ----------------
+        const int wg = warp >> 2, quarter = warp & 3;
+        const int row = quarter * 32 + lane;  // TMEM lane owned by this thread
+        const int my_h = row >> 6, my_p = row & 63;
+        const int col0 = wg * kCols;          // this thread's columns of each 64-column region
+        const uint32_t tlane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+        const bool decay_warp = warp >= kDecayWarp0;
+        uint32_t gk = 0;
 
-            // ---- P2: operands into shared memory ----
+        for (int unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
+            const int pair = unit % pairs;
+            const int bg = unit / pairs;
+            const int g = bg % dm.G, b = bg / dm.G;
+            const int h0 = g * dm.hpg + 2 * pair;
+            const uint32_t gk0 = gk;
+
+            // state of (head my_h, row my_p), columns n = col0 .. col0+kCols-1
+            float S[kCols];
+            if (p.h0) {
+                const float4 *src = reinterpret_cast<const float4 *>(
+                    p.h0 + (((size_t)b * dm.H + h0 + my_h) * kP + my_p) * kN + col0);
 #pragma unroll
-            for (int it = 0; it < 4; ++it) {
-                const int e = tid + kThreads * it;
-                const int jl = e & 7, c16 = (e >> 3) & 15, jg = e >> 7;
-                const int h = c16 >> 3, po = c16 & 7;
-                const int mgc = h ? 16 + po : po;
-                store8(sbase + OFF_XC + (jg * 24 + mgc) * 128 + jl * 16, cur.x[it], BF16);
-                const float w = V.w[h][jg * 8 + jl];
-                float xs[8];
+                for (int q = 0; q < kCols / 4; ++q) {
+                    const float4 v = __ldg(src + q);
+                    S[4 * q] = v.x; S[4 * q + 1] = v.y; S[4 * q + 2] = v.z; S[4 * q + 3] = v.w;
+                }
+            } else {
 #pragma unroll
-                for (int q = 0; q < 8; ++q) xs[q] = cur.x[it][q] * w;
-                store8(sbase + OFF_XT + (jg * 16 + 8 * h + po) * 128 + jl * 16, xs, BF16);
+                for (int n = 0; n < kCols; ++n) S[n] = 0.f;
             }
 #pragma unroll
-            for (int it = 0; it < 2; ++it) {
-                const int e = tid + kThreads * it;
-                const int jl = e & 7, ng = (e >> 3) & 7, jg = e >> 6;
-                store8(sbase + OFF_BB + (ng * 8 + jg) * 128 + jl * 16, cur.bm[it], BF16);
-                store8(sbase + OFF_CB2 + (ng * 16 + jg) * 128 + jl * 16, cur.cm[it], BF16);
-                store8(sbase + OFF_CB2 + (ng * 16 + jg + 8) * 128 + jl * 16, cur.cm[it], BF16);
+            for (int q = 0; q < kCols / 8; ++q) {
+                float v[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[e] = S[8 * q + e];
+                const int ng = (col0 >> 3) + q;
+                store8(sbase + OFF_S + (ng * 16 + (row >> 3)) * 128 + (row & 7) * 16, v, BF16);
             }
-            if (k + 1 < nchunks) load_chunk<IO>(p, b, g, h0, k + 1, tid, cur);
             tc::fence_smem_to_async();
-            tc::fence_before_sync();
-            __syncthreads();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(bar(BAR_S_FULL));
 
-            // ---- P3: G, dS and Yoff on the tensor cores ----
-            if (tid == 0) {
-                tc::fence_after_sync();
-#pragma unroll
-                for (int ks = 0; ks < kN / 16; ++ks)  // G = C B^T, K = n
-                    tc::mma_f16(tmem + TM_G, tc::desc(sbase + OFF_CB2 + ks * 4096, 2048, 128),
-                                tc::desc(sbase + OFF_BB + ks * 2048, 1024, 128), ID_KK, ks > 0);
-                tc::commit(bar_g);
-#pragma unroll
-                for (int ks = 0; ks < kQ / 16; ++ks)  // dS = Xw^T B, K = j
-                    tc::mma_f16(tmem + TM_DS, tc::desc(sbase + OFF_XT + ks * 4096, 2048, 128),
-                                tc::desc(sbase + OFF_BB + ks * 256, 128, 1024), ID_MNMN, ks > 0);
-#pragma unroll
-                for (int ks = 0; ks < kN / 16; ++ks)  // Yoff = S C^T, K = n
-                    tc::mma_f16(tmem + TM_YOFF, tc::desc(sbase + OFF_S + ks * 4096, 2048, 128),
-                                tc::desc(sbase + OFF_CB2 + ks * 4096, 2048, 128), ID_KK, ks > 0);
-                tc::commit(bar_b);
-            }
+            ChunkRegs cur;
+            load_chunk<IO>(p, dm, b, g, h0, 0, tid, warp, lane, cur);
+            if (decay_warp)
+                decay_vectors(p, dm, h0 + warp - kDecayWarp0, warp - kDecayWarp0, 0, lane, cur.dt0, cur.dt1,
+                              Vbuf[gk % 3]);
 
-            // ---- P4: masked, decayed C B^T -> Mcat ----
-            if (!timed_out && !tc::mbar_wait(bar_g, parity, kWaitNs)) timed_out = true;
-            tc::fence_after_sync();
-            {
-                float gv[32];
-                tc::tmem_ld32(tlane + TM_G + col0, gv);
-                const int i = row & 63, h = row >> 6;
-                const float csi = V.cs[h][i];
+            for (int k = 0; k < dm.nchunks; ++k, ++gk) {
+                const int buf = gk & 1;
+                const uint32_t ph = gk & 1u;
+                ChunkVec &V = Vbuf[gk % 3];
+                tc::named_barrier(1, kComputeThreads);  // decay vectors of chunk k are in
+
+                // ---- A: operands of chunk k into shared memory ----
+                {
+                    float wv[2];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    float m[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int j = col0 + 8 * q + e;
-                        m[e] = (j <= i) ? gv[8 * q + e] * expf(csi - V.cs[h][j]) * V.d[h][j] : 0.f;
+                    for (int it = 0; it < 2; ++it) {
+                        const int e = tid + kComputeThreads * it;
+                        const int jl = e & 7, c16 = (e >> 3) & 15, jg = e >> 7;
+                        wv[it] = V.w[c16 >> 3][jg * 8 + jl];
                     }
-                    const int kg = 8 * h + (col0 >> 3) + q;
-                    store8(sbase + OFF_MC + (kg * 8 + (i >> 3)) * 128 + (i & 7) * 16, m, BF16);
+                    const uint32_t xc = sbase + OFF_XC + buf * XC_BYTES;
+#pragma unroll
+                    for (int it = 0; it < 2; ++it) {
+                        const int e = tid + kComputeThreads * it;
+                        const int jl = e & 7, c16 = (e >> 3) & 15, jg = e >> 7;
+                        const int h = c16 >> 3, po = c16 & 7;
+                        const int mgc = h ? 16 + po : po;
+                        store8(xc + (jg * 24 + mgc) * 128 + jl * 16, cur.x[it], BF16);
+                        float xs[8];
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) xs[q] = cur.x[it][q] * wv[it];
+                        store8(sbase + OFF_XT + (jg * 16 + 8 * h + po) * 128 + jl * 16, xs, BF16);
+                    }
+                    const int e = tid;
+                    const int jl = e & 7, ng = (e >> 3) & 7, jg = e >> 6;
+                    store8(sbase + OFF_BB + (ng * 8 + jg) * 128 + jl * 16, cur.bm, BF16);
+                    store8(sbase + OFF_CB2 + (ng * 16 + jg) * 128 + jl * 16, cur.cm, BF16);
+                    store8(sbase + OFF_CB2 + (ng * 16 + jg + 8) * 128 + jl * 16, cur.cm, BF16);
                 }
-            }
-            tc::fence_smem_to_async();
-            tc::fence_before_sync();
-            __syncthreads();
+                tc::fence_smem_to_async();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(bar(BAR_OPS_FULL));
+                if (k + 1 < dm.nchunks) load_chunk<IO>(p, dm, b, g, h0, k + 1, tid, warp, lane, cur);
 
-            // ---- P5: Yint = blockdiag(X^T) Mcat ----
-            if (tid == 0) {
+                // ---- B: masked, decayed C B^T -> Mcat ----
+                {
+                    const int i = row & 63, h = row >> 6;
+                    const float csi = V.cs2[h][i];
+                    if (!timed_out && !tc::mbar_wait(bar(BAR_G_DONE), ph, kWaitNs)) timed_out = true;
+                    tc::fence_after_sync();
+                    const uint32_t mc = sbase + OFF_MC + buf * MC_BYTES;
+#pragma unroll
+                    for (int q = 0; q < kCols / 8; ++q) {
+                        const int j0 = col0 + 8 * q;
+                        float gv[8];
+                        tc::tmem_ld8(tlane + TM_G + j0, gv);
+                        const float4 c0 = *reinterpret_cast<const float4 *>(&V.cs2[h][j0]);
+                        const float4 c1 = *reinterpret_cast<const float4 *>(&V.cs2[h][j0 + 4]);
+                        const float4 d0 = *reinterpret_cast<const float4 *>(&V.d[h][j0]);
+                        const float4 d1 = *reinterpret_cast<const float4 *>(&V.d[h][j0 + 4]);
+                        const float cj[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+                        const float dj[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+                        float m[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const float v = gv[e] * ex2_approx(csi - cj[e]) * dj[e];
+                            m[e] = (j0 + e <= i) ? v : 0.f;
+                        }
+                        const int kg = 8 * h + (j0 >> 3);
+                        store8(mc + (kg * 8 + (i >> 3)) * 128 + (i & 7) * 16, m, BF16);
+                    }
+                    tc::fence_before_sync();
+                }
+                tc::fence_smem_to_async();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(bar(BAR_MCAT_FULL));
+
+                // ---- C: state update S <- exp(cs_last) S + dS ----
+                {
+                    const float a = V.a[my_h];
+                    if (!timed_out && !tc::mbar_wait(bar(BAR_DS_DONE), ph, kWaitNs)) timed_out = true;
+                    tc::fence_after_sync();
+                    float ds[kCols];
+                    tc::tmem_ld16(tlane + TM_DS + col0, ds);
+                    tc::fence_before_sync();
+#pragma unroll
+                    for (int n = 0; n < kCols; ++n) S[n] = fmaf(a, S[n], ds[n]);
+                    if (k + 1 < dm.nchunks) {
+#pragma unroll
+                        for (int q = 0; q < kCols / 8; ++q) {
+                            float v[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) v[e] = S[8 * q + e];
+                            const int ng = (col0 >> 3) + q;
+                            store8(sbase + OFF_S + (ng * 16 + (row >> 3)) * 128 + (row & 7) * 16, v, BF16);
+                        }
+                        tc::fence_smem_to_async();
+                        __syncwarp();
+                        if (lane == 0) tc::mbar_arrive(bar(BAR_S_FULL));
+                    }
+                }
+
+                // ---- D: epilogue of the previous chunk ----
+                if (k > 0) {
+                    const uint32_t gp = gk - 1;
+                    const int bp = gp & 1;
+                    if (!timed_out &&
+                        !tc::mbar_wait(bar(bp ? BAR_Y_DONE1 : BAR_Y_DONE0), (gp >> 1) & 1u, kWaitNs))
+                        timed_out = true;
+                    tc::fence_after_sync();
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf)
+                        epilogue8<IO>(p, dm, Vbuf[gp % 3], tlane, bp, col0 + 8 * hf, b, h0, my_h, my_p,
+                                      (k - 1) * kQ + col0 + 8 * hf);
+                }
+
+                // ---- decay vectors of the next chunk ----
+                if (decay_warp && k + 1 < dm.nchunks)
+                    decay_vectors(p, dm, h0 + warp - kDecayWarp0, warp - kDecayWarp0, (k + 1) * kQ, lane,
+                                  cur.dt0, cur.dt1, Vbuf[(gk + 1) % 3]);
+            }
+
+            // ---- drain: epilogue of the unit's last chunk, final state ----
+            {
+                const uint32_t gp = gk - 1;
+                const int bp = gp & 1;
+                if (!timed_out &&
+                    !tc::mbar_wait(bar(bp ? BAR_Y_DONE1 : BAR_Y_DONE0), (gp >> 1) & 1u, kWaitNs))
+                    timed_out = true;
                 tc::fence_after_sync();
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-                    for (int ks = 0; ks < kQ / 16; ++ks)
-                        tc::mma_f16(tmem + TM_YINT,
-                                    tc::desc(sbase + OFF_XC + hh * 1024 + ks * 6144, 3072, 128),
-                                    tc::desc(sbase + OFF_MC + hh * 8192 + ks * 2048, 1024, 128), ID_MNK,
-                                    (hh | ks) != 0);
-                tc::commit(bar_c);
+                for (int hf = 0; hf < 2; ++hf)
+                    epilogue8<IO>(p, dm, Vbuf[gp % 3], tlane, bp, col0 + 8 * hf, b, h0, my_h, my_p,
+                                  (int)(gp - gk0) * kQ + col0 + 8 * hf);
             }
-
-            // ---- P6: state update S <- exp(cs_last) S + dS ----
-            if (!timed_out && !tc::mbar_wait(bar_b, parity, kWaitNs)) timed_out = true;
-            tc::fence_after_sync();
-            {
-                float ds[32];
-                tc::tmem_ld32(tlane + TM_DS + col0, ds);
-                const float a = V.a[my_h];
+            if (p.final_state) {
+                float4 *dst = reinterpret_cast<float4 *>(
+                    p.final_state + (((size_t)b * dm.H + h0 + my_h) * kP + my_p) * kN + col0);
 #pragma unroll
-                for (int n = 0; n < 32; ++n) S[n] = fmaf(a, S[n], ds[n]);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    float v[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) v[e] = S[8 * q + e];
-                    const int ng = (col0 >> 3) + q;
-                    store8(sbase + OFF_S + (ng * 16 + (row >> 3)) * 128 + (row & 7) * 16, v, BF16);
-                }
+                for (int q = 0; q < kCols / 4; ++q)
+                    dst[q] = make_float4(S[4 * q], S[4 * q + 1], S[4 * q + 2], S[4 * q + 3]);
             }
-
-            // ---- P7: epilogue y = exp(cs) Yoff + Yint (+ D x) (* silu z) ----
-            if (!timed_out && !tc::mbar_wait(bar_c, parity, kWaitNs)) timed_out = true;
-            tc::fence_after_sync();
-            {
-                float yo[32], yi[32];
-                tc::tmem_ld32(tlane + TM_YOFF + col0, yo);
-                tc::tmem_ld32(tlane + TM_YINT + col0, yi);
-                const int h = h0 + my_h;
-                const float Dh = p.D ? __ldg(p.D + h) : 0.f;
-#pragma unroll
-                for (int ii = 0; ii < 32; ++ii) {
-                    const int i = col0 + ii, t = k * kQ + i;
-                    if (t >= p.L) continue;
-                    const size_t off = (((size_t)b * p.L + t) * p.H + h) * kP + my_p;
-                    float v = fmaf(V.ecs[my_h][i], yo[ii], yi[ii]);
-                    if (p.D) v = fmaf(Dh, ld_io<IO>(p.x, off), v);
-                    if (p.z) v *= silu_f(ld_io<IO>(p.z, off));
-                    st_io<IO>(p.y, off, v);
-                }
-            }
-            tc::fence_before_sync();
-            parity ^= 1u;
         }
-
-        if (p.final_state) {
-            float4 *dst = reinterpret_cast<float4 *>(
-                p.final_state + (((size_t)b * p.H + h0 + my_h) * kP + my_p) * kN + col0);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) dst[q] = make_float4(S[4 * q], S[4 * q + 1], S[4 * q + 2], S[4 * q + 3]);
-        }
-        __syncthreads();
     }
 
     if (timed_out) atomicOr(err, 1u);
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    if (warp == 0) tc::tmem_dealloc(tmem, TM_COLS);
+    if (warp == kMmaWarp) tc::tmem_dealloc(tmem, TM_COLS);
 }
 
 int g_num_sms = 0;
@@ -421,11 +567,8 @@ cudaError_t launch_typed(const Params &p, int units, unsigned int *err, cudaStre
     auto kern = ssd_fused_kernel<IO, BF16>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    if (per_sm < 1) per_sm = 1;
-    const int grid = units < num_sms() * per_sm ? units : num_sms() * per_sm;
+    // one CTA per SM: its shared memory and 512 TMEM columns fill the SM
+    const int grid = units < num_sms() ? units : num_sms();
     kern<<<grid, kThreads, SMEM_BYTES, s>>>(p, units, err);
     return cudaGetLastError();
 }
@@ -437,6 +580,9 @@ const char *fused_unsupported_reason(const ssd_fwd_args *a) {
     if ((a->H / a->G) % 2 != 0) return "needs an even number of heads per group";
     if (a->ops == SSD_OPS_F32) return "needs fp16 or bf16 operands (the fp32 path is the chunked plan)";
     if (fused_units(a) > 0x7fffffffLL) return "too many (batch, group, head pair) units";
+    for (const void *ptr : {static_cast<const void *>(a->x), static_cast<const void *>(a->Bm),
+                            static_cast<const void *>(a->Cm)})
+        if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return "needs 16-byte aligned x, B and C";
     return nullptr;
 }
 
