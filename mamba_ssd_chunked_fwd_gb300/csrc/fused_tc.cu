@@ -73,8 +73,14 @@ constexpr uint32_t XC_BYTES = 24576;
 constexpr uint32_t OFF_MC = 90112;    // 2 x Mcat, K-major B operand, 64 i x 128 (h', j), 16 KB each
 constexpr uint32_t MC_BYTES = 16384;
 constexpr uint32_t OFF_S = 122880;    // S, K-major, 128 (h,p) x 64 n, 16 KB
-constexpr uint32_t OFF_VEC = 139264;  // 3 x ChunkVec
-constexpr uint32_t VEC_BYTES = 2560;
+// TMA staging of one chunk's public x, B, C tiles, 128-byte swizzled boxes of
+// 64 rows x 128 bytes (8 KB each): x 4 boxes (fp32) or 2 (16-bit), B and C 2 or 1
+constexpr uint32_t OFF_STG_X = 139264;
+constexpr uint32_t OFF_STG_B = 172032;
+constexpr uint32_t OFF_STG_C = 188416;
+constexpr uint32_t BOX_BYTES = 8192;
+constexpr uint32_t OFF_VEC = 204800;  // 3 x ChunkVec
+constexpr uint32_t VEC_BYTES = 2064;
 constexpr uint32_t SMEM_BYTES = OFF_VEC + 3 * VEC_BYTES + 1024;  // + alignment slack
 
 // TMEM columns (512 allocated)
@@ -83,7 +89,16 @@ __device__ __forceinline__ uint32_t tm_yoff(int buf) { return 128u + 128u * buf;
 __device__ __forceinline__ uint32_t tm_yint(int buf) { return 192u + 128u * buf; }
 
 // mbarriers
-enum { BAR_OPS_FULL = 0, BAR_MCAT_FULL, BAR_S_FULL, BAR_G_DONE, BAR_DS_DONE, BAR_Y_DONE0, BAR_Y_DONE1, NBARS };
+enum {
+    BAR_OPS_FULL = 0, BAR_MCAT_FULL, BAR_S_FULL, BAR_G_DONE, BAR_DS_DONE, BAR_Y_DONE0, BAR_Y_DONE1,
+    BAR_STAGE_FULL, NBARS
+};
+
+// TMA descriptors of x [B,L,H*P] and B, C [B,L,G*N] as 3-D tensors
+// (innermost first: features, tokens, batch), boxes of 128 bytes x 64 tokens.
+struct TmaMaps {
+    CUtensorMap x, b, c;
+};
 
 // 16-byte aligned so that consecutive slots keep their float4 reads aligned
 struct alignas(16) ChunkVec {
@@ -93,7 +108,7 @@ struct alignas(16) ChunkVec {
     float w[2][kQ];    // exp(cs_last - cs) * d
     float a[2];        // exp(cs_last)
 };
-static_assert(sizeof(ChunkVec) % 16 == 0 && 3 * sizeof(ChunkVec) <= 3 * VEC_BYTES, "ChunkVec slots");
+static_assert(sizeof(ChunkVec) % 16 == 0 && sizeof(ChunkVec) <= VEC_BYTES, "ChunkVec slots");
 
 // 2^x on the MUFU unit (PTX ex2.approx, relative error ~2^-22, flushes below
 // 2^-126 to 0): used where the result is rounded to a 16-bit operand.
@@ -124,73 +139,53 @@ __device__ __forceinline__ void store8(uint32_t saddr, const float (&v)[8], bool
                  pack2(v[6], v[7], bf16));
 }
 
-// 8 consecutive elements of a public tensor as floats (zeros when !valid)
-template <int IO>
-__device__ __forceinline__ void load8(const void *base, size_t off, bool valid, float (&v)[8]) {
-    if (!valid) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = 0.f;
-        return;
-    }
-    if (IO == IO_F32) {
-        const float4 *p = reinterpret_cast<const float4 *>(static_cast<const float *>(base) + off);
-        const float4 a = __ldg(p), b = __ldg(p + 1);
-        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-    } else {
-        const uint4 u = __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(base) + off));
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            if (IO == IO_BF16) {
-                __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162 *>(&w[i]);
-                float2 f = __bfloat1622float2(h);
-                v[2 * i] = f.x; v[2 * i + 1] = f.y;
-            } else {
-                __half2 h = *reinterpret_cast<const __half2 *>(&w[i]);
-                float2 f = __half22float2(h);
-                v[2 * i] = f.x; v[2 * i + 1] = f.y;
-            }
-        }
-    }
-}
-
 // Shapes of one call, held in registers by every thread.
 struct Dims {
     int L, H, G, hpg, nchunks;
 };
 
-// Registers holding one chunk of inputs for one compute thread.
-struct ChunkRegs {
-    float x[2][8];   // 2 items of (token j, head h, 8 consecutive p)
-    float bm[8];     // (token j, 8 consecutive n)
-    float cm[8];
-    float dt0, dt1;  // decay warps: raw dt of tokens lane and lane + 32
+// Decay warps' registers: raw dt of tokens lane and lane + 32 of the next chunk.
+struct DtRegs {
+    float dt0, dt1;
 };
 
-template <int IO>
-__device__ __forceinline__ void load_chunk(const Params &p, const Dims &dm, int b, int g, int h0, int k,
-                                           int tid, int warp, int lane, ChunkRegs &r) {
-    const int tok0 = k * kQ;
+__device__ __forceinline__ void load_dt(const Params &p, const Dims &dm, int b, int h, int k, int lane,
+                                        DtRegs &r) {
+    const int t0 = k * kQ + lane, t1 = t0 + 32;
+    r.dt0 = t0 < dm.L ? __ldg(p.dt + ((size_t)b * dm.L + t0) * dm.H + h) : 0.f;
+    r.dt1 = t1 < dm.L ? __ldg(p.dt + ((size_t)b * dm.L + t1) * dm.H + h) : 0.f;
+}
+
+// 16-byte chunk c of row r in a 128-byte-swizzled TMA box (chunk index XOR row % 8)
+__device__ __forceinline__ uint32_t swz(uint32_t box, int r, int c) {
+    return box + r * 128 + ((c ^ (r & 7)) << 4);
+}
+
+__device__ __forceinline__ void unpack8(uint4 u, bool bf16, float (&v)[8]) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-    for (int it = 0; it < 2; ++it) {
-        const int e = tid + kComputeThreads * it;
-        const int jl = e & 7, c16 = (e >> 3) & 15, jg = e >> 7;
-        const int h = c16 >> 3, po = c16 & 7, t = tok0 + jg * 8 + jl;
-        load8<IO>(p.x, (((size_t)b * dm.L + t) * dm.H + h0 + h) * kP + 8 * po, t < dm.L, r.x[it]);
+    for (int i = 0; i < 4; ++i) {
+        float2 f;
+        if (bf16) f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[i]));
+        else f = __half22float2(*reinterpret_cast<const __half2 *>(&w[i]));
+        v[2 * i] = f.x; v[2 * i + 1] = f.y;
     }
-    {
-        const int e = tid;
-        const int jl = e & 7, ng = (e >> 3) & 7, jg = e >> 6;
-        const int t = tok0 + jg * 8 + jl;
-        const size_t off = (((size_t)b * dm.L + t) * dm.G + g) * kN + 8 * ng;
-        load8<IO>(p.Bm, off, t < dm.L, r.bm);
-        load8<IO>(p.Cm, off, t < dm.L, r.cm);
-    }
-    if (warp >= kDecayWarp0) {
-        const int h = h0 + warp - kDecayWarp0;
-        const int t0 = tok0 + lane, t1 = tok0 + lane + 32;
-        r.dt0 = t0 < dm.L ? __ldg(p.dt + ((size_t)b * dm.L + t0) * dm.H + h) : 0.f;
-        r.dt1 = t1 < dm.L ? __ldg(p.dt + ((size_t)b * dm.L + t1) * dm.H + h) : 0.f;
+}
+
+// 8 consecutive features [8c8, 8c8+8) of token row r from a staged tile whose
+// rows hold `row_feats` features split over boxes of 128 bytes.
+template <int IO>
+__device__ __forceinline__ void stage_read8(uint32_t base, int r, int c8, float (&v)[8]) {
+    if (IO == IO_F32) {  // 32 features per box, 8 floats = 2 chunks
+        const uint32_t box = base + (c8 >> 2) * BOX_BYTES;
+        const int c = 2 * (c8 & 3);
+        const uint4 a = tc::ld_shared_v4(swz(box, r, c)), b = tc::ld_shared_v4(swz(box, r, c + 1));
+        v[0] = __uint_as_float(a.x); v[1] = __uint_as_float(a.y); v[2] = __uint_as_float(a.z);
+        v[3] = __uint_as_float(a.w); v[4] = __uint_as_float(b.x); v[5] = __uint_as_float(b.y);
+        v[6] = __uint_as_float(b.z); v[7] = __uint_as_float(b.w);
+    } else {  // 64 features per box, 8 values = 1 chunk
+        const uint32_t box = base + (c8 >> 3) * BOX_BYTES;
+        unpack8(tc::ld_shared_v4(swz(box, r, c8 & 7)), IO == IO_BF16, v);
     }
 }
 
@@ -267,7 +262,8 @@ __device__ __forceinline__ void epilogue8(const Params &p, const Dims &dm, const
 
 template <int IO, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
-ssd_fused_kernel(const __grid_constant__ Params p, int n_units, unsigned int *err) {
+ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMaps tm, int n_units,
+                 unsigned int *err) {
     extern __shared__ unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t bars[NBARS];
     __shared__ uint32_t tmem_slot;
@@ -289,6 +285,7 @@ ssd_fused_kernel(const __grid_constant__ Params p, int n_units, unsigned int *er
         tc::mbar_init(bar(BAR_DS_DONE), 1);
         tc::mbar_init(bar(BAR_Y_DONE0), 1);
         tc::mbar_init(bar(BAR_Y_DONE1), 1);
+        tc::mbar_init(bar(BAR_STAGE_FULL), 1);
         tc::mbar_init_fence();
     }
     if (warp == kMmaWarp) {
@@ -314,6 +311,27 @@ ssd_fused_kernel(const __grid_constant__ Params p, int n_units, unsigned int *er
             constexpr uint32_t ID_KK = tc::idesc_f16(128, 64, BF16, false, false);
             constexpr uint32_t ID_MNMN = tc::idesc_f16(128, 64, BF16, true, true);
             constexpr uint32_t ID_MNK = tc::idesc_f16(128, 64, BF16, true, false);
+            // TMA of the public x, B, C tiles of chunk k of a unit into the staging area
+            constexpr uint32_t kStageBytes = (IO == IO_F32 ? 8u : 4u) * BOX_BYTES;
+            auto stage = [&](int unit, int k) {
+                const int pair = unit % pairs, bg = unit / pairs;
+                const int g = bg % dm.G, b = bg / dm.G;
+                const int h0 = g * dm.hpg + 2 * pair;
+                const int bw = IO == IO_F32 ? 32 : 64;  // features per box
+                tc::mbar_arrive_expect_tx(bar(BAR_STAGE_FULL), kStageBytes);
+#pragma unroll
+                for (int bx = 0; bx < 128 / bw; ++bx)
+                    tc::tma_load_3d(sbase + OFF_STG_X + bx * BOX_BYTES, &tm.x, h0 * kP + bx * bw, k * kQ, b,
+                                    bar(BAR_STAGE_FULL));
+#pragma unroll
+                for (int bx = 0; bx < 64 / bw; ++bx) {
+                    tc::tma_load_3d(sbase + OFF_STG_B + bx * BOX_BYTES, &tm.b, g * kN + bx * bw, k * kQ, b,
+                                    bar(BAR_STAGE_FULL));
+                    tc::tma_load_3d(sbase + OFF_STG_C + bx * BOX_BYTES, &tm.c, g * kN + bx * bw, k * kQ, b,
+                                    bar(BAR_STAGE_FULL));
+                }
+            };
+            if ((int)blockIdx.x < n_units) stage(blockIdx.x, 0);
             uint32_t gk = 0;
             for (int unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
                 for (int k = 0; k < dm.nchunks; ++k, ++gk) {
@@ -321,6 +339,9 @@ ssd_fused_kernel(const __grid_constant__ Params p, int n_units, unsigned int *er
                     const int buf = gk & 1;
                     if (!timed_out && !tc::mbar_wait(bar(BAR_OPS_FULL), ph, kWaitNs)) timed_out = true;
                     tc::fence_after_sync();
+                    // the compute warps are done with the staging area: fetch the next chunk
+                    if (k + 1 < dm.nchunks) stage(unit, k + 1);
+                    else if (unit + (int)gridDim.x < n_units) stage(unit + gridDim.x, 0);
 #pragma unroll
                     for (int ks = 0; ks < kN / 16; ++ks)  // G = C B^T, K = n
                         tc::mma_f16(tmem + TM_G, tc::desc(sbase + OFF_CB2 + ks * 4096, 2048, 128),
@@ -395,11 +416,12 @@ ssd_fused_kernel(const __grid_constant__ Params p, int n_units, unsigned int *er
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(bar(BAR_S_FULL));
 
-            ChunkRegs cur;
-            load_chunk<IO>(p, dm, b, g, h0, 0, tid, warp, lane, cur);
-            if (decay_warp)
+            DtRegs cur;
+            if (decay_warp) {
+                load_dt(p, dm, b, h0 + warp - kDecayWarp0, 0, lane, cur);
                 decay_vectors(p, dm, h0 + warp - kDecayWarp0, warp - kDecayWarp0, 0, lane, cur.dt0, cur.dt1,
                               Vbuf[gk % 3]);
+            }
 
             for (int k = 0; k < dm.nchunks; ++k, ++gk) {
                 const int buf = gk & 1;
@@ -408,6 +430,7 @@ ssd_fused_kernel(const __grid_constant__ Params p, int n_units, unsigned int *er
                 tc::named_barrier(1, kComputeThreads);  // decay vectors of chunk k are in
 
                 // ---- A: operands of chunk k into shared memory ----
+                if (!timed_out && !tc::mbar_wait(bar(BAR_STAGE_FULL), ph, kWaitNs)) timed_out = true;
                 {
                     float wv[2];
 #pragma unroll
@@ -423,22 +446,27 @@ ssd_fused_kernel(const __grid_constant__ Params p, int n_units, unsigned int *er
                         const int jl = e & 7, c16 = (e >> 3) & 15, jg = e >> 7;
                         const int h = c16 >> 3, po = c16 & 7;
                         const int mgc = h ? 16 + po : po;
-                        store8(xc + (jg * 24 + mgc) * 128 + jl * 16, cur.x[it], BF16);
+                        float xv[8];
+                        stage_read8<IO>(sbase + OFF_STG_X, jg * 8 + jl, c16, xv);
+                        store8(xc + (jg * 24 + mgc) * 128 + jl * 16, xv, BF16);
                         float xs[8];
 #pragma unroll
-                        for (int q = 0; q < 8; ++q) xs[q] = cur.x[it][q] * wv[it];
+                        for (int q = 0; q < 8; ++q) xs[q] = xv[q] * wv[it];
                         store8(sbase + OFF_XT + (jg * 16 + 8 * h + po) * 128 + jl * 16, xs, BF16);
                     }
                     const int e = tid;
                     const int jl = e & 7, ng = (e >> 3) & 7, jg = e >> 6;
-                    store8(sbase + OFF_BB + (ng * 8 + jg) * 128 + jl * 16, cur.bm, BF16);
-                    store8(sbase + OFF_CB2 + (ng * 16 + jg) * 128 + jl * 16, cur.cm, BF16);
-                    store8(sbase + OFF_CB2 + (ng * 16 + jg + 8) * 128 + jl * 16, cur.cm, BF16);
+                    float bv[8], cv[8];
+                    stage_read8<IO>(sbase + OFF_STG_B, jg * 8 + jl, ng, bv);
+                    stage_read8<IO>(sbase + OFF_STG_C, jg * 8 + jl, ng, cv);
+                    store8(sbase + OFF_BB + (ng * 8 + jg) * 128 + jl * 16, bv, BF16);
+                    store8(sbase + OFF_CB2 + (ng * 16 + jg) * 128 + jl * 16, cv, BF16);
+                    store8(sbase + OFF_CB2 + (ng * 16 + jg + 8) * 128 + jl * 16, cv, BF16);
                 }
                 tc::fence_smem_to_async();
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(bar(BAR_OPS_FULL));
-                if (k + 1 < dm.nchunks) load_chunk<IO>(p, dm, b, g, h0, k + 1, tid, warp, lane, cur);
+                if (decay_warp && k + 1 < dm.nchunks) load_dt(p, dm, b, h0 + warp - kDecayWarp0, k + 1, lane, cur);
 
                 // ---- B: masked, decayed C B^T -> Mcat ----
                 {
@@ -562,14 +590,55 @@ int num_sms() {
 
 int64_t fused_units(const ssd_fwd_args *a) { return a->B * a->G * ((a->H / a->G) / 2); }
 
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        cudaDriverEntryPointQueryResult q;
+        void *ptr = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+// [batch, tokens, features] tensor, boxes of 128 bytes x 64 tokens x 1, 128B swizzle,
+// zero fill past the end of the sequence.
+cudaError_t encode_map(CUtensorMap *m, const void *base, int io, int64_t feats, int64_t L, int64_t B) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    const size_t esz = io == IO_F32 ? 4 : 2;
+    const CUtensorMapDataType dt = io == IO_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : io == IO_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                   : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const cuuint64_t dims[3] = {(cuuint64_t)feats, (cuuint64_t)L, (cuuint64_t)B};
+    const cuuint64_t strides[2] = {(cuuint64_t)(feats * esz), (cuuint64_t)(feats * L * esz)};
+    const cuuint32_t box[3] = {(cuuint32_t)(128 / esz), (cuuint32_t)kQ, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, dt, 3, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <int IO, bool BF16>
 cudaError_t launch_typed(const Params &p, int units, unsigned int *err, cudaStream_t s) {
     auto kern = ssd_fused_kernel<IO, BF16>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
+    TmaMaps tm;
+    if ((e = encode_map(&tm.x, p.x, IO, (int64_t)p.H * kP, p.L, p.B)) != cudaSuccess) return e;
+    if ((e = encode_map(&tm.b, p.Bm, IO, (int64_t)p.G * kN, p.L, p.B)) != cudaSuccess) return e;
+    if ((e = encode_map(&tm.c, p.Cm, IO, (int64_t)p.G * kN, p.L, p.B)) != cudaSuccess) return e;
     // one CTA per SM: its shared memory and 512 TMEM columns fill the SM
     const int grid = units < num_sms() ? units : num_sms();
-    kern<<<grid, kThreads, SMEM_BYTES, s>>>(p, units, err);
+    kern<<<grid, kThreads, SMEM_BYTES, s>>>(p, tm, units, err);
     return cudaGetLastError();
 }
 
