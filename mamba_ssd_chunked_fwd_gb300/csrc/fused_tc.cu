@@ -32,13 +32,12 @@
 // MMA issue and the tensor core works on chunk k while the compute warps
 // finish chunk k-1:
 //
-//   compute, iteration k:  A_k  operands of chunk k -> smem        (arrive OPS_FULL)
-//                               prefetch chunk k+1 into registers
+//   compute, iteration k:  A_k  wait STAGE; operands of chunk k -> smem (arrive OPS_FULL)
+//                          D_k-1 wait Y_DONE; epilogue of chunk k-1 -> y (overlaps G_k)
 //                          B_k  wait G_DONE;  G -> Mcat             (arrive MCAT_FULL)
 //                          C_k  wait DS_DONE; S <- a S + dS -> smem (arrive S_FULL)
-//                          D_k-1 wait Y_DONE; epilogue of chunk k-1 -> y
 //                          decay vectors of chunk k+1 (warps 14, 15)
-//   MMA warp, chunk k:     wait OPS_FULL -> G (commit G_DONE);
+//   MMA warp, chunk k:     wait OPS_FULL -> G (commit G_DONE); TMA of chunk k+1;
 //                          wait S_FULL -> dS, Yoff (commit DS_DONE);
 //                          wait MCAT_FULL -> Yint (commit Y_DONE[k%2])
 //
@@ -339,14 +338,14 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                     const int buf = gk & 1;
                     if (!timed_out && !tc::mbar_wait(bar(BAR_OPS_FULL), ph, kWaitNs)) timed_out = true;
                     tc::fence_after_sync();
-                    // the compute warps are done with the staging area: fetch the next chunk
-                    if (k + 1 < dm.nchunks) stage(unit, k + 1);
-                    else if (unit + (int)gridDim.x < n_units) stage(unit + gridDim.x, 0);
 #pragma unroll
                     for (int ks = 0; ks < kN / 16; ++ks)  // G = C B^T, K = n
                         tc::mma_f16(tmem + TM_G, tc::desc(sbase + OFF_CB2 + ks * 4096, 2048, 128),
                                     tc::desc(sbase + OFF_BB + ks * 2048, 1024, 128), ID_KK, ks > 0);
                     tc::commit(bar(BAR_G_DONE));
+                    // the compute warps are done with the staging area: fetch the next chunk
+                    if (k + 1 < dm.nchunks) stage(unit, k + 1);
+                    else if (unit + (int)gridDim.x < n_units) stage(unit + gridDim.x, 0);
                     if (!timed_out && !tc::mbar_wait(bar(BAR_S_FULL), ph, kWaitNs)) timed_out = true;
                     tc::fence_after_sync();
 #pragma unroll
@@ -468,6 +467,20 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                 if (lane == 0) tc::mbar_arrive(bar(BAR_OPS_FULL));
                 if (decay_warp && k + 1 < dm.nchunks) load_dt(p, dm, b, h0 + warp - kDecayWarp0, k + 1, lane, cur);
 
+                // ---- D: epilogue of the previous chunk (overlaps the G MMA) ----
+                if (k > 0) {
+                    const uint32_t gp = gk - 1;
+                    const int bp = gp & 1;
+                    if (!timed_out &&
+                        !tc::mbar_wait(bar(bp ? BAR_Y_DONE1 : BAR_Y_DONE0), (gp >> 1) & 1u, kWaitNs))
+                        timed_out = true;
+                    tc::fence_after_sync();
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf)
+                        epilogue8<IO>(p, dm, Vbuf[gp % 3], tlane, bp, col0 + 8 * hf, b, h0, my_h, my_p,
+                                      (k - 1) * kQ + col0 + 8 * hf);
+                }
+
                 // ---- B: masked, decayed C B^T -> Mcat ----
                 {
                     const int i = row & 63, h = row >> 6;
@@ -524,20 +537,6 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                         __syncwarp();
                         if (lane == 0) tc::mbar_arrive(bar(BAR_S_FULL));
                     }
-                }
-
-                // ---- D: epilogue of the previous chunk ----
-                if (k > 0) {
-                    const uint32_t gp = gk - 1;
-                    const int bp = gp & 1;
-                    if (!timed_out &&
-                        !tc::mbar_wait(bar(bp ? BAR_Y_DONE1 : BAR_Y_DONE0), (gp >> 1) & 1u, kWaitNs))
-                        timed_out = true;
-                    tc::fence_after_sync();
-#pragma unroll
-                    for (int hf = 0; hf < 2; ++hf)
-                        epilogue8<IO>(p, dm, Vbuf[gp % 3], tlane, bp, col0 + 8 * hf, b, h0, my_h, my_p,
-                                      (k - 1) * kQ + col0 + 8 * hf);
                 }
 
                 // ---- decay vectors of the next chunk ----
