@@ -249,11 +249,13 @@ def run_gpu(args):
 
     # dominant kernel: time it alone with events on the launching stream
     hbm, peak_kind = peaks()
+    kernels = ssd.ssd_fwd_describe(a)
+    stages = None
     if plan == ssd.SSD_PLAN_FUSED:
         kname, kbytes, kms = "ssd_fused_kernel", ab["total"], ms
         launches_per_step = 1
     else:
-        kname, kbytes, kms = stage_timing(ssd, a, w, dev, sh, stream, args)
+        kname, kbytes, kms, stages = stage_timing(ssd, a, w, dev, sh, stream, args, kernels)
         launches_per_step = 4
     achieved = kbytes / (kms * 1e-3) / 1e9
     roofline = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1), "peak": hbm,
@@ -272,7 +274,7 @@ def run_gpu(args):
         "scaling": "weak",
         "vs_baseline": (round(value / PUBLISHED_TOKENS_PER_S[args.workload], 3)
                         if args.workload in PUBLISHED_TOKENS_PER_S else None),
-        "dtype": ops_name if plan == ssd.SSD_PLAN_FUSED else "f32",
+        "dtype": ops_name if any(k.endswith("_tc") or k == "ssd_fused_kernel" for k in kernels) else "f32",
         "data": "synthetic (seeded, pages' distributions)",
         "config": {"workload": f"{args.workload} {w.shape_tuple()} [B,L,H,P,N,chunk,G]"
                                + (" (batch overridden)" if args.batch else ""),
@@ -284,6 +286,8 @@ def run_gpu(args):
                    "path_frac_of_roofline": round(path_roofline_ms / ms, 4),
                    "parallelism": f"replica x{world}" if world > 1 else "1 GPU"},
         "roofline": roofline,
+        "kernels": kernels,
+        "stages": stages,
         "clocks": clocks,
         "gpu_launches": launches_per_step * args.steps,
         "e2e": e2e,
@@ -297,9 +301,10 @@ def run_gpu(args):
         print(json.dumps(line), flush=True)
 
 
-def stage_timing(ssd, a, w, dev, sh, stream, args):
+def stage_timing(ssd, a, w, dev, sh, stream, args, kernels):
     """Time the four chunked-plan kernels one by one (events between launches)
-    and return the dominant one with its algorithmic bytes."""
+    and return the dominant one with its algorithmic bytes, plus every stage's
+    time."""
     c = -(-w.L // w.chunk)
     dtp = torch.empty((w.B, w.H, c, w.chunk), device=dev)
     cs = torch.empty_like(dtp)
@@ -324,7 +329,9 @@ def stage_timing(ssd, a, w, dev, sh, stream, args):
     t = [sum(ev[r][i].elapsed_time(ev[r][i + 1]) for r in range(reps)) / reps for i in range(4)]
     sb = stage_bytes(w)
     i = max(range(4), key=lambda j: t[j])
-    return names[i], sb[names[i]], t[i]
+    stages = {kernels[j]: {"ms": round(t[j], 5), "alg_bytes": sb[names[j]],
+                           "GB_per_s": round(sb[names[j]] / (t[j] * 1e-3) / 1e9, 1)} for j in range(4)}
+    return kernels[i], sb[names[i]], t[i], stages
 
 
 def e2e_timing(ssd, inp, w, dev, args):

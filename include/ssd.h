@@ -125,6 +125,13 @@ ssd_status ssd_fwd_workspace_size(const ssd_fwd_args *args, size_t *bytes);
  * SSD_PLAN_FUSED), after resolving SSD_PLAN_AUTO. */
 ssd_status ssd_fwd_resolve_plan(const ssd_fwd_args *args, int32_t *plan);
 
+/* Names of the kernels ssd_fwd would launch for these arguments, in order,
+ * as a NUL-terminated comma-separated list written into `out` (capacity
+ * `cap` bytes, truncated if shorter), e.g. "chunk_cumsum,chunk_state_tc,
+ * state_passing,chunk_scan_tc" or "ssd_fused_kernel".  Pointers are
+ * inspected only for the alignment the tensor-core kernels need. */
+ssd_status ssd_fwd_describe(const ssd_fwd_args *args, char *out, size_t cap);
+
 /* The whole forward: y (and final_state when non-NULL).  Enqueue only. */
 ssd_status ssd_fwd(const ssd_fwd_args *args, void *stream);
 

@@ -27,7 +27,7 @@ __all__ = [
     "SSD_F32", "SSD_F16", "SSD_BF16", "SSD_OPS_F32", "SSD_OPS_F16", "SSD_OPS_BF16",
     "SSD_PLAN_AUTO", "SSD_PLAN_CHUNKED", "SSD_PLAN_FUSED", "SsdError", "SsdFwdArgs",
     "load_library", "library_path", "make_args", "ssd_fwd", "ssd_fwd_workspace_size",
-    "ssd_fwd_resolve_plan", "ssd_chunk_cumsum", "ssd_chunk_state", "ssd_state_passing",
+    "ssd_fwd_resolve_plan", "ssd_fwd_describe", "ssd_chunk_cumsum", "ssd_chunk_state", "ssd_state_passing",
     "ssd_chunk_scan", "ssd_fwd_host", "ssd_fwd_host_workspace_size", "ssd_check_device_error",
     "mamba2_ssd_fwd",
 ]
@@ -83,6 +83,7 @@ _SIGS = {
     "ssd_fwd_host_workspace_size": [_P, ctypes.POINTER(ctypes.c_size_t)],
     "ssd_fwd_host": [_P, ctypes.c_void_p],
     "ssd_check_device_error": [_P, ctypes.c_void_p],
+    "ssd_fwd_describe": [_P, ctypes.c_char_p, ctypes.c_size_t],
 }
 
 
@@ -172,6 +173,13 @@ def ssd_fwd_resolve_plan(args: SsdFwdArgs) -> int:
     _check(load_library().ssd_fwd_resolve_plan(ctypes.byref(args), ctypes.byref(out)),
            "ssd_fwd_resolve_plan")
     return int(out.value)
+
+
+def ssd_fwd_describe(args: SsdFwdArgs) -> list:
+    """Kernels ssd_fwd would launch for these arguments, in order."""
+    buf = ctypes.create_string_buffer(256)
+    _check(load_library().ssd_fwd_describe(ctypes.byref(args), buf, 256), "ssd_fwd_describe")
+    return buf.value.decode().split(",")
 
 
 def ssd_fwd(args: SsdFwdArgs, stream=None):

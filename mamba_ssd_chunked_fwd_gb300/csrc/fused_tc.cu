@@ -48,6 +48,7 @@
 
 #include "ssd_fused.cuh"
 #include "ssd_internal.cuh"
+#include "tc_operands.cuh"
 #include "tc_ptx.cuh"
 
 namespace ssd {
@@ -109,34 +110,10 @@ struct alignas(16) ChunkVec {
 };
 static_assert(sizeof(ChunkVec) % 16 == 0 && sizeof(ChunkVec) <= VEC_BYTES, "ChunkVec slots");
 
-// 2^x on the MUFU unit (PTX ex2.approx, relative error ~2^-22, flushes below
-// 2^-126 to 0): used where the result is rounded to a 16-bit operand.
-__device__ __forceinline__ float ex2_approx(float x) {
-    float r;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
-    return r;
-}
-
-__device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
-    if (bf16) {
-        __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-        return *reinterpret_cast<uint32_t *>(&v);
-    }
-    __half2 v = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<uint32_t *>(&v);
-}
-
-// 16-byte shared store of an MMA operand.  No "memory" clobber: operand
-// memory is only read by the tensor core, and the fences / barriers that
-// publish it carry the ordering.
-__device__ __forceinline__ void st_shared_v4(uint32_t saddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(a), "r"(b), "r"(c), "r"(d));
-}
-
-__device__ __forceinline__ void store8(uint32_t saddr, const float (&v)[8], bool bf16) {
-    st_shared_v4(saddr, pack2(v[0], v[1], bf16), pack2(v[2], v[3], bf16), pack2(v[4], v[5], bf16),
-                 pack2(v[6], v[7], bf16));
-}
+using tcop::ex2_approx;
+using tcop::pack2;
+using tcop::st_shared_v4;
+using tcop::store8;
 
 // Shapes of one call, held in registers by every thread.
 struct Dims {

@@ -126,6 +126,29 @@ size_t workspace_for(const ssd_fwd_args *a, int32_t plan) {
     return chunked_layout(a).total;
 }
 
+// Steps 2 and 4 run on the tensor cores when the operands are fp16 / bf16 and
+// the shape fits those kernels, else on the fp32 CUDA-core kernels.
+bool tc_ok(const ssd_fwd_args *a) {
+    for (const void *ptr : {static_cast<const void *>(a->x), static_cast<const void *>(a->Bm),
+                            static_cast<const void *>(a->Cm)})
+        if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return false;
+    return true;
+}
+
+cudaError_t launch_state_step(const ssd_fwd_args *a, const ssd::Params &p, const float *dtp, const float *cs,
+                              float *states, unsigned int *err, cudaStream_t s) {
+    if (ssd::chunk_tc_state_supported(p, a->ops) && tc_ok(a))
+        return ssd::launch_chunk_state_tc(p, a->x_dtype, a->ops, dtp, cs, states, err, s);
+    return ssd::launch_chunk_state(p, a->x_dtype, dtp, cs, states, s);
+}
+
+cudaError_t launch_scan_step(const ssd_fwd_args *a, const ssd::Params &p, const float *dtp, const float *cs,
+                             const float *states, unsigned int *err, cudaStream_t s) {
+    if (ssd::chunk_tc_scan_supported(p, a->ops) && tc_ok(a))
+        return ssd::launch_chunk_scan_tc(p, a->x_dtype, a->ops, dtp, cs, states, err, s);
+    return ssd::launch_chunk_scan(p, a->x_dtype, dtp, cs, states, s);
+}
+
 ssd_status run_chunked(const ssd_fwd_args *a, cudaStream_t s) {
     const ChunkedLayout l = chunked_layout(a);
     char *ws = static_cast<char *>(a->workspace);
@@ -138,11 +161,10 @@ ssd_status run_chunked(const ssd_fwd_args *a, cudaStream_t s) {
     cudaError_t e = cudaMemsetAsync(ws + l.err_off, 0, kAlign, s);
     if (e != cudaSuccess) return cuda_fail(e, "clearing the error word");
     if ((e = ssd::launch_chunk_cumsum(p, dtp, cs, s)) != cudaSuccess) return cuda_fail(e, "chunk_cumsum");
-    if ((e = ssd::launch_chunk_state(p, a->x_dtype, dtp, cs, states, s)) != cudaSuccess)
-        return cuda_fail(e, "chunk_state");
+    unsigned int *err = reinterpret_cast<unsigned int *>(ws + l.err_off);
+    if ((e = launch_state_step(a, p, dtp, cs, states, err, s)) != cudaSuccess) return cuda_fail(e, "chunk_state");
     if ((e = ssd::launch_state_passing(p, cs, states, s)) != cudaSuccess) return cuda_fail(e, "state_passing");
-    if ((e = ssd::launch_chunk_scan(p, a->x_dtype, dtp, cs, states, s)) != cudaSuccess)
-        return cuda_fail(e, "chunk_scan");
+    if ((e = launch_scan_step(a, p, dtp, cs, states, err, s)) != cudaSuccess) return cuda_fail(e, "chunk_scan");
     return ok();
 }
 
@@ -187,6 +209,23 @@ ssd_status ssd_fwd_workspace_size(const ssd_fwd_args *a, size_t *bytes) {
     return ok();
 }
 
+ssd_status ssd_fwd_describe(const ssd_fwd_args *a, char *out, size_t cap) {
+    int32_t plan = 0;
+    ssd_status st = ssd_fwd_resolve_plan(a, &plan);
+    if (st != SSD_OK) return st;
+    if (!out || cap == 0) return fail(SSD_ERR_INVALID_ARG, "out buffer required");
+    if (plan == SSD_PLAN_FUSED) {
+        snprintf(out, cap, "ssd_fused_kernel");
+        return ok();
+    }
+    const ssd::Params p = make_params(a);
+    const bool tc_state = ssd::chunk_tc_state_supported(p, a->ops) && tc_ok(a);
+    const bool tc_scan = ssd::chunk_tc_scan_supported(p, a->ops) && tc_ok(a);
+    snprintf(out, cap, "chunk_cumsum,%s,state_passing,%s", tc_state ? "chunk_state_tc" : "chunk_state",
+             tc_scan ? "chunk_scan_tc" : "chunk_scan");
+    return ok();
+}
+
 ssd_status ssd_fwd(const ssd_fwd_args *a, void *stream) {
     int32_t plan = 0;
     ssd_status st = ssd_fwd_resolve_plan(a, &plan);
@@ -222,8 +261,8 @@ ssd_status ssd_chunk_state(const ssd_fwd_args *a, const float *dtp, const float 
     if (st != SSD_OK) return st;
     if ((st = check_pointers(a, false)) != SSD_OK) return st;
     if (!dtp || !cs || !states) return fail(SSD_ERR_INVALID_ARG, "dtp, cs and states are required");
-    cudaError_t e = ssd::launch_chunk_state(make_params(a), a->x_dtype, dtp, cs, states,
-                                            static_cast<cudaStream_t>(stream));
+    const ssd::Params p = make_params(a);
+    cudaError_t e = launch_state_step(a, p, dtp, cs, states, nullptr, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "chunk_state");
     return ok();
 }
@@ -248,8 +287,8 @@ ssd_status ssd_chunk_scan(const ssd_fwd_args *a, const float *dtp, const float *
     if (st != SSD_OK) return st;
     if ((st = check_pointers(a, true)) != SSD_OK) return st;
     if (!dtp || !cs || !states) return fail(SSD_ERR_INVALID_ARG, "dtp, cs and states are required");
-    cudaError_t e = ssd::launch_chunk_scan(make_params(a), a->x_dtype, dtp, cs, states,
-                                           static_cast<cudaStream_t>(stream));
+    const ssd::Params p = make_params(a);
+    cudaError_t e = launch_scan_step(a, p, dtp, cs, states, nullptr, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "chunk_scan");
     return ok();
 }

@@ -96,4 +96,13 @@ cudaError_t launch_state_passing(const Params &p, const float *cs, float *states
 cudaError_t launch_chunk_scan(const Params &p, int io, const float *dtp, const float *cs,
                               const float *states, cudaStream_t s);
 
+// Tensor-core (tcgen05) versions of steps 2 and 4 for fp16 / bf16 operands.
+// `err` (may be NULL) receives bit 2 if a bounded wait gave up.
+bool chunk_tc_state_supported(const Params &p, int ops);
+bool chunk_tc_scan_supported(const Params &p, int ops);
+cudaError_t launch_chunk_state_tc(const Params &p, int io, int ops, const float *dtp, const float *cs,
+                                  float *states, unsigned int *err, cudaStream_t s);
+cudaError_t launch_chunk_scan_tc(const Params &p, int io, int ops, const float *dtp, const float *cs,
+                                 const float *states, unsigned int *err, cudaStream_t s);
+
 }  // namespace ssd

@@ -125,3 +125,26 @@ def test_fused_plan_request_is_checked():
     assert st in (0, 2)
     if st == 0:
         assert plan.value == ssd.SSD_PLAN_FUSED
+
+
+def test_describe_names_the_kernels_each_workload_runs():
+    """The named workloads run on the tensor cores (fused kernel or the
+    tensor-core chunk steps); only the fp32 tiny workload uses CUDA cores."""
+    import ssd_inputs
+    expect = {
+        "tiny": ["chunk_cumsum", "chunk_state", "state_passing", "chunk_scan"],
+        "same_device": ["chunk_cumsum", "chunk_state_tc", "state_passing", "chunk_scan_tc"],
+        "large_training": ["ssd_fused_kernel"],
+        "long_sequence": ["chunk_cumsum", "chunk_state_tc", "state_passing", "chunk_scan_tc"],
+        "gated_prefill": ["chunk_cumsum", "chunk_state_tc", "state_passing", "chunk_scan_tc"],
+    }
+    dt_of = {"f32": torch.float32, "bf16": torch.bfloat16}
+    for name, w in ssd_inputs.WORKLOADS.items():
+        xd = dt_of[w.x_dtype]
+        x = torch.empty((w.B, w.L, w.H, w.P), dtype=xd) if w.B * w.L * w.H * w.P < 2**28 else torch.empty((1,), dtype=xd)
+        a = ssd.make_args(torch.empty((1, 1, w.H, w.P), dtype=xd), torch.empty((1, 1, w.H)), torch.empty(w.H),
+                          torch.empty((1, 1, w.G, w.N), dtype=xd), torch.empty((1, 1, w.G, w.N), dtype=xd),
+                          w.chunk, ops=w.ops)
+        a.B, a.L = w.B, w.L
+        a.x = a.Bm = a.Cm = 4096  # any 16-byte aligned address: describe only inspects alignment
+        assert ssd.ssd_fwd_describe(a) == expect[name], name

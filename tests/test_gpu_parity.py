@@ -319,3 +319,63 @@ def test_fused_plan_rejects_unsupported_shape():
     with pytest.raises(ssd.SsdError) as ei:
         run_gpu(inp, ops="bf16", plan="fused")
     assert ei.value.status == 2
+
+
+# ---- tensor-core chunk_state / chunk_scan (chunked plan, fp16/bf16 operands) ------------
+
+def _stage_args(ssd, d, y, fin, Q, ops):
+    return ssd.make_args(d["x"], d["dt"], d["A"], d["B"], d["C"], Q, y=y, final_state=fin,
+                         D=d["D"], z=d["z"], dt_bias=d["dt_bias"],
+                         initial_states=d["initial_states"], dt_softplus=True, ops=ops)
+
+
+@pytest.mark.parametrize("shape,ops", [((2, 300, 4, 64, 128, 2, 128), "bf16"),
+                                       ((1, 512, 6, 64, 64, 3, 256), "f16"),
+                                       ((2, 200, 2, 64, 128, 1, 64), "bf16")])
+def test_stage_chunk_state_tensor_cores(oracle_mod, shape, ops):
+    import mamba_ssd_chunked_fwd_gb300 as ssd
+    B, L, H, P, N, G, Q = shape
+    _, inp = ssd_inputs.custom(B, L, H, P, N, G, Q, seed=51, dt_bias=True)
+    d = to_device(inp)
+    c = -(-L // Q)
+    args = _stage_args(ssd, d, torch.empty_like(d["x"]), None, Q, ops)
+    prob = oracle_problem(oracle_mod, inp)
+    rd, rc = oracle_mod.chunk_cumsum(prob, Q)
+    states = torch.full((B, c, H, P, N), float("nan"), device="cuda")
+    ssd.ssd_chunk_state(args, torch.from_numpy(rd).float().cuda(), torch.from_numpy(rc).float().cuda(), states)
+    torch.cuda.synchronize()
+    ref = oracle_mod.chunk_local_states(prob, Q)
+    got = states.permute(0, 2, 1, 3, 4).reshape(B * H, c, P, N)
+    assert_close(oracle_mod, got.double().cpu().numpy(), ref, ops, f"tc chunk states {shape}")
+
+
+@pytest.mark.parametrize("shape,ops", [((2, 300, 4, 64, 128, 2, 128), "bf16"),
+                                       ((1, 512, 6, 64, 64, 3, 256), "f16")])
+def test_stage_chunk_scan_tensor_cores(oracle_mod, shape, ops):
+    import mamba_ssd_chunked_fwd_gb300 as ssd
+    B, L, H, P, N, G, Q = shape
+    _, inp = ssd_inputs.custom(B, L, H, P, N, G, Q, seed=52, h0=True, D=True, z=True, dt_bias=True)
+    d = to_device(inp)
+    c = -(-L // Q)
+    y = torch.full_like(d["x"], float("nan"))
+    args = _stage_args(ssd, d, y, None, Q, ops)
+    prob = oracle_problem(oracle_mod, inp)
+    rd, rc = oracle_mod.chunk_cumsum(prob, Q)
+    rec = oracle_mod.recurrence(prob, chunk=Q, want_chunk_states=True)
+    states = torch.from_numpy(rec["chunk_states"].reshape(B, H, c, P, N)).float()
+    states = states.permute(0, 2, 1, 3, 4).contiguous().cuda()
+    ssd.ssd_chunk_scan(args, torch.from_numpy(rd).float().cuda(), torch.from_numpy(rc).float().cuda(), states)
+    torch.cuda.synchronize()
+    got = y.permute(0, 2, 1, 3).reshape(B * H, L, P)
+    assert_close(oracle_mod, got.double().cpu().numpy(), rec["y"], ops, f"tc chunk scan {shape}")
+
+
+@pytest.mark.parametrize("shape", [(1, 512, 4, 64, 64, 2, 256), (2, 384, 8, 64, 128, 2, 128),
+                                   (1, 700, 4, 64, 128, 1, 256)])
+@pytest.mark.parametrize("io,ops", [("f32", "bf16"), ("f32", "f16"), ("bf16", "bf16")])
+def test_chunked_plan_tensor_cores(oracle_mod, shape, io, ops):
+    B, L, H, P, N, G, Q = shape
+    _, inp = ssd_inputs.custom(B, L, H, P, N, G, Q, seed=53 + L, x_dtype=io, ops=ops, h0=True, D=True,
+                               z=True, dt_bias=True)
+    y, fin = run_gpu(inp, ops=ops, plan="chunked")
+    _full_compare(oracle_mod, inp, y, fin, ops, f"tc chunked {shape} {io}/{ops}")
