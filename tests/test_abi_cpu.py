@@ -141,7 +141,6 @@ def test_describe_names_the_kernels_each_workload_runs():
     dt_of = {"f32": torch.float32, "bf16": torch.bfloat16}
     for name, w in ssd_inputs.WORKLOADS.items():
         xd = dt_of[w.x_dtype]
-        x = torch.empty((w.B, w.L, w.H, w.P), dtype=xd) if w.B * w.L * w.H * w.P < 2**28 else torch.empty((1,), dtype=xd)
         a = ssd.make_args(torch.empty((1, 1, w.H, w.P), dtype=xd), torch.empty((1, 1, w.H)), torch.empty(w.H),
                           torch.empty((1, 1, w.G, w.N), dtype=xd), torch.empty((1, 1, w.G, w.N), dtype=xd),
                           w.chunk, ops=w.ops)
