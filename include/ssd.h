@@ -178,6 +178,27 @@ ssd_status ssd_chunk_scan(const ssd_fwd_args *args, const float *dtp, const floa
 ssd_status ssd_fwd_host_workspace_size(const ssd_fwd_args *args, size_t *bytes);
 ssd_status ssd_fwd_host(const ssd_fwd_args *args, void *stream);
 
+/*
+ * ssd_fwd without a caller-provided workspace, for callers that cannot
+ * allocate device memory (code that runs under an allocator it does not own,
+ * plugins barred from cudaMalloc, latency-critical paths that must not
+ * allocate).  The pages have no counterpart; this is a convenience of this
+ * library.  args->workspace and args->workspace_bytes are ignored: the scratch
+ * comes from a 64 MiB buffer built into the library, which every GPU that
+ * loads the library holds until the process exits.  A call whose
+ * ssd_fwd_workspace_size() exceeds 64 MiB returns SSD_ERR_WORKSPACE and
+ * enqueues nothing.  Nothing is allocated: no cudaMalloc, no cudaFree.
+ *  - The first call on a device, with that device current, looks up the
+ *    buffer's device address (cudaGetSymbolAddress); make that first call
+ *    before any stream capture.
+ *  - All calls share the one buffer, so calls that may overlap on the GPU
+ *    (different streams, other threads) race and must be serialised by the
+ *    caller.  Everything that must start at zero is cleared by each call.
+ *  - Device-side wait timeouts of these calls are not reachable through
+ *    ssd_check_device_error, which needs the workspace.
+ */
+ssd_status ssd_fwd_noalloc(const ssd_fwd_args *args, void *stream);
+
 /* Synchronises `stream`, then reads the device error word the last ssd_fwd
  * on this workspace left behind (bounded waits that gave up set it).
  * Returns SSD_OK or SSD_ERR_TIMEOUT (or SSD_ERR_CUDA). */

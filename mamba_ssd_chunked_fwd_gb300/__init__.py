@@ -27,7 +27,7 @@ __all__ = [
     "SSD_F32", "SSD_F16", "SSD_BF16", "SSD_OPS_F32", "SSD_OPS_F16", "SSD_OPS_BF16",
     "SSD_PLAN_AUTO", "SSD_PLAN_CHUNKED", "SSD_PLAN_FUSED", "SsdError", "SsdFwdArgs",
     "load_library", "library_path", "make_args", "ssd_fwd", "ssd_fwd_workspace_size",
-    "ssd_fwd_resolve_plan", "ssd_fwd_describe", "ssd_chunk_cumsum", "ssd_chunk_state", "ssd_state_passing",
+    "ssd_fwd_resolve_plan", "ssd_fwd_describe", "ssd_fwd_noalloc", "ssd_chunk_cumsum", "ssd_chunk_state", "ssd_state_passing",
     "ssd_chunk_scan", "ssd_fwd_host", "ssd_fwd_host_workspace_size", "ssd_check_device_error",
     "mamba2_ssd_fwd",
 ]
@@ -84,6 +84,7 @@ _SIGS = {
     "ssd_fwd_host": [_P, ctypes.c_void_p],
     "ssd_check_device_error": [_P, ctypes.c_void_p],
     "ssd_fwd_describe": [_P, ctypes.c_char_p, ctypes.c_size_t],
+    "ssd_fwd_noalloc": [_P, ctypes.c_void_p],
 }
 
 
@@ -185,6 +186,13 @@ def ssd_fwd_describe(args: SsdFwdArgs) -> list:
 def ssd_fwd(args: SsdFwdArgs, stream=None):
     s = stream if stream is not None else _stream_handle()
     _check(load_library().ssd_fwd(ctypes.byref(args), s), "ssd_fwd")
+
+
+def ssd_fwd_noalloc(args: SsdFwdArgs, stream=None):
+    """ssd_fwd with the scratch taken from the library's built-in 64 MiB
+    buffer instead of args.workspace (for callers that cannot allocate)."""
+    s = stream if stream is not None else _stream_handle()
+    _check(load_library().ssd_fwd_noalloc(ctypes.byref(args), s), "ssd_fwd_noalloc")
 
 
 def ssd_chunk_cumsum(args: SsdFwdArgs, dtp, cs, stream=None):

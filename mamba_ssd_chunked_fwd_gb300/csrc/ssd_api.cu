@@ -170,6 +170,8 @@ ssd_status run_chunked(const ssd_fwd_args *a, cudaStream_t s) {
 
 }  // namespace
 
+ssd_status ssd::report_error(ssd_status st, const char *msg) { return fail(st, "%s", msg); }
+
 extern "C" {
 
 int32_t ssd_abi_version(void) { return SSD_ABI_VERSION; }

@@ -105,4 +105,7 @@ cudaError_t launch_chunk_state_tc(const Params &p, int io, int ops, const float 
 cudaError_t launch_chunk_scan_tc(const Params &p, int io, int ops, const float *dtp, const float *cs,
                                  const float *states, unsigned int *err, cudaStream_t s);
 
+// Record `msg` as this thread's ssd_last_error_detail() and return `st`.
+ssd_status report_error(ssd_status st, const char *msg);
+
 }  // namespace ssd
