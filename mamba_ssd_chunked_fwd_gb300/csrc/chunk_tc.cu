@@ -42,6 +42,9 @@ constexpr int kThreads = 256;
 constexpr uint64_t kWaitNs = 2000000000ull;  // an mbarrier wait gives up after 2 s
 constexpr int kMaxQ = 256;
 
+template <int IO>
+__host__ __device__ constexpr size_t io_bytes() { return IO == IO_F32 ? 4 : 2; }
+
 __device__ __forceinline__ void report_timeout(unsigned int *err) {
     if (err) atomicOr(err, 2u);
 }
@@ -85,6 +88,17 @@ chunk_state_tc_kernel(const __grid_constant__ Params p, const float *__restrict_
     if (warp == 0) {
         tc::tmem_alloc(tc::smem_addr(&tmem_slot), N);
         tc::tmem_relinquish();
+    }
+    // pull the chunk's x rows (both heads) and B rows into L2 now; the 64-token
+    // blocks below then load from L2 instead of waiting on HBM one by one
+    for (int i = tid; i < Q; i += kThreads) {
+        const int t = k * Q + i;
+        if (t < L) {
+            tc::prefetch_l2(static_cast<const char *>(p.x) + (((size_t)b * L + t) * H + h0) * kP * io_bytes<IO>(),
+                            2 * kP * io_bytes<IO>());
+            tc::prefetch_l2(static_cast<const char *>(p.Bm) + (((size_t)b * L + t) * p.G + g) * N * io_bytes<IO>(),
+                            N * io_bytes<IO>());
+        }
     }
     // w[h][i] = exp(cs[Q-1] - cs[i]) * dtp[i] (exponent <= 0)
     for (int e = tid; e < 2 * Q; e += kThreads) {
@@ -208,6 +222,22 @@ chunk_scan_tc_kernel(const __grid_constant__ Params p, const float *__restrict__
     if (warp == 0) {
         tc::tmem_alloc(tc::smem_addr(&tmem_slot), 256);
         tc::tmem_relinquish();
+    }
+    // pull everything this CTA reads after C into L2 now: x and B rows of the
+    // source blocks, z rows of the tile, the two heads' entering states
+    for (int i = tid; i < i0 + 128; i += kThreads) {
+        const int t = k * Q + i;
+        if (t < L) {
+            const size_t xrow = (((size_t)b * L + t) * H + h0) * kP * io_bytes<IO>();
+            tc::prefetch_l2(static_cast<const char *>(p.x) + xrow, 2 * kP * io_bytes<IO>());
+            tc::prefetch_l2(static_cast<const char *>(p.Bm) + (((size_t)b * L + t) * p.G + g) * N * io_bytes<IO>(),
+                            N * io_bytes<IO>());
+            if (p.z && i >= i0) tc::prefetch_l2(static_cast<const char *>(p.z) + xrow, 2 * kP * io_bytes<IO>());
+        }
+    }
+    if (tid < 2 * kP * N * 4 / 16384) {  // 16 KB pieces of the 2 x [P, N] fp32 states
+        const char *st = reinterpret_cast<const char *>(states + (((size_t)b * p.nchunks + k) * H + h0) * kP * N);
+        tc::prefetch_l2(st + (size_t)tid * 16384, 16384);
     }
     for (int e = tid; e < 2 * Q; e += kThreads) {
         const int h = e / Q, i = e % Q;

@@ -83,6 +83,12 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// Ask the TMA unit to pull `bytes` of global memory into L2 (no destination,
+// no completion to wait for).  Address and size must be multiples of 16.
+__device__ __forceinline__ void prefetch_l2(const void *gptr, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gptr), "r"(bytes) : "memory");
+}
+
 // 16-byte shared load.
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t saddr) {
     uint4 v;
