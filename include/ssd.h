@@ -58,7 +58,7 @@ typedef enum { SSD_OPS_F32 = 0, SSD_OPS_F16 = 1, SSD_OPS_BF16 = 2 } ssd_operand_
  * with the chunk states in the workspace; FUSED runs one persistent
  * tensor-core kernel per call that keeps every state on chip (it needs
  * P = N = chunk = 64, an even number of heads per group, fp16/bf16 operands
- * and 16-byte aligned x, B and C).  AUTO picks the fastest plan the
+ * and 16-byte aligned x, B, C and y).  AUTO picks the fastest plan the
  * arguments support. */
 typedef enum { SSD_PLAN_AUTO = 0, SSD_PLAN_CHUNKED = 1, SSD_PLAN_FUSED = 2 } ssd_plan;
 

@@ -41,8 +41,11 @@
 //                          wait S_FULL -> dS, Yoff (commit DS_DONE);
 //                          wait MCAT_FULL -> Yint (commit Y_DONE[k%2])
 //
-// Xcat, Mcat and the Yoff / Yint TMEM accumulators are double-buffered, the
-// per-chunk decay vectors triple-buffered.  Every mbarrier wait gives up
+// Xcat and the Yoff / Yint TMEM accumulators are double-buffered, the
+// per-chunk decay vectors triple-buffered; Mcat needs one buffer because the
+// epilogue before it already waits for the previous intra-chunk MMA.  The
+// epilogue writes y into a swizzled staging tile that compute thread 0 sends
+// out with a TMA store after the next barrier.  Every mbarrier wait gives up
 // after 2 s (recorded in the workspace error word) instead of hanging.
 #include <stdio.h>
 
@@ -70,16 +73,17 @@ constexpr uint32_t OFF_BB = 16384;    // B blocks (j, n), 8 KB: K-major for G, M
 constexpr uint32_t OFF_XT = 24576;    // Xw^T, MN-major, 128 (h,p) x 64 j, 16 KB
 constexpr uint32_t OFF_XC = 40960;    // 2 x [X_h0 | 0 | X_h1], MN-major, 192 rows x 64 j, 24 KB each
 constexpr uint32_t XC_BYTES = 24576;
-constexpr uint32_t OFF_MC = 90112;    // 2 x Mcat, K-major B operand, 64 i x 128 (h', j), 16 KB each
-constexpr uint32_t MC_BYTES = 16384;
-constexpr uint32_t OFF_S = 122880;    // S, K-major, 128 (h,p) x 64 n, 16 KB
-// TMA staging of one chunk's public x, B, C tiles, 128-byte swizzled boxes of
-// 64 rows x 128 bytes (8 KB each): x 4 boxes (fp32) or 2 (16-bit), B and C 2 or 1
-constexpr uint32_t OFF_STG_X = 139264;
-constexpr uint32_t OFF_STG_B = 172032;
-constexpr uint32_t OFF_STG_C = 188416;
+constexpr uint32_t OFF_MC = 90112;    // Mcat, K-major B operand, 64 i x 128 (h', j), 16 KB
+constexpr uint32_t OFF_S = 106496;    // S, K-major, 128 (h,p) x 64 n, 16 KB
+// TMA staging, 128-byte swizzled boxes of 64 token rows x 128 bytes (8 KB
+// each): one chunk's y tile on its way out (4 boxes fp32, 2 16-bit), and the
+// next chunk's x, B, C tiles on their way in (x 4 or 2 boxes, B and C 2 or 1)
+constexpr uint32_t OFF_STG_Y = 122880;
+constexpr uint32_t OFF_STG_X = 155648;
+constexpr uint32_t OFF_STG_B = 188416;
+constexpr uint32_t OFF_STG_C = 204800;
 constexpr uint32_t BOX_BYTES = 8192;
-constexpr uint32_t OFF_VEC = 204800;  // 3 x ChunkVec
+constexpr uint32_t OFF_VEC = 221184;  // 3 x ChunkVec
 constexpr uint32_t VEC_BYTES = 2064;
 constexpr uint32_t SMEM_BYTES = OFF_VEC + 3 * VEC_BYTES + 1024;  // + alignment slack
 
@@ -97,7 +101,7 @@ enum {
 // TMA descriptors of x [B,L,H*P] and B, C [B,L,G*N] as 3-D tensors
 // (innermost first: features, tokens, batch), boxes of 128 bytes x 64 tokens.
 struct TmaMaps {
-    CUtensorMap x, b, c;
+    CUtensorMap x, b, c, y;
 };
 
 // 16-byte aligned so that consecutive slots keep their float4 reads aligned
@@ -195,11 +199,12 @@ __device__ __forceinline__ void decay_vectors(const Params &p, const Dims &dm, i
 }
 
 // y for one (head, p) and 8 consecutive tokens from tok_base, read from the
-// TMEM accumulators of buffer bp.  Every shared-memory value is read before
-// the first global store.
+// TMEM accumulators of buffer bp and written into the y staging tile (the
+// layout of a 128-byte-swizzled TMA box; the TMA store drops rows past L).
 template <int IO>
 __device__ __forceinline__ void epilogue8(const Params &p, const Dims &dm, const ChunkVec &V, uint32_t tlane,
-                                          int bp, int col, int b, int h0, int my_h, int my_p, int tok_base) {
+                                          int bp, int col, int b, int h0, int my_h, int my_p, int tok_base,
+                                          uint32_t ystage) {
     float yo[8], yi[8];
     tc::tmem_ld8(tlane + tm_yoff(bp) + col, yo);
     tc::tmem_ld8(tlane + tm_yint(bp) + col, yi);
@@ -211,6 +216,7 @@ __device__ __forceinline__ void epilogue8(const Params &p, const Dims &dm, const
     const int h = h0 + my_h;
     const size_t step = (size_t)dm.H * kP;
     const size_t off0 = (((size_t)b * dm.L + tok_base) * dm.H + h) * kP + my_p;
+    (void)off0;
     float v[8];
 #pragma unroll
     for (int ii = 0; ii < 8; ++ii) v[ii] = fmaf(ev[ii], yo[ii], yi[ii]);
@@ -231,9 +237,27 @@ __device__ __forceinline__ void epilogue8(const Params &p, const Dims &dm, const
 #pragma unroll
         for (int ii = 0; ii < 8; ++ii) v[ii] *= silu_f(zv[ii]);
     }
+    const int f = my_h * kP + my_p;  // feature within the pair's 128
 #pragma unroll
-    for (int ii = 0; ii < 8; ++ii)
-        if (tok_base + ii < dm.L) st_io<IO>(p.y, off0 + ii * step, v[ii]);
+    for (int ii = 0; ii < 8; ++ii) {
+        const int r = i0 + ii;
+        if (IO == IO_F32) {
+            const uint32_t a = ystage + (f >> 5) * BOX_BYTES + r * 128 + ((((f & 31) >> 2) ^ (r & 7)) << 4) + (f & 3) * 4;
+            asm volatile("st.shared.f32 [%0], %1;" ::"r"(a), "f"(v[ii]));
+        } else {
+            const uint32_t a = ystage + (f >> 6) * BOX_BYTES + r * 128 + ((((f & 63) >> 3) ^ (r & 7)) << 4) + (f & 7) * 2;
+            uint16_t hbits;
+            if (IO == IO_BF16) {
+                __nv_bfloat16 hv = __float2bfloat16_rn(v[ii]);
+                hbits = *reinterpret_cast<uint16_t *>(&hv);
+            } else {
+                __half hv = __float2half_rn(v[ii]);
+                hbits = *reinterpret_cast<uint16_t *>(&hv);
+            }
+            asm volatile("st.shared.b16 [%0], %1;" ::"r"(a), "h"(hbits));
+        }
+    }
+    tc::fence_smem_to_async();
 }
 
 template <int IO, bool BF16>
@@ -336,7 +360,7 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                     tc::commit(bar(BAR_DS_DONE));
                     if (!timed_out && !tc::mbar_wait(bar(BAR_MCAT_FULL), ph, kWaitNs)) timed_out = true;
                     tc::fence_after_sync();
-                    const uint32_t xc = sbase + OFF_XC + buf * XC_BYTES, mc = sbase + OFF_MC + buf * MC_BYTES;
+                    const uint32_t xc = sbase + OFF_XC + buf * XC_BYTES, mc = sbase + OFF_MC;
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
@@ -358,6 +382,23 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
         const uint32_t tlane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
         const bool decay_warp = warp >= kDecayWarp0;
         uint32_t gk = 0;
+        // the y tile staged last, not yet sent (every thread tracks it, thread 0 sends it)
+        int pend_b = -1, pend_tok = 0, pend_h0 = 0;
+        constexpr int bw = IO == IO_F32 ? 32 : 64;  // features per staging box
+        auto send_pending = [&]() {  // after a barrier over the compute threads
+            if (pend_b >= 0 && tid == 0) {
+#pragma unroll
+                for (int bx = 0; bx < 128 / bw; ++bx)
+                    tc::tma_store_3d(&tm.y, sbase + OFF_STG_Y + bx * BOX_BYTES, pend_h0 * kP + bx * bw, pend_tok,
+                                     pend_b);
+                tc::bulk_commit();
+            }
+            pend_b = -1;
+        };
+        auto staging_free = [&]() {  // before writing the y staging tile
+            if (tid == 0) tc::bulk_wait_read();
+            tc::named_barrier(2, kComputeThreads);
+        };
 
         for (int unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
             const int pair = unit % pairs;
@@ -404,6 +445,7 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                 const uint32_t ph = gk & 1u;
                 ChunkVec &V = Vbuf[gk % 3];
                 tc::named_barrier(1, kComputeThreads);  // decay vectors of chunk k are in
+                send_pending();
 
                 // ---- A: operands of chunk k into shared memory ----
                 if (!timed_out && !tc::mbar_wait(bar(BAR_STAGE_FULL), ph, kWaitNs)) timed_out = true;
@@ -448,6 +490,7 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                 if (k > 0) {
                     const uint32_t gp = gk - 1;
                     const int bp = gp & 1;
+                    staging_free();
                     if (!timed_out &&
                         !tc::mbar_wait(bar(bp ? BAR_Y_DONE1 : BAR_Y_DONE0), (gp >> 1) & 1u, kWaitNs))
                         timed_out = true;
@@ -455,7 +498,8 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
 #pragma unroll
                     for (int hf = 0; hf < 2; ++hf)
                         epilogue8<IO>(p, dm, Vbuf[gp % 3], tlane, bp, col0 + 8 * hf, b, h0, my_h, my_p,
-                                      (k - 1) * kQ + col0 + 8 * hf);
+                                      (k - 1) * kQ + col0 + 8 * hf, sbase + OFF_STG_Y);
+                    pend_b = b, pend_tok = (k - 1) * kQ, pend_h0 = h0;
                 }
 
                 // ---- B: masked, decayed C B^T -> Mcat ----
@@ -464,7 +508,7 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                     const float csi = V.cs2[h][i];
                     if (!timed_out && !tc::mbar_wait(bar(BAR_G_DONE), ph, kWaitNs)) timed_out = true;
                     tc::fence_after_sync();
-                    const uint32_t mc = sbase + OFF_MC + buf * MC_BYTES;
+                    const uint32_t mc = sbase + OFF_MC;
 #pragma unroll
                     for (int q = 0; q < kCols / 8; ++q) {
                         const int j0 = col0 + 8 * q;
@@ -526,6 +570,9 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
             {
                 const uint32_t gp = gk - 1;
                 const int bp = gp & 1;
+                tc::named_barrier(1, kComputeThreads);
+                send_pending();
+                staging_free();
                 if (!timed_out &&
                     !tc::mbar_wait(bar(bp ? BAR_Y_DONE1 : BAR_Y_DONE0), (gp >> 1) & 1u, kWaitNs))
                     timed_out = true;
@@ -533,7 +580,8 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf)
                     epilogue8<IO>(p, dm, Vbuf[gp % 3], tlane, bp, col0 + 8 * hf, b, h0, my_h, my_p,
-                                  (int)(gp - gk0) * kQ + col0 + 8 * hf);
+                                  (int)(gp - gk0) * kQ + col0 + 8 * hf, sbase + OFF_STG_Y);
+                pend_b = b, pend_tok = (int)(gp - gk0) * kQ, pend_h0 = h0;
             }
             if (p.final_state) {
                 float4 *dst = reinterpret_cast<float4 *>(
@@ -543,6 +591,10 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                     dst[q] = make_float4(S[4 * q], S[4 * q + 1], S[4 * q + 2], S[4 * q + 3]);
             }
         }
+        // the last staged tile, then wait until every store has completed
+        tc::named_barrier(1, kComputeThreads);
+        send_pending();
+        if (tid == 0) tc::bulk_wait_all();
     }
 
     if (timed_out) atomicOr(err, 1u);
@@ -612,6 +664,7 @@ cudaError_t launch_typed(const Params &p, int units, unsigned int *err, cudaStre
     if ((e = encode_map(&tm.x, p.x, IO, (int64_t)p.H * kP, p.L, p.B)) != cudaSuccess) return e;
     if ((e = encode_map(&tm.b, p.Bm, IO, (int64_t)p.G * kN, p.L, p.B)) != cudaSuccess) return e;
     if ((e = encode_map(&tm.c, p.Cm, IO, (int64_t)p.G * kN, p.L, p.B)) != cudaSuccess) return e;
+    if ((e = encode_map(&tm.y, p.y, IO, (int64_t)p.H * kP, p.L, p.B)) != cudaSuccess) return e;
     // one CTA per SM: its shared memory and 512 TMEM columns fill the SM
     const int grid = units < num_sms() ? units : num_sms();
     kern<<<grid, kThreads, SMEM_BYTES, s>>>(p, tm, units, err);
@@ -626,8 +679,8 @@ const char *fused_unsupported_reason(const ssd_fwd_args *a) {
     if (a->ops == SSD_OPS_F32) return "needs fp16 or bf16 operands (the fp32 path is the chunked plan)";
     if (fused_units(a) > 0x7fffffffLL) return "too many (batch, group, head pair) units";
     for (const void *ptr : {static_cast<const void *>(a->x), static_cast<const void *>(a->Bm),
-                            static_cast<const void *>(a->Cm)})
-        if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return "needs 16-byte aligned x, B and C";
+                            static_cast<const void *>(a->Cm), static_cast<const void *>(a->y)})
+        if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return "needs 16-byte aligned x, B, C and y";
     return nullptr;
 }
 
