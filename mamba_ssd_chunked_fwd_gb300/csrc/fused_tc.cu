@@ -26,27 +26,29 @@
 // row-major global layout (MN- or K-major as the tensors come), so nothing is
 // transposed.
 //
-// Warp roles (544 threads): warps 0-15 compute (thread = TMEM lane (head, p)
-// x 16 columns), warp 16 issues the MMAs from one thread.  They hand off
-// through mbarriers in both directions, so the compute warps never block on
-// MMA issue and the tensor core works on chunk k while the compute warps
-// finish chunk k-1:
+// Warp roles (640 threads, 20 warps): warps 0-15 compute (thread = TMEM lane
+// (head, p) x 16 columns), warp 16 issues the MMAs and warp 17 the TMA copies
+// (one thread each), warps 18-19 compute the per-chunk decay vectors of one
+// head each, up to two chunks ahead.  Every handoff is an mbarrier, so no role
+// waits for another's instruction issue, only for its results:
 //
-//   compute, iteration k:  A_k  wait STAGE; operands of chunk k -> smem (arrive OPS_FULL)
-//                          D_k-1 wait Y_DONE; epilogue of chunk k-1 -> y (overlaps G_k)
-//                          B_k  wait G_DONE;  G -> Mcat             (arrive MCAT_FULL)
-//                          C_k  wait DS_DONE; S <- a S + dS -> smem (arrive S_FULL)
-//                          decay vectors of chunk k+1 (warps 14, 15)
-//   MMA warp, chunk k:     wait OPS_FULL -> G (commit G_DONE); TMA of chunk k+1;
-//                          wait S_FULL -> dS, Yoff (commit DS_DONE);
-//                          wait MCAT_FULL -> Yint (commit Y_DONE[k%2])
+//   compute, chunk k:  wait VEC_FULL; A_k  wait STAGE; operands -> smem (arrive OPS_FULL)
+//                      D_k-1 wait Y_FREE, Y_DONE; epilogue of chunk k-1 -> y staging
+//                            (arrive Y_STAGED, VEC_EMPTY)           (overlaps G_k)
+//                      B_k  wait G_DONE;  G -> Mcat             (arrive MCAT_FULL)
+//                      C_k  wait DS_DONE; S <- a S + dS -> smem (arrive S_FULL)
+//   MMA, chunk k:      wait OPS_FULL -> G (commit G_DONE);
+//                      wait S_FULL -> dS, Yoff (commit DS_DONE);
+//                      wait MCAT_FULL -> Yint (commit Y_DONE[k%2])
+//   TMA, chunk k:      wait OPS_FULL -> load x, B, C of chunk k+1 (STAGE);
+//                      wait Y_STAGED -> store y of chunk k-1, wait for its reads (arrive Y_FREE)
+//   decay, chunk k:    wait VEC_EMPTY -> d, cumulative d A, exponentials (arrive VEC_FULL)
 //
 // Xcat and the Yoff / Yint TMEM accumulators are double-buffered, the
 // per-chunk decay vectors triple-buffered; Mcat needs one buffer because the
-// epilogue before it already waits for the previous intra-chunk MMA.  The
-// epilogue writes y into a swizzled staging tile that compute thread 0 sends
-// out with a TMA store after the next barrier.  Every mbarrier wait gives up
-// after 2 s (recorded in the workspace error word) instead of hanging.
+// epilogue before it already waits for the previous intra-chunk MMA.  Every
+// mbarrier wait gives up after 2 s (recorded in the workspace error word)
+// instead of hanging.
 #include <stdio.h>
 
 #include "ssd_fused.cuh"
@@ -62,9 +64,11 @@ constexpr int kQ = 64, kN = 64, kP = 64;
 constexpr int kComputeWarps = 16;
 constexpr int kComputeThreads = kComputeWarps * 32;
 constexpr int kMmaWarp = kComputeWarps;           // warp 16
-constexpr int kThreads = kComputeThreads + 32;    // 544
+constexpr int kTmaWarp = kComputeWarps + 1;       // warp 17
+constexpr int kDecayWarp0 = kComputeWarps + 2;    // warps 18, 19
+constexpr int kThreads = kComputeThreads + 4 * 32;  // 640
 constexpr int kCols = 16;                         // columns of each TMEM region per thread
-constexpr int kDecayWarp0 = 14;                   // warps 14, 15 compute the decay vectors
+constexpr int kVecSlots = 3;
 constexpr uint64_t kWaitNs = 2000000000ull;       // an mbarrier wait gives up after 2 s
 
 // shared-memory layout, bytes from a 1024-aligned base
@@ -75,9 +79,11 @@ constexpr uint32_t OFF_XC = 40960;    // 2 x [X_h0 | 0 | X_h1], MN-major, 192 ro
 constexpr uint32_t XC_BYTES = 24576;
 constexpr uint32_t OFF_MC = 90112;    // Mcat, K-major B operand, 64 i x 128 (h', j), 16 KB
 constexpr uint32_t OFF_S = 106496;    // S, K-major, 128 (h,p) x 64 n, 16 KB
-// TMA staging, 128-byte swizzled boxes of 64 token rows x 128 bytes (8 KB
-// each): one chunk's y tile on its way out (4 boxes fp32, 2 16-bit), and the
-// next chunk's x, B, C tiles on their way in (x 4 or 2 boxes, B and C 2 or 1)
+// TMA staging, boxes of 64 token rows x 128 bytes (8 KB each): one chunk's y
+// tile on its way out (4 boxes fp32, 2 16-bit; not swizzled, the epilogue
+// writes whole rows), and the next chunk's x, B, C tiles on their way in
+// (x 4 or 2 boxes, B and C 2 or 1; 128-byte swizzled for conflict-free
+// column reads)
 constexpr uint32_t OFF_STG_Y = 122880;
 constexpr uint32_t OFF_STG_X = 155648;
 constexpr uint32_t OFF_STG_B = 188416;
@@ -95,7 +101,8 @@ __device__ __forceinline__ uint32_t tm_yint(int buf) { return 192u + 128u * buf;
 // mbarriers
 enum {
     BAR_OPS_FULL = 0, BAR_MCAT_FULL, BAR_S_FULL, BAR_G_DONE, BAR_DS_DONE, BAR_Y_DONE0, BAR_Y_DONE1,
-    BAR_STAGE_FULL, NBARS
+    BAR_STAGE_FULL, BAR_Y_STAGED, BAR_Y_FREE, BAR_VEC_FULL0, BAR_VEC_EMPTY0 = BAR_VEC_FULL0 + kVecSlots,
+    NBARS = BAR_VEC_EMPTY0 + kVecSlots
 };
 
 // TMA descriptors of x [B,L,H*P] and B, C [B,L,G*N] as 3-D tensors
@@ -124,7 +131,7 @@ struct Dims {
     int L, H, G, hpg, nchunks;
 };
 
-// Decay warps' registers: raw dt of tokens lane and lane + 32 of the next chunk.
+// Decay warps' registers: raw dt of tokens lane and lane + 32 of a chunk.
 struct DtRegs {
     float dt0, dt1;
 };
@@ -199,8 +206,8 @@ __device__ __forceinline__ void decay_vectors(const Params &p, const Dims &dm, i
 }
 
 // y for one (head, p) and 8 consecutive tokens from tok_base, read from the
-// TMEM accumulators of buffer bp and written into the y staging tile (the
-// layout of a 128-byte-swizzled TMA box; the TMA store drops rows past L).
+// TMEM accumulators of buffer bp and written into the y staging tile (rows of
+// 128 bytes per box; the TMA store drops rows past L).
 template <int IO>
 __device__ __forceinline__ void epilogue8(const Params &p, const Dims &dm, const ChunkVec &V, uint32_t tlane,
                                           int bp, int col, int b, int h0, int my_h, int my_p, int tok_base,
@@ -238,14 +245,14 @@ __device__ __forceinline__ void epilogue8(const Params &p, const Dims &dm, const
         for (int ii = 0; ii < 8; ++ii) v[ii] *= silu_f(zv[ii]);
     }
     const int f = my_h * kP + my_p;  // feature within the pair's 128
+    const uint32_t a0 = IO == IO_F32 ? ystage + (f >> 5) * BOX_BYTES + i0 * 128 + (f & 31) * 4
+                                     : ystage + (f >> 6) * BOX_BYTES + i0 * 128 + (f & 63) * 2;
 #pragma unroll
     for (int ii = 0; ii < 8; ++ii) {
-        const int r = i0 + ii;
+        const uint32_t a = a0 + ii * 128;
         if (IO == IO_F32) {
-            const uint32_t a = ystage + (f >> 5) * BOX_BYTES + r * 128 + ((((f & 31) >> 2) ^ (r & 7)) << 4) + (f & 3) * 4;
             asm volatile("st.shared.f32 [%0], %1;" ::"r"(a), "f"(v[ii]));
         } else {
-            const uint32_t a = ystage + (f >> 6) * BOX_BYTES + r * 128 + ((((f & 63) >> 3) ^ (r & 7)) << 4) + (f & 7) * 2;
             uint16_t hbits;
             if (IO == IO_BF16) {
                 __nv_bfloat16 hv = __float2bfloat16_rn(v[ii]);
@@ -286,6 +293,12 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
         tc::mbar_init(bar(BAR_Y_DONE0), 1);
         tc::mbar_init(bar(BAR_Y_DONE1), 1);
         tc::mbar_init(bar(BAR_STAGE_FULL), 1);
+        tc::mbar_init(bar(BAR_Y_STAGED), kComputeWarps);
+        tc::mbar_init(bar(BAR_Y_FREE), 1);
+        for (int i = 0; i < kVecSlots; ++i) {
+            tc::mbar_init(bar(BAR_VEC_FULL0 + i), 2);
+            tc::mbar_init(bar(BAR_VEC_EMPTY0 + i), kComputeWarps);
+        }
         tc::mbar_init_fence();
     }
     if (warp == kMmaWarp) {
@@ -304,6 +317,11 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
     const uint32_t tmem = tmem_slot;
     const int pairs = dm.hpg >> 1;
     bool timed_out = false;
+    // wait on mbarrier i for the phase of the given parity; after one timeout a
+    // thread stops waiting (the error word is set and the output is void)
+    auto wait = [&](int i, uint32_t parity) {
+        if (!timed_out && !tc::mbar_wait(bar(i), parity, kWaitNs)) timed_out = true;
+    };
 
     if (warp == kMmaWarp) {
         // ---------------- MMA issue (one thread) ----------------
@@ -311,43 +329,19 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
             constexpr uint32_t ID_KK = tc::idesc_f16(128, 64, BF16, false, false);
             constexpr uint32_t ID_MNMN = tc::idesc_f16(128, 64, BF16, true, true);
             constexpr uint32_t ID_MNK = tc::idesc_f16(128, 64, BF16, true, false);
-            // TMA of the public x, B, C tiles of chunk k of a unit into the staging area
-            constexpr uint32_t kStageBytes = (IO == IO_F32 ? 8u : 4u) * BOX_BYTES;
-            auto stage = [&](int unit, int k) {
-                const int pair = unit % pairs, bg = unit / pairs;
-                const int g = bg % dm.G, b = bg / dm.G;
-                const int h0 = g * dm.hpg + 2 * pair;
-                const int bw = IO == IO_F32 ? 32 : 64;  // features per box
-                tc::mbar_arrive_expect_tx(bar(BAR_STAGE_FULL), kStageBytes);
-#pragma unroll
-                for (int bx = 0; bx < 128 / bw; ++bx)
-                    tc::tma_load_3d(sbase + OFF_STG_X + bx * BOX_BYTES, &tm.x, h0 * kP + bx * bw, k * kQ, b,
-                                    bar(BAR_STAGE_FULL));
-#pragma unroll
-                for (int bx = 0; bx < 64 / bw; ++bx) {
-                    tc::tma_load_3d(sbase + OFF_STG_B + bx * BOX_BYTES, &tm.b, g * kN + bx * bw, k * kQ, b,
-                                    bar(BAR_STAGE_FULL));
-                    tc::tma_load_3d(sbase + OFF_STG_C + bx * BOX_BYTES, &tm.c, g * kN + bx * bw, k * kQ, b,
-                                    bar(BAR_STAGE_FULL));
-                }
-            };
-            if ((int)blockIdx.x < n_units) stage(blockIdx.x, 0);
             uint32_t gk = 0;
             for (int unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
                 for (int k = 0; k < dm.nchunks; ++k, ++gk) {
                     const uint32_t ph = gk & 1u;
                     const int buf = gk & 1;
-                    if (!timed_out && !tc::mbar_wait(bar(BAR_OPS_FULL), ph, kWaitNs)) timed_out = true;
+                    wait(BAR_OPS_FULL, ph);
                     tc::fence_after_sync();
 #pragma unroll
                     for (int ks = 0; ks < kN / 16; ++ks)  // G = C B^T, K = n
                         tc::mma_f16(tmem + TM_G, tc::desc(sbase + OFF_CB2 + ks * 4096, 2048, 128),
                                     tc::desc(sbase + OFF_BB + ks * 2048, 1024, 128), ID_KK, ks > 0);
                     tc::commit(bar(BAR_G_DONE));
-                    // the compute warps are done with the staging area: fetch the next chunk
-                    if (k + 1 < dm.nchunks) stage(unit, k + 1);
-                    else if (unit + (int)gridDim.x < n_units) stage(unit + gridDim.x, 0);
-                    if (!timed_out && !tc::mbar_wait(bar(BAR_S_FULL), ph, kWaitNs)) timed_out = true;
+                    wait(BAR_S_FULL, ph);
                     tc::fence_after_sync();
 #pragma unroll
                     for (int ks = 0; ks < kQ / 16; ++ks)  // dS = Xw^T B, K = j
@@ -358,7 +352,7 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                         tc::mma_f16(tmem + tm_yoff(buf), tc::desc(sbase + OFF_S + ks * 4096, 2048, 128),
                                     tc::desc(sbase + OFF_CB2 + ks * 4096, 2048, 128), ID_KK, ks > 0);
                     tc::commit(bar(BAR_DS_DONE));
-                    if (!timed_out && !tc::mbar_wait(bar(BAR_MCAT_FULL), ph, kWaitNs)) timed_out = true;
+                    wait(BAR_MCAT_FULL, ph);
                     tc::fence_after_sync();
                     const uint32_t xc = sbase + OFF_XC + buf * XC_BYTES, mc = sbase + OFF_MC;
 #pragma unroll
@@ -373,6 +367,80 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
             }
         }
         __syncwarp();
+    } else if (warp == kTmaWarp) {
+        // ---------------- TMA loads and stores (one thread) ----------------
+        if (lane == 0) {
+            tc::prefetch_tensormap(&tm.x);
+            tc::prefetch_tensormap(&tm.b);
+            tc::prefetch_tensormap(&tm.c);
+            tc::prefetch_tensormap(&tm.y);
+            constexpr int bw = IO == IO_F32 ? 32 : 64;  // features per 128-byte box
+            constexpr uint32_t kStageBytes = (IO == IO_F32 ? 8u : 4u) * BOX_BYTES;
+            // the public x, B, C tiles of chunk k of a unit into the staging area
+            auto stage = [&](int unit, int k) {
+                const int pair = unit % pairs, bg = unit / pairs;
+                const int g = bg % dm.G, b = bg / dm.G;
+                const int h0 = g * dm.hpg + 2 * pair;
+                tc::mbar_arrive_expect_tx(bar(BAR_STAGE_FULL), kStageBytes);
+#pragma unroll
+                for (int bx = 0; bx < 128 / bw; ++bx)
+                    tc::tma_load_3d(sbase + OFF_STG_X + bx * BOX_BYTES, &tm.x, h0 * kP + bx * bw, k * kQ, b,
+                                    bar(BAR_STAGE_FULL));
+#pragma unroll
+                for (int bx = 0; bx < 64 / bw; ++bx) {
+                    tc::tma_load_3d(sbase + OFF_STG_B + bx * BOX_BYTES, &tm.b, g * kN + bx * bw, k * kQ, b,
+                                    bar(BAR_STAGE_FULL));
+                    tc::tma_load_3d(sbase + OFF_STG_C + bx * BOX_BYTES, &tm.c, g * kN + bx * bw, k * kQ, b,
+                                    bar(BAR_STAGE_FULL));
+                }
+            };
+            uint32_t yt = 0;  // y tiles stored so far
+            // the y tile of chunk k of (b, head pair from h0), once the compute warps staged it
+            auto store_y = [&](int b, int h0, int k) {
+                wait(BAR_Y_STAGED, yt & 1u);
+#pragma unroll
+                for (int bx = 0; bx < 128 / bw; ++bx)
+                    tc::tma_store_3d(&tm.y, sbase + OFF_STG_Y + bx * BOX_BYTES, h0 * kP + bx * bw, k * kQ, b);
+                tc::bulk_commit();
+                tc::bulk_wait_read();
+                tc::mbar_arrive(bar(BAR_Y_FREE));
+                ++yt;
+            };
+            if ((int)blockIdx.x < n_units) stage(blockIdx.x, 0);
+            uint32_t gk = 0;
+            for (int unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
+                const int pair = unit % pairs, bg = unit / pairs;
+                const int g = bg % dm.G, b = bg / dm.G;
+                const int h0 = g * dm.hpg + 2 * pair;
+                for (int k = 0; k < dm.nchunks; ++k, ++gk) {
+                    wait(BAR_OPS_FULL, gk & 1u);  // the compute warps are done with the staging area
+                    if (k + 1 < dm.nchunks) stage(unit, k + 1);
+                    else if (unit + (int)gridDim.x < n_units) stage(unit + gridDim.x, 0);
+                    if (k > 0) store_y(b, h0, k - 1);
+                }
+                store_y(b, h0, dm.nchunks - 1);
+            }
+            tc::bulk_wait_all();
+        }
+        __syncwarp();
+    } else if (warp >= kDecayWarp0) {
+        // ---------------- decay vectors, one head per warp ----------------
+        const int hh = warp - kDecayWarp0;
+        uint32_t gd = 0;
+        for (int unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
+            const int pair = unit % pairs, bg = unit / pairs;
+            const int g = bg % dm.G, b = bg / dm.G;
+            const int h = g * dm.hpg + 2 * pair + hh;
+            for (int k = 0; k < dm.nchunks; ++k, ++gd) {
+                DtRegs r;
+                load_dt(p, dm, b, h, k, lane, r);
+                const int slot = gd % kVecSlots;
+                if (gd >= (uint32_t)kVecSlots) wait(BAR_VEC_EMPTY0 + slot, (gd / kVecSlots - 1) & 1u);
+                decay_vectors(p, dm, h, hh, k * kQ, lane, r.dt0, r.dt1, Vbuf[slot]);
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(bar(BAR_VEC_FULL0 + slot));
+            }
+        }
     } else {
         // ---------------- compute warps ----------------
         const int wg = warp >> 2, quarter = warp & 3;
@@ -380,24 +448,24 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
         const int my_h = row >> 6, my_p = row & 63;
         const int col0 = wg * kCols;          // this thread's columns of each 64-column region
         const uint32_t tlane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-        const bool decay_warp = warp >= kDecayWarp0;
         uint32_t gk = 0;
-        // the y tile staged last, not yet sent (every thread tracks it, thread 0 sends it)
-        int pend_b = -1, pend_tok = 0, pend_h0 = 0;
-        constexpr int bw = IO == IO_F32 ? 32 : 64;  // features per staging box
-        auto send_pending = [&]() {  // after a barrier over the compute threads
-            if (pend_b >= 0 && tid == 0) {
+        uint32_t yt = 0;  // y tiles staged so far
+        // epilogue of global chunk gp (chunk kk of the unit) into the y staging tile
+        auto epilogue = [&](uint32_t gp, int kk, int b, int h0) {
+            const int bp = gp & 1;
+            if (yt > 0) wait(BAR_Y_FREE, (yt - 1) & 1u);  // the TMA unit has read the previous tile
+            wait(bp ? BAR_Y_DONE1 : BAR_Y_DONE0, (gp >> 1) & 1u);
+            tc::fence_after_sync();
 #pragma unroll
-                for (int bx = 0; bx < 128 / bw; ++bx)
-                    tc::tma_store_3d(&tm.y, sbase + OFF_STG_Y + bx * BOX_BYTES, pend_h0 * kP + bx * bw, pend_tok,
-                                     pend_b);
-                tc::bulk_commit();
+            for (int hf = 0; hf < 2; ++hf)
+                epilogue8<IO>(p, dm, Vbuf[gp % kVecSlots], tlane, bp, col0 + 8 * hf, b, h0, my_h, my_p,
+                              kk * kQ + col0 + 8 * hf, sbase + OFF_STG_Y);
+            __syncwarp();
+            if (lane == 0) {
+                tc::mbar_arrive(bar(BAR_Y_STAGED));
+                tc::mbar_arrive(bar(BAR_VEC_EMPTY0 + gp % kVecSlots));
             }
-            pend_b = -1;
-        };
-        auto staging_free = [&]() {  // before writing the y staging tile
-            if (tid == 0) tc::bulk_wait_read();
-            tc::named_barrier(2, kComputeThreads);
+            ++yt;
         };
 
         for (int unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
@@ -405,7 +473,6 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
             const int bg = unit / pairs;
             const int g = bg % dm.G, b = bg / dm.G;
             const int h0 = g * dm.hpg + 2 * pair;
-            const uint32_t gk0 = gk;
 
             // state of (head my_h, row my_p), columns n = col0 .. col0+kCols-1
             float S[kCols];
@@ -433,22 +500,14 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(bar(BAR_S_FULL));
 
-            DtRegs cur;
-            if (decay_warp) {
-                load_dt(p, dm, b, h0 + warp - kDecayWarp0, 0, lane, cur);
-                decay_vectors(p, dm, h0 + warp - kDecayWarp0, warp - kDecayWarp0, 0, lane, cur.dt0, cur.dt1,
-                              Vbuf[gk % 3]);
-            }
-
             for (int k = 0; k < dm.nchunks; ++k, ++gk) {
                 const int buf = gk & 1;
                 const uint32_t ph = gk & 1u;
-                ChunkVec &V = Vbuf[gk % 3];
-                tc::named_barrier(1, kComputeThreads);  // decay vectors of chunk k are in
-                send_pending();
+                ChunkVec &V = Vbuf[gk % kVecSlots];
+                wait(BAR_VEC_FULL0 + gk % kVecSlots, (gk / kVecSlots) & 1u);  // decay vectors of chunk k
 
                 // ---- A: operands of chunk k into shared memory ----
-                if (!timed_out && !tc::mbar_wait(bar(BAR_STAGE_FULL), ph, kWaitNs)) timed_out = true;
+                wait(BAR_STAGE_FULL, ph);
                 {
                     float wv[2];
 #pragma unroll
@@ -484,29 +543,15 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                 tc::fence_smem_to_async();
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(bar(BAR_OPS_FULL));
-                if (decay_warp && k + 1 < dm.nchunks) load_dt(p, dm, b, h0 + warp - kDecayWarp0, k + 1, lane, cur);
 
                 // ---- D: epilogue of the previous chunk (overlaps the G MMA) ----
-                if (k > 0) {
-                    const uint32_t gp = gk - 1;
-                    const int bp = gp & 1;
-                    staging_free();
-                    if (!timed_out &&
-                        !tc::mbar_wait(bar(bp ? BAR_Y_DONE1 : BAR_Y_DONE0), (gp >> 1) & 1u, kWaitNs))
-                        timed_out = true;
-                    tc::fence_after_sync();
-#pragma unroll
-                    for (int hf = 0; hf < 2; ++hf)
-                        epilogue8<IO>(p, dm, Vbuf[gp % 3], tlane, bp, col0 + 8 * hf, b, h0, my_h, my_p,
-                                      (k - 1) * kQ + col0 + 8 * hf, sbase + OFF_STG_Y);
-                    pend_b = b, pend_tok = (k - 1) * kQ, pend_h0 = h0;
-                }
+                if (k > 0) epilogue(gk - 1, k - 1, b, h0);
 
                 // ---- B: masked, decayed C B^T -> Mcat ----
                 {
                     const int i = row & 63, h = row >> 6;
                     const float csi = V.cs2[h][i];
-                    if (!timed_out && !tc::mbar_wait(bar(BAR_G_DONE), ph, kWaitNs)) timed_out = true;
+                    wait(BAR_G_DONE, ph);
                     tc::fence_after_sync();
                     const uint32_t mc = sbase + OFF_MC;
 #pragma unroll
@@ -538,7 +583,7 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                 // ---- C: state update S <- exp(cs_last) S + dS ----
                 {
                     const float a = V.a[my_h];
-                    if (!timed_out && !tc::mbar_wait(bar(BAR_DS_DONE), ph, kWaitNs)) timed_out = true;
+                    wait(BAR_DS_DONE, ph);
                     tc::fence_after_sync();
                     float ds[kCols];
                     tc::tmem_ld16(tlane + TM_DS + col0, ds);
@@ -559,30 +604,10 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                         if (lane == 0) tc::mbar_arrive(bar(BAR_S_FULL));
                     }
                 }
-
-                // ---- decay vectors of the next chunk ----
-                if (decay_warp && k + 1 < dm.nchunks)
-                    decay_vectors(p, dm, h0 + warp - kDecayWarp0, warp - kDecayWarp0, (k + 1) * kQ, lane,
-                                  cur.dt0, cur.dt1, Vbuf[(gk + 1) % 3]);
             }
 
             // ---- drain: epilogue of the unit's last chunk, final state ----
-            {
-                const uint32_t gp = gk - 1;
-                const int bp = gp & 1;
-                tc::named_barrier(1, kComputeThreads);
-                send_pending();
-                staging_free();
-                if (!timed_out &&
-                    !tc::mbar_wait(bar(bp ? BAR_Y_DONE1 : BAR_Y_DONE0), (gp >> 1) & 1u, kWaitNs))
-                    timed_out = true;
-                tc::fence_after_sync();
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf)
-                    epilogue8<IO>(p, dm, Vbuf[gp % 3], tlane, bp, col0 + 8 * hf, b, h0, my_h, my_p,
-                                  (int)(gp - gk0) * kQ + col0 + 8 * hf, sbase + OFF_STG_Y);
-                pend_b = b, pend_tok = (int)(gp - gk0) * kQ, pend_h0 = h0;
-            }
+            epilogue(gk - 1, dm.nchunks - 1, b, h0);
             if (p.final_state) {
                 float4 *dst = reinterpret_cast<float4 *>(
                     p.final_state + (((size_t)b * dm.H + h0 + my_h) * kP + my_p) * kN + col0);
@@ -591,10 +616,6 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                     dst[q] = make_float4(S[4 * q], S[4 * q + 1], S[4 * q + 2], S[4 * q + 3]);
             }
         }
-        // the last staged tile, then wait until every store has completed
-        tc::named_barrier(1, kComputeThreads);
-        send_pending();
-        if (tid == 0) tc::bulk_wait_all();
     }
 
     if (timed_out) atomicOr(err, 1u);
@@ -636,9 +657,10 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// [batch, tokens, features] tensor, boxes of 128 bytes x 64 tokens x 1, 128B swizzle,
-// zero fill past the end of the sequence.
-cudaError_t encode_map(CUtensorMap *m, const void *base, int io, int64_t feats, int64_t L, int64_t B) {
+// [batch, tokens, features] tensor, boxes of 128 bytes x 64 tokens x 1 (128-byte
+// swizzle or none), zero fill past the end of the sequence.
+cudaError_t encode_map(CUtensorMap *m, const void *base, int io, int64_t feats, int64_t L, int64_t B,
+                       bool swizzle = true) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return cudaErrorNotSupported;
     const size_t esz = io == IO_F32 ? 4 : 2;
@@ -650,7 +672,8 @@ cudaError_t encode_map(CUtensorMap *m, const void *base, int io, int64_t feats, 
     const cuuint32_t box[3] = {(cuuint32_t)(128 / esz), (cuuint32_t)kQ, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(m, dt, 3, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
@@ -664,7 +687,7 @@ cudaError_t launch_typed(const Params &p, int units, unsigned int *err, cudaStre
     if ((e = encode_map(&tm.x, p.x, IO, (int64_t)p.H * kP, p.L, p.B)) != cudaSuccess) return e;
     if ((e = encode_map(&tm.b, p.Bm, IO, (int64_t)p.G * kN, p.L, p.B)) != cudaSuccess) return e;
     if ((e = encode_map(&tm.c, p.Cm, IO, (int64_t)p.G * kN, p.L, p.B)) != cudaSuccess) return e;
-    if ((e = encode_map(&tm.y, p.y, IO, (int64_t)p.H * kP, p.L, p.B)) != cudaSuccess) return e;
+    if ((e = encode_map(&tm.y, p.y, IO, (int64_t)p.H * kP, p.L, p.B, false)) != cudaSuccess) return e;
     // one CTA per SM: its shared memory and 512 TMEM columns fill the SM
     const int grid = units < num_sms() ? units : num_sms();
     kern<<<grid, kThreads, SMEM_BYTES, s>>>(p, tm, units, err);

@@ -96,6 +96,12 @@ __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.w
 // Wait until the committed bulk stores are complete.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// Pull a TMA descriptor (a kernel parameter's generic address) into the
+// descriptor cache ahead of its first use.
+__device__ __forceinline__ void prefetch_tensormap(const void *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
+}
+
 // Ask the TMA unit to pull `bytes` of global memory into L2 (no destination,
 // no completion to wait for).  Address and size must be multiples of 16.
 __device__ __forceinline__ void prefetch_l2(const void *gptr, uint32_t bytes) {
