@@ -289,6 +289,17 @@ def test_fused_plan(oracle_mod, shape, feat, io, ops):
     _full_compare(oracle_mod, inp, y, fin, ops, f"fused {shape} {feat} {io}/{ops}")
 
 
+@pytest.mark.parametrize("feat", ["plain", "all"])
+def test_fused_plan_steep_decay(oracle_mod, feat):
+    """Per-head decay rates from gentle to steep (|d A| up to ~24 per token):
+    within-chunk decays far below fp32's range next to chunks that barely decay."""
+    f = dict(D=True, z=True, dt_bias=True, h0=True) if feat == "all" else {}
+    _, inp = ssd_inputs.custom(2, 448, 8, 64, 64, 2, 64, seed=81, ops="bf16",
+                               dt_dist=("uniform", -3.0, 3.0), A_dist=("neg_uniform", 0.25, 8.0), **f)
+    y, fin = run_gpu(inp, ops="bf16", plan="fused")
+    _full_compare(oracle_mod, inp, y, fin, "bf16", f"fused steep decay {feat}")
+
+
 def test_fused_plan_many_units(oracle_mod):
     """More units than CTAs, so each CTA walks several units in turn."""
     _, inp = ssd_inputs.custom(4, 128, 128, 64, 64, 32, 64, seed=77, ops="bf16", h0=True)
