@@ -301,6 +301,76 @@ def run_gpu(args):
         print(json.dumps(line), flush=True)
 
 
+def run_decode(args):
+    """Decode path: one ``ssd_decode_step`` per step for every sequence of the
+    workload's batch (its final state is the carried state).  Each timed step
+    follows a 256 MiB L2 flush, since the state of the large training shape
+    (67 MB) would otherwise stay in the 129 MB L2; the flush buffer is written
+    and then read back, so that the step does not pay for writing the flush's
+    dirty lines back to HBM.  Prints its own JSON line."""
+    import mamba_ssd_chunked_fwd_gb300 as ssd
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    w = ssd_inputs.WORKLOADS[args.workload]
+    if args.batch:
+        w = w.with_(B=args.batch)
+    one = ssd_inputs.make(w.with_(L=1))
+    cu = {k: (v[:, 0].to(dev).contiguous() if k in ("x", "dt", "B", "C", "z") and v is not None
+              else (v.to(dev) if isinstance(v, torch.Tensor) else v)) for k, v in one.items()}
+    gen = torch.Generator().manual_seed(w.seed + 77)
+    state = (torch.randn((w.B, w.H, w.P, w.N), generator=gen) * 0.5).to(dev)
+    y = torch.empty_like(cu["x"])
+    a = ssd.make_decode_args(cu["x"], cu["dt"], cu["A"], cu["B"], cu["C"], state, y=y, D=cu["D"], z=cu["z"],
+                             dt_bias=cu["dt_bias"], dt_softplus=w.dt_softplus)
+    sh = ssd._stream_handle(dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    for _ in range(args.warmup):
+        ssd.ssd_decode_step(a, sh)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(dev.index, enabled=not args.no_clocks) as clk:
+        torch.cuda.synchronize(dev)
+        sink = torch.zeros((), device=dev)
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            sink += flush.sum()
+            starts[i].record(stream)
+            ssd.ssd_decode_step(a, sh)
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+        if not args.no_clocks:
+            extra_until = time.time() + 0.5
+            while time.time() < extra_until:
+                ssd.ssd_decode_step(a, sh)
+            torch.cuda.synchronize(dev)
+    per_step = sorted(s.elapsed_time(e) for s, e in zip(starts, ends))
+    ms = per_step[len(per_step) // 2]
+    io = {"f32": 4, "f16": 2, "bf16": 2}[w.x_dtype]
+    nbytes = (2 * w.B * w.H * w.P * w.N * 4                       # state read + written
+              + w.B * w.H * w.P * io * (2 + (1 if w.z else 0))    # x, y (, z)
+              + 2 * w.B * w.G * w.N * io + w.B * w.H * 4          # B, C, dt
+              + w.H * 4 * (1 + (w.D_std is not None) + (w.dt_bias_std is not None)))
+    hbm, peak_kind = peaks()
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    line = {
+        "metric": f"SSD decode step tokens/s ({args.workload} state [{w.B},{w.H},{w.P},{w.N}])",
+        "value": round(w.B / (ms * 1e-3), 1), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 6), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded, pages' distributions)",
+        "config": {"workload": f"decode, {args.workload} [B,H,P,N,G] = {[w.B, w.H, w.P, w.N, w.G]}",
+                   "l2": "flushed before every timed step (256 MiB written, then read)",
+                   "timing": "median of per-step events"},
+        "roofline": {"bound": "hbm", "kernel": "decode_step_kernel", "achieved": round(achieved, 1),
+                     "peak": hbm, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                     "traffic": traffic_for("decode_step_kernel", args.workload),
+                     "alg_bytes_per_launch": nbytes, "launch_ms": round(ms, 6)},
+        "clocks": clk.summary(),
+        "gpu_launches": args.steps,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def stage_timing(ssd, a, w, dev, sh, stream, args, kernels):
     """Time the four chunked-plan kernels one by one (events between launches)
     and return the dominant one with its algorithmic bytes, plus every stage's
@@ -444,6 +514,9 @@ def main():
     ap.add_argument("--no-clocks", action="store_true", help="skip the nvidia-smi clock sampler")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch size (a smaller case of the same shape)")
+    ap.add_argument("--path", choices=["forward", "decode"], default="forward",
+                    help="forward (default): the whole SSD forward; decode: one decode step per "
+                         "sequence from a carried state")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
@@ -452,6 +525,9 @@ def main():
         return
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA GPU (the reference arm runs with --impl reference)")
+    if args.path == "decode":
+        run_decode(args)
+        return
     run_gpu(args)
 
 

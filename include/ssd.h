@@ -40,7 +40,7 @@
 extern "C" {
 #endif
 
-#define SSD_ABI_VERSION 1
+#define SSD_ABI_VERSION 2
 
 /* Element types of the public tensors. */
 typedef enum { SSD_F32 = 0, SSD_F16 = 1, SSD_BF16 = 2 } ssd_dtype;
@@ -198,6 +198,69 @@ ssd_status ssd_fwd_host(const ssd_fwd_args *args, void *stream);
  *    ssd_check_device_error, which needs the workspace.
  */
 ssd_status ssd_fwd_noalloc(const ssd_fwd_args *args, void *stream);
+
+/*
+ * Decode: one recurrent step for a single new token of each of B sequences,
+ * continuing from their carried states (the final_state of a forward, or of
+ * the previous step) -- the "final_state for the decode stage" of the
+ * ops-transformer MambaV2 article, section 4.4.  For every (b, h), g = h/(H/G):
+ *
+ *     d      = clamp(softplus(dt[b,h] + dt_bias[h]))   bias / softplus / clamp optional
+ *     S[p,:] = exp(d A[h]) S[p,:] + d x[b,h,p] B[b,g,:]     S = state[b,h], updated IN PLACE
+ *     y[b,h,p] = (S[p,:] . C[b,g,:] + D[h] x[b,h,p]) * silu(z[b,h,p])
+ *
+ * i.e. the forward's recurrence for L = 1 with initial_state = final_state =
+ * state.  Shapes and types:
+ *   x, z, y  [B,H,P]   x_dtype (z optional)
+ *   dt       [B,H]     fp32        A, D, dt_bias  [H] fp32 (D, dt_bias optional)
+ *   Bm, Cm   [B,G,N]   x_dtype
+ *   state    [B,H,P,N] fp32, read and written
+ * Every product is fp32 on the CUDA cores.  N <= 128, any P, H % G == 0.
+ * No workspace; enqueue only; the same validation rules as ssd_fwd.
+ */
+typedef struct {
+    int64_t B, H, P, N, G;
+    const void *x;
+    const float *dt;
+    const float *A;
+    const void *Bm;
+    const void *Cm;
+    const float *D;
+    const void *z;
+    const float *dt_bias;
+    float *state;
+    void *y;
+    int32_t x_dtype;     /* ssd_dtype of x, B, C, z and y */
+    int32_t dt_softplus; /* nonzero: softplus(dt + bias) */
+    float dt_min, dt_max;
+} ssd_decode_args;
+
+ssd_status ssd_decode_step(const ssd_decode_args *args, void *stream);
+
+/*
+ * Sequence-parallel exchange.  A sequence split into consecutive token
+ * segments (one per rank) is composed from each segment's affine state map
+ *     S_out = exp(a) * S_in + S_seg
+ * per (b, h): a = the segment's total sum of d_t * A[h], S_seg = the segment's
+ * final state from a zero start -- the rule chunk_state_passing applies
+ * between chunks (ops-transformer MambaV2 article, section 4.4), here between
+ * segments.  A rank computes (a, S_seg) for its segment, all ranks exchange
+ * them, each folds the maps of the segments before its own into the state
+ * entering its segment and reruns its segment from there.
+ */
+
+/* a[b,h] = sum over the L tokens of args of d_t * A[h], d_t processed as in
+ * ssd_fwd (bias, softplus, clamp), accumulated in fp64 in token order.
+ * log_decay: [B,H] fp32, device.  Needs x-free args: only dt, A, dt_bias and
+ * the shape are read.  Enqueue only. */
+ssd_status ssd_segment_log_decay(const ssd_fwd_args *args, float *log_decay, void *stream);
+
+/* out = fold of nseg consecutive segment maps from a zero start:
+ *     S = 0;  for q = 0 .. nseg-1:  S = exp(log_decay[q]) * S + states[q]
+ * log_decay [nseg,B,H], states [nseg,B,H,P,N], out [B,H,P,N]; fp32, device.
+ * nseg = 0 writes zeros.  Enqueue only. */
+ssd_status ssd_state_fold(int64_t nseg, int64_t B, int64_t H, int64_t P, int64_t N, const float *log_decay,
+                          const float *states, float *out, void *stream);
 
 /* Synchronises `stream`, then reads the device error word the last ssd_fwd
  * on this workspace left behind (bounded waits that gave up set it).

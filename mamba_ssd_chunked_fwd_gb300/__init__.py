@@ -29,7 +29,8 @@ __all__ = [
     "load_library", "library_path", "make_args", "ssd_fwd", "ssd_fwd_workspace_size",
     "ssd_fwd_resolve_plan", "ssd_fwd_describe", "ssd_fwd_noalloc", "ssd_chunk_cumsum", "ssd_chunk_state", "ssd_state_passing",
     "ssd_chunk_scan", "ssd_fwd_host", "ssd_fwd_host_workspace_size", "ssd_check_device_error",
-    "mamba2_ssd_fwd",
+    "mamba2_ssd_fwd", "SsdDecodeArgs", "make_decode_args", "ssd_decode_step", "mamba2_ssd_decode",
+    "ssd_segment_log_decay", "ssd_state_fold",
 ]
 
 SSD_F32, SSD_F16, SSD_BF16 = 0, 1, 2
@@ -67,6 +68,19 @@ class SsdFwdArgs(ctypes.Structure):
     ]
 
 
+class SsdDecodeArgs(ctypes.Structure):
+    """Mirror of ``ssd_decode_args`` in include/ssd.h."""
+    _fields_ = [
+        ("B", ctypes.c_int64), ("H", ctypes.c_int64), ("P", ctypes.c_int64),
+        ("N", ctypes.c_int64), ("G", ctypes.c_int64),
+        ("x", ctypes.c_void_p), ("dt", ctypes.c_void_p), ("A", ctypes.c_void_p),
+        ("Bm", ctypes.c_void_p), ("Cm", ctypes.c_void_p), ("D", ctypes.c_void_p),
+        ("z", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p), ("state", ctypes.c_void_p),
+        ("y", ctypes.c_void_p), ("x_dtype", ctypes.c_int32), ("dt_softplus", ctypes.c_int32),
+        ("dt_min", ctypes.c_float), ("dt_max", ctypes.c_float),
+    ]
+
+
 _lock = threading.Lock()
 _lib = None
 
@@ -85,6 +99,10 @@ _SIGS = {
     "ssd_check_device_error": [_P, ctypes.c_void_p],
     "ssd_fwd_describe": [_P, ctypes.c_char_p, ctypes.c_size_t],
     "ssd_fwd_noalloc": [_P, ctypes.c_void_p],
+    "ssd_decode_step": [ctypes.POINTER(SsdDecodeArgs), ctypes.c_void_p],
+    "ssd_segment_log_decay": [_P, ctypes.c_void_p, ctypes.c_void_p],
+    "ssd_state_fold": [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                       ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p],
 }
 
 
@@ -236,6 +254,26 @@ def ssd_check_device_error(args: SsdFwdArgs, stream=None):
     _check(load_library().ssd_check_device_error(ctypes.byref(args), s), "ssd_check_device_error")
 
 
+def ssd_segment_log_decay(args: SsdFwdArgs, log_decay, stream=None):
+    """log_decay [B,H] fp32 <- sum over the segment's tokens of d_t * A[h]."""
+    s = stream if stream is not None else _stream_handle()
+    _check(load_library().ssd_segment_log_decay(ctypes.byref(args), _ptr(log_decay), s),
+           "ssd_segment_log_decay")
+
+
+def ssd_state_fold(log_decay, states, out, stream=None):
+    """out [B,H,P,N] <- fold of the segment maps (log_decay [nseg,B,H],
+    states [nseg,B,H,P,N], fp32): S = 0; S = exp(a_q) S + S_q for each q."""
+    nseg, Bb, H, P, N = states.shape
+    if tuple(log_decay.shape) != (nseg, Bb, H) or tuple(out.shape) != (Bb, H, P, N):
+        raise ValueError("ssd_state_fold: log_decay [nseg,B,H], states [nseg,B,H,P,N], out [B,H,P,N]")
+    if any(t.dtype != torch.float32 for t in (log_decay, states, out)):
+        raise ValueError("ssd_state_fold takes fp32 tensors")
+    s = stream if stream is not None else _stream_handle()
+    _check(load_library().ssd_state_fold(nseg, Bb, H, P, N, _ptr(log_decay), _ptr(states), _ptr(out), s),
+           "ssd_state_fold")
+
+
 # ---- the README-style call ---------------------------------------------------
 
 def mamba2_ssd_fwd(x, dt, A, B, C, chunk_size, dt_softplus=False, return_final_state=False, *,
@@ -267,3 +305,49 @@ def mamba2_ssd_fwd(x, dt, A, B, C, chunk_size, dt_softplus=False, return_final_s
     args.workspace, args.workspace_bytes = workspace.data_ptr(), workspace.numel()
     ssd_fwd(args, _stream_handle(x.device))
     return (y, fin) if return_final_state else y
+
+
+# ---- decode: one recurrent step from a carried state ---------------------------
+
+def make_decode_args(x, dt, A, B, C, state, *, y=None, D=None, z=None, dt_bias=None,
+                     dt_softplus=False, dt_limit=(0.0, math.inf)) -> SsdDecodeArgs:
+    """Fill an ``ssd_decode_args`` from tensors: x/z/y [B,H,P], dt [B,H],
+    B/C [B,G,N], state [B,H,P,N] fp32 (updated in place)."""
+    Bb, H, P = x.shape
+    G, N = B.shape[1], B.shape[2]
+    io = _DTYPE_CODES.get(x.dtype)
+    if io is None:
+        raise ValueError(f"unsupported dtype {x.dtype}")
+    for t in (B, C) + ((z,) if z is not None else ()) + ((y,) if y is not None else ()):
+        if t.dtype != x.dtype:
+            raise ValueError("x, B, C, z and y must share one dtype")
+    if state.dtype != torch.float32:
+        raise ValueError("state must be fp32")
+    a = SsdDecodeArgs()
+    a.B, a.H, a.P, a.N, a.G = Bb, H, P, N, G
+    a.x, a.dt, a.A, a.Bm, a.Cm = _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C)
+    a.D, a.z, a.dt_bias, a.state, a.y = _ptr(D), _ptr(z), _ptr(dt_bias), _ptr(state), _ptr(y)
+    a.x_dtype = io
+    a.dt_softplus = 1 if dt_softplus else 0
+    a.dt_min, a.dt_max = float(dt_limit[0]), float(dt_limit[1])
+    return a
+
+
+def ssd_decode_step(args: SsdDecodeArgs, stream=None):
+    s = stream if stream is not None else _stream_handle()
+    _check(load_library().ssd_decode_step(ctypes.byref(args), s), "ssd_decode_step")
+
+
+def mamba2_ssd_decode(x, dt, A, B, C, state, dt_softplus=False, *, D=None, z=None, dt_bias=None,
+                      dt_limit=(0.0, math.inf), out=None):
+    """One decode step on the GPU: advances ``state`` [B,H,P,N] (fp32, in
+    place) by one token and returns y [B,H,P] in x's dtype.  x/z [B,H,P],
+    dt [B,H] fp32, B/C [B,G,N].  All compute runs in libssd_gb300.so on the
+    current stream."""
+    if not x.is_cuda:
+        raise ValueError("mamba2_ssd_decode takes CUDA tensors")
+    y = out if out is not None else torch.empty_like(x)
+    args = make_decode_args(x, dt, A, B, C, state, y=y, D=D, z=z, dt_bias=dt_bias,
+                            dt_softplus=dt_softplus, dt_limit=dt_limit)
+    ssd_decode_step(args, _stream_handle(x.device))
+    return y

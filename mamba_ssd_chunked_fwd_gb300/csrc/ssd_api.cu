@@ -247,6 +247,58 @@ ssd_status ssd_fwd(const ssd_fwd_args *a, void *stream) {
     return run_chunked(a, s);
 }
 
+ssd_status ssd_decode_step(const ssd_decode_args *a, void *stream) {
+    if (!a) return fail(SSD_ERR_INVALID_ARG, "args is NULL");
+    if (a->B <= 0 || a->H <= 0 || a->P <= 0 || a->N <= 0 || a->G <= 0)
+        return fail(SSD_ERR_INVALID_ARG, "every dim must be > 0 (B=%lld H=%lld P=%lld N=%lld G=%lld)",
+                    (long long)a->B, (long long)a->H, (long long)a->P, (long long)a->N, (long long)a->G);
+    if (a->H % a->G != 0)
+        return fail(SSD_ERR_INVALID_ARG, "H (%lld) must be a multiple of G (%lld)", (long long)a->H,
+                    (long long)a->G);
+    if (a->N > 128) return fail(SSD_ERR_UNSUPPORTED, "N must be <= 128 (got %lld)", (long long)a->N);
+    if (a->B * a->H > 0x7fffffffLL) return fail(SSD_ERR_UNSUPPORTED, "B*H must be < 2^31");
+    if (a->x_dtype != SSD_F32 && a->x_dtype != SSD_F16 && a->x_dtype != SSD_BF16)
+        return fail(SSD_ERR_INVALID_ARG, "unknown dtype code %d", a->x_dtype);
+    if (!(a->dt_min <= a->dt_max) || isnan(a->dt_min) || isnan(a->dt_max))
+        return fail(SSD_ERR_INVALID_ARG, "dt_limit must satisfy dt_min <= dt_max");
+    if (!a->x || !a->dt || !a->A || !a->Bm || !a->Cm || !a->state || !a->y)
+        return fail(SSD_ERR_INVALID_ARG, "x, dt, A, B, C, state and y are required");
+    ssd::DecodeParams p;
+    p.B = (int)a->B; p.H = (int)a->H; p.P = (int)a->P; p.N = (int)a->N; p.G = (int)a->G;
+    p.x = a->x; p.dt = a->dt; p.A = a->A; p.Bm = a->Bm; p.Cm = a->Cm; p.D = a->D; p.z = a->z;
+    p.dt_bias = a->dt_bias; p.state = a->state; p.y = a->y;
+    p.dt_softplus = a->dt_softplus ? 1 : 0;
+    p.has_limit = !(a->dt_min == 0.f && isinf(a->dt_max) && a->dt_max > 0.f);
+    p.dt_min = a->dt_min; p.dt_max = a->dt_max;
+    cudaError_t e = ssd::launch_decode_step(p, a->x_dtype, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "decode step");
+    return ok();
+}
+
+ssd_status ssd_segment_log_decay(const ssd_fwd_args *a, float *log_decay, void *stream) {
+    ssd_status st = check_shape(a);
+    if (st != SSD_OK) return st;
+    if (!a->dt || !a->A) return fail(SSD_ERR_INVALID_ARG, "dt and A are required");
+    if (!log_decay) return fail(SSD_ERR_INVALID_ARG, "log_decay is required");
+    cudaError_t e = ssd::launch_segment_log_decay(make_params(a), log_decay, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "segment_log_decay");
+    return ok();
+}
+
+ssd_status ssd_state_fold(int64_t nseg, int64_t B, int64_t H, int64_t P, int64_t N, const float *log_decay,
+                          const float *states, float *out, void *stream) {
+    if (nseg < 0 || B <= 0 || H <= 0 || P <= 0 || N <= 0)
+        return fail(SSD_ERR_INVALID_ARG, "nseg >= 0 and B, H, P, N > 0 required");
+    if (B * H > 0x7fffffffLL || P * N > 0x7fffffffLL || nseg > 0x7fffffffLL || B * H * P * N > (1LL << 38))
+        return fail(SSD_ERR_UNSUPPORTED, "state too large (B*H*P*N <= 2^38)");
+    if (!out || (nseg > 0 && (!log_decay || !states)))
+        return fail(SSD_ERR_INVALID_ARG, "out (and log_decay, states when nseg > 0) are required");
+    cudaError_t e = ssd::launch_state_fold((int)nseg, (long long)(B * H), (int)(P * N), log_decay, states, out,
+                                           static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "state_fold");
+    return ok();
+}
+
 ssd_status ssd_chunk_cumsum(const ssd_fwd_args *a, float *dtp, float *cs, void *stream) {
     ssd_status st = check_shape(a);
     if (st != SSD_OK) return st;

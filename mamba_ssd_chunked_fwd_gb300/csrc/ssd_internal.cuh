@@ -87,6 +87,30 @@ __device__ __forceinline__ float dt_processed(const Params &p, float raw, int h)
 
 __device__ __forceinline__ float silu_f(float v) { return v / (1.f + expf(-v)); }
 
+// One decode step (decode.cu): the shape of ssd_decode_args in device form.
+struct DecodeParams {
+    int B, H, P, N, G;
+    const void *x;
+    const float *dt;
+    const float *A;
+    const void *Bm;
+    const void *Cm;
+    const float *D;
+    const void *z;
+    const float *dt_bias;
+    float *state;
+    void *y;
+    int dt_softplus;
+    int has_limit;
+    float dt_min, dt_max;
+};
+cudaError_t launch_decode_step(const DecodeParams &p, int io, cudaStream_t s);
+
+// The sequence-parallel exchange (seqpar.cu).
+cudaError_t launch_segment_log_decay(const Params &p, float *out, cudaStream_t s);
+cudaError_t launch_state_fold(int nseg, long long bh_count, int pn, const float *log_decay, const float *states,
+                              float *out, cudaStream_t s);
+
 // Launchers of the chunked plan (CUDA-core fp32 kernels).
 cudaError_t launch_chunk_cumsum(const Params &p, float *dtp, float *cs, cudaStream_t s);
 cudaError_t launch_chunk_state(const Params &p, int io, const float *dtp, const float *cs,

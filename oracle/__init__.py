@@ -226,6 +226,27 @@ def chunk_local_states(prob: Problem, chunk: int, bh=None, nthreads=0):
     return out
 
 
+def decode_step(x, dt, A, B, C, state, *, D=None, z=None, dt_bias=None, dt_softplus=True,
+                dt_limit=(0.0, math.inf)):
+    """One recurrent step for a single new token, continuing from ``state``:
+    the recurrence above for L = 1 with initial state ``state``
+    (ops-transformer MambaV2 article, section 4.4: the final state feeds the
+    decode stage).  x/z [B,H,P], dt [B,H], B/C [B,G,N], state [B,H,P,N]
+    (widened to float32, exact for fp32 input).  Returns (y [B,H,P],
+    new_state [B,H,P,N]) in float64.  Parity of this step rests on the pins of
+    the recurrence; the continuation test pins the slicing done here."""
+    def one(t):
+        if t is None:
+            return None
+        t = _f32(t)
+        return t.reshape((t.shape[0], 1) + t.shape[1:])
+
+    prob = Problem(one(x), one(dt), A, one(B), one(C), D=D, z=one(z), dt_bias=dt_bias,
+                   initial_states=state, dt_softplus=dt_softplus, dt_limit=dt_limit)
+    y, fin = forward(prob)
+    return y[:, 0], fin
+
+
 def compare(got, ref):
     """Global error metrics in float64: rel-L2, max|diff|/max|ref|, max|diff|."""
     g = np.asarray(got, dtype=np.float64)

@@ -24,7 +24,7 @@ def test_library_exports_every_declared_symbol():
     assert "ssd_fwd" in names and "ssd_chunk_scan" in names
     for name in names:
         assert hasattr(lib, name), f"missing export {name}"
-    assert lib.ssd_abi_version() == 1
+    assert lib.ssd_abi_version() == 2
 
 
 def test_status_strings():
@@ -147,3 +147,27 @@ def test_describe_names_the_kernels_each_workload_runs():
         a.B, a.L = w.B, w.L
         a.x = a.Bm = a.Cm = 4096  # any 16-byte aligned address: describe only inspects alignment
         assert ssd.ssd_fwd_describe(a) == expect[name], name
+
+
+def _decode_args(**over):
+    a = ssd.SsdDecodeArgs()
+    a.B, a.H, a.P, a.N, a.G = 2, 4, 64, 64, 2
+    fake = 1 << 20  # never dereferenced: every case below fails validation first
+    a.x = a.dt = a.A = a.Bm = a.Cm = a.state = a.y = fake
+    a.x_dtype, a.dt_softplus, a.dt_min, a.dt_max = 0, 1, 0.0, float("inf")
+    for k, v in over.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("B", 0, 1), ("H", -1, 1), ("P", 0, 1), ("G", 3, 1), ("N", 256, 2), ("x_dtype", 7, 1),
+    ("state", None, 1), ("y", None, 1), ("Bm", None, 1), ("dt_min", 1.0, 1),
+])
+def test_decode_validation_rejects(field, value, code):
+    lib = ssd.load_library()
+    a = _decode_args(**{field: value})
+    if field == "dt_min":
+        a.dt_max = 0.5
+    assert lib.ssd_decode_step(ctypes.byref(a), None) == code
+    assert lib.ssd_last_error_detail().decode()

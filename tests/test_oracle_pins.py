@@ -350,3 +350,38 @@ def test_oracle_rejects_bad_arguments(oracle_mod):
         oracle_mod.recurrence(prob, [(0, 5)])
     with pytest.raises(ValueError):
         oracle_mod.recurrence(prob, [(3, 0)])
+
+
+# ---- decode step (one token from a carried state) -------------------------------
+
+def test_decode_step_scalar_closed_form(oracle_mod):
+    """B = H = G = P = N = 1: one step by hand, s' = a s + d x b, y = (c s' + D x) silu(z)."""
+    s0, x, dt, A, b, c, D, z, bias = 0.3, -1.2, 0.4, -0.7, 0.9, -1.1, 0.25, 0.6, -0.2
+    f = lambda v, shp: np.full(shp, v, np.float32)
+    yo, so = oracle_mod.decode_step(f(x, (1, 1, 1)), f(dt, (1, 1)), f(A, (1,)), f(b, (1, 1, 1)),
+                                    f(c, (1, 1, 1)), f(s0, (1, 1, 1, 1)), D=f(D, (1,)),
+                                    z=f(z, (1, 1, 1)), dt_bias=f(bias, (1,)))
+    # the inputs were rounded to float32 on the way in: recompute from those values
+    r = lambda v: float(np.float32(v))
+    d = math.log1p(math.exp(r(dt) + r(bias)))
+    s1 = math.exp(d * r(A)) * r(s0) + d * r(x) * r(b)
+    y = (r(c) * s1 + r(D) * r(x)) * (r(z) / (1.0 + math.exp(-r(z))))
+    assert abs(so[0, 0, 0, 0] - s1) <= 1e-12 * abs(s1)
+    assert abs(yo[0, 0, 0] - y) <= 1e-12 * abs(y)
+
+
+def test_decode_continues_the_forward(oracle_mod):
+    """Stepping the last token from the state after L-1 tokens gives the
+    forward's last output and final state (group broadcast G < H, D, z, bias)."""
+    _, inp = ssd_inputs.custom(2, 33, 4, 8, 16, 2, 16, seed=21, D=True, z=True, dt_bias=True, h0=True)
+    prob = _problem(oracle_mod, inp)
+    y_full, fin_full = oracle_mod.forward(prob)
+    head = {k: (v[:, :-1] if k in ("x", "dt", "B", "C", "z") else v) for k, v in inp.items()}
+    _, fin_head = oracle_mod.forward(_problem(oracle_mod, head))
+    t = -1
+    yd, sd = oracle_mod.decode_step(inp["x"][:, t], inp["dt"][:, t], inp["A"], inp["B"][:, t],
+                                    inp["C"][:, t], fin_head.astype(np.float32), D=inp["D"],
+                                    z=inp["z"][:, t], dt_bias=inp["dt_bias"])
+    # the carried state passes through float32 once: agreement to float32 rounding
+    assert oracle_mod.compare(yd, y_full[:, t])["rel_l2"] < 1e-6
+    assert oracle_mod.compare(sd, fin_full)["rel_l2"] < 1e-6
