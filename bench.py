@@ -371,6 +371,74 @@ def run_decode(args):
     print(json.dumps(line), flush=True)
 
 
+def run_varlen(args):
+    """Packed variable-length path: the workload's B*L tokens as B sequences
+    of seeded random lengths (each 25-175 % of L, summing to B*L) packed along
+    one batch row, one ``ssd_fwd_varlen`` per step.  Prints its own JSON line."""
+    import mamba_ssd_chunked_fwd_gb300 as ssd
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    w = ssd_inputs.WORKLOADS[args.workload]
+    if args.batch:
+        w = w.with_(B=args.batch)
+    T = w.B * w.L
+    gen = torch.Generator().manual_seed(w.seed + 91)
+    frac = torch.rand(w.B, generator=gen) * 1.5 + 0.25
+    lengths = (frac / frac.sum() * T).long()
+    lengths[-1] += T - int(lengths.sum())
+    cu = torch.cat([torch.zeros(1, dtype=torch.long), torch.cumsum(lengths, 0)])
+    packed = w.with_(B=1, L=T)
+    inp = ssd_inputs.make(packed)
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    y = torch.empty_like(d["x"])
+    fin = torch.empty((w.B, w.H, w.P, w.N), device=dev) if w.return_final_state else None
+    a = ssd.make_args(d["x"], d["dt"], d["A"], d["B"], d["C"], w.chunk, y=y, final_state=fin, D=d["D"], z=d["z"],
+                      dt_bias=d["dt_bias"], dt_softplus=w.dt_softplus, ops=args.ops or w.ops, plan=args.plan)
+    nws = ssd.ssd_fwd_varlen_workspace_size(a, cu)
+    ws = torch.zeros(max(nws, 256), dtype=torch.uint8, device=dev)
+    a.workspace, a.workspace_bytes = ws.data_ptr(), nws
+    sh = ssd._stream_handle(dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        ssd.ssd_fwd_varlen(a, cu, sh)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(dev.index, enabled=not args.no_clocks) as clk:
+        torch.cuda.synchronize(dev)
+        for i in range(args.steps):
+            starts[i].record(stream)
+            ssd.ssd_fwd_varlen(a, cu, sh)
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+        if not args.no_clocks:
+            extra_until = time.time() + 0.5
+            while time.time() < extra_until:
+                ssd.ssd_fwd_varlen(a, cu, sh)
+            torch.cuda.synchronize(dev)
+    ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / args.steps
+    ab = algorithmic_bytes(w)
+    hbm, peak_kind = peaks()
+    achieved = ab["total"] / (ms * 1e-3) / 1e9
+    line = {
+        "metric": f"SSD fwd tokens/s, packed variable-length sequences ({args.workload} tokens)",
+        "value": round(T / (ms * 1e-3), 1), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": {0: "f32", 1: "f16", 2: "bf16"}[a.ops],
+        "data": "synthetic (seeded, pages' distributions)",
+        "config": {"workload": f"varlen: {w.B} sequences, lengths {lengths.tolist()}, total {T} tokens, "
+                               f"[H,P,N,chunk,G] = {[w.H, w.P, w.N, w.chunk, w.G]}",
+                   # the fused plan's workspace is the error word and the offsets; the chunked
+                   # plan's holds one sequence's chunk states
+                   "plan": "fused" if nws < 65536 else "chunked, per sequence"},
+        "roofline": {"bound": "hbm", "kernel": "ssd_fused_kernel (varlen)", "achieved": round(achieved, 1),
+                     "peak": hbm, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                     "traffic": None, "alg_bytes_per_launch": ab["total"], "launch_ms": round(ms, 5)},
+        "clocks": clk.summary(),
+        "gpu_launches": args.steps,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def stage_timing(ssd, a, w, dev, sh, stream, args, kernels):
     """Time the four chunked-plan kernels one by one (events between launches)
     and return the dominant one with its algorithmic bytes, plus every stage's
@@ -514,9 +582,10 @@ def main():
     ap.add_argument("--no-clocks", action="store_true", help="skip the nvidia-smi clock sampler")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch size (a smaller case of the same shape)")
-    ap.add_argument("--path", choices=["forward", "decode"], default="forward",
+    ap.add_argument("--path", choices=["forward", "decode", "varlen"], default="forward",
                     help="forward (default): the whole SSD forward; decode: one decode step per "
-                         "sequence from a carried state")
+                         "sequence from a carried state; varlen: the forward over packed sequences "
+                         "of random lengths")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
@@ -527,6 +596,9 @@ def main():
         raise SystemExit("bench.py needs a CUDA GPU (the reference arm runs with --impl reference)")
     if args.path == "decode":
         run_decode(args)
+        return
+    if args.path == "varlen":
+        run_varlen(args)
         return
     run_gpu(args)
 

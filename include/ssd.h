@@ -238,6 +238,27 @@ typedef struct {
 ssd_status ssd_decode_step(const ssd_decode_args *args, void *stream);
 
 /*
+ * Packed variable-length sequences ("varlen"): nseq sequences of different
+ * lengths stored back to back along L of a B = 1 call, sequence s holding
+ * tokens [cu_seqlens[s], cu_seqlens[s+1]).  Each sequence is an independent
+ * forward: the state starts at initial_state[s] (or 0) at its first token and
+ * final_state[s] is the state after its last token; nothing crosses a
+ * boundary.  Equivalent to nseq separate ssd_fwd calls with B = 1.
+ *   args          as for ssd_fwd with B = 1 and L = cu_seqlens[nseq]; except
+ *                 initial_state, final_state  [nseq,H,P,N] fp32
+ *   cu_seqlens    HOST array of nseq + 1 int64 offsets, cu_seqlens[0] = 0,
+ *                 non-decreasing (empty sequences allowed); read during the
+ *                 call only (copied into the workspace when the fused plan runs)
+ * The fused plan takes the call when its shape rules hold (the chunked plan
+ * otherwise, one sequence after another).  Returns INVALID_ARG for B != 1 or
+ * malformed offsets; the workspace must hold ssd_fwd_varlen_workspace_size()
+ * bytes.  Enqueue only.
+ */
+ssd_status ssd_fwd_varlen_workspace_size(const ssd_fwd_args *args, const int64_t *cu_seqlens, int64_t nseq,
+                                         size_t *bytes);
+ssd_status ssd_fwd_varlen(const ssd_fwd_args *args, const int64_t *cu_seqlens, int64_t nseq, void *stream);
+
+/*
  * Sequence-parallel exchange.  A sequence split into consecutive token
  * segments (one per rank) is composed from each segment's affine state map
  *     S_out = exp(a) * S_in + S_seg

@@ -30,7 +30,8 @@ __all__ = [
     "ssd_fwd_resolve_plan", "ssd_fwd_describe", "ssd_fwd_noalloc", "ssd_chunk_cumsum", "ssd_chunk_state", "ssd_state_passing",
     "ssd_chunk_scan", "ssd_fwd_host", "ssd_fwd_host_workspace_size", "ssd_check_device_error",
     "mamba2_ssd_fwd", "SsdDecodeArgs", "make_decode_args", "ssd_decode_step", "mamba2_ssd_decode",
-    "ssd_segment_log_decay", "ssd_state_fold",
+    "ssd_segment_log_decay", "ssd_state_fold", "ssd_fwd_varlen", "ssd_fwd_varlen_workspace_size",
+    "mamba2_ssd_fwd_varlen",
 ]
 
 SSD_F32, SSD_F16, SSD_BF16 = 0, 1, 2
@@ -101,6 +102,8 @@ _SIGS = {
     "ssd_fwd_noalloc": [_P, ctypes.c_void_p],
     "ssd_decode_step": [ctypes.POINTER(SsdDecodeArgs), ctypes.c_void_p],
     "ssd_segment_log_decay": [_P, ctypes.c_void_p, ctypes.c_void_p],
+    "ssd_fwd_varlen_workspace_size": [_P, ctypes.c_void_p, ctypes.c_int64, ctypes.POINTER(ctypes.c_size_t)],
+    "ssd_fwd_varlen": [_P, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p],
     "ssd_state_fold": [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p],
 }
@@ -254,6 +257,27 @@ def ssd_check_device_error(args: SsdFwdArgs, stream=None):
     _check(load_library().ssd_check_device_error(ctypes.byref(args), s), "ssd_check_device_error")
 
 
+def _cu_host(cu_seqlens):
+    cu = torch.as_tensor(cu_seqlens, dtype=torch.int64).cpu().contiguous()
+    return cu, cu.numel() - 1
+
+
+def ssd_fwd_varlen_workspace_size(args: SsdFwdArgs, cu_seqlens) -> int:
+    cu, nseq = _cu_host(cu_seqlens)
+    out = ctypes.c_size_t(0)
+    _check(load_library().ssd_fwd_varlen_workspace_size(ctypes.byref(args), cu.data_ptr(), nseq,
+                                                        ctypes.byref(out)), "ssd_fwd_varlen_workspace_size")
+    return int(out.value)
+
+
+def ssd_fwd_varlen(args: SsdFwdArgs, cu_seqlens, stream=None):
+    """Packed variable-length forward; cu_seqlens (nseq + 1 offsets) stays on
+    the host (any int sequence or CPU tensor)."""
+    cu, nseq = _cu_host(cu_seqlens)
+    s = stream if stream is not None else _stream_handle()
+    _check(load_library().ssd_fwd_varlen(ctypes.byref(args), cu.data_ptr(), nseq, s), "ssd_fwd_varlen")
+
+
 def ssd_segment_log_decay(args: SsdFwdArgs, log_decay, stream=None):
     """log_decay [B,H] fp32 <- sum over the segment's tokens of d_t * A[h]."""
     s = stream if stream is not None else _stream_handle()
@@ -351,3 +375,27 @@ def mamba2_ssd_decode(x, dt, A, B, C, state, dt_softplus=False, *, D=None, z=Non
                             dt_softplus=dt_softplus, dt_limit=dt_limit)
     ssd_decode_step(args, _stream_handle(x.device))
     return y
+
+
+def mamba2_ssd_fwd_varlen(x, dt, A, B, C, chunk_size, cu_seqlens, dt_softplus=False, return_final_state=False,
+                          *, D=None, z=None, dt_bias=None, dt_limit=(0.0, math.inf), initial_states=None,
+                          ops=None, plan="auto", out=None):
+    """Packed variable-length SSD forward on the GPU: x [1,T,H,P], dt [1,T,H],
+    B/C [1,T,G,N], z like x; sequence s holds tokens [cu_seqlens[s],
+    cu_seqlens[s+1]) and starts from initial_states[s] (or 0).  Returns y, or
+    (y, final_state [nseq,H,P,N]).  All compute runs in libssd_gb300.so."""
+    if not x.is_cuda:
+        raise ValueError("mamba2_ssd_fwd_varlen takes CUDA tensors")
+    cu, nseq = _cu_host(cu_seqlens)
+    y = out if out is not None else torch.empty_like(x)
+    fin = None
+    if return_final_state:
+        fin = torch.empty((nseq, x.shape[2], x.shape[3], B.shape[3]), device=x.device, dtype=torch.float32)
+    args = make_args(x, dt, A, B, C, chunk_size, y=y, final_state=fin, D=D, z=z, dt_bias=dt_bias,
+                     initial_states=initial_states, dt_softplus=dt_softplus, dt_limit=dt_limit, ops=ops,
+                     plan=plan)
+    nbytes = ssd_fwd_varlen_workspace_size(args, cu)
+    ws = torch.empty(max(nbytes, 256), device=x.device, dtype=torch.uint8)
+    args.workspace, args.workspace_bytes = ws.data_ptr(), ws.numel()
+    ssd_fwd_varlen(args, cu, _stream_handle(x.device))
+    return (y, fin) if return_final_state else y

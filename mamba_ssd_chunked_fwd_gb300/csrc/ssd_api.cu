@@ -168,6 +168,62 @@ ssd_status run_chunked(const ssd_fwd_args *a, cudaStream_t s) {
     return ok();
 }
 
+// Packed variable-length input: checks of the offsets, the longest sequence.
+ssd_status check_varlen(const ssd_fwd_args *a, const int64_t *cu, int64_t nseq, int64_t *max_len) {
+    ssd_status st = check_shape(a);
+    if (st != SSD_OK) return st;
+    if (a->B != 1) return fail(SSD_ERR_INVALID_ARG, "packed sequences need B = 1 (got %lld)", (long long)a->B);
+    if (!cu || nseq < 1) return fail(SSD_ERR_INVALID_ARG, "cu_seqlens and nseq >= 1 are required");
+    if (nseq > 0x7fffffffLL / 64) return fail(SSD_ERR_UNSUPPORTED, "too many sequences");
+    if (cu[0] != 0) return fail(SSD_ERR_INVALID_ARG, "cu_seqlens[0] must be 0");
+    int64_t mx = 0;
+    for (int64_t s = 0; s < nseq; ++s) {
+        if (cu[s + 1] < cu[s])
+            return fail(SSD_ERR_INVALID_ARG, "cu_seqlens must not decrease (entry %lld)", (long long)(s + 1));
+        if (cu[s + 1] - cu[s] > mx) mx = cu[s + 1] - cu[s];
+    }
+    if (cu[nseq] != a->L)
+        return fail(SSD_ERR_INVALID_ARG, "cu_seqlens[nseq] (%lld) must equal L (%lld)", (long long)cu[nseq],
+                    (long long)a->L);
+    *max_len = mx;
+    return SSD_OK;
+}
+
+bool varlen_fused(const ssd_fwd_args *a, int64_t nseq) {
+    if (a->plan == SSD_PLAN_CHUNKED || !ssd::fused_supported(a)) return false;
+    return (int64_t)nseq * a->G * ((a->H / a->G) / 2) <= 0x7fffffffLL;
+}
+
+// one sequence's call of the chunked plan: B = 1 views into the packed tensors
+ssd_fwd_args sequence_args(const ssd_fwd_args *a, const int64_t *cu, int64_t s) {
+    ssd_fwd_args o = *a;
+    const int64_t t0 = cu[s];
+    o.B = 1;
+    o.L = cu[s + 1] - cu[s];
+    const size_t io = io_size(a->x_dtype);
+    auto adv = [](const void *ptr, size_t bytes) -> const char * {
+        return ptr ? static_cast<const char *>(ptr) + bytes : nullptr;
+    };
+    o.x = adv(a->x, (size_t)t0 * a->H * a->P * io);
+    o.z = adv(a->z, (size_t)t0 * a->H * a->P * io);
+    o.y = const_cast<char *>(adv(a->y, (size_t)t0 * a->H * a->P * io));
+    o.dt = reinterpret_cast<const float *>(adv(a->dt, (size_t)t0 * a->H * 4));
+    o.Bm = adv(a->Bm, (size_t)t0 * a->G * a->N * io);
+    o.Cm = adv(a->Cm, (size_t)t0 * a->G * a->N * io);
+    const size_t st = (size_t)s * a->H * a->P * a->N * 4;
+    o.initial_state = reinterpret_cast<const float *>(adv(a->initial_state, st));
+    o.final_state = reinterpret_cast<float *>(const_cast<char *>(adv(a->final_state, st)));
+    return o;
+}
+
+size_t varlen_workspace(const ssd_fwd_args *a, int64_t nseq, int64_t max_len) {
+    if (varlen_fused(a, nseq)) return kAlign + align_up((size_t)(nseq + 1) * sizeof(long long));
+    ssd_fwd_args o = *a;
+    o.B = 1;
+    o.L = max_len > 0 ? max_len : 1;
+    return chunked_layout(&o).total;
+}
+
 }  // namespace
 
 ssd_status ssd::report_error(ssd_status st, const char *msg) { return fail(st, "%s", msg); }
@@ -245,6 +301,53 @@ ssd_status ssd_fwd(const ssd_fwd_args *a, void *stream) {
         return ok();
     }
     return run_chunked(a, s);
+}
+
+ssd_status ssd_fwd_varlen_workspace_size(const ssd_fwd_args *a, const int64_t *cu, int64_t nseq, size_t *bytes) {
+    int64_t mx = 0;
+    ssd_status st = check_varlen(a, cu, nseq, &mx);
+    if (st != SSD_OK) return st;
+    if (!bytes) return fail(SSD_ERR_INVALID_ARG, "bytes is NULL");
+    *bytes = varlen_workspace(a, nseq, mx);
+    return ok();
+}
+
+ssd_status ssd_fwd_varlen(const ssd_fwd_args *a, const int64_t *cu, int64_t nseq, void *stream) {
+    int64_t mx = 0;
+    ssd_status st = check_varlen(a, cu, nseq, &mx);
+    if (st != SSD_OK) return st;
+    if (a->plan == SSD_PLAN_FUSED && !varlen_fused(a, nseq))
+        return fail(SSD_ERR_UNSUPPORTED, "the fused plan does not support this shape: %s",
+                    ssd::fused_unsupported_reason(a) ? ssd::fused_unsupported_reason(a) : "too many units");
+    if ((st = check_pointers(a, true)) != SSD_OK) return st;
+    const size_t need = varlen_workspace(a, nseq, mx);
+    if (!a->workspace || a->workspace_bytes < need)
+        return fail(SSD_ERR_WORKSPACE, "workspace of %zu bytes required (%zu given)", need,
+                    a->workspace ? a->workspace_bytes : (size_t)0);
+    if (!aligned(a->workspace, kAlign)) return fail(SSD_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (varlen_fused(a, nseq)) {
+        long long *cu_dev = reinterpret_cast<long long *>(static_cast<char *>(a->workspace) + kAlign);
+        cudaError_t e = cudaMemcpyAsync(cu_dev, cu, (size_t)(nseq + 1) * sizeof(long long),
+                                        cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess) return cuda_fail(e, "copying cu_seqlens");
+        if ((e = ssd::run_fused(a, s, cu_dev, (int)nseq)) != cudaSuccess) return cuda_fail(e, "fused kernel");
+        return ok();
+    }
+    for (int64_t q = 0; q < nseq; ++q) {
+        const ssd_fwd_args o = sequence_args(a, cu, q);
+        if (o.L == 0) {  // no tokens: the final state is the initial state
+            if (!o.final_state) continue;
+            const size_t bytes = (size_t)a->H * a->P * a->N * 4;
+            cudaError_t e = o.initial_state
+                                ? cudaMemcpyAsync(o.final_state, o.initial_state, bytes, cudaMemcpyDeviceToDevice, s)
+                                : cudaMemsetAsync(o.final_state, 0, bytes, s);
+            if (e != cudaSuccess) return cuda_fail(e, "empty sequence");
+            continue;
+        }
+        if ((st = run_chunked(&o, s)) != SSD_OK) return st;
+    }
+    return ok();
 }
 
 ssd_status ssd_decode_step(const ssd_decode_args *a, void *stream) {

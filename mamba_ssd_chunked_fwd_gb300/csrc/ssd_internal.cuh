@@ -28,6 +28,10 @@ struct Params {
     int dt_softplus;
     int has_limit;
     float dt_min, dt_max;
+    // packed variable-length sequences (fused plan): B == 1 and sequence s
+    // holds tokens [cu[s], cu[s+1]); states are indexed by s.  NULL otherwise.
+    const long long *cu = nullptr;
+    int nseq = 0;
 };
 
 enum IoType { IO_F32 = SSD_F32, IO_F16 = SSD_F16, IO_BF16 = SSD_BF16 };

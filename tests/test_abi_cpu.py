@@ -171,3 +171,30 @@ def test_decode_validation_rejects(field, value, code):
         a.dt_max = 0.5
     assert lib.ssd_decode_step(ctypes.byref(a), None) == code
     assert lib.ssd_last_error_detail().decode()
+
+
+@pytest.mark.parametrize("cu,code", [
+    ([0, 10, 5, 64], 1),     # decreasing
+    ([1, 10, 64], 1),        # does not start at 0
+    ([0, 10, 63], 1),        # does not end at L
+    ([0], 1),                # no sequence
+])
+def test_varlen_offsets_are_validated(cu, code):
+    lib = ssd.load_library()
+    a = _args(B=1, L=64)
+    arr = (ctypes.c_int64 * len(cu))(*cu)
+    out = ctypes.c_size_t(0)
+    assert lib.ssd_fwd_varlen_workspace_size(ctypes.byref(a), arr, len(cu) - 1, ctypes.byref(out)) == code
+    assert lib.ssd_fwd_varlen(ctypes.byref(a), arr, len(cu) - 1, None) == code
+    assert lib.ssd_last_error_detail().decode()
+
+
+def test_varlen_needs_a_single_batch_row():
+    lib = ssd.load_library()
+    a = _args(B=2, L=64)
+    arr = (ctypes.c_int64 * 3)(0, 30, 64)
+    out = ctypes.c_size_t(0)
+    assert lib.ssd_fwd_varlen_workspace_size(ctypes.byref(a), arr, 2, ctypes.byref(out)) == 1
+    a = _args(B=1, L=64)
+    assert lib.ssd_fwd_varlen_workspace_size(ctypes.byref(a), arr, 2, ctypes.byref(out)) == 0
+    assert out.value >= 256
