@@ -55,6 +55,10 @@
 // mbarrier wait gives up after 2 s (recorded in the workspace error word)
 // instead of hanging.
 #include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <vector>
 
 #include "ssd_fused.cuh"
 #include "ssd_internal.cuh"
@@ -143,8 +147,12 @@ struct Span {
     int b, sb, g, h0, t0, len, nch;
 };
 
+// `unit` is the walk position: every CTA walks positions blockIdx.x,
+// blockIdx.x + gridDim.x, ...; for packed sequences the host's schedule maps a
+// position to the unit it runs there.
 template <bool VARLEN>
 __device__ __forceinline__ Span unit_span(const Params &p, const Dims &dm, int unit) {
+    if (VARLEN) unit = p.sched_units[unit];
     const int pairs = dm.hpg >> 1;
     const int pair = unit % pairs, bg = unit / pairs;
     Span u;
@@ -842,7 +850,9 @@ bool fused_preferred(const ssd_fwd_args *a) { return fused_units(a) >= num_sms()
 
 size_t fused_workspace_size(const ssd_fwd_args *) { return 256; }
 
-cudaError_t run_fused(const ssd_fwd_args *a, cudaStream_t s, const long long *cu_dev, int nseq) {
+namespace {
+
+Params fused_params(const ssd_fwd_args *a) {
     Params p;
     p.B = (int)a->B; p.L = (int)a->L; p.H = (int)a->H; p.P = (int)a->P; p.N = (int)a->N;
     p.G = (int)a->G; p.Q = (int)a->chunk;
@@ -853,12 +863,12 @@ cudaError_t run_fused(const ssd_fwd_args *a, cudaStream_t s, const long long *cu
     p.dt_softplus = a->dt_softplus ? 1 : 0;
     p.has_limit = !(a->dt_min == 0.f && isinf(a->dt_max) && a->dt_max > 0.f);
     p.dt_min = a->dt_min; p.dt_max = a->dt_max;
-    p.cu = cu_dev;
-    p.nseq = nseq;
-    unsigned int *err = static_cast<unsigned int *>(a->workspace);
+    return p;
+}
+
+cudaError_t launch(const ssd_fwd_args *a, const Params &p, int units, unsigned int *err, cudaStream_t s) {
     cudaError_t e = cudaMemsetAsync(err, 0, 256, s);
     if (e != cudaSuccess) return e;
-    const int units = cu_dev ? (int)((int64_t)nseq * a->G * ((a->H / a->G) / 2)) : (int)fused_units(a);
     const bool bf16 = a->ops == SSD_OPS_BF16;
     switch (a->x_dtype) {
         case SSD_F32: return bf16 ? launch_typed<IO_F32, true>(p, units, err, s) : launch_typed<IO_F32, false>(p, units, err, s);
@@ -866,6 +876,55 @@ cudaError_t run_fused(const ssd_fwd_args *a, cudaStream_t s, const long long *cu
         case SSD_BF16: return bf16 ? launch_typed<IO_BF16, true>(p, units, err, s) : launch_typed<IO_BF16, false>(p, units, err, s);
     }
     return cudaErrorInvalidValue;
+}
+
+size_t up256(size_t v) { return (v + 255) / 256 * 256; }
+
+}  // namespace
+
+cudaError_t run_fused(const ssd_fwd_args *a, cudaStream_t s) {
+    return launch(a, fused_params(a), (int)fused_units(a), static_cast<unsigned int *>(a->workspace), s);
+}
+
+size_t fused_varlen_workspace_size(const ssd_fwd_args *a, int64_t nseq) {
+    const int64_t units = nseq * a->G * ((a->H / a->G) / 2);
+    return 256 + up256((size_t)(nseq + 1) * 8) + up256((size_t)units * 4);
+}
+
+cudaError_t run_fused_varlen(const ssd_fwd_args *a, const int64_t *cu, int nseq, cudaStream_t s) {
+    const int pairs = (int)((a->H / a->G) / 2);
+    const int units = nseq * (int)a->G * pairs;
+    const int grid = units < num_sms() ? units : num_sms();
+    // Longest first, dealt to the CTAs in snake order (round r goes forward
+    // when r is even, back when odd): walk position i = r * grid + CTA runs the
+    // unit sorted at r * grid + (r even ? CTA : m - 1 - CTA), m the round's
+    // size.  Every CTA keeps the same number of units and the long ones spread
+    // first.
+    std::vector<int> nch(units), order(units);
+    for (int u = 0; u < units; ++u) {
+        const int q = (u / pairs) / (int)a->G;
+        nch[u] = (int)((cu[q + 1] - cu[q] + 63) / 64);
+        order[u] = u;
+    }
+    std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return nch[x] > nch[y]; });
+    // workspace: error word | cu [nseq+1] int64 | schedule [units] int32
+    const size_t o_cu = 256, o_sched = o_cu + up256((size_t)(nseq + 1) * 8), total = o_sched + (size_t)units * 4;
+    std::vector<unsigned char> host(total - o_cu);
+    memcpy(host.data(), cu, (size_t)(nseq + 1) * 8);
+    int *sched = reinterpret_cast<int *>(host.data() + (o_sched - o_cu));
+    for (int i = 0; i < units; ++i) {
+        const int round = i / grid, c = i % grid;
+        const int base = round * grid, m = std::min(grid, units - base);  // m < grid: the last round
+        sched[i] = order[base + ((round & 1) ? m - 1 - c : c)];
+    }
+    char *ws = static_cast<char *>(a->workspace);
+    cudaError_t e = cudaMemcpyAsync(ws + o_cu, host.data(), host.size(), cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return e;
+    Params p = fused_params(a);
+    p.cu = reinterpret_cast<const long long *>(ws + o_cu);
+    p.nseq = nseq;
+    p.sched_units = reinterpret_cast<const int *>(ws + o_sched);
+    return launch(a, p, units, reinterpret_cast<unsigned int *>(ws), s);
 }
 
 }  // namespace ssd

@@ -191,7 +191,8 @@ ssd_status check_varlen(const ssd_fwd_args *a, const int64_t *cu, int64_t nseq, 
 
 bool varlen_fused(const ssd_fwd_args *a, int64_t nseq) {
     if (a->plan == SSD_PLAN_CHUNKED || !ssd::fused_supported(a)) return false;
-    return (int64_t)nseq * a->G * ((a->H / a->G) / 2) <= 0x7fffffffLL;
+    // the host builds a schedule over the units: keep it small
+    return (int64_t)nseq * a->G * ((a->H / a->G) / 2) <= (1LL << 24);
 }
 
 // one sequence's call of the chunked plan: B = 1 views into the packed tensors
@@ -217,7 +218,7 @@ ssd_fwd_args sequence_args(const ssd_fwd_args *a, const int64_t *cu, int64_t s) 
 }
 
 size_t varlen_workspace(const ssd_fwd_args *a, int64_t nseq, int64_t max_len) {
-    if (varlen_fused(a, nseq)) return kAlign + align_up((size_t)(nseq + 1) * sizeof(long long));
+    if (varlen_fused(a, nseq)) return ssd::fused_varlen_workspace_size(a, nseq);
     ssd_fwd_args o = *a;
     o.B = 1;
     o.L = max_len > 0 ? max_len : 1;
@@ -327,11 +328,8 @@ ssd_status ssd_fwd_varlen(const ssd_fwd_args *a, const int64_t *cu, int64_t nseq
     if (!aligned(a->workspace, kAlign)) return fail(SSD_ERR_WORKSPACE, "workspace must be 256-byte aligned");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (varlen_fused(a, nseq)) {
-        long long *cu_dev = reinterpret_cast<long long *>(static_cast<char *>(a->workspace) + kAlign);
-        cudaError_t e = cudaMemcpyAsync(cu_dev, cu, (size_t)(nseq + 1) * sizeof(long long),
-                                        cudaMemcpyHostToDevice, s);
-        if (e != cudaSuccess) return cuda_fail(e, "copying cu_seqlens");
-        if ((e = ssd::run_fused(a, s, cu_dev, (int)nseq)) != cudaSuccess) return cuda_fail(e, "fused kernel");
+        cudaError_t e = ssd::run_fused_varlen(a, cu, (int)nseq, s);
+        if (e != cudaSuccess) return cuda_fail(e, "fused kernel");
         return ok();
     }
     for (int64_t q = 0; q < nseq; ++q) {

@@ -13,8 +13,11 @@ bool fused_supported(const ssd_fwd_args *a);
 const char *fused_unsupported_reason(const ssd_fwd_args *a);
 bool fused_preferred(const ssd_fwd_args *a);
 size_t fused_workspace_size(const ssd_fwd_args *a);
-// cu_dev (device, nseq + 1 offsets): packed variable-length sequences along L
-// of a B = 1 call, states indexed by sequence; NULL for the regular layout.
-cudaError_t run_fused(const ssd_fwd_args *a, cudaStream_t s, const long long *cu_dev = nullptr, int nseq = 0);
+cudaError_t run_fused(const ssd_fwd_args *a, cudaStream_t s);
+// Packed variable-length sequences along L of a B = 1 call (cu: host, nseq + 1
+// offsets; states indexed by sequence).  The workspace holds the error word,
+// the offsets and the host-built schedule of units over CTAs.
+size_t fused_varlen_workspace_size(const ssd_fwd_args *a, int64_t nseq);
+cudaError_t run_fused_varlen(const ssd_fwd_args *a, const int64_t *cu, int nseq, cudaStream_t s);
 
 }  // namespace ssd

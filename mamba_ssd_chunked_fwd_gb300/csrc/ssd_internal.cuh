@@ -32,6 +32,9 @@ struct Params {
     // holds tokens [cu[s], cu[s+1]); states are indexed by s.  NULL otherwise.
     const long long *cu = nullptr;
     int nseq = 0;
+    // packed sequences: the unit at walk position i (CTA i % grid, its
+    // (i / grid)-th unit), from the host's schedule
+    const int *sched_units = nullptr;
 };
 
 enum IoType { IO_F32 = SSD_F32, IO_F16 = SSD_F16, IO_BF16 = SSD_BF16 };
