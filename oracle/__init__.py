@@ -77,6 +77,11 @@ def _load():
         lib.oracle_chunk_local_states.argtypes = [
             ctypes.POINTER(_Problem), ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
             ctypes.c_void_p, ctypes.c_int]
+        lib.oracle_backward.restype = ctypes.c_int
+        lib.oracle_backward.argtypes = [
+            ctypes.POINTER(_Problem), ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
         _lib = lib
     return _lib
 
@@ -223,6 +228,56 @@ def chunk_local_states(prob: Problem, chunk: int, bh=None, nthreads=0):
     if lib.oracle_chunk_local_states(ctypes.byref(st), bha.ctypes.data, bha.shape[0],
                                      int(chunk), out.ctypes.data, int(nthreads)):
         raise ValueError("oracle_chunk_local_states rejected its arguments")
+    return out
+
+
+def backward(prob: Problem, dy, dfinal=None, *, nthreads=0):
+    """Gradients of L = sum(dy * y) + sum(dfinal * final_state) with respect
+    to every input of the forward, by the adjoint of the token recurrence (the
+    SSD backward named in the "Mamba-2 SSD for Ascend NPU" README, "Limitations
+    and roadmap"; the recurrence of the README's "Implementation").
+
+    dy [B,L,H,P], dfinal [B,H,P,N] or None.  Returns float64 arrays in the
+    public layouts: dx [B,L,H,P], dB, dC [B,L,G,N] (heads of a group summed),
+    ddt [B,L,H] (with respect to the raw dt), dA, dD, ddt_bias [H] (batch
+    summed), dz [B,L,H,P] (zeros without z), dh0 [B,H,P,N].
+    """
+    lib = _load()
+    Bb, L, H, P, N, G = prob.dims
+    bha = _bh_array(prob, None)
+    nbh = bha.shape[0]
+    dy32 = _f32(dy)
+    assert dy32.shape == (Bb, L, H, P)
+    dy_pairs = np.ascontiguousarray(dy32.transpose(0, 2, 1, 3).reshape(nbh, L, P))
+    df = None
+    if dfinal is not None:
+        df = _f32(dfinal)
+        assert df.shape == (Bb, H, P, N)
+        df = np.ascontiguousarray(df.reshape(nbh, P, N))
+    dx = np.empty((nbh, L, P)); dBh = np.empty((nbh, L, N)); dCh = np.empty((nbh, L, N))
+    ddt = np.empty((nbh, L)); dA = np.empty(nbh); dD = np.empty(nbh); dbias = np.empty(nbh)
+    dz = np.empty((nbh, L, P)); dh0 = np.empty((nbh, P, N))
+    st = prob._struct()
+    ptr = lambda a: None if a is None else a.ctypes.data
+    rc = lib.oracle_backward(ctypes.byref(st), bha.ctypes.data, nbh, dy_pairs.ctypes.data, ptr(df),
+                             dx.ctypes.data, dBh.ctypes.data, dCh.ctypes.data, ddt.ctypes.data,
+                             dA.ctypes.data, dD.ctypes.data, dbias.ctypes.data, dz.ctypes.data,
+                             dh0.ctypes.data, int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_backward rejected its arguments")
+    hpg = H // G
+    per_head = lambda a, w: a.reshape(Bb, H, L, w).transpose(0, 2, 1, 3)  # [B,L,H,w]
+    out = {
+        "dx": np.ascontiguousarray(per_head(dx, P)),
+        "dB": per_head(dBh, N).reshape(Bb, L, G, hpg, N).sum(axis=3),
+        "dC": per_head(dCh, N).reshape(Bb, L, G, hpg, N).sum(axis=3),
+        "ddt": np.ascontiguousarray(ddt.reshape(Bb, H, L).transpose(0, 2, 1)),
+        "dA": dA.reshape(Bb, H).sum(axis=0),
+        "dD": dD.reshape(Bb, H).sum(axis=0),
+        "ddt_bias": dbias.reshape(Bb, H).sum(axis=0),
+        "dz": np.ascontiguousarray(per_head(dz, P)),
+        "dh0": dh0.reshape(Bb, H, P, N),
+    }
     return out
 
 

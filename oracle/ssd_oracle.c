@@ -249,3 +249,149 @@ int oracle_chunk_local_states(const oracle_problem *p, const int64_t *bh, int64_
     }
     return 0;
 }
+
+/*
+ * Backward of the recurrence above (the SSD backward: gradients of
+ * L = sum_t dy_t . y_t + <dfinal, final_state> with respect to every input).
+ * Written as the adjoint of the token recurrence, in reverse token order:
+ *
+ *   g        = dfinal                                  (dL/dh_{L-1} via the final state)
+ *   for t = L-1 .. 0:
+ *     dyp_t  = dy_t * silu(z_t)                        (no gate: dyp_t = dy_t)
+ *     dz_t   = dy_t * (h_t . C_t + D x_t) * silu'(z_t)
+ *     g     += dyp_t (outer) C_t                       (now dL/dh_t)
+ *     dC_t   = sum_p dyp_t[p] h_t[p,:]
+ *     dx_t   = d_t (g B_t) + D dyp_t
+ *     dB_t   = d_t (g^T x_t)
+ *     dd_t   = <g, x_t (outer) B_t> + A a_t <g, h_{t-1}>
+ *     dA    += d_t a_t <g, h_{t-1}>,  dD += dyp_t . x_t
+ *     ddt_t  = dd_t * softplus'(dt_t + bias) (* 1 inside the dt_limit clamp, 0 outside)
+ *     dbias += ddt_t
+ *     g      = a_t g                                   (dL/dh_{t-1})
+ *   dh0 = g
+ *
+ * per (b, h) pair listed in bh; dB and dC are this head's contributions (the
+ * caller sums the heads of a group), dA, dD and dbias this pair's (summed
+ * over b by the caller).  Keeps every h_t of the pair: [L,P,N] doubles.
+ * Outputs (nbh leading): dx [L,P], dB, dC [L,N], ddt [L], dA, dD, dbias [1],
+ * dz [L,P] (or NULL), dh0 [P,N].
+ */
+int oracle_backward(const oracle_problem *p, const int64_t *bh, int64_t nbh, const float *dy,
+                    const float *dfinal, double *dx, double *dB, double *dC, double *ddt, double *dA,
+                    double *dD, double *dbias, double *dz, double *dh0, int nthreads)
+{
+    if (!p || !bh || nbh < 0 || !dy) return -1;
+    if (p->B < 0 || p->L < 0 || p->H <= 0 || p->P <= 0 || p->N <= 0 || p->G <= 0) return -1;
+    if (p->H % p->G != 0) return -1;
+    const int64_t L = p->L, H = p->H, P = p->P, N = p->N, G = p->G;
+    const int64_t heads_per_group = H / G;
+    for (int64_t i = 0; i < nbh; ++i)
+        if (bh[2 * i] < 0 || bh[2 * i] >= p->B || bh[2 * i + 1] < 0 || bh[2 * i + 1] >= H) return -1;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+    int status = 0;
+#pragma omp parallel
+    {
+        double *hs = (double *)malloc(sizeof(double) * (size_t)((L + 1) * P * N));  /* h_{-1} .. h_{L-1} */
+        double *g = (double *)malloc(sizeof(double) * (size_t)(P * N));
+        double *dd_raw = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
+        double *av = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
+        if (!hs || !g || !dd_raw || !av) {
+#pragma omp atomic write
+            status = -1;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t i = 0; i < nbh; ++i) {
+            if (!hs || !g || !dd_raw || !av) continue;
+            const int64_t b = bh[2 * i], h = bh[2 * i + 1];
+            const int64_t gg = h / heads_per_group;
+            const double Ah = (double)p->A[h];
+            const double Dh = p->D ? (double)p->D[h] : 0.0;
+            /* forward, keeping every state */
+            for (int64_t e = 0; e < P * N; ++e)
+                hs[e] = p->h0 ? (double)p->h0[(b * H + h) * P * N + e] : 0.0;
+            for (int64_t t = 0; t < L; ++t) {
+                const double raw = (double)p->dt[(b * L + t) * H + h];
+                const double d = oracle_dt_processed(p, raw, h);
+                const double a = exp(d * Ah);
+                av[t] = a;
+                dd_raw[t] = d;
+                const float *xt = p->x + ((b * L + t) * H + h) * P;
+                const float *Bt = p->Bm + ((b * L + t) * G + gg) * N;
+                const double *prev = hs + t * P * N;
+                double *cur = hs + (t + 1) * P * N;
+                for (int64_t pp = 0; pp < P; ++pp)
+                    for (int64_t n = 0; n < N; ++n)
+                        cur[pp * N + n] = a * prev[pp * N + n] + d * (double)xt[pp] * (double)Bt[n];
+            }
+            /* backward */
+            for (int64_t e = 0; e < P * N; ++e) g[e] = dfinal ? (double)dfinal[i * P * N + e] : 0.0;
+            double sA = 0.0, sD = 0.0, sbias = 0.0;
+            for (int64_t t = L - 1; t >= 0; --t) {
+                const double d = dd_raw[t], a = av[t];
+                const float *xt = p->x + ((b * L + t) * H + h) * P;
+                const float *Bt = p->Bm + ((b * L + t) * G + gg) * N;
+                const float *Ct = p->Cm + ((b * L + t) * G + gg) * N;
+                const float *zt = p->z ? p->z + ((b * L + t) * H + h) * P : NULL;
+                const double *ht = hs + (t + 1) * P * N, *hprev = hs + t * P * N;
+                const float *dyt = dy + (i * L + t) * P;
+                for (int64_t pp = 0; pp < P; ++pp) {
+                    double dyp = (double)dyt[pp];
+                    if (zt) {
+                        const double zv = (double)zt[pp];
+                        const double sg = 1.0 / (1.0 + exp(-zv));
+                        double ypre = Dh * (double)xt[pp];
+                        for (int64_t n = 0; n < N; ++n) ypre += ht[pp * N + n] * (double)Ct[n];
+                        if (dz) dz[(i * L + t) * P + pp] = dyp * ypre * sg * (1.0 + zv * (1.0 - sg));
+                        dyp *= zv * sg;
+                    } else if (dz) {
+                        dz[(i * L + t) * P + pp] = 0.0;
+                    }
+                    sD += dyp * (double)xt[pp];
+                    for (int64_t n = 0; n < N; ++n) g[pp * N + n] += dyp * (double)Ct[n];
+                    if (dx) dx[(i * L + t) * P + pp] = Dh * dyp;  /* + d (g B)[p] below */
+                    if (dC)
+                        for (int64_t n = 0; n < N; ++n)
+                            dC[(i * L + t) * N + n] = (pp == 0 ? 0.0 : dC[(i * L + t) * N + n]) + dyp * ht[pp * N + n];
+                }
+                double e_t = 0.0, q_t = 0.0;
+                for (int64_t n = 0; n < N; ++n) if (dB) dB[(i * L + t) * N + n] = 0.0;
+                for (int64_t pp = 0; pp < P; ++pp) {
+                    double gb = 0.0;
+                    for (int64_t n = 0; n < N; ++n) {
+                        const double gv = g[pp * N + n];
+                        gb += gv * (double)Bt[n];
+                        q_t += gv * hprev[pp * N + n];
+                        if (dB) dB[(i * L + t) * N + n] += d * gv * (double)xt[pp];
+                    }
+                    e_t += gb * (double)xt[pp];
+                    if (dx) dx[(i * L + t) * P + pp] += d * gb;
+                }
+                const double ddv = e_t + Ah * a * q_t;
+                sA += d * a * q_t;
+                /* through the clamp and softplus, back to the raw dt */
+                double u = (double)p->dt[(b * L + t) * H + h];
+                if (p->dt_bias) u += (double)p->dt_bias[h];
+                double dpre = p->dt_softplus ? oracle_softplus(u) : u;
+                double gr = ddv;
+                if (p->has_dt_limit && (dpre < p->dt_min || dpre > p->dt_max)) gr = 0.0;
+                if (p->dt_softplus) gr *= 1.0 / (1.0 + exp(-u));
+                if (ddt) ddt[i * L + t] = gr;
+                sbias += gr;
+                for (int64_t e = 0; e < P * N; ++e) g[e] *= a;
+            }
+            if (dA) dA[i] = sA;
+            if (dD) dD[i] = sD;
+            if (dbias) dbias[i] = sbias;
+            if (dh0) memcpy(dh0 + i * P * N, g, sizeof(double) * (size_t)(P * N));
+        }
+        free(hs);
+        free(g);
+        free(dd_raw);
+        free(av);
+    }
+    return status;
+}

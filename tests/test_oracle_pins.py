@@ -385,3 +385,68 @@ def test_decode_continues_the_forward(oracle_mod):
     # the carried state passes through float32 once: agreement to float32 rounding
     assert oracle_mod.compare(yd, y_full[:, t])["rel_l2"] < 1e-6
     assert oracle_mod.compare(sd, fin_full)["rel_l2"] < 1e-6
+
+
+# ---- backward (adjoint) against finite differences of the forward ------------------
+
+def _loss(oracle_mod, tensors, flags, dy, dfinal):
+    prob = oracle_mod.Problem(tensors["x"], tensors["dt"], tensors["A"], tensors["B"], tensors["C"],
+                              D=tensors.get("D"), z=tensors.get("z"), dt_bias=tensors.get("dt_bias"),
+                              initial_states=tensors.get("h0"), **flags)
+    y, fin = oracle_mod.forward(prob)
+    return float(np.sum(y * dy) + np.sum(fin * dfinal))
+
+
+@pytest.mark.parametrize("case", ["all_features", "grouped", "clamped"])
+def test_backward_matches_central_differences(oracle_mod, case):
+    """Every gradient of the adjoint recurrence, coordinate by coordinate,
+    against (L(t + e) - L(t - e)) / (t+ - t-) of the forward oracle, with t+-
+    the float32 values actually fed to it.  Linear inputs (x, B, C, D, h0) are
+    exact up to rounding; dt, A, bias and z carry an O(e^2) truncation."""
+    if case == "grouped":
+        _, inp = ssd_inputs.custom(2, 5, 4, 3, 2, 2, 16, seed=31, D=True, dt_bias=True, h0=True)
+        flags = dict(dt_softplus=True)
+    elif case == "clamped":
+        _, inp = ssd_inputs.custom(1, 6, 2, 2, 3, 1, 16, seed=32, D=True, h0=True,
+                                   dt_dist=("uniform", -0.5, 2.0))
+        flags = dict(dt_softplus=True, dt_limit=(0.3, 1.2))
+    else:
+        _, inp = ssd_inputs.custom(1, 6, 2, 3, 4, 1, 16, seed=33, D=True, z=True, dt_bias=True, h0=True)
+        flags = dict(dt_softplus=True)
+    rng = np.random.default_rng(7)
+    Bb, L, H, P = inp["x"].shape
+    N = inp["B"].shape[3]
+    dy = rng.standard_normal((Bb, L, H, P)).astype(np.float32)
+    dfinal = rng.standard_normal((Bb, H, P, N)).astype(np.float32)
+    t = {"x": inp["x"].numpy(), "dt": inp["dt"].numpy(), "A": inp["A"].numpy(), "B": inp["B"].numpy(),
+         "C": inp["C"].numpy(), "D": inp["D"].numpy(), "h0": inp["initial_states"].numpy()}
+    if inp["z"] is not None:
+        t["z"] = inp["z"].numpy()
+    if inp["dt_bias"] is not None:
+        t["dt_bias"] = inp["dt_bias"].numpy()
+    prob = oracle_mod.Problem(t["x"], t["dt"], t["A"], t["B"], t["C"], D=t["D"], z=t.get("z"),
+                              dt_bias=t.get("dt_bias"), initial_states=t["h0"], **flags)
+    g = oracle_mod.backward(prob, dy, dfinal)
+    names = {"x": "dx", "dt": "ddt", "A": "dA", "B": "dB", "C": "dC", "D": "dD", "h0": "dh0", "z": "dz",
+             "dt_bias": "ddt_bias"}
+    for name, gname in names.items():
+        if name not in t:
+            continue
+        base = t[name]
+        fd = np.zeros(base.shape)
+        for idx in np.ndindex(base.shape):
+            eps = 1e-3 * max(1.0, abs(float(base[idx])))
+            plus, minus = base.copy(), base.copy()
+            plus[idx] = np.float32(base[idx] + eps)
+            minus[idx] = np.float32(base[idx] - eps)
+            lp = _loss(oracle_mod, {**t, name: plus}, flags, dy, dfinal)
+            lm = _loss(oracle_mod, {**t, name: minus}, flags, dy, dfinal)
+            fd[idx] = (lp - lm) / (float(plus[idx]) - float(minus[idx]))
+        got = np.asarray(g[gname], dtype=np.float64).reshape(fd.shape)
+        scale = max(1.0, float(np.max(np.abs(fd))))
+        assert np.max(np.abs(got - fd)) <= 2e-5 * scale, (case, name, np.max(np.abs(got - fd)), scale)
+    if case == "clamped":
+        # some steps sit outside the clamp: their raw-dt gradient is exactly zero
+        d = np.logaddexp(0.0, t["dt"].astype(np.float64))
+        outside = (d < 0.3) | (d > 1.2)
+        assert outside.any() and np.all(g["ddt"][outside] == 0.0)
