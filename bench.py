@@ -439,6 +439,72 @@ def run_varlen(args):
     print(json.dumps(line), flush=True)
 
 
+def run_bwd(args):
+    """Backward path: one ``ssd_bwd`` per step at the workload's shape (dy and
+    dfinal seeded, all gradients written).  Prints its own JSON line; the
+    roofline counts the backward's public I/O once (inputs x, dt, B, C, dy,
+    dfinal, h0, z; outputs dx, ddt, dB, dC, dh0, dz)."""
+    import mamba_ssd_chunked_fwd_gb300 as ssd
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    w = ssd_inputs.WORKLOADS[args.workload]
+    if args.batch:
+        w = w.with_(B=args.batch)
+    inp = ssd_inputs.make(w)
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    gen = torch.Generator().manual_seed(w.seed + 300)
+    dy = torch.randn(inp["x"].shape, generator=gen).to(inp["x"].dtype).to(dev)
+    dfinal = torch.randn((w.B, w.H, w.P, w.N), generator=gen).to(dev)
+    f32 = dict(device=dev, dtype=torch.float32)
+    g = {"dx": torch.empty_like(d["x"]), "ddt": torch.empty((w.B, w.L, w.H), **f32), "dA": torch.empty(w.H, **f32),
+         "dB": torch.empty_like(d["B"]), "dC": torch.empty_like(d["C"]), "dh0": torch.empty((w.B, w.H, w.P, w.N), **f32),
+         "dD": torch.empty(w.H, **f32) if d["D"] is not None else None,
+         "dz": torch.empty_like(d["z"]) if d["z"] is not None else None,
+         "ddt_bias": torch.empty(w.H, **f32) if d["dt_bias"] is not None else None}
+    a = ssd.SsdBwdArgs()
+    a.fwd = ssd.make_args(d["x"], d["dt"], d["A"], d["B"], d["C"], w.chunk, D=d["D"], z=d["z"], dt_bias=d["dt_bias"],
+                          initial_states=d["initial_states"], dt_softplus=w.dt_softplus)
+    a.dy, a.dfinal = dy.data_ptr(), dfinal.data_ptr()
+    for k in ("dx", "ddt", "dA", "dB", "dC", "dh0", "dD", "dz", "ddt_bias"):
+        setattr(a, k, None if g[k] is None else g[k].data_ptr())
+    nws = ssd.ssd_bwd_workspace_size(a)
+    ws = torch.empty(nws, dtype=torch.uint8, device=dev)
+    a.workspace, a.workspace_bytes = ws.data_ptr(), nws
+    sh = ssd._stream_handle(dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        ssd.ssd_bwd(a, sh)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(dev.index, enabled=not args.no_clocks) as clk:
+        torch.cuda.synchronize(dev)
+        for i in range(args.steps):
+            starts[i].record(stream)
+            ssd.ssd_bwd(a, sh)
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+    ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / args.steps
+    ab = algorithmic_bytes(w)
+    nbytes = (2 * (ab["x"] + ab["B"] + ab["C"] + ab["dt"] + ab["z"]) + ab["x"]  # inputs and gradients, dy
+              + 2 * w.B * w.H * w.P * w.N * 4 + ab["h0"])                           # dfinal, dh0, h0
+    hbm, peak_kind = peaks()
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    line = {
+        "metric": f"SSD backward tokens/s ({args.workload} {w.shape_tuple()})",
+        "value": round(w.tokens / (ms * 1e-3), 1), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded, pages' distributions)",
+        "config": {"workload": f"backward, {args.workload} {w.shape_tuple()} [B,L,H,P,N,chunk,G]",
+                   "workspace_gb": round(nws / 1e9, 2)},
+        "roofline": {"bound": "hbm", "kernel": "whole backward (8 launches)", "achieved": round(achieved, 1),
+                     "peak": hbm, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                     "traffic": None, "alg_bytes_per_launch": nbytes, "launch_ms": round(ms, 4)},
+        "clocks": clk.summary(),
+        "gpu_launches": 11 * args.steps,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def stage_timing(ssd, a, w, dev, sh, stream, args, kernels):
     """Time the four chunked-plan kernels one by one (events between launches)
     and return the dominant one with its algorithmic bytes, plus every stage's
@@ -582,7 +648,7 @@ def main():
     ap.add_argument("--no-clocks", action="store_true", help="skip the nvidia-smi clock sampler")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch size (a smaller case of the same shape)")
-    ap.add_argument("--path", choices=["forward", "decode", "varlen"], default="forward",
+    ap.add_argument("--path", choices=["forward", "decode", "varlen", "bwd"], default="forward",
                     help="forward (default): the whole SSD forward; decode: one decode step per "
                          "sequence from a carried state; varlen: the forward over packed sequences "
                          "of random lengths")
@@ -599,6 +665,9 @@ def main():
         return
     if args.path == "varlen":
         run_varlen(args)
+        return
+    if args.path == "bwd":
+        run_bwd(args)
         return
     run_gpu(args)
 

@@ -238,6 +238,47 @@ typedef struct {
 ssd_status ssd_decode_step(const ssd_decode_args *args, void *stream);
 
 /*
+ * Backward of the forward: gradients of L = sum(dy * y) + sum(dfinal *
+ * final_state) with respect to x, dt, A, B, C, D, z, dt_bias and the initial
+ * state (the SSD backward of the "Mamba-2 SSD for Ascend NPU" README,
+ * "Limitations and roadmap").  Chunked like the forward: the chunk states
+ * are recomputed by its first three steps, the adjoint state is passed
+ * backwards between chunks, and one kernel per (batch, head, chunk) forms the
+ * local gradients; all arithmetic is fp32 on the CUDA cores (args.fwd.ops
+ * and .plan are ignored).  Needs chunk <= 64, P <= 64, N <= 64.
+ *   fwd        the forward's arguments: shapes, dtypes, x, dt, A, Bm, Cm and
+ *              the optional D, z, dt_bias, initial_state, dt_softplus,
+ *              dt_limit (y, final_state, workspace of fwd are ignored)
+ *   dy         [B,L,H,P] x_dtype          dfinal  [B,H,P,N] fp32 or NULL
+ *   dx         [B,L,H,P] x_dtype          ddt     [B,L,H] fp32 (raw dt)
+ *   dB, dC     [B,L,G,N] x_dtype          dA      [H] fp32
+ *   dD         [H] fp32, required with D  dz      [B,L,H,P] x_dtype, required with z
+ *   ddt_bias   [H] fp32, required with dt_bias
+ *   dh0        [B,H,P,N] fp32 or NULL
+ *   workspace  device, 256-byte aligned, ssd_bwd_workspace_size() bytes
+ * Every sum runs in a fixed order: bitwise reproducible.  Enqueue only.
+ */
+typedef struct {
+    ssd_fwd_args fwd;
+    const void *dy;
+    const float *dfinal;
+    void *dx;
+    float *ddt;
+    float *dA;
+    void *dB;
+    void *dC;
+    float *dD;
+    void *dz;
+    float *ddt_bias;
+    float *dh0;
+    void *workspace;
+    size_t workspace_bytes;
+} ssd_bwd_args;
+
+ssd_status ssd_bwd_workspace_size(const ssd_bwd_args *args, size_t *bytes);
+ssd_status ssd_bwd(const ssd_bwd_args *args, void *stream);
+
+/*
  * Packed variable-length sequences ("varlen"): nseq sequences of different
  * lengths stored back to back along L of a B = 1 call, sequence s holding
  * tokens [cu_seqlens[s], cu_seqlens[s+1]).  Each sequence is an independent

@@ -31,7 +31,7 @@ __all__ = [
     "ssd_chunk_scan", "ssd_fwd_host", "ssd_fwd_host_workspace_size", "ssd_check_device_error",
     "mamba2_ssd_fwd", "SsdDecodeArgs", "make_decode_args", "ssd_decode_step", "mamba2_ssd_decode",
     "ssd_segment_log_decay", "ssd_state_fold", "ssd_fwd_varlen", "ssd_fwd_varlen_workspace_size",
-    "mamba2_ssd_fwd_varlen",
+    "mamba2_ssd_fwd_varlen", "SsdBwdArgs", "ssd_bwd", "ssd_bwd_workspace_size", "mamba2_ssd_bwd",
 ]
 
 SSD_F32, SSD_F16, SSD_BF16 = 0, 1, 2
@@ -82,6 +82,16 @@ class SsdDecodeArgs(ctypes.Structure):
     ]
 
 
+class SsdBwdArgs(ctypes.Structure):
+    """Mirror of ``ssd_bwd_args`` in include/ssd.h."""
+    _fields_ = [
+        ("fwd", SsdFwdArgs), ("dy", ctypes.c_void_p), ("dfinal", ctypes.c_void_p), ("dx", ctypes.c_void_p),
+        ("ddt", ctypes.c_void_p), ("dA", ctypes.c_void_p), ("dB", ctypes.c_void_p), ("dC", ctypes.c_void_p),
+        ("dD", ctypes.c_void_p), ("dz", ctypes.c_void_p), ("ddt_bias", ctypes.c_void_p), ("dh0", ctypes.c_void_p),
+        ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+    ]
+
+
 _lock = threading.Lock()
 _lib = None
 
@@ -103,6 +113,8 @@ _SIGS = {
     "ssd_decode_step": [ctypes.POINTER(SsdDecodeArgs), ctypes.c_void_p],
     "ssd_segment_log_decay": [_P, ctypes.c_void_p, ctypes.c_void_p],
     "ssd_fwd_varlen_workspace_size": [_P, ctypes.c_void_p, ctypes.c_int64, ctypes.POINTER(ctypes.c_size_t)],
+    "ssd_bwd_workspace_size": [ctypes.POINTER(SsdBwdArgs), ctypes.POINTER(ctypes.c_size_t)],
+    "ssd_bwd": [ctypes.POINTER(SsdBwdArgs), ctypes.c_void_p],
     "ssd_fwd_varlen": [_P, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p],
     "ssd_state_fold": [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p],
@@ -399,3 +411,51 @@ def mamba2_ssd_fwd_varlen(x, dt, A, B, C, chunk_size, cu_seqlens, dt_softplus=Fa
     args.workspace, args.workspace_bytes = ws.data_ptr(), ws.numel()
     ssd_fwd_varlen(args, cu, _stream_handle(x.device))
     return (y, fin) if return_final_state else y
+
+
+# ---- backward ------------------------------------------------------------------
+
+def ssd_bwd_workspace_size(args: SsdBwdArgs) -> int:
+    out = ctypes.c_size_t(0)
+    _check(load_library().ssd_bwd_workspace_size(ctypes.byref(args), ctypes.byref(out)), "ssd_bwd_workspace_size")
+    return int(out.value)
+
+
+def ssd_bwd(args: SsdBwdArgs, stream=None):
+    s = stream if stream is not None else _stream_handle()
+    _check(load_library().ssd_bwd(ctypes.byref(args), s), "ssd_bwd")
+
+
+def mamba2_ssd_bwd(x, dt, A, B, C, chunk_size, dy, dt_softplus=False, *, dfinal=None, D=None, z=None,
+                   dt_bias=None, dt_limit=(0.0, math.inf), initial_states=None, want_dh0=True):
+    """Gradients of sum(dy * y) + sum(dfinal * final_state) of the forward with
+    these inputs, on the GPU.  Returns a dict: dx, ddt, dA, dB, dC and, when
+    the matching input is given, dD, dz, ddt_bias, plus dh0 (if want_dh0).
+    Tensors as for mamba2_ssd_fwd; dy like x, dfinal [B,H,P,N] fp32.  All
+    compute runs in libssd_gb300.so on the current stream."""
+    if not x.is_cuda:
+        raise ValueError("mamba2_ssd_bwd takes CUDA tensors")
+    Bb, L, H, P = x.shape
+    N = B.shape[3]
+    f32 = dict(device=x.device, dtype=torch.float32)
+    g = {"dx": torch.empty_like(x), "ddt": torch.empty((Bb, L, H), **f32), "dA": torch.empty((H,), **f32),
+         "dB": torch.empty_like(B), "dC": torch.empty_like(C)}
+    if D is not None:
+        g["dD"] = torch.empty((H,), **f32)
+    if z is not None:
+        g["dz"] = torch.empty_like(z)
+    if dt_bias is not None:
+        g["ddt_bias"] = torch.empty((H,), **f32)
+    if want_dh0:
+        g["dh0"] = torch.empty((Bb, H, P, N), **f32)
+    a = SsdBwdArgs()
+    a.fwd = make_args(x, dt, A, B, C, chunk_size, D=D, z=z, dt_bias=dt_bias, initial_states=initial_states,
+                      dt_softplus=dt_softplus, dt_limit=dt_limit)
+    a.dy, a.dfinal = _ptr(dy), _ptr(dfinal)
+    a.dx, a.ddt, a.dA, a.dB, a.dC = (_ptr(g[k]) for k in ("dx", "ddt", "dA", "dB", "dC"))
+    a.dD, a.dz, a.ddt_bias, a.dh0 = (_ptr(g.get(k)) for k in ("dD", "dz", "ddt_bias", "dh0"))
+    nbytes = ssd_bwd_workspace_size(a)
+    ws = torch.empty(max(nbytes, 256), device=x.device, dtype=torch.uint8)
+    a.workspace, a.workspace_bytes = ws.data_ptr(), ws.numel()
+    ssd_bwd(a, _stream_handle(x.device))
+    return g

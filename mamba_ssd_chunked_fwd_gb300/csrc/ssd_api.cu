@@ -225,6 +225,53 @@ size_t varlen_workspace(const ssd_fwd_args *a, int64_t nseq, int64_t max_len) {
     return chunked_layout(&o).total;
 }
 
+struct BwdLayout {
+    size_t dtp, cs, states, adj, dyp, ypre, dBh, dCh, partA, partD, partBias, total;
+};
+
+BwdLayout bwd_layout(const ssd_fwd_args *a) {
+    const size_t c = (size_t)((a->L + a->chunk - 1) / a->chunk);
+    const size_t vec = (size_t)a->B * a->H * c * a->chunk * 4;
+    const size_t st = (size_t)a->B * c * a->H * a->P * a->N * 4;
+    const size_t tok = (size_t)a->B * a->L * a->H * a->P;
+    const size_t tokn = (size_t)a->B * a->L * a->H * a->N * 4;
+    const size_t part = (size_t)a->B * c * a->H * 4;
+    BwdLayout l;
+    size_t o = kAlign;  // the error word (unused by the backward; kept for the forward steps)
+    l.dtp = o; o += align_up(vec);
+    l.cs = o; o += align_up(vec);
+    l.states = o; o += align_up(st);
+    l.adj = o; o += align_up(st);
+    l.dyp = o; o += align_up(tok * 4);
+    l.ypre = o; o += a->z ? align_up(tok * io_size(a->x_dtype)) : 0;
+    l.dBh = o; o += align_up(tokn);
+    l.dCh = o; o += align_up(tokn);
+    l.partA = o; o += align_up(part);
+    l.partD = o; o += align_up(part);
+    l.partBias = o; o += align_up(part);
+    l.total = o;
+    return l;
+}
+
+ssd_status check_bwd(const ssd_bwd_args *b) {
+    if (!b) return fail(SSD_ERR_INVALID_ARG, "args is NULL");
+    const ssd_fwd_args *a = &b->fwd;
+    ssd_status st = check_shape(a);
+    if (st != SSD_OK) return st;
+    if (a->chunk > 64 || a->P > 64 || a->N > 64)
+        return fail(SSD_ERR_UNSUPPORTED, "the backward needs chunk, P, N <= 64 (chunk=%lld P=%lld N=%lld)",
+                    (long long)a->chunk, (long long)a->P, (long long)a->N);
+    if ((st = check_pointers(a, false)) != SSD_OK) return st;
+    if (!b->dy || !b->dx || !b->ddt || !b->dA || !b->dB || !b->dC)
+        return fail(SSD_ERR_INVALID_ARG, "dy, dx, ddt, dA, dB and dC are required");
+    if (a->D && !b->dD) return fail(SSD_ERR_INVALID_ARG, "dD is required when D is given");
+    if (a->z && !b->dz) return fail(SSD_ERR_INVALID_ARG, "dz is required when z is given");
+    if (a->dt_bias && !b->ddt_bias) return fail(SSD_ERR_INVALID_ARG, "ddt_bias is required when dt_bias is given");
+    if ((b->dfinal && !aligned(b->dfinal, 16)) || (b->dh0 && !aligned(b->dh0, 16)))
+        return fail(SSD_ERR_INVALID_ARG, "dfinal and dh0 must be 16-byte aligned");
+    return SSD_OK;
+}
+
 }  // namespace
 
 ssd_status ssd::report_error(ssd_status st, const char *msg) { return fail(st, "%s", msg); }
@@ -345,6 +392,62 @@ ssd_status ssd_fwd_varlen(const ssd_fwd_args *a, const int64_t *cu, int64_t nseq
         }
         if ((st = run_chunked(&o, s)) != SSD_OK) return st;
     }
+    return ok();
+}
+
+ssd_status ssd_bwd_workspace_size(const ssd_bwd_args *b, size_t *bytes) {
+    ssd_status st = check_bwd(b);
+    if (st != SSD_OK) return st;
+    if (!bytes) return fail(SSD_ERR_INVALID_ARG, "bytes is NULL");
+    *bytes = bwd_layout(&b->fwd).total;
+    return ok();
+}
+
+ssd_status ssd_bwd(const ssd_bwd_args *b, void *stream) {
+    ssd_status st = check_bwd(b);
+    if (st != SSD_OK) return st;
+    const ssd_fwd_args *a = &b->fwd;
+    const BwdLayout l = bwd_layout(a);
+    if (!b->workspace || b->workspace_bytes < l.total)
+        return fail(SSD_ERR_WORKSPACE, "workspace of %zu bytes required (%zu given)", l.total,
+                    b->workspace ? b->workspace_bytes : (size_t)0);
+    if (!aligned(b->workspace, kAlign)) return fail(SSD_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char *ws = static_cast<char *>(b->workspace);
+    ssd::Params p = make_params(a);
+    p.y = nullptr;
+    p.final_state = nullptr;
+    float *dtp = reinterpret_cast<float *>(ws + l.dtp), *cs = reinterpret_cast<float *>(ws + l.cs);
+    float *states = reinterpret_cast<float *>(ws + l.states);
+    // the forward's steps 1-3 (fp32 kernels): states entering every chunk
+    cudaError_t e;
+    if ((e = ssd::launch_chunk_cumsum(p, dtp, cs, s)) != cudaSuccess) return cuda_fail(e, "chunk_cumsum");
+    if ((e = ssd::launch_chunk_state(p, a->x_dtype, dtp, cs, states, s)) != cudaSuccess)
+        return cuda_fail(e, "chunk_state");
+    if ((e = ssd::launch_state_passing(p, cs, states, s)) != cudaSuccess) return cuda_fail(e, "state_passing");
+    void *ypre = nullptr;
+    if (a->z) {  // y before the gate, for dz
+        ypre = ws + l.ypre;
+        ssd::Params q = p;
+        q.z = nullptr;
+        q.y = ypre;
+        if ((e = ssd::launch_chunk_scan(q, a->x_dtype, dtp, cs, states, s)) != cudaSuccess)
+            return cuda_fail(e, "chunk_scan");
+    }
+    ssd::BwdBuffers w;
+    w.dtp = dtp; w.cs = cs; w.states = states;
+    w.adj = reinterpret_cast<float *>(ws + l.adj);
+    w.dy = b->dy; w.ypre = ypre;
+    w.dyp = reinterpret_cast<float *>(ws + l.dyp);
+    w.dfinal = b->dfinal;
+    w.dx = b->dx; w.dz = b->dz; w.dB = b->dB; w.dC = b->dC;
+    w.ddt = b->ddt; w.dA = b->dA; w.dD = b->dD; w.dbias = b->ddt_bias; w.dh0 = b->dh0;
+    w.dBh = reinterpret_cast<float *>(ws + l.dBh);
+    w.dCh = reinterpret_cast<float *>(ws + l.dCh);
+    w.partA = reinterpret_cast<float *>(ws + l.partA);
+    w.partD = reinterpret_cast<float *>(ws + l.partD);
+    w.partBias = reinterpret_cast<float *>(ws + l.partBias);
+    if ((e = ssd::launch_bwd(p, a->x_dtype, w, s)) != cudaSuccess) return cuda_fail(e, "backward");
     return ok();
 }
 

@@ -113,6 +113,23 @@ struct DecodeParams {
 };
 cudaError_t launch_decode_step(const DecodeParams &p, int io, cudaStream_t s);
 
+// The backward (bwd.cu): buffers of one call (device pointers).
+struct BwdBuffers {
+    const float *dtp, *cs;      // [B,H,c,Q] from the forward's chunk_cumsum
+    const float *states;        // [B,c,H,P,N] states entering each chunk
+    float *adj;                 // [B,c,H,P,N] scratch: adjoint at each chunk's end
+    const void *dy;             // [B,L,H,P] public dtype
+    const void *ypre;           // [B,L,H,P] y before the gate (only with z)
+    float *dyp;                 // [B,L,H,P] scratch: dy after the gate
+    const float *dfinal;        // [B,H,P,N] or NULL
+    void *dx, *dz, *dB, *dC;    // outputs in the public dtype (dz only with z)
+    float *ddt, *dA, *dD, *dbias, *dh0;  // outputs (dD, dbias, dh0 may be NULL)
+    float *dBh, *dCh;           // [B,L,H,N] scratch: per-head dB, dC
+    float *partA, *partD, *partBias;     // [B,c,H] scratch
+};
+size_t bwd_chunk_smem_bytes();
+cudaError_t launch_bwd(const Params &p, int io, const BwdBuffers &w, cudaStream_t s);
+
 // The sequence-parallel exchange (seqpar.cu).
 cudaError_t launch_segment_log_decay(const Params &p, float *out, cudaStream_t s);
 cudaError_t launch_state_fold(int nseg, long long bh_count, int pn, const float *log_decay, const float *states,
