@@ -49,13 +49,39 @@ __global__ void bwd_gate_kernel(Params p, const void *dy, const void *ypre, floa
     st_io<IO>(dz, e, g * ld_io<IO>(ypre, e) * sg * (1.f + zv * (1.f - sg)));
 }
 
+// 16 outputs per thread as a 4 x 4 register tile of a 64 x 64 result: rows
+// r0 + 16 a, columns c0 + 16 b (r0 = tid / 16, c0 = tid % 16), so that a warp's
+// loads of one operand are broadcast and of the other conflict-free (rows of
+// 65 floats).  acc[a][b] += sum_k A(r, k) * B(c, k) over k < K.
+template <class FA, class FB>
+__device__ __forceinline__ void tile4x4(float (&acc)[4][4], int K, int r0, int c0, FA fa, FB fb) {
+    for (int k = 0; k < K; ++k) {
+        float av[4], bv[4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) av[a] = fa(r0 + 16 * a, k);
+#pragma unroll
+        for (int b = 0; b < 4; ++b) bv[b] = fb(c0 + 16 * b, k);
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(av[a], bv[b], acc[a][b]);
+    }
+}
+
+__device__ __forceinline__ void zero4x4(float (&acc)[4][4]) {
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
+}
+
 // ---- per chunk: sum_i exp(cs_i) dyp_i (outer) C_i  [P,N] ----
 template <int IO>
 __global__ void __launch_bounds__(kThreads)
 bwd_chunk_adjoint_kernel(Params p, const float *__restrict__ cs, const float *__restrict__ dyp,
                          float *__restrict__ adj) {
-    __shared__ float ds[kMax][kMax];
-    __shared__ float cc[kMax][kMax];
+    __shared__ float ds[kMax][kMax + 1];  // [i][p]
+    __shared__ float cc[kMax][kMax + 1];  // [i][n]
     const int k = blockIdx.y, bh = blockIdx.x;
     const int b = bh / p.H, h = bh % p.H, g = h / p.hpg;
     const int P = p.P, N = p.N, Q = p.Q, L = p.L;
@@ -69,35 +95,49 @@ bwd_chunk_adjoint_kernel(Params p, const float *__restrict__ cs, const float *__
         cc[i][n] = t < L ? ld_io<IO>(p.Cm, (((size_t)b * L + t) * p.G + g) * N + n) : 0.f;
     }
     __syncthreads();
+    const int r0 = threadIdx.x >> 4, c0 = threadIdx.x & 15;
+    float acc[4][4];
+    zero4x4(acc);
+    tile4x4(acc, Q, r0, c0, [&](int pp, int i) { return ds[i][pp]; }, [&](int n, int i) { return cc[i][n]; });
     float *out = adj + ((((size_t)b * p.nchunks + k) * p.H + h) * P) * N;
-    for (int e = threadIdx.x; e < P * N; e += kThreads) {
-        const int pp = e / N, n = e % N;
-        float acc = 0.f;
-        for (int i = 0; i < Q; ++i) acc = fmaf(ds[i][pp], cc[i][n], acc);
-        out[e] = acc;
-    }
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const int pp = r0 + 16 * a, n = c0 + 16 * c;
+            if (pp < P && n < N) out[(size_t)pp * N + n] = acc[a][c];
+        }
 }
 
 // ---- reverse state passing: adj[k] <- G_k (adjoint at the end of chunk k), dh0 ----
+// Four consecutive elements per thread; the next chunk's values are loaded
+// before the current ones are stored.
 __global__ void __launch_bounds__(kThreads)
 bwd_state_passing_kernel(Params p, const float *__restrict__ cs, const float *__restrict__ dfinal,
                          float *__restrict__ adj, float *__restrict__ dh0) {
     const int bh = blockIdx.x;
     const int b = bh / p.H, h = bh % p.H;
     const int PN = p.P * p.N;
-    const int e = blockIdx.y * kThreads + threadIdx.x;
+    const int e = (blockIdx.y * kThreads + threadIdx.x) * 4;
     if (e >= PN) return;
     const int c = p.nchunks;
     const size_t crow = ((size_t)b * p.H + h) * c;
     const size_t kstride = (size_t)p.H * PN;
     float *base = adj + (((size_t)b * c) * p.H + h) * PN + e;
-    float gsum = dfinal ? __ldg(dfinal + ((size_t)b * p.H + h) * PN + e) : 0.f;
+    float4 gs = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (dfinal) gs = __ldg(reinterpret_cast<const float4 *>(dfinal + ((size_t)b * p.H + h) * PN + e));
+    float4 nxt = *reinterpret_cast<const float4 *>(base + (size_t)(c - 1) * kstride);
     for (int k = c - 1; k >= 0; --k) {
-        const float loc = base[(size_t)k * kstride];
-        base[(size_t)k * kstride] = gsum;
-        gsum = fmaf(expf(__ldg(cs + (crow + k) * p.Q + p.Q - 1)), gsum, loc);
+        const float4 loc = nxt;
+        if (k > 0) nxt = *reinterpret_cast<const float4 *>(base + (size_t)(k - 1) * kstride);
+        *reinterpret_cast<float4 *>(base + (size_t)k * kstride) = gs;
+        const float a = expf(__ldg(cs + (crow + k) * p.Q + p.Q - 1));
+        gs.x = fmaf(a, gs.x, loc.x);
+        gs.y = fmaf(a, gs.y, loc.y);
+        gs.z = fmaf(a, gs.z, loc.z);
+        gs.w = fmaf(a, gs.w, loc.w);
     }
-    if (dh0) dh0[((size_t)b * p.H + h) * PN + e] = gsum;
+    if (dh0) *reinterpret_cast<float4 *>(dh0 + ((size_t)b * p.H + h) * PN + e) = gs;
 }
 
 // ---- within one chunk: dx, dB, dC (per head), ddt, and partial dA, dD, dbias ----
@@ -107,7 +147,7 @@ struct ChunkSmem {
     float CB[kMax][kMax + 1], DX[kMax][kMax + 1], V[kMax][kMax + 1];
     float T[kMax][kMax + 1];  // dxs, then S^T dyp
     float GB[kMax][kMax + 1];
-    float cs[kMax], d[kMax], ecs[kMax], el[kMax], dd1[kMax], w[kMax], z[kMax], dcs[kMax];
+    float cs[kMax], d[kMax], ecs[kMax], el[kMax], dd1[kMax], w[kMax], z[kMax], dcs[kMax], u[kMax];
     float red[kThreads];
 };
 
@@ -122,6 +162,7 @@ bwd_chunk_kernel(Params p, const float *__restrict__ dtp, const float *__restric
     const int k = blockIdx.y, bh = blockIdx.x;
     const int b = bh / p.H, h = bh % p.H, g = h / p.hpg;
     const int P = p.P, N = p.N, Q = p.Q, L = p.L, tid = threadIdx.x;
+    const int r0 = tid >> 4, c0 = tid & 15;  // 4 x 4 tiles of 64 x 64 results
     const size_t crow = (((size_t)b * p.H + h) * p.nchunks + k) * Q;
     const size_t st_off = ((((size_t)b * p.nchunks + k) * p.H + h) * P) * N;
     const float A = __ldg(p.A + h);
@@ -129,8 +170,12 @@ bwd_chunk_kernel(Params p, const float *__restrict__ dtp, const float *__restric
 
     // (1) tiles; past L: x, dy, B, C = 0 and d = 0 (cs keeps its last value)
     for (int e = tid; e < Q; e += kThreads) {
+        const bool in = k * Q + e < L;
         sm.cs[e] = __ldg(cs + crow + e);
-        sm.d[e] = (k * Q + e < L) ? __ldg(dtp + crow + e) : 0.f;
+        sm.d[e] = in ? __ldg(dtp + crow + e) : 0.f;
+        float u = in ? __ldg(p.dt + ((size_t)b * L + k * Q + e) * p.H + h) : 0.f;
+        if (p.dt_bias) u += __ldg(p.dt_bias + h);
+        sm.u[e] = u;
     }
     for (int e = tid; e < Q * P; e += kThreads) {
         const int i = e / P, pp = e % P, t = k * Q + i;
@@ -154,43 +199,60 @@ bwd_chunk_kernel(Params p, const float *__restrict__ dtp, const float *__restric
         sm.ecs[e] = expf(sm.cs[e]);
         sm.el[e] = expf(cs_last - sm.cs[e]);
     }
-    // (2) CB = C B^T, DX = dyp x^T
-    for (int e = tid; e < Q * Q; e += kThreads) {
-        const int i = e / Q, j = e % Q;
-        float cb = 0.f, dxv = 0.f;
-        for (int n = 0; n < N; ++n) cb = fmaf(sm.C[i][n], sm.B[j][n], cb);
-        for (int pp = 0; pp < P; ++pp) dxv = fmaf(sm.dy[i][pp], sm.x[j][pp], dxv);
-        sm.CB[i][j] = cb;
-        sm.DX[i][j] = dxv;
+    // (2) CB = C B^T, DX = dyp x^T, then the masked decay: CB <- E CB, DX <- E DX,
+    //     V = E CB DX d_j  (rows i, columns j of 4 x 4 tiles; past Q: unused)
+    {
+        float cb[4][4], dxm[4][4];
+        zero4x4(cb);
+        zero4x4(dxm);
+        tile4x4(cb, N, r0, c0, [&](int i, int n) { return sm.C[i][n]; }, [&](int j, int n) { return sm.B[j][n]; });
+        tile4x4(dxm, P, r0, c0, [&](int i, int pp) { return sm.dy[i][pp]; },
+                [&](int j, int pp) { return sm.x[j][pp]; });
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int i = r0 + 16 * a, j = c0 + 16 * c;
+                if (i < Q && j < Q) {
+                    const float E = j <= i ? expf(sm.cs[i] - sm.cs[j]) : 0.f;
+                    const float a1 = E * cb[a][c];
+                    sm.V[i][j] = a1 * dxm[a][c] * sm.d[j];
+                    sm.CB[i][j] = a1;
+                    sm.DX[i][j] = E * dxm[a][c];
+                }
+            }
     }
     __syncthreads();
-    // (3) masked decay: CB <- E CB, DX <- E DX, V = E CB DX d_j
-    for (int e = tid; e < Q * Q; e += kThreads) {
-        const int i = e / Q, j = e % Q;
-        const float E = j <= i ? expf(sm.cs[i] - sm.cs[j]) : 0.f;
-        const float a1 = E * sm.CB[i][j], a2 = E * sm.DX[i][j];
-        sm.V[i][j] = a1 * sm.DX[i][j] * sm.d[j];
-        sm.CB[i][j] = a1;
-        sm.DX[i][j] = a2;
-    }
-    __syncthreads();
-    // (4) dxs = (E CB)^T dyp + el * (G B) ; GB = G B_t (per token)
-    for (int e = tid; e < Q * P; e += kThreads) {
-        const int t = e / P, pp = e % P;
-        float acc = 0.f, gb = 0.f;
-        for (int i = t; i < Q; ++i) acc = fmaf(sm.CB[i][t], sm.dy[i][pp], acc);
-        for (int n = 0; n < N; ++n) gb = fmaf(sm.Gm[pp][n], sm.B[t][n], gb);
-        sm.GB[t][pp] = gb;
-        sm.T[t][pp] = fmaf(sm.el[t], gb, acc);
-    }
-    // (5) dB_t = d_t ((E DX)^T C + el * G^T x_t)
-    for (int e = tid; e < Q * N; e += kThreads) {
-        const int t = e / N, n = e % N;
-        float acc = 0.f, gx = 0.f;
-        for (int i = t; i < Q; ++i) acc = fmaf(sm.DX[i][t], sm.C[i][n], acc);
-        for (int pp = 0; pp < P; ++pp) gx = fmaf(sm.Gm[pp][n], sm.x[t][pp], gx);
-        if (k * Q + t < L)
-            dBh[(((size_t)b * L + k * Q + t) * p.H + h) * N + n] = sm.d[t] * fmaf(sm.el[t], gx, acc);
+    // (4) T = dxs = (E CB)^T dyp + el (G B) ; GB = G B_t  (rows t, columns p)
+    // (5) dB_t = d_t ((E DX)^T C + el G^T x_t)  (rows t, columns n)
+    {
+        float acc[4][4], gb[4][4];
+        zero4x4(acc);
+        zero4x4(gb);
+        tile4x4(acc, Q, r0, c0, [&](int t, int i) { return sm.CB[i][t]; }, [&](int pp, int i) { return sm.dy[i][pp]; });
+        tile4x4(gb, N, r0, c0, [&](int t, int n) { return sm.B[t][n]; }, [&](int pp, int n) { return sm.Gm[pp][n]; });
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int t = r0 + 16 * a, pp = c0 + 16 * c;
+                if (t < Q && pp < P) {
+                    sm.GB[t][pp] = gb[a][c];
+                    sm.T[t][pp] = fmaf(sm.el[t], gb[a][c], acc[a][c]);
+                }
+            }
+        zero4x4(acc);
+        zero4x4(gb);
+        tile4x4(acc, Q, r0, c0, [&](int t, int i) { return sm.DX[i][t]; }, [&](int n, int i) { return sm.C[i][n]; });
+        tile4x4(gb, P, r0, c0, [&](int t, int pp) { return sm.x[t][pp]; }, [&](int n, int pp) { return sm.Gm[pp][n]; });
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int t = r0 + 16 * a, n = c0 + 16 * c;
+                if (t < Q && n < N && k * Q + t < L)
+                    dBh[(((size_t)b * L + k * Q + t) * p.H + h) * N + n] = sm.d[t] * fmaf(sm.el[t], gb[a][c], acc[a][c]);
+            }
     }
     __syncthreads();
     // dx, and per token dd1 = x . dxs, z = x . GB
@@ -210,14 +272,25 @@ bwd_chunk_kernel(Params p, const float *__restrict__ dtp, const float *__restric
         sm.z[tid] = zz;
     }
     __syncthreads();
-    // (6) dC_i = ecs_i (S^T dyp_i) + (E DX d) B ; T <- S^T dyp
-    for (int e = tid; e < Q * N; e += kThreads) {
-        const int i = e / N, n = e % N;
-        float sd = 0.f, acc = 0.f;
-        for (int pp = 0; pp < P; ++pp) sd = fmaf(sm.S[pp][n], sm.dy[i][pp], sd);
-        for (int j = 0; j <= i; ++j) acc = fmaf(sm.DX[i][j] * sm.d[j], sm.B[j][n], acc);
-        sm.T[i][n] = sd;
-        if (k * Q + i < L) dCh[(((size_t)b * L + k * Q + i) * p.H + h) * N + n] = fmaf(sm.ecs[i], sd, acc);
+    // (6) dC_i = ecs_i (S^T dyp_i) + (E DX d) B ; T <- S^T dyp  (rows i, columns n)
+    {
+        float sd[4][4], acc[4][4];
+        zero4x4(sd);
+        zero4x4(acc);
+        tile4x4(sd, P, r0, c0, [&](int i, int pp) { return sm.dy[i][pp]; }, [&](int n, int pp) { return sm.S[pp][n]; });
+        tile4x4(acc, Q, r0, c0, [&](int i, int j) { return sm.DX[i][j] * sm.d[j]; },
+                [&](int n, int j) { return sm.B[j][n]; });
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int i = r0 + 16 * a, n = c0 + 16 * c;
+                if (i < Q && n < N) {
+                    sm.T[i][n] = sd[a][c];
+                    if (k * Q + i < L)
+                        dCh[(((size_t)b * L + k * Q + i) * p.H + h) * N + n] = fmaf(sm.ecs[i], sd[a][c], acc[a][c]);
+                }
+            }
     }
     // <G, S> (fixed-order block reduction)
     {
@@ -231,7 +304,7 @@ bwd_chunk_kernel(Params p, const float *__restrict__ dtp, const float *__restric
         __syncthreads();
     }
     const float gs = sm.red[0];
-    // (7) u_i = C_i . T_i ; dcs
+    // (7) u_i = C_i . T_i ; dcs ; per-token raw-dt gradient factor
     if (tid < Q) {
         float uu = 0.f;
         for (int n = 0; n < N; ++n) uu = fmaf(sm.C[tid][n], sm.T[tid][n], uu);
@@ -241,35 +314,38 @@ bwd_chunk_kernel(Params p, const float *__restrict__ dtp, const float *__restric
         const float w = sm.el[tid] * sm.d[tid] * sm.z[tid];
         sm.w[tid] = w;
         sm.dcs[tid] = sm.ecs[tid] * uu + R - K - w;
+        // d(raw dt) / d(d): softplus' = sigmoid, 0 outside the clamp
+        const float u = sm.u[tid];
+        const float dpre = p.dt_softplus ? softplus_f(u) : u;
+        float f = (p.has_limit && (dpre < p.dt_min || dpre > p.dt_max)) ? 0.f : 1.f;
+        if (p.dt_softplus) f *= 1.f / (1.f + expf(-u));
+        sm.u[tid] = f;
     }
     __syncthreads();
     if (tid == 0) {
         float wsum = 0.f;
         for (int j = 0; j < Q; ++j) wsum += sm.w[j];
         sm.dcs[Q - 1] += expf(cs_last) * gs + wsum;
-        // reverse cumsum, dA, dD, dd, ddt, dbias (fixed order)
-        float run = 0.f, sA = 0.f, sD = 0.f, sBias = 0.f;
+        // reverse cumsum; dd, dA, dbias (fixed order)
+        float run = 0.f, sA = 0.f, sBias = 0.f, sD = 0.f;
         for (int t = Q - 1; t >= 0; --t) {
             run += sm.dcs[t];
-            if (k * Q + t >= L) continue;
-            sA = fmaf(sm.d[t], run, sA);
-            const float dd = fmaf(A, run, sm.dd1[t]);
-            float u = __ldg(p.dt + ((size_t)b * L + k * Q + t) * p.H + h);
-            if (p.dt_bias) u += __ldg(p.dt_bias + h);
-            float dpre = p.dt_softplus ? softplus_f(u) : u;
-            float gr = dd;
-            if (p.has_limit && (dpre < p.dt_min || dpre > p.dt_max)) gr = 0.f;
-            if (p.dt_softplus) gr *= 1.f / (1.f + expf(-u));
-            ddt[((size_t)b * L + k * Q + t) * p.H + h] = gr;
-            sBias += gr;
+            sm.dcs[t] = run;
         }
-        for (int t = 0; t < Q; ++t)
-            for (int pp = 0; pp < P; ++pp) sD = fmaf(sm.dy[t][pp], sm.x[t][pp], sD);
+        for (int t = 0; t < Q; ++t) {
+            sD += sm.DX[t][t];  // E = 1 on the diagonal: dyp_t . x_t
+            if (k * Q + t >= L) continue;
+            sA = fmaf(sm.d[t], sm.dcs[t], sA);
+            sBias = fmaf(fmaf(A, sm.dcs[t], sm.dd1[t]), sm.u[t], sBias);
+        }
         const size_t pi = ((size_t)b * p.nchunks + k) * p.H + h;
         partA[pi] = sA;
         partD[pi] = sD;
         partBias[pi] = sBias;
     }
+    __syncthreads();
+    for (int t = tid; t < Q; t += kThreads)
+        if (k * Q + t < L) ddt[((size_t)b * L + k * Q + t) * p.H + h] = fmaf(A, sm.dcs[t], sm.dd1[t]) * sm.u[t];
 }
 
 // ---- dB, dC: heads of a group summed; dA, dD, dbias: (batch, chunk) summed ----
@@ -321,8 +397,8 @@ cudaError_t launch_bwd(const Params &p, int io, const BwdBuffers &w, cudaStream_
         case IO_F16: bwd_chunk_adjoint_kernel<IO_F16><<<grid, kThreads, 0, s>>>(p, w.cs, w.dyp, w.adj); break;
         case IO_BF16: bwd_chunk_adjoint_kernel<IO_BF16><<<grid, kThreads, 0, s>>>(p, w.cs, w.dyp, w.adj); break;
     }
-    const int PN = p.P * p.N;
-    bwd_state_passing_kernel<<<dim3(p.B * p.H, (PN + kThreads - 1) / kThreads), kThreads, 0, s>>>(
+    const int PN = p.P * p.N;  // a multiple of 256: P, N are multiples of 16
+    bwd_state_passing_kernel<<<dim3(p.B * p.H, (PN / 4 + kThreads - 1) / kThreads), kThreads, 0, s>>>(
         p, w.cs, w.dfinal, w.adj, w.dh0);
     const int smem = (int)sizeof(ChunkSmem);
     cudaError_t e;
