@@ -302,6 +302,43 @@ def decode_step(x, dt, A, B, C, state, *, D=None, z=None, dt_bias=None, dt_softp
     return y[:, 0], fin
 
 
+def causal_conv1d(x, w, bias=None, *, silu=True):
+    """Depthwise causal convolution along the sequence, then SiLU
+    (ops-transformer MambaV2 article, sections 1.4 and 4.1: kernel width 4,
+    bias, SiLU; the reference there is a grouped convolution with W-1 zeros of
+    left padding, truncated to the first S steps).  x [B,D,S], w [D,W],
+    bias [D]:  out[b,d,t] = silu(bias[d] + sum_k w[d,k] x[b,d,t-(W-1)+k]),
+    x = 0 before the first step.  float64; written out term by term."""
+    x = np.asarray(x, dtype=np.float64)
+    w = np.asarray(w, dtype=np.float64)
+    Bb, D, S = x.shape
+    W = w.shape[1]
+    out = np.zeros((Bb, D, S))
+    for k in range(W):
+        shift = W - 1 - k  # tap k reads the input `shift` steps back
+        out[:, :, shift:] += w[None, :, k, None] * x[:, :, :S - shift]
+    if bias is not None:
+        out += np.asarray(bias, dtype=np.float64)[None, :, None]
+    if silu:
+        out = out / (1.0 + np.exp(-out))
+    return out
+
+
+def gated_rmsnorm(x, z, w, groups, eps):
+    """Gated, grouped RMSNorm (ops-transformer MambaV2 article, section 4.6):
+    v = x * silu(z), normalised by the root mean square of v over each of the
+    `groups` runs of D/groups consecutive channels (plus eps inside the root),
+    times w.  x, z [..., D], w [D].  float64."""
+    x = np.asarray(x, dtype=np.float64)
+    z = np.asarray(z, dtype=np.float64)
+    w = np.asarray(w, dtype=np.float64)
+    D = x.shape[-1]
+    v = x * (z / (1.0 + np.exp(-z)))
+    vg = v.reshape(v.shape[:-1] + (groups, D // groups))
+    r = np.sqrt(np.mean(vg * vg, axis=-1, keepdims=True) + eps)
+    return (vg / r).reshape(v.shape) * w
+
+
 def compare(got, ref):
     """Global error metrics in float64: rel-L2, max|diff|/max|ref|, max|diff|."""
     g = np.asarray(got, dtype=np.float64)

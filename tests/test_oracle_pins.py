@@ -450,3 +450,54 @@ def test_backward_matches_central_differences(oracle_mod, case):
         d = np.logaddexp(0.0, t["dt"].astype(np.float64))
         outside = (d < 0.3) | (d > 1.2)
         assert outside.any() and np.all(g["ddt"][outside] == 0.0)
+
+
+# ---- the SSD's neighbours: causal conv1d + SiLU, gated RMSNorm -------------------
+
+def test_causal_conv1d_matches_numpy_convolve(oracle_mod):
+    """Each channel is numpy's full convolution with the reversed taps, first S
+    outputs (the causal part), plus bias, through SiLU."""
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((2, 5, 17))
+    w = rng.standard_normal((5, 4))
+    bias = rng.standard_normal(5)
+    out = oracle_mod.causal_conv1d(x, w, bias)
+    for b in range(2):
+        for d in range(5):
+            full = np.convolve(x[b, d], w[d][::-1])[:17] + bias[d]
+            ref = full / (1.0 + np.exp(-full))
+            assert np.allclose(out[b, d], ref, rtol=1e-13, atol=1e-13)
+
+
+def test_causal_conv1d_impulse_and_causality(oracle_mod):
+    """A unit impulse at step 3 reproduces the taps (in order) from step 3 on
+    and nothing before it; no bias, no SiLU."""
+    x = np.zeros((1, 2, 12))
+    x[0, :, 3] = 1.0
+    w = np.array([[1.0, 2.0, 3.0, 4.0], [0.5, -1.0, 0.0, 2.0]])
+    out = oracle_mod.causal_conv1d(x, w, silu=False)
+    assert np.all(out[0, :, :3] == 0.0)
+    assert np.allclose(out[0, 0, 3:7], [4.0, 3.0, 2.0, 1.0]) and np.allclose(out[0, 1, 3:7], [2.0, 0.0, -1.0, 0.5])
+    assert np.all(out[0, :, 7:] == 0.0)
+
+
+def test_gated_rmsnorm_closed_forms(oracle_mod):
+    """With the gate at z -> +inf (silu(z) ~ z, here z large so silu(z)/z = 1 to
+    1e-15) a group of equal values v normalises to sign(v) * w; scaling x
+    leaves the output unchanged when eps = 0; one group of D equals the plain
+    RMSNorm of the whole row."""
+    D, G = 12, 3
+    x = np.full((2, D), -2.5)
+    z = np.full((2, D), 40.0)
+    w = np.linspace(0.5, 2.0, D)
+    out = oracle_mod.gated_rmsnorm(x, z, w, G, 0.0)
+    assert np.allclose(out, -w[None, :], rtol=1e-12)
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal((3, D))
+    z = rng.standard_normal((3, D))
+    a = oracle_mod.gated_rmsnorm(x, z, w, G, 0.0)
+    b = oracle_mod.gated_rmsnorm(7.0 * x, z, w, G, 0.0)
+    assert np.allclose(a, b, rtol=1e-12)
+    v = x * z / (1.0 + np.exp(-z))
+    one = v / np.sqrt(np.mean(v * v, axis=-1, keepdims=True) + 1e-5) * w
+    assert np.allclose(oracle_mod.gated_rmsnorm(x, z, w, 1, 1e-5), one, rtol=1e-12)
