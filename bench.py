@@ -505,6 +505,72 @@ def run_bwd(args):
     print(json.dumps(line), flush=True)
 
 
+def run_neighbor(args):
+    """The SSD's neighbours, each timed alone (L2 flushed before every step):
+    conv1d at the pages' test shape (B 1, D 10240, S 1024, W 4, fp32, bias,
+    SiLU); gated RMSNorm at the y of the workload ([B, L, H*P], G groups, fp32).
+    Prints its own JSON line."""
+    import mamba_ssd_chunked_fwd_gb300 as ssd
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    g = torch.Generator().manual_seed(17)
+    w = ssd_inputs.WORKLOADS[args.workload]
+    if args.path == "conv1d":
+        B, D, S, W = 1, 10240, 1024, 4
+        x = torch.randn((B, D, S), generator=g).to(dev)
+        wt = (torch.randn((D, W), generator=g) * 0.5).to(dev)
+        bias = torch.randn(D, generator=g).to(dev)
+        out = torch.empty_like(x)
+        call = lambda sh: ssd.ssd_causal_conv1d(x, wt, bias, out, True, sh)
+        nbytes = 2 * x.numel() * 4 + wt.numel() * 4 + D * 4
+        name, cfg = "causal_conv1d_kernel", f"conv1d [B,D,S,W] = [{B},{D},{S},{W}] fp32, bias, SiLU"
+        units = B * S
+    else:
+        B, L, D, G = w.B, w.L, w.H * w.P, w.G
+        x = torch.randn((B, L, D), generator=g).to(dev)
+        z = torch.randn((B, L, D), generator=g).to(dev)
+        wn = (torch.rand(D, generator=g) + 0.5).to(dev)
+        out = torch.empty_like(x)
+        call = lambda sh: ssd.ssd_gated_rmsnorm(x, z, wn, G, 1e-5, out, sh)
+        nbytes = 3 * x.numel() * 4 + D * 4
+        name, cfg = "gated_rmsnorm_kernel", f"gated RMSNorm [B,L,D,G] = [{B},{L},{D},{G}] fp32"
+        units = B * L
+    sh = ssd._stream_handle(dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    sink = torch.zeros((), device=dev)
+    for _ in range(args.warmup):
+        call(sh)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(dev.index, enabled=not args.no_clocks) as clk:
+        torch.cuda.synchronize(dev)
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            sink += flush.sum()
+            starts[i].record(stream)
+            call(sh)
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+    per = sorted(s.elapsed_time(e) for s, e in zip(starts, ends))
+    ms = per[len(per) // 2]
+    hbm, peak_kind = peaks()
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    line = {
+        "metric": f"{args.path} tokens/s ({cfg})", "value": round(units / (ms * 1e-3), 1), "unit": "tokens/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded)",
+        "config": {"workload": cfg, "l2": "flushed before every timed step (256 MiB written, then read)",
+                   "timing": "median of per-step events"},
+        "roofline": {"bound": "hbm", "kernel": name, "achieved": round(achieved, 1), "peak": hbm,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": None,
+                     "alg_bytes_per_launch": nbytes, "launch_ms": round(ms, 5)},
+        "clocks": clk.summary(), "gpu_launches": args.steps,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def stage_timing(ssd, a, w, dev, sh, stream, args, kernels):
     """Time the four chunked-plan kernels one by one (events between launches)
     and return the dominant one with its algorithmic bytes, plus every stage's
@@ -648,7 +714,7 @@ def main():
     ap.add_argument("--no-clocks", action="store_true", help="skip the nvidia-smi clock sampler")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch size (a smaller case of the same shape)")
-    ap.add_argument("--path", choices=["forward", "decode", "varlen", "bwd"], default="forward",
+    ap.add_argument("--path", choices=["forward", "decode", "varlen", "bwd", "conv1d", "rmsnorm"], default="forward",
                     help="forward (default): the whole SSD forward; decode: one decode step per "
                          "sequence from a carried state; varlen: the forward over packed sequences "
                          "of random lengths")
@@ -668,6 +734,9 @@ def main():
         return
     if args.path == "bwd":
         run_bwd(args)
+        return
+    if args.path in ("conv1d", "rmsnorm"):
+        run_neighbor(args)
         return
     run_gpu(args)
 

@@ -324,6 +324,26 @@ ssd_status ssd_segment_log_decay(const ssd_fwd_args *args, float *log_decay, voi
 ssd_status ssd_state_fold(int64_t nseg, int64_t B, int64_t H, int64_t P, int64_t N, const float *log_decay,
                           const float *states, float *out, void *stream);
 
+/*
+ * The SSD's neighbours in the Mamba-2 block (ops-transformer MambaV2 article,
+ * sections 1.4, 4.1 and 4.6).  fp32 arithmetic; x, z and out share `dtype`
+ * (ssd_dtype); weights and biases are fp32.  Enqueue only.
+ *
+ * Causal conv1d + SiLU: a depthwise convolution of width W along the
+ * sequence, with W-1 zeros before the first step, plus bias, then SiLU:
+ *     out[b,d,t] = silu(bias[d] + sum_{k<W} w[d,k] x[b,d,t-(W-1)+k])
+ * x, out [B,D,S]; w [D,W]; bias [D] or NULL; 1 <= W <= 8; silu = 0 skips SiLU.
+ */
+ssd_status ssd_causal_conv1d(int64_t B, int64_t D, int64_t S, int64_t W, int32_t dtype, const void *x,
+                             const float *w, const float *bias, int32_t silu, void *out, void *stream);
+
+/* Gated grouped RMSNorm: v = x * silu(z), normalised by the root mean square
+ * of v over each of `groups` runs of D/groups consecutive channels (eps inside
+ * the root), times w:  out = v / sqrt(mean(v^2) + eps) * w.
+ * x, z, out [rows, D]; w [D]; D % groups == 0; eps >= 0. */
+ssd_status ssd_gated_rmsnorm(int64_t rows, int64_t D, int64_t groups, float eps, int32_t dtype, const void *x,
+                             const void *z, const float *w, void *out, void *stream);
+
 /* Synchronises `stream`, then reads the device error word the last ssd_fwd
  * on this workspace left behind (bounded waits that gave up set it).
  * Returns SSD_OK or SSD_ERR_TIMEOUT (or SSD_ERR_CUDA). */

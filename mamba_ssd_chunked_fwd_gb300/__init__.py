@@ -32,6 +32,7 @@ __all__ = [
     "mamba2_ssd_fwd", "SsdDecodeArgs", "make_decode_args", "ssd_decode_step", "mamba2_ssd_decode",
     "ssd_segment_log_decay", "ssd_state_fold", "ssd_fwd_varlen", "ssd_fwd_varlen_workspace_size",
     "mamba2_ssd_fwd_varlen", "SsdBwdArgs", "ssd_bwd", "ssd_bwd_workspace_size", "mamba2_ssd_bwd",
+    "ssd_causal_conv1d", "ssd_gated_rmsnorm", "causal_conv1d", "gated_rmsnorm",
 ]
 
 SSD_F32, SSD_F16, SSD_BF16 = 0, 1, 2
@@ -115,6 +116,11 @@ _SIGS = {
     "ssd_fwd_varlen_workspace_size": [_P, ctypes.c_void_p, ctypes.c_int64, ctypes.POINTER(ctypes.c_size_t)],
     "ssd_bwd_workspace_size": [ctypes.POINTER(SsdBwdArgs), ctypes.POINTER(ctypes.c_size_t)],
     "ssd_bwd": [ctypes.POINTER(SsdBwdArgs), ctypes.c_void_p],
+    "ssd_causal_conv1d": [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
+                          ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
+                          ctypes.c_void_p],
+    "ssd_gated_rmsnorm": [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_float, ctypes.c_int32,
+                          ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p],
     "ssd_fwd_varlen": [_P, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p],
     "ssd_state_fold": [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p],
@@ -459,3 +465,36 @@ def mamba2_ssd_bwd(x, dt, A, B, C, chunk_size, dy, dt_softplus=False, *, dfinal=
     a.workspace, a.workspace_bytes = ws.data_ptr(), ws.numel()
     ssd_bwd(a, _stream_handle(x.device))
     return g
+
+
+# ---- the SSD's neighbours ----------------------------------------------------------
+
+def ssd_causal_conv1d(x, w, bias, out, silu=True, stream=None):
+    """C entry: x, out [B,D,S]; w [D,W] fp32; bias [D] fp32 or None."""
+    Bb, D, S = x.shape
+    s = stream if stream is not None else _stream_handle()
+    _check(load_library().ssd_causal_conv1d(Bb, D, S, w.shape[1], _DTYPE_CODES[x.dtype], _ptr(x), _ptr(w),
+                                            _ptr(bias), 1 if silu else 0, _ptr(out), s), "ssd_causal_conv1d")
+
+
+def ssd_gated_rmsnorm(x, z, w, groups, eps, out, stream=None):
+    """C entry: x, z, out [..., D] (rows = the leading dims); w [D] fp32."""
+    D = x.shape[-1]
+    rows = x.numel() // D
+    s = stream if stream is not None else _stream_handle()
+    _check(load_library().ssd_gated_rmsnorm(rows, D, groups, float(eps), _DTYPE_CODES[x.dtype], _ptr(x), _ptr(z),
+                                            _ptr(w), _ptr(out), s), "ssd_gated_rmsnorm")
+
+
+def causal_conv1d(x, w, bias=None, silu=True):
+    """Depthwise causal conv1d (+ bias) then SiLU on the GPU; x [B,D,S]."""
+    out = torch.empty_like(x)
+    ssd_causal_conv1d(x, w, bias, out, silu, _stream_handle(x.device))
+    return out
+
+
+def gated_rmsnorm(x, z, w, groups, eps=1e-5):
+    """(x * silu(z)) normalised per group of D/groups channels, times w, on the GPU."""
+    out = torch.empty_like(x)
+    ssd_gated_rmsnorm(x, z, w, groups, eps, out, _stream_handle(x.device))
+    return out

@@ -451,6 +451,42 @@ ssd_status ssd_bwd(const ssd_bwd_args *b, void *stream) {
     return ok();
 }
 
+ssd_status ssd_causal_conv1d(int64_t B, int64_t D, int64_t S, int64_t W, int32_t dtype, const void *x,
+                             const float *w, const float *bias, int32_t silu, void *out, void *stream) {
+    if (B <= 0 || D <= 0 || S <= 0 || W <= 0)
+        return fail(SSD_ERR_INVALID_ARG, "B, D, S, W must be > 0 (B=%lld D=%lld S=%lld W=%lld)", (long long)B,
+                    (long long)D, (long long)S, (long long)W);
+    if (W > 8) return fail(SSD_ERR_UNSUPPORTED, "W must be <= 8 (got %lld)", (long long)W);
+    if (B > 65535 || D > 65535 || S > 0x7fffffffLL - 1024)
+        return fail(SSD_ERR_UNSUPPORTED, "B, D <= 65535 and S < 2^31 required");
+    if (dtype != SSD_F32 && dtype != SSD_F16 && dtype != SSD_BF16)
+        return fail(SSD_ERR_INVALID_ARG, "unknown dtype code %d", dtype);
+    if (!x || !w || !out) return fail(SSD_ERR_INVALID_ARG, "x, w and out are required");
+    cudaError_t e = ssd::launch_causal_conv1d((int)B, (int)D, (int)S, (int)W, dtype, x, w, bias, silu, out,
+                                              static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "causal_conv1d");
+    return ok();
+}
+
+ssd_status ssd_gated_rmsnorm(int64_t rows, int64_t D, int64_t groups, float eps, int32_t dtype, const void *x,
+                             const void *z, const float *w, void *out, void *stream) {
+    if (rows <= 0 || D <= 0 || groups <= 0)
+        return fail(SSD_ERR_INVALID_ARG, "rows, D, groups must be > 0");
+    if (D % groups != 0)
+        return fail(SSD_ERR_INVALID_ARG, "D (%lld) must be a multiple of groups (%lld)", (long long)D,
+                    (long long)groups);
+    if (!(eps >= 0.f)) return fail(SSD_ERR_INVALID_ARG, "eps must be >= 0");
+    if (D > 0x7fffffffLL || rows * groups > 0x7fffffffLL * 8LL)
+        return fail(SSD_ERR_UNSUPPORTED, "D < 2^31 and rows * groups < 2^34 required");
+    if (dtype != SSD_F32 && dtype != SSD_F16 && dtype != SSD_BF16)
+        return fail(SSD_ERR_INVALID_ARG, "unknown dtype code %d", dtype);
+    if (!x || !z || !w || !out) return fail(SSD_ERR_INVALID_ARG, "x, z, w and out are required");
+    cudaError_t e = ssd::launch_gated_rmsnorm(rows, (int)D, (int)groups, eps, dtype, x, z, w, out,
+                                              static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "gated_rmsnorm");
+    return ok();
+}
+
 ssd_status ssd_decode_step(const ssd_decode_args *a, void *stream) {
     if (!a) return fail(SSD_ERR_INVALID_ARG, "args is NULL");
     if (a->B <= 0 || a->H <= 0 || a->P <= 0 || a->N <= 0 || a->G <= 0)

@@ -130,6 +130,12 @@ struct BwdBuffers {
 size_t bwd_chunk_smem_bytes();
 cudaError_t launch_bwd(const Params &p, int io, const BwdBuffers &w, cudaStream_t s);
 
+// The SSD's neighbours (neighbors.cu).
+cudaError_t launch_causal_conv1d(int B, int D, int S, int W, int io, const void *x, const float *w,
+                                 const float *bias, int silu, void *out, cudaStream_t s);
+cudaError_t launch_gated_rmsnorm(long long rows, int D, int groups, float eps, int io, const void *x, const void *z,
+                                 const float *w, void *out, cudaStream_t s);
+
 // The sequence-parallel exchange (seqpar.cu).
 cudaError_t launch_segment_log_decay(const Params &p, float *out, cudaStream_t s);
 cudaError_t launch_state_fold(int nseg, long long bh_count, int pn, const float *log_decay, const float *states,

@@ -198,3 +198,17 @@ def test_varlen_needs_a_single_batch_row():
     a = _args(B=1, L=64)
     assert lib.ssd_fwd_varlen_workspace_size(ctypes.byref(a), arr, 2, ctypes.byref(out)) == 0
     assert out.value >= 256
+
+
+def test_neighbour_validation_without_a_gpu():
+    lib = ssd.load_library()
+    fake = ctypes.c_void_p(1 << 20)
+    # conv1d: W too wide, zero dims, missing pointer, unknown dtype
+    assert lib.ssd_causal_conv1d(1, 8, 16, 9, 0, fake, fake, None, 1, fake, None) == 2
+    assert lib.ssd_causal_conv1d(1, 0, 16, 4, 0, fake, fake, None, 1, fake, None) == 1
+    assert lib.ssd_causal_conv1d(1, 8, 16, 4, 0, None, fake, None, 1, fake, None) == 1
+    assert lib.ssd_causal_conv1d(1, 8, 16, 4, 5, fake, fake, None, 1, fake, None) == 1
+    # RMSNorm: groups not dividing D, negative eps, missing z
+    assert lib.ssd_gated_rmsnorm(4, 10, 3, 1e-5, 0, fake, fake, fake, fake, None) == 1
+    assert lib.ssd_gated_rmsnorm(4, 12, 3, -1.0, 0, fake, fake, fake, fake, None) == 1
+    assert lib.ssd_gated_rmsnorm(4, 12, 3, 1e-5, 0, fake, None, fake, fake, None) == 1
