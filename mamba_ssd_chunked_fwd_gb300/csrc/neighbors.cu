@@ -7,11 +7,13 @@
 //                          over `groups` runs of D/groups consecutive channels
 //
 // Both are HBM-bound elementwise-plus-reduction passes, fp32 arithmetic.
-//   conv1d: one CTA per (1024-token tile, channel, batch); the tile and its
-//           W-1 token halo go through shared memory, loads and stores are
-//           coalesced along the sequence.
-//   RMSNorm: one warp per (row, group); the group's sum of squares is a warp
-//           reduction, a second pass (from L1/L2) writes the output.
+//   conv1d: one CTA per (1024-token tile, 4 channels, batch); each channel's
+//           tile and its W-1 token halo go through shared memory, loads and
+//           stores are coalesced along the sequence (16 bytes per thread when
+//           fp32 rows allow it), 16 KB of loads in flight per CTA.
+//   RMSNorm: one warp per (row, group); the group's values stay in registers
+//           (up to 512 channels per group; wider groups take a second pass
+//           from L1/L2) and its sum of squares is a warp reduction.
 #include "ssd_internal.cuh"
 
 namespace ssd {
@@ -19,42 +21,82 @@ namespace ssd {
 namespace {
 
 constexpr int kConvThreads = 256;
-constexpr int kConvPer = 4;  // outputs per thread
+constexpr int kConvPer = 4;  // consecutive outputs per thread and channel
 constexpr int kConvTile = kConvThreads * kConvPer;
+constexpr int kConvRows = 4;  // channels per CTA
 constexpr int kMaxW = 8;
+constexpr int kPad = 8;       // the halo slot in front of each channel's tile (>= W-1, keeps float4 alignment)
 
-template <int IO>
+// VEC: fp32 rows with S % 4 == 0 (16-byte aligned rows): float4 loads and stores.
+template <int IO, bool VEC>
 __global__ void __launch_bounds__(kConvThreads)
 causal_conv1d_kernel(int S, int D, int W, const void *x, const float *__restrict__ w, const float *__restrict__ bias,
                      int silu, void *out) {
-    __shared__ float xs[kConvTile + kMaxW - 1];
-    const int s0 = blockIdx.x * kConvTile, d = blockIdx.y, b = blockIdx.z;
-    const size_t row = ((size_t)b * D + d) * S;
+    __shared__ __align__(16) float xs[kConvRows][kPad + kConvTile];
+    const int s0 = blockIdx.x * kConvTile, d0 = blockIdx.y * kConvRows, b = blockIdx.z;
     const int halo = W - 1;
-    for (int i = threadIdx.x; i < kConvTile + halo; i += kConvThreads) {
-        const int t = s0 - halo + i;
-        xs[i] = (t >= 0 && t < S) ? ld_io<IO>(x, row + t) : 0.f;
-    }
-    float wk[kMaxW];
+    // tiles: xs[r][kPad + i] = x[t = s0 + i], xs[r][kPad - m] = x[s0 - m] (halo)
 #pragma unroll
-    for (int k = 0; k < kMaxW; ++k) wk[k] = k < W ? __ldg(w + (size_t)d * W + k) : 0.f;
-    const float bv = bias ? __ldg(bias + d) : 0.f;
+    for (int r = 0; r < kConvRows; ++r) {
+        const int d = d0 + r;
+        if (d >= D) break;
+        const size_t row = ((size_t)b * D + d) * S;
+        if (VEC) {
+            const int t = s0 + 4 * threadIdx.x;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (t < S) v = __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(x) + row + t));
+            *reinterpret_cast<float4 *>(&xs[r][kPad + 4 * threadIdx.x]) = v;
+        } else {
+#pragma unroll
+            for (int i = 0; i < kConvPer; ++i) {
+                const int j = threadIdx.x + kConvThreads * i, t = s0 + j;
+                xs[r][kPad + j] = t < S ? ld_io<IO>(x, row + t) : 0.f;
+            }
+        }
+        if (threadIdx.x < halo) {
+            const int t = s0 - halo + threadIdx.x;
+            xs[r][kPad - halo + threadIdx.x] = t >= 0 ? ld_io<IO>(x, row + t) : 0.f;
+        }
+    }
     __syncthreads();
 #pragma unroll
-    for (int i = 0; i < kConvPer; ++i) {
-        const int j = threadIdx.x + kConvThreads * i;  // output within the tile
-        const int t = s0 + j;
-        if (t >= S) continue;
-        float acc = bv;
+    for (int r = 0; r < kConvRows; ++r) {
+        const int d = d0 + r;
+        if (d >= D) break;
+        const size_t row = ((size_t)b * D + d) * S;
+        float wk[kMaxW];
 #pragma unroll
-        for (int k = 0; k < kMaxW; ++k)
-            if (k < W) acc = fmaf(wk[k], xs[j + k], acc);  // xs[j + k] is x[t - (W-1) + k]
-        if (silu) acc = acc / (1.f + expf(-acc));
-        st_io<IO>(out, row + t, acc);
+        for (int k = 0; k < kMaxW; ++k) wk[k] = k < W ? __ldg(w + (size_t)d * W + k) : 0.f;
+        const float bv = bias ? __ldg(bias + d) : 0.f;
+        float o[kConvPer];
+#pragma unroll
+        for (int i = 0; i < kConvPer; ++i) {
+            // VEC: the thread's 4 outputs are consecutive; else strided by the block
+            const int j = VEC ? 4 * threadIdx.x + i : threadIdx.x + kConvThreads * i;
+            float acc = bv;
+#pragma unroll
+            for (int k = 0; k < kMaxW; ++k)
+                if (k < W) acc = fmaf(wk[k], xs[r][kPad - halo + j + k], acc);  // x[t - (W-1) + k]
+            if (silu) acc = acc / (1.f + expf(-acc));
+            o[i] = acc;
+        }
+        if (VEC) {
+            const int t = s0 + 4 * threadIdx.x;
+            if (t < S)
+                *reinterpret_cast<float4 *>(static_cast<float *>(out) + row + t) = make_float4(o[0], o[1], o[2], o[3]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < kConvPer; ++i) {
+                const int t = s0 + threadIdx.x + kConvThreads * i;
+                if (t < S) st_io<IO>(out, row + t, o[i]);
+            }
+        }
     }
 }
 
-template <int IO>
+// PER: values each lane keeps in registers (PER * 32 >= the group size), 0 for
+// groups wider than 512 channels (second pass).
+template <int IO, int PER>
 __global__ void __launch_bounds__(256)
 gated_rmsnorm_kernel(long long rows, int D, int groups, float eps, const void *x, const void *z,
                      const float *__restrict__ w, void *out) {
@@ -66,18 +108,41 @@ gated_rmsnorm_kernel(long long rows, int D, int groups, float eps, const void *x
     const int gs = D / groups;
     const size_t base = (size_t)r * D + (size_t)g * gs;
     float ss = 0.f;
-    for (int i = lane; i < gs; i += 32) {
-        const float zv = ld_io<IO>(z, base + i);
-        const float v = ld_io<IO>(x, base + i) * (zv / (1.f + expf(-zv)));
-        ss = fmaf(v, v, ss);
-    }
+    if constexpr (PER > 0) {
+        float v[PER];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-    const float inv = rsqrtf(ss / (float)gs + eps);
-    for (int i = lane; i < gs; i += 32) {
-        const float zv = ld_io<IO>(z, base + i);
-        const float v = ld_io<IO>(x, base + i) * (zv / (1.f + expf(-zv)));
-        st_io<IO>(out, base + i, v * inv * __ldg(w + g * gs + i));
+        for (int k = 0; k < PER; ++k) {  // every load first
+            const int i = lane + 32 * k;
+            v[k] = 0.f;
+            if (i < gs) {
+                const float zv = ld_io<IO>(z, base + i);
+                v[k] = ld_io<IO>(x, base + i) * (zv / (1.f + expf(-zv)));
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < PER; ++k) ss = fmaf(v[k], v[k], ss);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        const float inv = rsqrtf(ss / (float)gs + eps);
+#pragma unroll
+        for (int k = 0; k < PER; ++k) {
+            const int i = lane + 32 * k;
+            if (i < gs) st_io<IO>(out, base + i, v[k] * inv * __ldg(w + g * gs + i));
+        }
+    } else {
+        for (int i = lane; i < gs; i += 32) {
+            const float zv = ld_io<IO>(z, base + i);
+            const float v = ld_io<IO>(x, base + i) * (zv / (1.f + expf(-zv)));
+            ss = fmaf(v, v, ss);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        const float inv = rsqrtf(ss / (float)gs + eps);
+        for (int i = lane; i < gs; i += 32) {  // second pass, from L1/L2
+            const float zv = ld_io<IO>(z, base + i);
+            const float v = ld_io<IO>(x, base + i) * (zv / (1.f + expf(-zv)));
+            st_io<IO>(out, base + i, v * inv * __ldg(w + g * gs + i));
+        }
     }
 }
 
@@ -85,11 +150,16 @@ gated_rmsnorm_kernel(long long rows, int D, int groups, float eps, const void *x
 
 cudaError_t launch_causal_conv1d(int B, int D, int S, int W, int io, const void *x, const float *w,
                                  const float *bias, int silu, void *out, cudaStream_t s) {
-    const dim3 grid((unsigned)((S + kConvTile - 1) / kConvTile), (unsigned)D, (unsigned)B);
+    const dim3 grid((unsigned)((S + kConvTile - 1) / kConvTile), (unsigned)((D + kConvRows - 1) / kConvRows),
+                    (unsigned)B);
+    const bool vec = S % 4 == 0 && reinterpret_cast<uintptr_t>(x) % 16 == 0 && reinterpret_cast<uintptr_t>(out) % 16 == 0;
     switch (io) {
-        case IO_F32: causal_conv1d_kernel<IO_F32><<<grid, kConvThreads, 0, s>>>(S, D, W, x, w, bias, silu, out); break;
-        case IO_F16: causal_conv1d_kernel<IO_F16><<<grid, kConvThreads, 0, s>>>(S, D, W, x, w, bias, silu, out); break;
-        case IO_BF16: causal_conv1d_kernel<IO_BF16><<<grid, kConvThreads, 0, s>>>(S, D, W, x, w, bias, silu, out); break;
+        case IO_F32:
+            if (vec) causal_conv1d_kernel<IO_F32, true><<<grid, kConvThreads, 0, s>>>(S, D, W, x, w, bias, silu, out);
+            else causal_conv1d_kernel<IO_F32, false><<<grid, kConvThreads, 0, s>>>(S, D, W, x, w, bias, silu, out);
+            break;
+        case IO_F16: causal_conv1d_kernel<IO_F16, false><<<grid, kConvThreads, 0, s>>>(S, D, W, x, w, bias, silu, out); break;
+        case IO_BF16: causal_conv1d_kernel<IO_BF16, false><<<grid, kConvThreads, 0, s>>>(S, D, W, x, w, bias, silu, out); break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
@@ -99,12 +169,21 @@ cudaError_t launch_gated_rmsnorm(long long rows, int D, int groups, float eps, i
                                  const float *w, void *out, cudaStream_t s) {
     const long long warps = rows * groups;
     const unsigned blocks = (unsigned)((warps + 7) / 8);
-    switch (io) {
-        case IO_F32: gated_rmsnorm_kernel<IO_F32><<<blocks, 256, 0, s>>>(rows, D, groups, eps, x, z, w, out); break;
-        case IO_F16: gated_rmsnorm_kernel<IO_F16><<<blocks, 256, 0, s>>>(rows, D, groups, eps, x, z, w, out); break;
-        case IO_BF16: gated_rmsnorm_kernel<IO_BF16><<<blocks, 256, 0, s>>>(rows, D, groups, eps, x, z, w, out); break;
-        default: return cudaErrorInvalidValue;
+    const int gs = D / groups;
+#define SSD_RMS_LAUNCH(PER)                                                                                  \
+    switch (io) {                                                                                            \
+        case IO_F32: gated_rmsnorm_kernel<IO_F32, PER><<<blocks, 256, 0, s>>>(rows, D, groups, eps, x, z, w, out); break; \
+        case IO_F16: gated_rmsnorm_kernel<IO_F16, PER><<<blocks, 256, 0, s>>>(rows, D, groups, eps, x, z, w, out); break; \
+        case IO_BF16: gated_rmsnorm_kernel<IO_BF16, PER><<<blocks, 256, 0, s>>>(rows, D, groups, eps, x, z, w, out); break; \
+        default: return cudaErrorInvalidValue;                                                               \
     }
+    if (gs <= 32) { SSD_RMS_LAUNCH(1) }
+    else if (gs <= 64) { SSD_RMS_LAUNCH(2) }
+    else if (gs <= 128) { SSD_RMS_LAUNCH(4) }
+    else if (gs <= 256) { SSD_RMS_LAUNCH(8) }
+    else if (gs <= 512) { SSD_RMS_LAUNCH(16) }
+    else { SSD_RMS_LAUNCH(0) }
+#undef SSD_RMS_LAUNCH
     return cudaGetLastError();
 }
 

@@ -12,7 +12,8 @@ pytestmark = pytest.mark.gpu
 _DT = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
 
 
-@pytest.mark.parametrize("shape", [(1, 10240, 1024, 4), (2, 96, 1500, 4), (3, 5, 7, 2), (1, 64, 2049, 8), (2, 33, 300, 1)])
+@pytest.mark.parametrize("shape", [(1, 10240, 1024, 4), (2, 96, 1500, 4), (3, 5, 7, 2), (1, 64, 2049, 8), (2, 33, 300, 1),
+                                   (2, 7, 3072, 8)])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("feats", [(True, True), (False, False)])
 def test_causal_conv1d(oracle_mod, shape, dtype, feats):
@@ -30,7 +31,9 @@ def test_causal_conv1d(oracle_mod, shape, dtype, feats):
     assert_close(oracle_mod, out.double().cpu().numpy(), ref, dtype, f"conv1d {shape} {dtype}")
 
 
-@pytest.mark.parametrize("shape", [(2, 512, 16384, 64), (3, 7, 96, 3), (1, 5, 4096, 1), (4, 33, 200, 8)])
+# group sizes 256, 32, 4096 (two passes), 25, 512, 500, 128, 60
+@pytest.mark.parametrize("shape", [(2, 512, 16384, 64), (3, 7, 96, 3), (1, 5, 4096, 1), (4, 33, 200, 8),
+                                   (2, 9, 1024, 2), (1, 3, 1000, 2), (1, 17, 384, 3), (2, 11, 300, 5)])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_gated_rmsnorm(oracle_mod, shape, dtype):
     import mamba_ssd_chunked_fwd_gb300 as ssd
@@ -43,6 +46,20 @@ def test_gated_rmsnorm(oracle_mod, shape, dtype):
     torch.cuda.synchronize()
     ref = oracle_mod.gated_rmsnorm(x.double().numpy(), z.double().numpy(), w.numpy(), G, 1e-5)
     assert_close(oracle_mod, out.double().cpu().numpy(), ref, dtype, f"rmsnorm {shape} {dtype}")
+
+
+def test_causal_conv1d_unaligned_rows(oracle_mod):
+    """fp32 rows that start off a 16-byte boundary take the scalar loads."""
+    import mamba_ssd_chunked_fwd_gb300 as ssd
+    B, D, S, W = 2, 6, 1028, 4
+    g = torch.Generator().manual_seed(17)
+    flat = torch.randn(B * D * S + 1, generator=g)
+    w = torch.randn((D, W), generator=g) * 0.5
+    x = flat.cuda()[1:].view(B, D, S)
+    out = ssd.causal_conv1d(x, w.cuda(), None, silu=True)
+    torch.cuda.synchronize()
+    ref = oracle_mod.causal_conv1d(flat[1:].view(B, D, S).double().numpy(), w.numpy(), None, silu=True)
+    assert_close(oracle_mod, out.double().cpu().numpy(), ref, "f32", "conv1d unaligned")
 
 
 def test_neighbours_are_deterministic():
