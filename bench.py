@@ -78,6 +78,38 @@ def algorithmic_bytes(w) -> dict:
     return b
 
 
+# fp32 FMA lanes: 152 SMs x 4 sub-partitions x 32 lanes, 2 flops per FMA, at
+# the maximum SM clock (2070 MHz): the ceiling of CUDA-core fp32 arithmetic.
+SM_COUNT = 152
+FP32_LANES_PER_SM = 128
+SM_MAX_MHZ = 2070.0
+
+
+def fp32_alu_peak_tflops():
+    try:
+        mhz = float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["sm_max_mhz"])
+    except Exception:
+        mhz = SM_MAX_MHZ
+    return SM_COUNT * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12
+
+
+def bwd_flops(w) -> int:
+    """Algorithmic flops of one backward (2 per multiply-add), counting the
+    contractions per (batch, head, chunk): the recomputed chunk state (Q P N),
+    the adjoint's per-chunk sum (Q P N), C B^T once per group (Q^2 N), dyp x^T
+    (Q^2 P), the intra-chunk parts of dx (Q^2 P), dB and dC (Q^2 N each), the
+    inter-chunk parts of dx, dB and dC (Q P N each), and with z the recomputed
+    pre-gate output (Q^2 N per group, Q^2 P, Q P N).  Elementwise work (decays,
+    gate, reductions) is not counted."""
+    Q, P, N = w.chunk, w.P, w.N
+    hpg = w.H // w.G
+    per = 5 * Q * P * N + 2 * Q * Q * P + 2 * Q * Q * N + Q * Q * N / hpg
+    if w.z:
+        per += Q * Q * N / hpg + Q * Q * P + Q * P * N
+    chunks = -(-w.L // w.chunk)
+    return int(2 * per * w.B * w.H * chunks)
+
+
 def stage_bytes(w) -> dict:
     """Compulsory bytes of each chunked-plan kernel (its own inputs read once,
     its own outputs written once)."""
@@ -487,8 +519,11 @@ def run_bwd(args):
     ab = algorithmic_bytes(w)
     nbytes = (2 * (ab["x"] + ab["B"] + ab["C"] + ab["dt"] + ab["z"]) + ab["x"]  # inputs and gradients, dy
               + 2 * w.B * w.H * w.P * w.N * 4 + ab["h0"])                           # dfinal, dh0, h0
-    hbm, peak_kind = peaks()
-    achieved = nbytes / (ms * 1e-3) / 1e9
+    hbm, _ = peaks()
+    flops = bwd_flops(w)
+    tflops = flops / (ms * 1e-3) / 1e12
+    alu = fp32_alu_peak_tflops()
+    launches = 10 + (d["z"] is not None)  # 3 (+1 with z) recompute, gate, adjoint, passing, chunk, 2 group sums, head sum
     line = {
         "metric": f"SSD backward tokens/s ({args.workload} {w.shape_tuple()})",
         "value": round(w.tokens / (ms * 1e-3), 1), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
@@ -496,11 +531,15 @@ def run_bwd(args):
         "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded, pages' distributions)",
         "config": {"workload": f"backward, {args.workload} {w.shape_tuple()} [B,L,H,P,N,chunk,G]",
                    "workspace_gb": round(nws / 1e9, 2)},
-        "roofline": {"bound": "hbm", "kernel": "whole backward (8 launches)", "achieved": round(achieved, 1),
-                     "peak": hbm, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / hbm, 4),
-                     "traffic": None, "alg_bytes_per_launch": nbytes, "launch_ms": round(ms, 4)},
+        "roofline": {"bound": "alu", "kernel": f"whole backward ({launches} launches, fp32 CUDA cores)",
+                     "achieved": round(tflops, 3), "peak": round(alu, 1),
+                     "peak_kind": "derived: 152 SMs x 128 fp32 lanes x 2 flops x max SM clock",
+                     "unit": "TFLOP/s", "frac": round(tflops / alu, 4), "traffic": None,
+                     "alg_flops_per_step": flops, "launch_ms": round(ms, 4),
+                     "hbm_view": {"alg_bytes_per_step": nbytes,
+                                  "achieved_gbs": round(nbytes / (ms * 1e-3) / 1e9, 1), "peak_gbs": hbm}},
         "clocks": clk.summary(),
-        "gpu_launches": 11 * args.steps,
+        "gpu_launches": launches * args.steps,
     }
     print(json.dumps(line), flush=True)
 

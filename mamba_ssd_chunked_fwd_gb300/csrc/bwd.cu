@@ -86,13 +86,24 @@ bwd_chunk_adjoint_kernel(Params p, const float *__restrict__ cs, const float *__
     const int b = bh / p.H, h = bh % p.H, g = h / p.hpg;
     const int P = p.P, N = p.N, Q = p.Q, L = p.L;
     const size_t crow = (((size_t)b * p.H + h) * p.nchunks + k) * Q;
-    for (int e = threadIdx.x; e < Q * P; e += kThreads) {
-        const int i = e / P, pp = e % P, t = k * Q + i;
-        ds[i][pp] = t < L ? dyp[(((size_t)b * L + t) * p.H + h) * P + pp] * expf(__ldg(cs + crow + i)) : 0.f;
-    }
-    for (int e = threadIdx.x; e < Q * N; e += kThreads) {
-        const int i = e / N, n = e % N, t = k * Q + i;
-        cc[i][n] = t < L ? ld_io<IO>(p.Cm, (((size_t)b * L + t) * p.G + g) * N + n) : 0.f;
+    {
+        // every global load issued before the shared-memory stores; 0 outside (Q, P, N) and past L
+        constexpr int kPer = kMax * kMax / kThreads;
+        float rd[kPer], rc[kPer], re[kPer];
+#pragma unroll
+        for (int q = 0; q < kPer; ++q) {
+            const int e = threadIdx.x + kThreads * q, i = e >> 6, col = e & (kMax - 1), t = k * Q + i;
+            const bool row_in = i < Q && t < L;
+            rd[q] = row_in && col < P ? __ldg(dyp + (((size_t)b * L + t) * p.H + h) * P + col) : 0.f;
+            rc[q] = row_in && col < N ? ld_io<IO>(p.Cm, (((size_t)b * L + t) * p.G + g) * N + col) : 0.f;
+            re[q] = row_in ? __ldg(cs + crow + i) : 0.f;
+        }
+#pragma unroll
+        for (int q = 0; q < kPer; ++q) {
+            const int e = threadIdx.x + kThreads * q, i = e >> 6, col = e & (kMax - 1);
+            ds[i][col] = rd[q] * expf(re[q]);
+            cc[i][col] = rc[q];
+        }
     }
     __syncthreads();
     const int r0 = threadIdx.x >> 4, c0 = threadIdx.x & 15;
@@ -141,15 +152,26 @@ bwd_state_passing_kernel(Params p, const float *__restrict__ cs, const float *__
 }
 
 // ---- within one chunk: dx, dB, dC (per head), ddt, and partial dA, dD, dbias ----
+// Row sums of 4 x 4 tiles reduce over the 16 lanes that share a tile row
+// (a half warp); column sums over the two tile rows of a warp, then over the
+// 8 warps through shared memory in warp order.  Every order is fixed.
 struct ChunkSmem {
     float x[kMax][kMax + 1], dy[kMax][kMax + 1], B[kMax][kMax + 1], C[kMax][kMax + 1];
     float S[kMax][kMax + 1], Gm[kMax][kMax + 1];
-    float CB[kMax][kMax + 1], DX[kMax][kMax + 1], V[kMax][kMax + 1];
-    float T[kMax][kMax + 1];  // dxs, then S^T dyp
-    float GB[kMax][kMax + 1];
+    float CB[kMax][kMax + 1];  // E CB (masked decayed C B^T)
+    float DX[kMax][kMax + 1];  // E DX d_j (masked decayed dyp x^T, column j scaled by d_j)
+    float Kp[kThreads / 32][kMax];
     float cs[kMax], d[kMax], ecs[kMax], el[kMax], dd1[kMax], w[kMax], z[kMax], dcs[kMax], u[kMax];
-    float red[kThreads];
+    float R[kMax], uu[kMax], dxd[kMax];
+    float red[kThreads / 32];
 };
+
+// sum over the 16 lanes of a half warp (lanes sharing a tile row)
+__device__ __forceinline__ float half_warp_sum(float v) {
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    return v;
+}
 
 template <int IO>
 __global__ void __launch_bounds__(kThreads)
@@ -162,45 +184,62 @@ bwd_chunk_kernel(Params p, const float *__restrict__ dtp, const float *__restric
     const int k = blockIdx.y, bh = blockIdx.x;
     const int b = bh / p.H, h = bh % p.H, g = h / p.hpg;
     const int P = p.P, N = p.N, Q = p.Q, L = p.L, tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
     const int r0 = tid >> 4, c0 = tid & 15;  // 4 x 4 tiles of 64 x 64 results
     const size_t crow = (((size_t)b * p.H + h) * p.nchunks + k) * Q;
     const size_t st_off = ((((size_t)b * p.nchunks + k) * p.H + h) * P) * N;
     const float A = __ldg(p.A + h);
     const float Dh = p.D ? __ldg(p.D + h) : 0.f;
 
-    // (1) tiles; past L: x, dy, B, C = 0 and d = 0 (cs keeps its last value)
-    for (int e = tid; e < Q; e += kThreads) {
-        const bool in = k * Q + e < L;
-        sm.cs[e] = __ldg(cs + crow + e);
-        sm.d[e] = in ? __ldg(dtp + crow + e) : 0.f;
+    // (1) tiles, every global load issued before the shared-memory stores.
+    //     Outside (Q, P, N) and past L: 0, and d = 0 (cs keeps its last value).
+    if (tid < kMax) {
+        const int e = tid;
+        const bool inq = e < Q, in = inq && k * Q + e < L;
+        const float c = inq ? __ldg(cs + crow + e) : 0.f;
         float u = in ? __ldg(p.dt + ((size_t)b * L + k * Q + e) * p.H + h) : 0.f;
         if (p.dt_bias) u += __ldg(p.dt_bias + h);
+        sm.cs[e] = c;
+        sm.d[e] = in ? __ldg(dtp + crow + e) : 0.f;
         sm.u[e] = u;
     }
-    for (int e = tid; e < Q * P; e += kThreads) {
-        const int i = e / P, pp = e % P, t = k * Q + i;
-        const size_t o = (((size_t)b * L + t) * p.H + h) * P + pp;
-        sm.x[i][pp] = t < L ? ld_io<IO>(p.x, o) : 0.f;
-        sm.dy[i][pp] = t < L ? dyp[o] : 0.f;
-    }
-    for (int e = tid; e < Q * N; e += kThreads) {
-        const int i = e / N, n = e % N, t = k * Q + i;
-        const size_t o = (((size_t)b * L + t) * p.G + g) * N + n;
-        sm.B[i][n] = t < L ? ld_io<IO>(p.Bm, o) : 0.f;
-        sm.C[i][n] = t < L ? ld_io<IO>(p.Cm, o) : 0.f;
-    }
-    for (int e = tid; e < P * N; e += kThreads) {
-        sm.S[e / N][e % N] = __ldg(states + st_off + e);
-        sm.Gm[e / N][e % N] = __ldg(adj + st_off + e);
+    {
+        constexpr int kPer = kMax * kMax / kThreads;  // 16 elements per thread and tile
+        float rx[kPer], rdy[kPer], rb[kPer], rc[kPer], rs[kPer], rg[kPer];
+#pragma unroll
+        for (int q = 0; q < kPer; ++q) {
+            const int e = tid + kThreads * q, i = e >> 6, col = e & (kMax - 1), t = k * Q + i;
+            const bool row_in = i < Q && t < L;
+            const size_t ox = (((size_t)b * L + t) * p.H + h) * P + col;
+            const size_t ob = (((size_t)b * L + t) * p.G + g) * N + col;
+            rx[q] = row_in && col < P ? ld_io<IO>(p.x, ox) : 0.f;
+            rdy[q] = row_in && col < P ? __ldg(dyp + ox) : 0.f;
+            rb[q] = row_in && col < N ? ld_io<IO>(p.Bm, ob) : 0.f;
+            rc[q] = row_in && col < N ? ld_io<IO>(p.Cm, ob) : 0.f;
+            const bool sin = i < P && col < N;  // i: state row p, col: n
+            rs[q] = sin ? __ldg(states + st_off + (size_t)i * N + col) : 0.f;
+            rg[q] = sin ? __ldg(adj + st_off + (size_t)i * N + col) : 0.f;
+        }
+#pragma unroll
+        for (int q = 0; q < kPer; ++q) {
+            const int e = tid + kThreads * q, i = e >> 6, col = e & (kMax - 1);
+            sm.x[i][col] = rx[q];
+            sm.dy[i][col] = rdy[q];
+            sm.B[i][col] = rb[q];
+            sm.C[i][col] = rc[q];
+            sm.S[i][col] = rs[q];
+            sm.Gm[i][col] = rg[q];
+        }
     }
     __syncthreads();
     const float cs_last = sm.cs[Q - 1];
-    for (int e = tid; e < Q; e += kThreads) {
-        sm.ecs[e] = expf(sm.cs[e]);
-        sm.el[e] = expf(cs_last - sm.cs[e]);
+    if (tid < kMax) {
+        const int e = tid;
+        sm.ecs[e] = e < Q ? expf(sm.cs[e]) : 0.f;
+        sm.el[e] = e < Q ? expf(cs_last - sm.cs[e]) : 0.f;
     }
-    // (2) CB = C B^T, DX = dyp x^T, then the masked decay: CB <- E CB, DX <- E DX,
-    //     V = E CB DX d_j  (rows i, columns j of 4 x 4 tiles; past Q: unused)
+    // (2) CB = C B^T, DX = dyp x^T, then the masked decay: CB <- E CB,
+    //     DX <- E DX d_j; V = E CB DX d_j only as its row sums R and column sums K
     {
         float cb[4][4], dxm[4][4];
         zero4x4(cb);
@@ -208,39 +247,64 @@ bwd_chunk_kernel(Params p, const float *__restrict__ dtp, const float *__restric
         tile4x4(cb, N, r0, c0, [&](int i, int n) { return sm.C[i][n]; }, [&](int j, int n) { return sm.B[j][n]; });
         tile4x4(dxm, P, r0, c0, [&](int i, int pp) { return sm.dy[i][pp]; },
                 [&](int j, int pp) { return sm.x[j][pp]; });
+        float rp[4] = {0.f, 0.f, 0.f, 0.f}, cp[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int a = 0; a < 4; ++a)
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 const int i = r0 + 16 * a, j = c0 + 16 * c;
-                if (i < Q && j < Q) {
-                    const float E = j <= i ? expf(sm.cs[i] - sm.cs[j]) : 0.f;
-                    const float a1 = E * cb[a][c];
-                    sm.V[i][j] = a1 * dxm[a][c] * sm.d[j];
-                    sm.CB[i][j] = a1;
-                    sm.DX[i][j] = E * dxm[a][c];
-                }
+                const float E = (i < Q && j <= i) ? expf(sm.cs[i] - sm.cs[j]) : 0.f;
+                const float a1 = E * cb[a][c], dm = E * dxm[a][c] * sm.d[j];
+                const float v = a1 * dxm[a][c] * sm.d[j];
+                rp[a] += v;
+                cp[c] += v;
+                sm.CB[i][j] = a1;
+                sm.DX[i][j] = dm;
+                if (i == j) sm.dxd[i] = dxm[a][c];  // E = 1 on the diagonal: dyp_i . x_i
             }
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+            const float r = half_warp_sum(rp[a]);
+            if (c0 == 0) sm.R[r0 + 16 * a] = r;
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const float s = cp[c] + __shfl_xor_sync(0xffffffffu, cp[c], 16);  // tile rows 2w and 2w+1
+            if (lane < 16) sm.Kp[warp][c0 + 16 * c] = s;
+        }
     }
     __syncthreads();
-    // (4) T = dxs = (E CB)^T dyp + el (G B) ; GB = G B_t  (rows t, columns p)
-    // (5) dB_t = d_t ((E DX)^T C + el G^T x_t)  (rows t, columns n)
+    // (4) dxs = (E CB)^T dyp + el (G B)  (rows t, columns p) -> dx = d dxs + D dyp,
+    //     dd1_t = x_t . dxs_t, z_t = x_t . (G B_t)
+    // (5) dB_t = (E DX d)^T C + d_t el_t G^T x_t  (rows t, columns n)
     {
         float acc[4][4], gb[4][4];
         zero4x4(acc);
         zero4x4(gb);
         tile4x4(acc, Q, r0, c0, [&](int t, int i) { return sm.CB[i][t]; }, [&](int pp, int i) { return sm.dy[i][pp]; });
         tile4x4(gb, N, r0, c0, [&](int t, int n) { return sm.B[t][n]; }, [&](int pp, int n) { return sm.Gm[pp][n]; });
+        float dp[4] = {0.f, 0.f, 0.f, 0.f}, zp[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int a = 0; a < 4; ++a)
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 const int t = r0 + 16 * a, pp = c0 + 16 * c;
-                if (t < Q && pp < P) {
-                    sm.GB[t][pp] = gb[a][c];
-                    sm.T[t][pp] = fmaf(sm.el[t], gb[a][c], acc[a][c]);
-                }
+                const float T = fmaf(sm.el[t], gb[a][c], acc[a][c]);
+                const float xv = sm.x[t][pp];
+                dp[a] = fmaf(xv, T, dp[a]);
+                zp[a] = fmaf(xv, gb[a][c], zp[a]);
+                if (t < Q && pp < P && k * Q + t < L)
+                    st_io<IO>(dx, (((size_t)b * L + k * Q + t) * p.H + h) * P + pp,
+                              fmaf(sm.d[t], T, Dh * sm.dy[t][pp]));
             }
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+            const float s1 = half_warp_sum(dp[a]), s2 = half_warp_sum(zp[a]);
+            if (c0 == 0) {
+                sm.dd1[r0 + 16 * a] = s1;
+                sm.z[r0 + 16 * a] = s2;
+            }
+        }
         zero4x4(acc);
         zero4x4(gb);
         tile4x4(acc, Q, r0, c0, [&](int t, int i) { return sm.DX[i][t]; }, [&](int n, int i) { return sm.C[i][n]; });
@@ -251,69 +315,53 @@ bwd_chunk_kernel(Params p, const float *__restrict__ dtp, const float *__restric
             for (int c = 0; c < 4; ++c) {
                 const int t = r0 + 16 * a, n = c0 + 16 * c;
                 if (t < Q && n < N && k * Q + t < L)
-                    dBh[(((size_t)b * L + k * Q + t) * p.H + h) * N + n] = sm.d[t] * fmaf(sm.el[t], gb[a][c], acc[a][c]);
+                    dBh[(((size_t)b * L + k * Q + t) * p.H + h) * N + n] =
+                        fmaf(sm.d[t] * sm.el[t], gb[a][c], acc[a][c]);
             }
     }
-    __syncthreads();
-    // dx, and per token dd1 = x . dxs, z = x . GB
-    for (int e = tid; e < Q * P; e += kThreads) {
-        const int t = e / P, pp = e % P;
-        if (k * Q + t < L)
-            st_io<IO>(dx, (((size_t)b * L + k * Q + t) * p.H + h) * P + pp,
-                      fmaf(sm.d[t], sm.T[t][pp], Dh * sm.dy[t][pp]));
-    }
-    if (tid < Q) {
-        float a = 0.f, zz = 0.f;
-        for (int pp = 0; pp < P; ++pp) {
-            a = fmaf(sm.x[tid][pp], sm.T[tid][pp], a);
-            zz = fmaf(sm.x[tid][pp], sm.GB[tid][pp], zz);
-        }
-        sm.dd1[tid] = a;
-        sm.z[tid] = zz;
-    }
-    __syncthreads();
-    // (6) dC_i = ecs_i (S^T dyp_i) + (E DX d) B ; T <- S^T dyp  (rows i, columns n)
+    // (6) dC_i = ecs_i (S^T dyp_i) + (E DX d) B ;  uu_i = C_i . (S^T dyp_i)  (rows i, columns n)
     {
         float sd[4][4], acc[4][4];
         zero4x4(sd);
         zero4x4(acc);
         tile4x4(sd, P, r0, c0, [&](int i, int pp) { return sm.dy[i][pp]; }, [&](int n, int pp) { return sm.S[pp][n]; });
-        tile4x4(acc, Q, r0, c0, [&](int i, int j) { return sm.DX[i][j] * sm.d[j]; },
-                [&](int n, int j) { return sm.B[j][n]; });
+        tile4x4(acc, Q, r0, c0, [&](int i, int j) { return sm.DX[i][j]; }, [&](int n, int j) { return sm.B[j][n]; });
+        float up[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int a = 0; a < 4; ++a)
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 const int i = r0 + 16 * a, n = c0 + 16 * c;
-                if (i < Q && n < N) {
-                    sm.T[i][n] = sd[a][c];
-                    if (k * Q + i < L)
-                        dCh[(((size_t)b * L + k * Q + i) * p.H + h) * N + n] = fmaf(sm.ecs[i], sd[a][c], acc[a][c]);
-                }
+                up[a] = fmaf(sm.C[i][n], sd[a][c], up[a]);
+                if (i < Q && n < N && k * Q + i < L)
+                    dCh[(((size_t)b * L + k * Q + i) * p.H + h) * N + n] = fmaf(sm.ecs[i], sd[a][c], acc[a][c]);
             }
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+            const float s = half_warp_sum(up[a]);
+            if (c0 == 0) sm.uu[r0 + 16 * a] = s;
+        }
     }
-    // <G, S> (fixed-order block reduction)
+    // <G, S>: per warp, then over the warps in order
     {
         float part = 0.f;
-        for (int e = tid; e < P * N; e += kThreads) part = fmaf(sm.Gm[e / N][e % N], sm.S[e / N][e % N], part);
-        sm.red[tid] = part;
+        for (int e = tid; e < kMax * kMax; e += kThreads) part = fmaf(sm.Gm[e >> 6][e & 63], sm.S[e >> 6][e & 63], part);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+        if (lane == 0) sm.red[warp] = part;
     }
     __syncthreads();
-    for (int s = kThreads / 2; s > 0; s >>= 1) {
-        if (tid < s) sm.red[tid] += sm.red[tid + s];
-        __syncthreads();
-    }
-    const float gs = sm.red[0];
-    // (7) u_i = C_i . T_i ; dcs ; per-token raw-dt gradient factor
+    float gs = 0.f;
+#pragma unroll
+    for (int q = 0; q < kThreads / 32; ++q) gs += sm.red[q];
+    // (7) dcs and the per-token raw-dt gradient factor
     if (tid < Q) {
-        float uu = 0.f;
-        for (int n = 0; n < N; ++n) uu = fmaf(sm.C[tid][n], sm.T[tid][n], uu);
-        float R = 0.f, K = 0.f;
-        for (int j = 0; j < Q; ++j) R += sm.V[tid][j];
-        for (int i = 0; i < Q; ++i) K += sm.V[i][tid];
+        float K = 0.f;
+#pragma unroll
+        for (int q = 0; q < kThreads / 32; ++q) K += sm.Kp[q][tid];
         const float w = sm.el[tid] * sm.d[tid] * sm.z[tid];
         sm.w[tid] = w;
-        sm.dcs[tid] = sm.ecs[tid] * uu + R - K - w;
+        sm.dcs[tid] = sm.ecs[tid] * sm.uu[tid] + sm.R[tid] - K - w;
         // d(raw dt) / d(d): softplus' = sigmoid, 0 outside the clamp
         const float u = sm.u[tid];
         const float dpre = p.dt_softplus ? softplus_f(u) : u;
@@ -333,7 +381,7 @@ bwd_chunk_kernel(Params p, const float *__restrict__ dtp, const float *__restric
             sm.dcs[t] = run;
         }
         for (int t = 0; t < Q; ++t) {
-            sD += sm.DX[t][t];  // E = 1 on the diagonal: dyp_t . x_t
+            sD += sm.dxd[t];
             if (k * Q + t >= L) continue;
             sA = fmaf(sm.d[t], sm.dcs[t], sA);
             sBias = fmaf(fmaf(A, sm.dcs[t], sm.dd1[t]), sm.u[t], sBias);

@@ -10,7 +10,8 @@
 // CUDA-core fp32 version (the exact plan).  One CTA per (batch*head, chunk,
 // tile of 32 tokens); 256 threads as 16 token rows x 16 head-dim lanes, each
 // owning 2 x (P/16) outputs.  C of the tile stays in shared memory; the
-// state, then B / x tiles of 32 tokens, stream through it.
+// state, then B / x tiles of 32 tokens, stream through it.  MT (4 or 8) bounds
+// the per-thread outputs at compile time, so P <= 64 issues no idle work.
 #include "ssd_internal.cuh"
 
 namespace ssd {
@@ -38,7 +39,7 @@ struct ScanSmem {
     float M[kTI][kTJ + 1];
 };
 
-template <int IO>
+template <int IO, int MT>
 __global__ void __launch_bounds__(kThreads)
 chunk_scan_kernel(Params p, const float *__restrict__ dtp, const float *__restrict__ cs,
                   const float *__restrict__ states) {
@@ -66,11 +67,11 @@ chunk_scan_kernel(Params p, const float *__restrict__ dtp, const float *__restri
         sm.C[i][n] = v;
     }
 
-    float acc[2][8];
+    float acc[2][MT];
 #pragma unroll
     for (int m = 0; m < 2; ++m)
 #pragma unroll
-        for (int a = 0; a < 8; ++a) acc[m][a] = 0.f;
+        for (int a = 0; a < MT; ++a) acc[m][a] = 0.f;
 
     // inter-chunk part: C_i . S_k[p, :]
     const float *S = states + ((((size_t)b * p.nchunks + k) * H + h) * P) * N;
@@ -85,7 +86,7 @@ chunk_scan_kernel(Params p, const float *__restrict__ dtp, const float *__restri
         for (int n = 0; n < kNC; ++n) {
             const float c0 = sm.C[ti][n0 + n], c1 = sm.C[ti + 16][n0 + n];
 #pragma unroll
-            for (int a = 0; a < 8; ++a) {
+            for (int a = 0; a < MT; ++a) {
                 if (a < PT) {
                     const float sv = sm.u.S[tp + 16 * a][n];
                     acc[0][a] = fmaf(c0, sv, acc[0][a]);
@@ -98,7 +99,7 @@ chunk_scan_kernel(Params p, const float *__restrict__ dtp, const float *__restri
         const float e0 = expf(sm.cs[min(i0 + ti, Q - 1)]);
         const float e1 = expf(sm.cs[min(i0 + ti + 16, Q - 1)]);
 #pragma unroll
-        for (int a = 0; a < 8; ++a) {
+        for (int a = 0; a < MT; ++a) {
             acc[0][a] *= e0;
             acc[1][a] *= e1;
         }
@@ -149,7 +150,7 @@ chunk_scan_kernel(Params p, const float *__restrict__ dtp, const float *__restri
         for (int j = 0; j < kTJ; ++j) {
             const float m0 = sm.M[ti][j], m1 = sm.M[ti + 16][j];
 #pragma unroll
-            for (int a = 0; a < 8; ++a) {
+            for (int a = 0; a < MT; ++a) {
                 if (a < PT) {
                     const float xv = sm.u.bx.X[j][tp + 16 * a];
                     acc[0][a] = fmaf(m0, xv, acc[0][a]);
@@ -168,7 +169,7 @@ chunk_scan_kernel(Params p, const float *__restrict__ dtp, const float *__restri
         if (i >= nI || t >= L) continue;
         const size_t rowoff = (((size_t)b * L + t) * H + h) * P;
 #pragma unroll
-        for (int a = 0; a < 8; ++a) {
+        for (int a = 0; a < MT; ++a) {
             if (a >= PT) continue;
             const int pp = tp + 16 * a;
             float v = acc[m][a];
@@ -179,6 +180,16 @@ chunk_scan_kernel(Params p, const float *__restrict__ dtp, const float *__restri
     }
 }
 
+template <int IO, int MT>
+cudaError_t run_scan(const Params &p, const float *dtp, const float *cs, const float *states, dim3 grid, size_t smem,
+                     cudaStream_t s) {
+    const cudaError_t err =
+        cudaFuncSetAttribute(chunk_scan_kernel<IO, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    chunk_scan_kernel<IO, MT><<<grid, kThreads, smem, s>>>(p, dtp, cs, states);
+    return cudaSuccess;
+}
+
 }  // namespace
 
 cudaError_t launch_chunk_scan(const Params &p, int io, const float *dtp, const float *cs,
@@ -187,23 +198,15 @@ cudaError_t launch_chunk_scan(const Params &p, int io, const float *dtp, const f
         return cudaErrorInvalidValue;
     const size_t smem = sizeof(ScanSmem);
     dim3 grid(p.B * p.H, p.nchunks, (p.Q + kTI - 1) / kTI);
+    const bool small = p.P <= 64;
     cudaError_t err = cudaSuccess;
     switch (io) {
-        case IO_F32:
-            err = cudaFuncSetAttribute(chunk_scan_kernel<IO_F32>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            if (err == cudaSuccess) chunk_scan_kernel<IO_F32><<<grid, kThreads, smem, s>>>(p, dtp, cs, states);
-            break;
-        case IO_F16:
-            err = cudaFuncSetAttribute(chunk_scan_kernel<IO_F16>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            if (err == cudaSuccess) chunk_scan_kernel<IO_F16><<<grid, kThreads, smem, s>>>(p, dtp, cs, states);
-            break;
-        case IO_BF16:
-            err = cudaFuncSetAttribute(chunk_scan_kernel<IO_BF16>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            if (err == cudaSuccess) chunk_scan_kernel<IO_BF16><<<grid, kThreads, smem, s>>>(p, dtp, cs, states);
-            break;
+        case IO_F32: err = small ? run_scan<IO_F32, 4>(p, dtp, cs, states, grid, smem, s)
+                                 : run_scan<IO_F32, 8>(p, dtp, cs, states, grid, smem, s); break;
+        case IO_F16: err = small ? run_scan<IO_F16, 4>(p, dtp, cs, states, grid, smem, s)
+                                 : run_scan<IO_F16, 8>(p, dtp, cs, states, grid, smem, s); break;
+        case IO_BF16: err = small ? run_scan<IO_BF16, 4>(p, dtp, cs, states, grid, smem, s)
+                                  : run_scan<IO_BF16, 8>(p, dtp, cs, states, grid, smem, s); break;
         default: return cudaErrorInvalidValue;
     }
     if (err != cudaSuccess) return err;

@@ -7,7 +7,8 @@
 // CUDA-core fp32 version (the exact plan): one CTA per (chunk, batch*head),
 // 256 threads as a 16 x 16 grid over (p, n), each owning a strided
 // (P/16) x (N/16) block of the [P,N] output.  Tokens stream through shared
-// memory 32 at a time.  Grid: x = batch*head, y = chunk.
+// memory 32 at a time.  Grid: x = batch*head, y = chunk.  MT (4 or 8) bounds
+// the block at compile time, so P, N <= 64 issue no idle multiply-adds.
 #include "ssd_internal.cuh"
 
 namespace ssd {
@@ -18,7 +19,7 @@ constexpr int kThreads = 256;
 constexpr int kTok = 32;
 constexpr int kMaxDim = 128;
 
-template <int IO>
+template <int IO, int MT>
 __global__ void __launch_bounds__(kThreads)
 chunk_state_kernel(Params p, const float *__restrict__ dtp, const float *__restrict__ cs,
                    float *__restrict__ states) {
@@ -34,11 +35,11 @@ chunk_state_kernel(Params p, const float *__restrict__ dtp, const float *__restr
     const size_t crow = (((size_t)b * p.H + h) * p.nchunks + k) * Q;
     const float cs_last = __ldg(cs + crow + Q - 1);
 
-    float acc[8][8];
+    float acc[MT][MT];
 #pragma unroll
-    for (int a = 0; a < 8; ++a)
+    for (int a = 0; a < MT; ++a)
 #pragma unroll
-        for (int c = 0; c < 8; ++c) acc[a][c] = 0.f;
+        for (int c = 0; c < MT; ++c) acc[a][c] = 0.f;
 
     for (int i0 = 0; i0 < Q; i0 += kTok) {
         const int ntok = min(kTok, Q - i0);
@@ -66,24 +67,24 @@ chunk_state_kernel(Params p, const float *__restrict__ dtp, const float *__restr
         }
         __syncthreads();
         for (int i = 0; i < ntok; ++i) {
-            float xv[8], bv[8];
+            float xv[MT], bv[MT];
 #pragma unroll
-            for (int a = 0; a < 8; ++a) xv[a] = (a < PT) ? xs[i][tp + 16 * a] : 0.f;
+            for (int a = 0; a < MT; ++a) xv[a] = (a < PT) ? xs[i][tp + 16 * a] : 0.f;
 #pragma unroll
-            for (int c = 0; c < 8; ++c) bv[c] = (c < NT) ? bs[i][tn + 16 * c] : 0.f;
+            for (int c = 0; c < MT; ++c) bv[c] = (c < NT) ? bs[i][tn + 16 * c] : 0.f;
 #pragma unroll
-            for (int a = 0; a < 8; ++a)
+            for (int a = 0; a < MT; ++a)
 #pragma unroll
-                for (int c = 0; c < 8; ++c) acc[a][c] = fmaf(xv[a], bv[c], acc[a][c]);
+                for (int c = 0; c < MT; ++c) acc[a][c] = fmaf(xv[a], bv[c], acc[a][c]);
         }
         __syncthreads();
     }
 
     float *out = states + ((((size_t)b * p.nchunks + k) * p.H + h) * P) * N;
 #pragma unroll
-    for (int a = 0; a < 8; ++a)
+    for (int a = 0; a < MT; ++a)
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
+        for (int c = 0; c < MT; ++c)
             if (a < PT && c < NT) out[(size_t)(tp + 16 * a) * N + tn + 16 * c] = acc[a][c];
 }
 
@@ -93,12 +94,17 @@ cudaError_t launch_chunk_state(const Params &p, int io, const float *dtp, const 
                                float *states, cudaStream_t s) {
     if (p.P > kMaxDim || p.N > kMaxDim || (p.P & 15) || (p.N & 15)) return cudaErrorInvalidValue;
     dim3 grid(p.B * p.H, p.nchunks);
+    const bool small = p.P <= 64 && p.N <= 64;
+#define SSD_STATE_LAUNCH(IOV)                                                                  \
+    if (small) chunk_state_kernel<IOV, 4><<<grid, kThreads, 0, s>>>(p, dtp, cs, states);       \
+    else chunk_state_kernel<IOV, 8><<<grid, kThreads, 0, s>>>(p, dtp, cs, states);
     switch (io) {
-        case IO_F32: chunk_state_kernel<IO_F32><<<grid, kThreads, 0, s>>>(p, dtp, cs, states); break;
-        case IO_F16: chunk_state_kernel<IO_F16><<<grid, kThreads, 0, s>>>(p, dtp, cs, states); break;
-        case IO_BF16: chunk_state_kernel<IO_BF16><<<grid, kThreads, 0, s>>>(p, dtp, cs, states); break;
+        case IO_F32: SSD_STATE_LAUNCH(IO_F32) break;
+        case IO_F16: SSD_STATE_LAUNCH(IO_F16) break;
+        case IO_BF16: SSD_STATE_LAUNCH(IO_BF16) break;
         default: return cudaErrorInvalidValue;
     }
+#undef SSD_STATE_LAUNCH
     return cudaGetLastError();
 }
 
