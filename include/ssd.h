@@ -171,9 +171,17 @@ ssd_status ssd_chunk_scan(const ssd_fwd_args *args, const float *dtp, const floa
  * End-to-end call with HOST buffers: every tensor pointer in args is host
  * memory (pinned for overlap; pageable works but serialises).  The library
  * copies the inputs into the device workspace, runs ssd_fwd there and copies
- * y and final_state back, all enqueued on `stream`; the host outputs are
- * valid after the caller synchronises the stream.  The workspace (device)
- * must hold ssd_fwd_host_workspace_size() bytes.
+ * y and final_state back; the host outputs are valid after the caller
+ * synchronises `stream`.  The batch is cut into up to 8 slices (one slice when
+ * a per-batch stride is not a multiple of 256 bytes): the copies in run on an
+ * internal stream, each slice's forward on `stream` once its inputs are in,
+ * its copies out on a second internal stream, so both copy directions and the
+ * kernels overlap.  Work enqueued on `stream` before the call is ordered before
+ * it, and the call as a whole is complete on `stream`.  The two internal
+ * streams and four events are created once per device on first use and kept
+ * until exit; concurrent calls from several threads are serialised while they
+ * enqueue.  The workspace (device) must hold ssd_fwd_host_workspace_size()
+ * bytes; the host buffers must stay valid until the stream completes.
  */
 ssd_status ssd_fwd_host_workspace_size(const ssd_fwd_args *args, size_t *bytes);
 ssd_status ssd_fwd_host(const ssd_fwd_args *args, void *stream);

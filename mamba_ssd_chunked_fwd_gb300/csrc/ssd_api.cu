@@ -1,11 +1,14 @@
 // ssd_api.cu -- the C ABI declared in include/ssd.h: argument validation,
 // plan choice, workspace layout and launches.  Everything here runs on the
 // host; nothing allocates device memory or synchronises a stream except
-// ssd_check_device_error.
+// ssd_check_device_error.  ssd_fwd_host creates, once per device, two copy
+// streams and four events for its pipeline.
 #include <math.h>
 #include <stdarg.h>
 #include <stdio.h>
 #include <string.h>
+
+#include <mutex>
 
 #include "ssd_fused.cuh"
 #include "ssd_internal.cuh"
@@ -619,6 +622,49 @@ HostLayout host_layout(const ssd_fwd_args *a, int32_t plan) {
     return l;
 }
 
+// The host-buffer pipeline: batch slices copied in on `in`, computed on the
+// caller's stream, copied out on `out`, so that the copies in both directions
+// and the kernels of different slices overlap.  One set per device, created on
+// first use; `mu` serialises the enqueue sequences of concurrent callers (the
+// events are re-recorded per slice).
+struct HostPipe {
+    bool ready = false;
+    cudaStream_t in = nullptr, out = nullptr;
+    cudaEvent_t start = nullptr, copied = nullptr, computed = nullptr, done = nullptr;
+};
+constexpr int kMaxDevices = 64;
+std::mutex g_pipe_mu;
+HostPipe g_pipes[kMaxDevices];
+
+cudaError_t host_pipe(HostPipe **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    HostPipe &hp = g_pipes[dev];
+    if (!hp.ready) {
+        if ((e = cudaStreamCreateWithFlags(&hp.in, cudaStreamNonBlocking)) != cudaSuccess) return e;
+        if ((e = cudaStreamCreateWithFlags(&hp.out, cudaStreamNonBlocking)) != cudaSuccess) return e;
+        for (cudaEvent_t *ev : {&hp.start, &hp.copied, &hp.computed, &hp.done})
+            if ((e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming)) != cudaSuccess) return e;
+        hp.ready = true;
+    }
+    *out = &hp;
+    return cudaSuccess;
+}
+
+// Batch entries per slice: up to 8 slices, and one slice when a per-batch
+// stride would break the 256-byte alignment of the device copies.
+int64_t host_slice_batch(const ssd_fwd_args *a) {
+    const size_t io = io_size(a->x_dtype);
+    const size_t strides[] = {(size_t)a->L * a->H * a->P * io, (size_t)a->L * a->H * 4,
+                              (size_t)a->L * a->G * a->N * io, (size_t)a->H * a->P * a->N * 4};
+    for (size_t st : strides)
+        if (st % kAlign != 0) return a->B;
+    const int64_t nslices = a->B < 8 ? a->B : 8;
+    return (a->B + nslices - 1) / nslices;
+}
+
 }  // namespace
 
 ssd_status ssd_fwd_host_workspace_size(const ssd_fwd_args *a, size_t *bytes) {
@@ -643,36 +689,89 @@ ssd_status ssd_fwd_host(const ssd_fwd_args *a, void *stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     char *ws = static_cast<char *>(a->workspace);
     const size_t io = io_size(a->x_dtype);
-    const size_t nx = (size_t)a->B * a->L * a->H * a->P;
-    const size_t nbc = (size_t)a->B * a->L * a->G * a->N;
-    const size_t nst = (size_t)a->B * a->H * a->P * a->N;
+    // per batch entry: elements of x / y / z, of dt, of B / C, of a state
+    const size_t ex = (size_t)a->L * a->H * a->P, edt = (size_t)a->L * a->H, ebc = (size_t)a->L * a->G * a->N;
+    const size_t est = (size_t)a->H * a->P * a->N;
+    // the whole call on the device copies, every slice on the same plan
     ssd_fwd_args d = *a;
-    cudaError_t e = cudaSuccess;
-    auto h2d = [&](size_t off, const void *src, size_t bytes) -> void * {
-        if (!src || bytes == 0) return nullptr;
-        if (e == cudaSuccess) e = cudaMemcpyAsync(ws + off, src, bytes, cudaMemcpyHostToDevice, s);
-        return ws + off;
-    };
-    d.x = h2d(l.x, a->x, nx * io);
-    d.dt = static_cast<const float *>(h2d(l.dt, a->dt, (size_t)a->B * a->L * a->H * 4));
-    d.A = static_cast<const float *>(h2d(l.A, a->A, (size_t)a->H * 4));
-    d.Bm = h2d(l.Bm, a->Bm, nbc * io);
-    d.Cm = h2d(l.Cm, a->Cm, nbc * io);
-    d.D = static_cast<const float *>(h2d(l.D, a->D, (size_t)a->H * 4));
-    d.z = h2d(l.z, a->z, nx * io);
-    d.dt_bias = static_cast<const float *>(h2d(l.dt_bias, a->dt_bias, (size_t)a->H * 4));
-    d.initial_state = static_cast<const float *>(h2d(l.h0, a->initial_state, nst * 4));
-    if (e != cudaSuccess) return cuda_fail(e, "host-to-device copy");
+    d.x = ws + l.x;
+    d.dt = reinterpret_cast<const float *>(ws + l.dt);
+    d.A = reinterpret_cast<const float *>(ws + l.A);
+    d.Bm = ws + l.Bm;
+    d.Cm = ws + l.Cm;
+    d.D = a->D ? reinterpret_cast<const float *>(ws + l.D) : nullptr;
+    d.z = a->z ? ws + l.z : nullptr;
+    d.dt_bias = a->dt_bias ? reinterpret_cast<const float *>(ws + l.dt_bias) : nullptr;
+    d.initial_state = a->initial_state ? reinterpret_cast<const float *>(ws + l.h0) : nullptr;
     d.y = ws + l.y;
     d.final_state = a->final_state ? reinterpret_cast<float *>(ws + l.fin) : nullptr;
     d.workspace = ws + l.fwd_ws;
     d.workspace_bytes = workspace_for(a, plan);
     d.plan = plan;
-    if ((st = ssd_fwd(&d, stream)) != SSD_OK) return st;
-    e = cudaMemcpyAsync(a->y, d.y, nx * io, cudaMemcpyDeviceToHost, s);
-    if (e == cudaSuccess && a->final_state)
-        e = cudaMemcpyAsync(a->final_state, d.final_state, nst * 4, cudaMemcpyDeviceToHost, s);
-    if (e != cudaSuccess) return cuda_fail(e, "device-to-host copy");
+    int64_t per = host_slice_batch(a);
+    auto slice = [&](int64_t b0, int64_t nb) {
+        ssd_fwd_args o = d;
+        o.B = nb;
+        o.x = static_cast<const char *>(d.x) + b0 * ex * io;
+        o.dt = d.dt + b0 * edt;
+        o.Bm = static_cast<const char *>(d.Bm) + b0 * ebc * io;
+        o.Cm = static_cast<const char *>(d.Cm) + b0 * ebc * io;
+        if (o.z) o.z = static_cast<const char *>(d.z) + b0 * ex * io;
+        if (o.initial_state) o.initial_state = d.initial_state + b0 * est;
+        o.y = static_cast<char *>(d.y) + b0 * ex * io;
+        if (o.final_state) o.final_state = d.final_state + b0 * est;
+        return o;
+    };
+    if (per < a->B) {  // every slice must take the call's plan
+        const ssd_fwd_args o = slice(0, per);
+        int32_t pl = 0;
+        if (ssd_fwd_resolve_plan(&o, &pl) != SSD_OK || pl != plan) per = a->B;
+    }
+    std::lock_guard<std::mutex> lock(g_pipe_mu);
+    HostPipe *hp = nullptr;
+    cudaError_t e = host_pipe(&hp);
+    if (e != cudaSuccess) return cuda_fail(e, "creating the copy streams");
+    // the copy streams start after the caller's earlier work on `stream`
+    if ((e = cudaEventRecord(hp->start, s)) != cudaSuccess) return cuda_fail(e, "event record");
+    if ((e = cudaStreamWaitEvent(hp->in, hp->start, 0)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(hp->out, hp->start, 0)) != cudaSuccess)
+        return cuda_fail(e, "stream wait");
+    auto h2d = [&](void *dst, const void *src, size_t bytes) {
+        if (e == cudaSuccess && src && bytes) e = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, hp->in);
+    };
+    auto d2h = [&](void *dst, const void *src, size_t bytes) {
+        if (e == cudaSuccess && dst && bytes) e = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToHost, hp->out);
+    };
+    h2d(ws + l.A, a->A, (size_t)a->H * 4);
+    h2d(ws + l.D, a->D, (size_t)a->H * 4);
+    h2d(ws + l.dt_bias, a->dt_bias, (size_t)a->H * 4);
+    ssd_status st2 = SSD_OK;
+    for (int64_t b0 = 0; b0 < a->B && e == cudaSuccess && st2 == SSD_OK; b0 += per) {
+        const int64_t nb = a->B - b0 < per ? a->B - b0 : per;
+        const ssd_fwd_args o = slice(b0, nb);
+        h2d(const_cast<void *>(o.x), static_cast<const char *>(a->x) + b0 * ex * io, nb * ex * io);
+        h2d(const_cast<float *>(o.dt), a->dt + b0 * edt, nb * edt * 4);
+        h2d(const_cast<void *>(o.Bm), static_cast<const char *>(a->Bm) + b0 * ebc * io, nb * ebc * io);
+        h2d(const_cast<void *>(o.Cm), static_cast<const char *>(a->Cm) + b0 * ebc * io, nb * ebc * io);
+        if (a->z) h2d(const_cast<void *>(o.z), static_cast<const char *>(a->z) + b0 * ex * io, nb * ex * io);
+        if (a->initial_state) h2d(const_cast<float *>(o.initial_state), a->initial_state + b0 * est, nb * est * 4);
+        if (e != cudaSuccess) break;
+        if ((e = cudaEventRecord(hp->copied, hp->in)) != cudaSuccess) break;
+        if ((e = cudaStreamWaitEvent(s, hp->copied, 0)) != cudaSuccess) break;
+        if ((st2 = ssd_fwd(&o, stream)) != SSD_OK) break;
+        if ((e = cudaEventRecord(hp->computed, s)) != cudaSuccess) break;
+        if ((e = cudaStreamWaitEvent(hp->out, hp->computed, 0)) != cudaSuccess) break;
+        d2h(static_cast<char *>(a->y) + b0 * ex * io, o.y, nb * ex * io);
+        if (a->final_state) d2h(a->final_state + b0 * est, o.final_state, nb * est * 4);
+    }
+    // join: the call is complete on `stream` once both copy streams are
+    cudaError_t ej = cudaEventRecord(hp->computed, hp->in);
+    if (ej == cudaSuccess) ej = cudaStreamWaitEvent(s, hp->computed, 0);
+    if (ej == cudaSuccess) ej = cudaEventRecord(hp->done, hp->out);
+    if (ej == cudaSuccess) ej = cudaStreamWaitEvent(s, hp->done, 0);
+    if (st2 != SSD_OK) return st2;
+    if (e != cudaSuccess) return cuda_fail(e, "host pipeline copy");
+    if (ej != cudaSuccess) return cuda_fail(ej, "joining the copy streams");
     return ok();
 }
 

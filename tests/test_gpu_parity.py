@@ -251,6 +251,70 @@ def test_host_buffer_entry_matches_device_entry():
     assert torch.equal(y, yd.cpu()) and torch.equal(fin, fd.cpu())
 
 
+def _host_call(ssd, inp, chunk, ops, stream=None):
+    h = {k: (v.contiguous().pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    y = torch.full_like(h["x"], float("nan")).pin_memory()
+    B, L, H, P = h["x"].shape
+    fin = torch.full((B, H, P, h["B"].shape[3]), float("nan")).pin_memory()
+    args = ssd.make_args(h["x"], h["dt"], h["A"], h["B"], h["C"], chunk, y=y, final_state=fin, D=h["D"], z=h["z"],
+                         dt_bias=h["dt_bias"], initial_states=h["initial_states"], dt_softplus=True, ops=ops)
+    nws = ssd.ssd_fwd_host_workspace_size(args)
+    ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
+    args.workspace, args.workspace_bytes = ws.data_ptr(), nws
+    ssd.ssd_fwd_host(args, stream)
+    return y, fin, (h, ws, args)
+
+
+@pytest.mark.parametrize("B,L,H,P,G,ops", [
+    (5, 192, 8, 64, 2, "bf16"),    # fused plan, 5 slices of one batch entry
+    (11, 128, 4, 64, 1, "bf16"),   # 6 slices of 2, the last of 1
+    (3, 33, 3, 16, 1, "f32"),      # per-batch strides not 256-byte multiples: one slice
+])
+def test_host_buffer_pipeline_matches_device_entry(B, L, H, P, G, ops):
+    import mamba_ssd_chunked_fwd_gb300 as ssd
+    _, inp = ssd_inputs.custom(B, L, H, P, 64 if P == 64 else 32, G, 64 if P == 64 else 16, seed=B + L,
+                               h0=True, D=True, z=True, dt_bias=True)
+    chunk = 64 if P == 64 else 16
+    d = to_device(inp)
+    yd, fd = ssd.mamba2_ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], chunk, dt_softplus=True,
+                                return_final_state=True, D=d["D"], z=d["z"], dt_bias=d["dt_bias"],
+                                initial_states=d["initial_states"], ops=ops)
+    y, fin, _ = _host_call(ssd, inp, chunk, ops)
+    torch.cuda.synchronize()
+    assert torch.equal(y, yd.cpu()) and torch.equal(fin, fd.cpu())
+
+
+def test_host_buffer_calls_back_to_back_stay_ordered():
+    """Two calls on one stream with no synchronisation between them: the
+    second call's copies in wait for the first call to finish."""
+    import mamba_ssd_chunked_fwd_gb300 as ssd
+    _, inp1 = ssd_inputs.custom(4, 256, 8, 64, 64, 2, 64, seed=61, h0=True)
+    _, inp2 = ssd_inputs.custom(4, 256, 8, 64, 64, 2, 64, seed=62, h0=True)
+    ref = []
+    for inp in (inp1, inp2):
+        d = to_device(inp)
+        ref.append(ssd.mamba2_ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], 64, dt_softplus=True,
+                                      return_final_state=True, initial_states=d["initial_states"], ops="bf16"))
+    h = {k: (v.contiguous().pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in inp1.items()}
+    h2 = {k: (v.contiguous().pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in inp2.items()}
+    outs = []
+    ws = None
+    for hh in (h, h2):
+        y = torch.full_like(hh["x"], float("nan")).pin_memory()
+        fin = torch.full((4, 8, 64, 64), float("nan")).pin_memory()
+        args = ssd.make_args(hh["x"], hh["dt"], hh["A"], hh["B"], hh["C"], 64, y=y, final_state=fin,
+                             initial_states=hh["initial_states"], dt_softplus=True, ops="bf16")
+        if ws is None:
+            nws = ssd.ssd_fwd_host_workspace_size(args)
+            ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
+        args.workspace, args.workspace_bytes = ws.data_ptr(), ws.numel()  # one workspace for both calls
+        ssd.ssd_fwd_host(args)
+        outs.append((y, fin, args))
+    torch.cuda.synchronize()
+    for (y, fin, _), (yr, fr) in zip(outs, ref):
+        assert torch.equal(y, yr.cpu()) and torch.equal(fin, fr.cpu())
+
+
 def test_small_workspace_is_an_error_not_a_fault():
     import mamba_ssd_chunked_fwd_gb300 as ssd
     _, inp = ssd_inputs.custom(1, 128, 2, 64, 64, 1, 64, seed=45)
