@@ -523,7 +523,10 @@ def run_bwd(args):
     flops = bwd_flops(w)
     tflops = flops / (ms * 1e-3) / 1e12
     alu = fp32_alu_peak_tflops()
-    launches = 10 + (d["z"] is not None)  # 3 (+1 with z) recompute, gate, adjoint, passing, chunk, 2 group sums, head sum
+    has_z = d["z"] is not None
+    # recompute 3 (+ chunk_scan with z); the gate (skipped for fp32 dy without z); adjoint, passing,
+    # chunk, 2 group sums, head sum
+    launches = 3 + has_z + (has_z or w.x_dtype != "f32") + 6
     line = {
         "metric": f"SSD backward tokens/s ({args.workload} {w.shape_tuple()})",
         "value": round(w.tokens / (ms * 1e-3), 1), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,

@@ -49,25 +49,6 @@ __global__ void bwd_gate_kernel(Params p, const void *dy, const void *ypre, floa
     st_io<IO>(dz, e, g * ld_io<IO>(ypre, e) * sg * (1.f + zv * (1.f - sg)));
 }
 
-// 16 outputs per thread as a 4 x 4 register tile of a 64 x 64 result: rows
-// r0 + 16 a, columns c0 + 16 b (r0 = tid / 16, c0 = tid % 16), so that a warp's
-// loads of one operand are broadcast and of the other conflict-free (rows of
-// 65 floats).  acc[a][b] += sum_k A(r, k) * B(c, k) over k < K.
-template <class FA, class FB>
-__device__ __forceinline__ void tile4x4(float (&acc)[4][4], int K, int r0, int c0, FA fa, FB fb) {
-    for (int k = 0; k < K; ++k) {
-        float av[4], bv[4];
-#pragma unroll
-        for (int a = 0; a < 4; ++a) av[a] = fa(r0 + 16 * a, k);
-#pragma unroll
-        for (int b = 0; b < 4; ++b) bv[b] = fb(c0 + 16 * b, k);
-#pragma unroll
-        for (int a = 0; a < 4; ++a)
-#pragma unroll
-            for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(av[a], bv[b], acc[a][b]);
-    }
-}
-
 __device__ __forceinline__ void zero4x4(float (&acc)[4][4]) {
 #pragma unroll
     for (int a = 0; a < 4; ++a)
@@ -75,24 +56,79 @@ __device__ __forceinline__ void zero4x4(float (&acc)[4][4]) {
         for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
 }
 
+// ---- 4 x 4 register tiles over shared operands (adjoint and chunk kernels) ----
+// Every product is a 64 x 64 result in 4 x 4 register tiles: thread (r0, c0)
+// = (tid / 16, tid % 16) owns rows 4 r0 .. 4 r0 + 3 and columns 4 c0 .. 4 c0 + 3,
+// and each step of the contraction reads one float4 of each operand from
+// shared memory.  Operands are 64 x 64 fp32 in one of two layouts:
+//   N: element (r, c) at [r][c];
+//   T: element (r, c) at row c, 16-byte chunk (r / 4) ^ s(c) with
+//      s(c) = (c % 8) ^ ((c / 4) % 8), so that four consecutive r at one c are
+//      one aligned float4.  16-byte accesses are served 8 lanes at a time, and
+//      s keeps those 8 lanes on 8 different bank groups in every pattern used
+//      here: one row at 8 consecutive chunks, one chunk of 8 consecutive rows,
+//      and one chunk of rows 4 j + o for 8 consecutive j.
+// A product sum_k A(r, k) B(c, k) reads A as row k, chunk r0 (the same float4
+// for a half warp) and B as row k, chunk c0.
+__device__ __forceinline__ int tsw(int row, int chunk) {
+    return row * kMax + 4 * (chunk ^ ((row & 7) ^ ((row >> 2) & 7)));
+}
+__device__ __forceinline__ float4 ld4n(const float *m, int row, int chunk) {
+    return *reinterpret_cast<const float4 *>(m + row * kMax + 4 * chunk);
+}
+__device__ __forceinline__ float4 ld4t(const float *m, int row, int chunk) {
+    return *reinterpret_cast<const float4 *>(m + tsw(row, chunk));
+}
+__device__ __forceinline__ void st4n(float *m, int row, int chunk, float4 v) {
+    *reinterpret_cast<float4 *>(m + row * kMax + 4 * chunk) = v;
+}
+__device__ __forceinline__ void st4t(float *m, int row, int chunk, float4 v) {
+    *reinterpret_cast<float4 *>(m + tsw(row, chunk)) = v;
+}
+__device__ __forceinline__ float f4(const float4 &v, int i) { return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w; }
+
+// acc[a][b] += sum_{k0 <= k < k1} A(4 r0 + a, k) B(4 c0 + b, k); fa(k), fb(k)
+// return the float4s; k1 - k0 is a multiple of 4.
+template <class FA, class FB>
+__device__ __forceinline__ void tile4v(float (&acc)[4][4], int k0, int k1, FA fa, FB fb) {
+#pragma unroll 4
+    for (int k = k0; k < k1; ++k) {
+        const float4 av = fa(k), bv = fb(k);
+        const float ar[4] = {av.x, av.y, av.z, av.w}, br[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(ar[a], br[b], acc[a][b]);
+    }
+}
+
+// sum over the 16 lanes of a half warp (lanes sharing a tile's rows)
+__device__ __forceinline__ float half_warp_sum(float v) {
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    return v;
+}
+
+
 // ---- per chunk: sum_i exp(cs_i) dyp_i (outer) C_i  [P,N] ----
 template <int IO>
 __global__ void __launch_bounds__(kThreads)
 bwd_chunk_adjoint_kernel(Params p, const float *__restrict__ cs, const float *__restrict__ dyp,
                          float *__restrict__ adj) {
-    __shared__ float ds[kMax][kMax + 1];  // [i][p]
-    __shared__ float cc[kMax][kMax + 1];  // [i][n]
+    __shared__ __align__(16) float ds[kMax * kMax];  // exp(cs_i) dyp_i, [i][p] (N)
+    __shared__ __align__(16) float cc[kMax * kMax];  // C, [i][n] (N)
     const int k = blockIdx.y, bh = blockIdx.x;
     const int b = bh / p.H, h = bh % p.H, g = h / p.hpg;
-    const int P = p.P, N = p.N, Q = p.Q, L = p.L;
+    const int P = p.P, N = p.N, Q = p.Q, L = p.L, tid = threadIdx.x;
     const size_t crow = (((size_t)b * p.H + h) * p.nchunks + k) * Q;
     {
         // every global load issued before the shared-memory stores; 0 outside (Q, P, N) and past L
         constexpr int kPer = kMax * kMax / kThreads;
+        const int col = tid & (kMax - 1), rb = tid >> 6;
         float rd[kPer], rc[kPer], re[kPer];
 #pragma unroll
         for (int q = 0; q < kPer; ++q) {
-            const int e = threadIdx.x + kThreads * q, i = e >> 6, col = e & (kMax - 1), t = k * Q + i;
+            const int i = rb * kPer + q, t = k * Q + i;
             const bool row_in = i < Q && t < L;
             rd[q] = row_in && col < P ? __ldg(dyp + (((size_t)b * L + t) * p.H + h) * P + col) : 0.f;
             rc[q] = row_in && col < N ? ld_io<IO>(p.Cm, (((size_t)b * L + t) * p.G + g) * N + col) : 0.f;
@@ -100,24 +136,24 @@ bwd_chunk_adjoint_kernel(Params p, const float *__restrict__ cs, const float *__
         }
 #pragma unroll
         for (int q = 0; q < kPer; ++q) {
-            const int e = threadIdx.x + kThreads * q, i = e >> 6, col = e & (kMax - 1);
-            ds[i][col] = rd[q] * expf(re[q]);
-            cc[i][col] = rc[q];
+            const int i = rb * kPer + q;
+            ds[i * kMax + col] = rd[q] * expf(re[q]);
+            cc[i * kMax + col] = rc[q];
         }
     }
     __syncthreads();
-    const int r0 = threadIdx.x >> 4, c0 = threadIdx.x & 15;
+    const int r0 = tid >> 4, c0 = tid & 15;
     float acc[4][4];
     zero4x4(acc);
-    tile4x4(acc, Q, r0, c0, [&](int pp, int i) { return ds[i][pp]; }, [&](int n, int i) { return cc[i][n]; });
+    tile4v(acc, 0, Q, [&](int i) { return ld4n(ds, i, r0); }, [&](int i) { return ld4n(cc, i, c0); });
     float *out = adj + ((((size_t)b * p.nchunks + k) * p.H + h) * P) * N;
 #pragma unroll
-    for (int a = 0; a < 4; ++a)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const int pp = r0 + 16 * a, n = c0 + 16 * c;
-            if (pp < P && n < N) out[(size_t)pp * N + n] = acc[a][c];
-        }
+    for (int a = 0; a < 4; ++a) {
+        const int pp = 4 * r0 + a;
+        if (pp < P && 4 * c0 < N)
+            *reinterpret_cast<float4 *>(out + (size_t)pp * N + 4 * c0) =
+                make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
+    }
 }
 
 // ---- reverse state passing: adj[k] <- G_k (adjoint at the end of chunk k), dh0 ----
@@ -152,26 +188,22 @@ bwd_state_passing_kernel(Params p, const float *__restrict__ cs, const float *__
 }
 
 // ---- within one chunk: dx, dB, dC (per head), ddt, and partial dA, dD, dbias ----
-// Row sums of 4 x 4 tiles reduce over the 16 lanes that share a tile row
-// (a half warp); column sums over the two tile rows of a warp, then over the
-// 8 warps through shared memory in warp order.  Every order is fixed.
+// Row sums of a tile reduce over the 16 lanes that share its rows (a half
+// warp); column sums over the two tile rows of a warp, then over the 8 warps
+// through shared memory in warp order.  Every order is fixed.  The masked
+// products stop at the warp's own rows: (E CB)[i][t] and (E DX)[i][t] vanish
+// for i < t.
 struct ChunkSmem {
-    float x[kMax][kMax + 1], dy[kMax][kMax + 1], B[kMax][kMax + 1], C[kMax][kMax + 1];
-    float S[kMax][kMax + 1], Gm[kMax][kMax + 1];
-    float CB[kMax][kMax + 1];  // E CB (masked decayed C B^T)
-    float DX[kMax][kMax + 1];  // E DX d_j (masked decayed dyp x^T, column j scaled by d_j)
+    float xt[kMax * kMax], dyt[kMax * kMax], dy[kMax * kMax];  // x^T, dyp^T (T); dyp (N)
+    float Bt[kMax * kMax], B[kMax * kMax], Ct[kMax * kMax], C[kMax * kMax];
+    float S[kMax * kMax], G[kMax * kMax], Gt[kMax * kMax];  // S, G [p][n] (N); G^T (T)
+    float CB[kMax * kMax];                                  // E CB (N)
+    float DX[kMax * kMax], DXt[kMax * kMax];                // E DX d_j (N and T)
     float Kp[kThreads / 32][kMax];
     float cs[kMax], d[kMax], ecs[kMax], el[kMax], dd1[kMax], w[kMax], z[kMax], dcs[kMax], u[kMax];
     float R[kMax], uu[kMax], dxd[kMax];
     float red[kThreads / 32];
 };
-
-// sum over the 16 lanes of a half warp (lanes sharing a tile row)
-__device__ __forceinline__ float half_warp_sum(float v) {
-#pragma unroll
-    for (int off = 8; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-    return v;
-}
 
 template <int IO>
 __global__ void __launch_bounds__(kThreads)
@@ -179,20 +211,22 @@ bwd_chunk_kernel(Params p, const float *__restrict__ dtp, const float *__restric
                  const float *__restrict__ states, const float *__restrict__ adj, const float *__restrict__ dyp,
                  void *dx, float *__restrict__ ddt, float *__restrict__ dBh, float *__restrict__ dCh,
                  float *__restrict__ partA, float *__restrict__ partD, float *__restrict__ partBias) {
-    extern __shared__ unsigned char smem_raw[];
+    extern __shared__ __align__(16) unsigned char smem_raw[];
     ChunkSmem &sm = *reinterpret_cast<ChunkSmem *>(smem_raw);
     const int k = blockIdx.y, bh = blockIdx.x;
     const int b = bh / p.H, h = bh % p.H, g = h / p.hpg;
     const int P = p.P, N = p.N, Q = p.Q, L = p.L, tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
-    const int r0 = tid >> 4, c0 = tid & 15;  // 4 x 4 tiles of 64 x 64 results
+    const int r0 = tid >> 4, c0 = tid & 15;
     const size_t crow = (((size_t)b * p.H + h) * p.nchunks + k) * Q;
     const size_t st_off = ((((size_t)b * p.nchunks + k) * p.H + h) * P) * N;
     const float A = __ldg(p.A + h);
     const float Dh = p.D ? __ldg(p.D + h) : 0.f;
 
-    // (1) tiles, every global load issued before the shared-memory stores.
+    // (1) operands, every global load issued before the shared-memory stores.
     //     Outside (Q, P, N) and past L: 0, and d = 0 (cs keeps its last value).
+    //     Thread: column col of rows 16 rb .. 16 rb + 15 (coalesced rows; four
+    //     float4 of consecutive rows for the T copies).
     if (tid < kMax) {
         const int e = tid;
         const bool inq = e < Q, in = inq && k * Q + e < L;
@@ -204,31 +238,40 @@ bwd_chunk_kernel(Params p, const float *__restrict__ dtp, const float *__restric
         sm.u[e] = u;
     }
     {
-        constexpr int kPer = kMax * kMax / kThreads;  // 16 elements per thread and tile
-        float rx[kPer], rdy[kPer], rb[kPer], rc[kPer], rs[kPer], rg[kPer];
+        constexpr int kPer = kMax * kMax / kThreads;  // 16
+        const int col = tid & (kMax - 1), rb = tid >> 6;
+        float rx[kPer], rdy[kPer], rb_[kPer], rc[kPer], rs[kPer], rg[kPer];
 #pragma unroll
         for (int q = 0; q < kPer; ++q) {
-            const int e = tid + kThreads * q, i = e >> 6, col = e & (kMax - 1), t = k * Q + i;
+            const int i = rb * kPer + q, t = k * Q + i;
             const bool row_in = i < Q && t < L;
             const size_t ox = (((size_t)b * L + t) * p.H + h) * P + col;
             const size_t ob = (((size_t)b * L + t) * p.G + g) * N + col;
             rx[q] = row_in && col < P ? ld_io<IO>(p.x, ox) : 0.f;
             rdy[q] = row_in && col < P ? __ldg(dyp + ox) : 0.f;
-            rb[q] = row_in && col < N ? ld_io<IO>(p.Bm, ob) : 0.f;
+            rb_[q] = row_in && col < N ? ld_io<IO>(p.Bm, ob) : 0.f;
             rc[q] = row_in && col < N ? ld_io<IO>(p.Cm, ob) : 0.f;
-            const bool sin = i < P && col < N;  // i: state row p, col: n
+            const bool sin = i < P && col < N;  // state row p = i, column n = col
             rs[q] = sin ? __ldg(states + st_off + (size_t)i * N + col) : 0.f;
             rg[q] = sin ? __ldg(adj + st_off + (size_t)i * N + col) : 0.f;
         }
 #pragma unroll
         for (int q = 0; q < kPer; ++q) {
-            const int e = tid + kThreads * q, i = e >> 6, col = e & (kMax - 1);
-            sm.x[i][col] = rx[q];
-            sm.dy[i][col] = rdy[q];
-            sm.B[i][col] = rb[q];
-            sm.C[i][col] = rc[q];
-            sm.S[i][col] = rs[q];
-            sm.Gm[i][col] = rg[q];
+            const int i = rb * kPer + q;
+            sm.dy[i * kMax + col] = rdy[q];
+            sm.B[i * kMax + col] = rb_[q];
+            sm.C[i * kMax + col] = rc[q];
+            sm.S[i * kMax + col] = rs[q];
+            sm.G[i * kMax + col] = rg[q];
+        }
+#pragma unroll
+        for (int m = 0; m < kPer / 4; ++m) {
+            const int ch = rb * (kPer / 4) + m;  // chunk of rows 16 rb + 4 m .. + 3
+            st4t(sm.xt, col, ch, make_float4(rx[4 * m], rx[4 * m + 1], rx[4 * m + 2], rx[4 * m + 3]));
+            st4t(sm.dyt, col, ch, make_float4(rdy[4 * m], rdy[4 * m + 1], rdy[4 * m + 2], rdy[4 * m + 3]));
+            st4t(sm.Bt, col, ch, make_float4(rb_[4 * m], rb_[4 * m + 1], rb_[4 * m + 2], rb_[4 * m + 3]));
+            st4t(sm.Ct, col, ch, make_float4(rc[4 * m], rc[4 * m + 1], rc[4 * m + 2], rc[4 * m + 3]));
+            st4t(sm.Gt, col, ch, make_float4(rg[4 * m], rg[4 * m + 1], rg[4 * m + 2], rg[4 * m + 3]));
         }
     }
     __syncthreads();
@@ -244,108 +287,148 @@ bwd_chunk_kernel(Params p, const float *__restrict__ dtp, const float *__restric
         float cb[4][4], dxm[4][4];
         zero4x4(cb);
         zero4x4(dxm);
-        tile4x4(cb, N, r0, c0, [&](int i, int n) { return sm.C[i][n]; }, [&](int j, int n) { return sm.B[j][n]; });
-        tile4x4(dxm, P, r0, c0, [&](int i, int pp) { return sm.dy[i][pp]; },
-                [&](int j, int pp) { return sm.x[j][pp]; });
+        tile4v(cb, 0, N, [&](int n) { return ld4t(sm.Ct, n, r0); }, [&](int n) { return ld4t(sm.Bt, n, c0); });
+        tile4v(dxm, 0, P, [&](int pp) { return ld4t(sm.dyt, pp, r0); }, [&](int pp) { return ld4t(sm.xt, pp, c0); });
         float rp[4] = {0.f, 0.f, 0.f, 0.f}, cp[4] = {0.f, 0.f, 0.f, 0.f};
+        float dm[4][4];
 #pragma unroll
-        for (int a = 0; a < 4; ++a)
+        for (int a = 0; a < 4; ++a) {
+            const int i = 4 * r0 + a;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                const int i = r0 + 16 * a, j = c0 + 16 * c;
+                const int j = 4 * c0 + c;
                 const float E = (i < Q && j <= i) ? expf(sm.cs[i] - sm.cs[j]) : 0.f;
-                const float a1 = E * cb[a][c], dm = E * dxm[a][c] * sm.d[j];
-                const float v = a1 * dxm[a][c] * sm.d[j];
+                const float dj = sm.d[j];
+                const float a1 = E * cb[a][c];
+                dm[a][c] = E * dxm[a][c] * dj;
+                const float v = a1 * dxm[a][c] * dj;
                 rp[a] += v;
                 cp[c] += v;
-                sm.CB[i][j] = a1;
-                sm.DX[i][j] = dm;
+                cb[a][c] = a1;
                 if (i == j) sm.dxd[i] = dxm[a][c];  // E = 1 on the diagonal: dyp_i . x_i
             }
+            st4n(sm.CB, i, c0, make_float4(cb[a][0], cb[a][1], cb[a][2], cb[a][3]));
+            st4n(sm.DX, i, c0, make_float4(dm[a][0], dm[a][1], dm[a][2], dm[a][3]));
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) st4t(sm.DXt, 4 * c0 + c, r0, make_float4(dm[0][c], dm[1][c], dm[2][c], dm[3][c]));
 #pragma unroll
         for (int a = 0; a < 4; ++a) {
             const float r = half_warp_sum(rp[a]);
-            if (c0 == 0) sm.R[r0 + 16 * a] = r;
+            if (c0 == 0) sm.R[4 * r0 + a] = r;
         }
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
             const float s = cp[c] + __shfl_xor_sync(0xffffffffu, cp[c], 16);  // tile rows 2w and 2w+1
-            if (lane < 16) sm.Kp[warp][c0 + 16 * c] = s;
+            if (lane < 16) sm.Kp[warp][4 * c0 + c] = s;
         }
     }
     __syncthreads();
+    const int tri_lo = 8 * warp;                              // first row of the warp's tiles
+    const int tri_hi = min(8 * warp + 8, Q);                  // one past its last row (within Q)
     // (4) dxs = (E CB)^T dyp + el (G B)  (rows t, columns p) -> dx = d dxs + D dyp,
-    //     dd1_t = x_t . dxs_t, z_t = x_t . (G B_t)
-    // (5) dB_t = (E DX d)^T C + d_t el_t G^T x_t  (rows t, columns n)
+    //     dd1_t = x_t . dxs_t, z_t = x_t . (G B_t).  (E CB)[i][t] = 0 for i < t.
     {
         float acc[4][4], gb[4][4];
         zero4x4(acc);
         zero4x4(gb);
-        tile4x4(acc, Q, r0, c0, [&](int t, int i) { return sm.CB[i][t]; }, [&](int pp, int i) { return sm.dy[i][pp]; });
-        tile4x4(gb, N, r0, c0, [&](int t, int n) { return sm.B[t][n]; }, [&](int pp, int n) { return sm.Gm[pp][n]; });
+        tile4v(acc, tri_lo < Q ? tri_lo : Q, Q, [&](int i) { return ld4n(sm.CB, i, r0); },
+               [&](int i) { return ld4n(sm.dy, i, c0); });
+        tile4v(gb, 0, N, [&](int n) { return ld4t(sm.Bt, n, r0); }, [&](int n) { return ld4t(sm.Gt, n, c0); });
+        float4 xx[4], dd[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) xx[c] = ld4t(sm.xt, 4 * c0 + c, r0);  // x at rows 4 r0 .., column 4 c0 + c
+#pragma unroll
+        for (int a = 0; a < 4; ++a) dd[a] = ld4n(sm.dy, 4 * r0 + a, c0);
         float dp[4] = {0.f, 0.f, 0.f, 0.f}, zp[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int a = 0; a < 4; ++a)
+        for (int a = 0; a < 4; ++a) {
+            const int t = 4 * r0 + a;
+            const float elt = sm.el[t], dt_ = sm.d[t];
+            const bool row_ok = t < Q && k * Q + t < L;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                const int t = r0 + 16 * a, pp = c0 + 16 * c;
-                const float T = fmaf(sm.el[t], gb[a][c], acc[a][c]);
-                const float xv = sm.x[t][pp];
+                const int pp = 4 * c0 + c;
+                const float T = fmaf(elt, gb[a][c], acc[a][c]);
+                const float xv = f4(xx[c], a);
                 dp[a] = fmaf(xv, T, dp[a]);
                 zp[a] = fmaf(xv, gb[a][c], zp[a]);
-                if (t < Q && pp < P && k * Q + t < L)
-                    st_io<IO>(dx, (((size_t)b * L + k * Q + t) * p.H + h) * P + pp,
-                              fmaf(sm.d[t], T, Dh * sm.dy[t][pp]));
+                if (row_ok && pp < P)
+                    st_io<IO>(dx, (((size_t)b * L + k * Q + t) * p.H + h) * P + pp, fmaf(dt_, T, Dh * f4(dd[a], c)));
             }
+        }
 #pragma unroll
         for (int a = 0; a < 4; ++a) {
             const float s1 = half_warp_sum(dp[a]), s2 = half_warp_sum(zp[a]);
             if (c0 == 0) {
-                sm.dd1[r0 + 16 * a] = s1;
-                sm.z[r0 + 16 * a] = s2;
+                sm.dd1[4 * r0 + a] = s1;
+                sm.z[4 * r0 + a] = s2;
             }
         }
+    }
+    // (5) dB_t = (E DX d)^T C + d_t el_t G^T x_t  (rows t, columns n).  (E DX)[i][t] = 0 for i < t.
+    {
+        float acc[4][4], gb[4][4];
         zero4x4(acc);
         zero4x4(gb);
-        tile4x4(acc, Q, r0, c0, [&](int t, int i) { return sm.DX[i][t]; }, [&](int n, int i) { return sm.C[i][n]; });
-        tile4x4(gb, P, r0, c0, [&](int t, int pp) { return sm.x[t][pp]; }, [&](int n, int pp) { return sm.Gm[pp][n]; });
+        tile4v(acc, tri_lo < Q ? tri_lo : Q, Q, [&](int i) { return ld4n(sm.DX, i, r0); },
+               [&](int i) { return ld4n(sm.C, i, c0); });
+        tile4v(gb, 0, P, [&](int pp) { return ld4t(sm.xt, pp, r0); }, [&](int pp) { return ld4n(sm.G, pp, c0); });
 #pragma unroll
-        for (int a = 0; a < 4; ++a)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int t = r0 + 16 * a, n = c0 + 16 * c;
-                if (t < Q && n < N && k * Q + t < L)
-                    dBh[(((size_t)b * L + k * Q + t) * p.H + h) * N + n] =
-                        fmaf(sm.d[t] * sm.el[t], gb[a][c], acc[a][c]);
+        for (int a = 0; a < 4; ++a) {
+            const int t = 4 * r0 + a;
+            if (t < Q && k * Q + t < L && 4 * c0 < N) {
+                const float f = sm.d[t] * sm.el[t];
+                float4 o;
+                o.x = fmaf(f, gb[a][0], acc[a][0]);
+                o.y = fmaf(f, gb[a][1], acc[a][1]);
+                o.z = fmaf(f, gb[a][2], acc[a][2]);
+                o.w = fmaf(f, gb[a][3], acc[a][3]);
+                *reinterpret_cast<float4 *>(dBh + (((size_t)b * L + k * Q + t) * p.H + h) * N + 4 * c0) = o;
             }
+        }
     }
-    // (6) dC_i = ecs_i (S^T dyp_i) + (E DX d) B ;  uu_i = C_i . (S^T dyp_i)  (rows i, columns n)
+    // (6) dC_i = ecs_i (S^T dyp_i) + (E DX d) B ;  uu_i = C_i . (S^T dyp_i)  (rows i, columns n).
+    //     (E DX)[i][j] = 0 for j > i.
     {
         float sd[4][4], acc[4][4];
         zero4x4(sd);
         zero4x4(acc);
-        tile4x4(sd, P, r0, c0, [&](int i, int pp) { return sm.dy[i][pp]; }, [&](int n, int pp) { return sm.S[pp][n]; });
-        tile4x4(acc, Q, r0, c0, [&](int i, int j) { return sm.DX[i][j]; }, [&](int n, int j) { return sm.B[j][n]; });
+        tile4v(sd, 0, P, [&](int pp) { return ld4t(sm.dyt, pp, r0); }, [&](int pp) { return ld4n(sm.S, pp, c0); });
+        tile4v(acc, 0, tri_hi > 0 ? tri_hi : 0, [&](int j) { return ld4t(sm.DXt, j, r0); },
+               [&](int j) { return ld4n(sm.B, j, c0); });
         float up[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int a = 0; a < 4; ++a)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int i = r0 + 16 * a, n = c0 + 16 * c;
-                up[a] = fmaf(sm.C[i][n], sd[a][c], up[a]);
-                if (i < Q && n < N && k * Q + i < L)
-                    dCh[(((size_t)b * L + k * Q + i) * p.H + h) * N + n] = fmaf(sm.ecs[i], sd[a][c], acc[a][c]);
+        for (int a = 0; a < 4; ++a) {
+            const int i = 4 * r0 + a;
+            const float4 cv = ld4n(sm.C, i, c0);
+            up[a] = fmaf(cv.x, sd[a][0], fmaf(cv.y, sd[a][1], fmaf(cv.z, sd[a][2], fmaf(cv.w, sd[a][3], up[a]))));
+            if (i < Q && k * Q + i < L && 4 * c0 < N) {
+                const float e = sm.ecs[i];
+                float4 o;
+                o.x = fmaf(e, sd[a][0], acc[a][0]);
+                o.y = fmaf(e, sd[a][1], acc[a][1]);
+                o.z = fmaf(e, sd[a][2], acc[a][2]);
+                o.w = fmaf(e, sd[a][3], acc[a][3]);
+                *reinterpret_cast<float4 *>(dCh + (((size_t)b * L + k * Q + i) * p.H + h) * N + 4 * c0) = o;
             }
+        }
 #pragma unroll
         for (int a = 0; a < 4; ++a) {
             const float s = half_warp_sum(up[a]);
-            if (c0 == 0) sm.uu[r0 + 16 * a] = s;
+            if (c0 == 0) sm.uu[4 * r0 + a] = s;
         }
     }
     // <G, S>: per warp, then over the warps in order
     {
         float part = 0.f;
-        for (int e = tid; e < kMax * kMax; e += kThreads) part = fmaf(sm.Gm[e >> 6][e & 63], sm.S[e >> 6][e & 63], part);
+#pragma unroll
+        for (int q = 0; q < kMax * kMax / 4 / kThreads; ++q) {
+            const int e4 = tid + kThreads * q;  // float4 index
+            const float4 gv = reinterpret_cast<const float4 *>(sm.G)[e4];
+            const float4 sv = reinterpret_cast<const float4 *>(sm.S)[e4];
+            part = fmaf(gv.x, sv.x, fmaf(gv.y, sv.y, fmaf(gv.z, sv.z, fmaf(gv.w, sv.w, part))));
+        }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
         if (lane == 0) sm.red[warp] = part;
@@ -397,17 +480,28 @@ bwd_chunk_kernel(Params p, const float *__restrict__ dtp, const float *__restric
 }
 
 // ---- dB, dC: heads of a group summed; dA, dD, dbias: (batch, chunk) summed ----
+// Four consecutive n per thread (N is a multiple of 16), heads in order.
 template <int IO>
 __global__ void bwd_group_sum_kernel(Params p, const float *__restrict__ perhead, void *out) {
-    const size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x;  // element of [B,L,G,N]
-    const size_t total = (size_t)p.B * p.L * p.G * p.N;
-    if (e >= total) return;
-    const int n = e % p.N;
-    const size_t bt = e / ((size_t)p.G * p.N);
-    const int g = (e / p.N) % p.G;
-    float acc = 0.f;
-    for (int hh = 0; hh < p.hpg; ++hh) acc += perhead[(bt * p.H + g * p.hpg + hh) * p.N + n];
-    st_io<IO>(out, e, acc);
+    const size_t e4 = (size_t)blockIdx.x * blockDim.x + threadIdx.x;  // float4 of [B,L,G,N]
+    const int N4 = p.N / 4;
+    if (e4 >= (size_t)p.B * p.L * p.G * N4) return;
+    const int n4 = (int)(e4 % N4);
+    const int g = (int)((e4 / N4) % p.G);
+    const size_t bt = e4 / ((size_t)p.G * N4);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int hh = 0; hh < p.hpg; ++hh) {
+        const float4 v = __ldg(reinterpret_cast<const float4 *>(perhead + (bt * p.H + g * p.hpg + hh) * p.N) + n4);
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
+    }
+    const size_t e = e4 * 4;
+    st_io<IO>(out, e, acc.x);
+    st_io<IO>(out, e + 1, acc.y);
+    st_io<IO>(out, e + 2, acc.z);
+    st_io<IO>(out, e + 3, acc.w);
 }
 
 __global__ void bwd_head_sum_kernel(Params p, const float *__restrict__ partA, const float *__restrict__ partD,
@@ -433,17 +527,23 @@ size_t bwd_chunk_smem_bytes() { return sizeof(ChunkSmem); }
 cudaError_t launch_bwd(const Params &p, int io, const BwdBuffers &w, cudaStream_t s) {
     const size_t count = (size_t)p.B * p.L * p.H * p.P;
     const unsigned eb = (unsigned)((count + 255) / 256);
-    switch (io) {
-        case IO_F32: bwd_gate_kernel<IO_F32><<<eb, 256, 0, s>>>(p, w.dy, w.ypre, w.dyp, w.dz, count); break;
-        case IO_F16: bwd_gate_kernel<IO_F16><<<eb, 256, 0, s>>>(p, w.dy, w.ypre, w.dyp, w.dz, count); break;
-        case IO_BF16: bwd_gate_kernel<IO_BF16><<<eb, 256, 0, s>>>(p, w.dy, w.ypre, w.dyp, w.dz, count); break;
-        default: return cudaErrorInvalidValue;
+    // without z the gate is the identity: fp32 dy is read in place
+    const float *dyp = w.dyp;
+    if (!p.z && io == IO_F32) {
+        dyp = static_cast<const float *>(w.dy);
+    } else {
+        switch (io) {
+            case IO_F32: bwd_gate_kernel<IO_F32><<<eb, 256, 0, s>>>(p, w.dy, w.ypre, w.dyp, w.dz, count); break;
+            case IO_F16: bwd_gate_kernel<IO_F16><<<eb, 256, 0, s>>>(p, w.dy, w.ypre, w.dyp, w.dz, count); break;
+            case IO_BF16: bwd_gate_kernel<IO_BF16><<<eb, 256, 0, s>>>(p, w.dy, w.ypre, w.dyp, w.dz, count); break;
+            default: return cudaErrorInvalidValue;
+        }
     }
     const dim3 grid(p.B * p.H, p.nchunks);
     switch (io) {
-        case IO_F32: bwd_chunk_adjoint_kernel<IO_F32><<<grid, kThreads, 0, s>>>(p, w.cs, w.dyp, w.adj); break;
-        case IO_F16: bwd_chunk_adjoint_kernel<IO_F16><<<grid, kThreads, 0, s>>>(p, w.cs, w.dyp, w.adj); break;
-        case IO_BF16: bwd_chunk_adjoint_kernel<IO_BF16><<<grid, kThreads, 0, s>>>(p, w.cs, w.dyp, w.adj); break;
+        case IO_F32: bwd_chunk_adjoint_kernel<IO_F32><<<grid, kThreads, 0, s>>>(p, w.cs, dyp, w.adj); break;
+        case IO_F16: bwd_chunk_adjoint_kernel<IO_F16><<<grid, kThreads, 0, s>>>(p, w.cs, dyp, w.adj); break;
+        case IO_BF16: bwd_chunk_adjoint_kernel<IO_BF16><<<grid, kThreads, 0, s>>>(p, w.cs, dyp, w.adj); break;
     }
     const int PN = p.P * p.N;  // a multiple of 256: P, N are multiples of 16
     bwd_state_passing_kernel<<<dim3(p.B * p.H, (PN / 4 + kThreads - 1) / kThreads), kThreads, 0, s>>>(
@@ -455,25 +555,25 @@ cudaError_t launch_bwd(const Params &p, int io, const BwdBuffers &w, cudaStream_
             if ((e = cudaFuncSetAttribute(bwd_chunk_kernel<IO_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           smem)) != cudaSuccess)
                 return e;
-            bwd_chunk_kernel<IO_F32><<<grid, kThreads, smem, s>>>(p, w.dtp, w.cs, w.states, w.adj, w.dyp, w.dx,
+            bwd_chunk_kernel<IO_F32><<<grid, kThreads, smem, s>>>(p, w.dtp, w.cs, w.states, w.adj, dyp, w.dx,
                                                                   w.ddt, w.dBh, w.dCh, w.partA, w.partD, w.partBias);
             break;
         case IO_F16:
             if ((e = cudaFuncSetAttribute(bwd_chunk_kernel<IO_F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           smem)) != cudaSuccess)
                 return e;
-            bwd_chunk_kernel<IO_F16><<<grid, kThreads, smem, s>>>(p, w.dtp, w.cs, w.states, w.adj, w.dyp, w.dx,
+            bwd_chunk_kernel<IO_F16><<<grid, kThreads, smem, s>>>(p, w.dtp, w.cs, w.states, w.adj, dyp, w.dx,
                                                                   w.ddt, w.dBh, w.dCh, w.partA, w.partD, w.partBias);
             break;
         case IO_BF16:
             if ((e = cudaFuncSetAttribute(bwd_chunk_kernel<IO_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           smem)) != cudaSuccess)
                 return e;
-            bwd_chunk_kernel<IO_BF16><<<grid, kThreads, smem, s>>>(p, w.dtp, w.cs, w.states, w.adj, w.dyp, w.dx,
+            bwd_chunk_kernel<IO_BF16><<<grid, kThreads, smem, s>>>(p, w.dtp, w.cs, w.states, w.adj, dyp, w.dx,
                                                                    w.ddt, w.dBh, w.dCh, w.partA, w.partD, w.partBias);
             break;
     }
-    const size_t gtotal = (size_t)p.B * p.L * p.G * p.N;
+    const size_t gtotal = (size_t)p.B * p.L * p.G * p.N / 4;
     const unsigned gb = (unsigned)((gtotal + 255) / 256);
     switch (io) {
         case IO_F32:

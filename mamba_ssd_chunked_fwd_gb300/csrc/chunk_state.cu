@@ -8,7 +8,9 @@
 // 256 threads as a 16 x 16 grid over (p, n), each owning a strided
 // (P/16) x (N/16) block of the [P,N] output.  Tokens stream through shared
 // memory 32 at a time.  Grid: x = batch*head, y = chunk.  MT (4 or 8) bounds
-// the block at compile time, so P, N <= 64 issue no idle multiply-adds.
+// the block at compile time, so P, N <= 64 issue no idle multiply-adds; with
+// MT = 4 a thread owns the consecutive p = 4 tp .. 4 tp + 3, n = 4 tn .. 4 tn + 3
+// and reads each token's operands as two float4 (one broadcast per 16 lanes).
 #include "ssd_internal.cuh"
 
 namespace ssd {
@@ -23,8 +25,8 @@ template <int IO, int MT>
 __global__ void __launch_bounds__(kThreads)
 chunk_state_kernel(Params p, const float *__restrict__ dtp, const float *__restrict__ cs,
                    float *__restrict__ states) {
-    __shared__ float xs[kTok][kMaxDim];
-    __shared__ float bs[kTok][kMaxDim];
+    __shared__ __align__(16) float xs[kTok][kMaxDim];
+    __shared__ __align__(16) float bs[kTok][kMaxDim];
     __shared__ float w_s[kTok];
     const int k = blockIdx.y;
     const int bh = blockIdx.x;
@@ -68,10 +70,17 @@ chunk_state_kernel(Params p, const float *__restrict__ dtp, const float *__restr
         __syncthreads();
         for (int i = 0; i < ntok; ++i) {
             float xv[MT], bv[MT];
+            if constexpr (MT == 4) {
+                const float4 x4 = *reinterpret_cast<const float4 *>(&xs[i][4 * tp]);
+                const float4 b4 = *reinterpret_cast<const float4 *>(&bs[i][4 * tn]);
+                xv[0] = x4.x; xv[1] = x4.y; xv[2] = x4.z; xv[3] = x4.w;
+                bv[0] = b4.x; bv[1] = b4.y; bv[2] = b4.z; bv[3] = b4.w;
+            } else {
 #pragma unroll
-            for (int a = 0; a < MT; ++a) xv[a] = (a < PT) ? xs[i][tp + 16 * a] : 0.f;
+                for (int a = 0; a < MT; ++a) xv[a] = (a < PT) ? xs[i][tp + 16 * a] : 0.f;
 #pragma unroll
-            for (int c = 0; c < MT; ++c) bv[c] = (c < NT) ? bs[i][tn + 16 * c] : 0.f;
+                for (int c = 0; c < MT; ++c) bv[c] = (c < NT) ? bs[i][tn + 16 * c] : 0.f;
+            }
 #pragma unroll
             for (int a = 0; a < MT; ++a)
 #pragma unroll
@@ -81,11 +90,19 @@ chunk_state_kernel(Params p, const float *__restrict__ dtp, const float *__restr
     }
 
     float *out = states + ((((size_t)b * p.nchunks + k) * p.H + h) * P) * N;
+    if constexpr (MT == 4) {  // rows 4 tp + a, columns 4 tn .. 4 tn + 3 (beyond P or N: not stored)
 #pragma unroll
-    for (int a = 0; a < MT; ++a)
+        for (int a = 0; a < 4; ++a)
+            if (4 * tp + a < P && 4 * tn < N)
+                *reinterpret_cast<float4 *>(out + (size_t)(4 * tp + a) * N + 4 * tn) =
+                    make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
+    } else {
 #pragma unroll
-        for (int c = 0; c < MT; ++c)
-            if (a < PT && c < NT) out[(size_t)(tp + 16 * a) * N + tn + 16 * c] = acc[a][c];
+        for (int a = 0; a < MT; ++a)
+#pragma unroll
+            for (int c = 0; c < MT; ++c)
+                if (a < PT && c < NT) out[(size_t)(tp + 16 * a) * N + tn + 16 * c] = acc[a][c];
+    }
 }
 
 }  // namespace
@@ -94,7 +111,8 @@ cudaError_t launch_chunk_state(const Params &p, int io, const float *dtp, const 
                                float *states, cudaStream_t s) {
     if (p.P > kMaxDim || p.N > kMaxDim || (p.P & 15) || (p.N & 15)) return cudaErrorInvalidValue;
     dim3 grid(p.B * p.H, p.nchunks);
-    const bool small = p.P <= 64 && p.N <= 64;
+    // the float4 stores of the 4-wide variant need a 16-byte aligned output
+    const bool small = p.P <= 64 && p.N <= 64 && reinterpret_cast<uintptr_t>(states) % 16 == 0;
 #define SSD_STATE_LAUNCH(IOV)                                                                  \
     if (small) chunk_state_kernel<IOV, 4><<<grid, kThreads, 0, s>>>(p, dtp, cs, states);       \
     else chunk_state_kernel<IOV, 8><<<grid, kThreads, 0, s>>>(p, dtp, cs, states);
