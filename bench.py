@@ -471,6 +471,85 @@ def run_varlen(args):
     print(json.dumps(line), flush=True)
 
 
+def run_norm(args):
+    """Forward + gated RMSNorm (a Mamba-2 block's SSD and the norm after it):
+    the workload with a seeded z [B,L,H,P] and norm weight [H*P], groups of
+    (H/G)*P channels.  Times the norm inside the fused kernel, and beside it
+    the two-kernel route (the forward without its gate, then the norm kernel
+    over y).  Prints its own JSON line."""
+    import mamba_ssd_chunked_fwd_gb300 as ssd
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    w = ssd_inputs.WORKLOADS[args.workload]
+    if args.batch:
+        w = w.with_(B=args.batch)
+    inp = ssd_inputs.make(w)
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    gen = torch.Generator().manual_seed(w.seed + 77)
+    z = torch.randn(inp["x"].shape, generator=gen).to(inp["x"].dtype).to(dev)
+    nw = (torch.rand(w.H * w.P, generator=gen) + 0.5).to(dev)
+    y = torch.empty_like(d["x"])
+    fin = torch.empty((w.B, w.H, w.P, w.N), device=dev) if w.return_final_state else None
+    ops = args.ops or w.ops
+    fused = ssd.make_args(d["x"], d["dt"], d["A"], d["B"], d["C"], w.chunk, y=y, final_state=fin, D=d["D"], z=z,
+                          dt_bias=d["dt_bias"], initial_states=d["initial_states"], dt_softplus=w.dt_softplus,
+                          ops=ops, plan=args.plan, norm_weight=nw, norm_eps=1e-5)
+    plain = ssd.make_args(d["x"], d["dt"], d["A"], d["B"], d["C"], w.chunk, y=y, final_state=fin, D=d["D"],
+                          dt_bias=d["dt_bias"], initial_states=d["initial_states"], dt_softplus=w.dt_softplus,
+                          ops=ops, plan=args.plan)
+    kernels = ",".join(ssd.ssd_fwd_describe(fused))
+    ws = torch.zeros(max(ssd.ssd_fwd_workspace_size(plain), ssd.ssd_fwd_workspace_size(fused), 256),
+                     dtype=torch.uint8, device=dev)
+    for a in (fused, plain):
+        a.workspace, a.workspace_bytes = ws.data_ptr(), ws.numel()
+    sh = ssd._stream_handle(dev)
+    stream = torch.cuda.current_stream(dev)
+    Bb, L, H, P = y.shape
+    y2, z2 = y.view(Bb * L, H * P), z.view(Bb * L, H * P)
+
+    def two_kernels():
+        ssd.ssd_fwd(plain, sh)
+        ssd.ssd_gated_rmsnorm(y2, z2, nw, w.G, 1e-5, y2, sh)
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        st = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        en = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        torch.cuda.synchronize(dev)
+        for i in range(args.steps):
+            st[i].record(stream)
+            fn()
+            en[i].record(stream)
+        torch.cuda.synchronize(dev)
+        return sum(s_.elapsed_time(e_) for s_, e_ in zip(st, en)) / args.steps
+
+    with ClockSampler(dev.index, enabled=not args.no_clocks) as clk:
+        ms = timed(lambda: ssd.ssd_fwd(fused, sh))
+        ms_two = timed(two_kernels)
+    ab = algorithmic_bytes(w)
+    nbytes = ab["total"] + y.numel() * y.element_size() + w.H * w.P * 4  # + z read, + the weight
+    hbm, peak_kind = peaks()
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    line = {
+        "metric": f"SSD fwd + gated RMSNorm tokens/s ({args.workload} {w.shape_tuple()})",
+        "value": round(w.tokens / (ms * 1e-3), 1), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": {0: "f32", 1: "f16", 2: "bf16"}[fused.ops],
+        "data": "synthetic (seeded, pages' distributions; z ~ N(0,1), weight ~ U(0.5, 1.5))",
+        "config": {"workload": f"forward + gated RMSNorm, {args.workload} {w.shape_tuple()} [B,L,H,P,N,chunk,G], "
+                               f"norm groups of {w.H // w.G * w.P} channels",
+                   "kernels": kernels, "two_kernel_ms": round(ms_two, 5),
+                   "l2": "inputs larger than L2, no flush"},
+        "roofline": {"bound": "hbm", "kernel": kernels, "achieved": round(achieved, 1), "peak": hbm,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": None,
+                     "alg_bytes_per_launch": nbytes, "launch_ms": round(ms, 5)},
+        "clocks": clk.summary(),
+        "gpu_launches": args.steps * len(kernels.split(",")),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_bwd(args):
     """Backward path: one ``ssd_bwd`` per step at the workload's shape (dy and
     dfinal seeded, all gradients written).  Prints its own JSON line; the
@@ -756,10 +835,12 @@ def main():
     ap.add_argument("--no-clocks", action="store_true", help="skip the nvidia-smi clock sampler")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch size (a smaller case of the same shape)")
-    ap.add_argument("--path", choices=["forward", "decode", "varlen", "bwd", "conv1d", "rmsnorm"], default="forward",
+    ap.add_argument("--path", choices=["forward", "decode", "varlen", "bwd", "conv1d", "rmsnorm", "norm"],
+                    default="forward",
                     help="forward (default): the whole SSD forward; decode: one decode step per "
                          "sequence from a carried state; varlen: the forward over packed sequences "
-                         "of random lengths")
+                         "of random lengths; bwd: the backward; conv1d, rmsnorm: the neighbours alone; "
+                         "norm: the forward with the gated RMSNorm of its output")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
@@ -776,6 +857,9 @@ def main():
         return
     if args.path == "bwd":
         run_bwd(args)
+        return
+    if args.path == "norm":
+        run_norm(args)
         return
     if args.path in ("conv1d", "rmsnorm"):
         run_neighbor(args)

@@ -40,7 +40,7 @@
 extern "C" {
 #endif
 
-#define SSD_ABI_VERSION 2
+#define SSD_ABI_VERSION 3
 
 /* Element types of the public tensors. */
 typedef enum { SSD_F32 = 0, SSD_F16 = 1, SSD_BF16 = 2 } ssd_dtype;
@@ -112,6 +112,17 @@ typedef struct ssd_fwd_args {
     float dt_min, dt_max;
     void *workspace;                              /* device, 256-byte aligned */
     size_t workspace_bytes;
+    /* Optional gated RMSNorm on the output (ops-transformer MambaV2 article,
+     * section 4.6), the step after the SSD in a Mamba-2 block.  When
+     * norm_weight (fp32 [H*P]) is non-NULL, z is required and
+     *   y[b,t,:] = rmsnorm_g(ssd[b,t,:] * silu(z[b,t,:])) * norm_weight,
+     * where ssd is the output above without its own z gate and rmsnorm_g
+     * divides each run of (H/G)*P consecutive channels (the heads of one B/C
+     * group) by sqrt(mean of squares + norm_eps).  The fused plan does it in
+     * its store stage when H/G <= 8; other plans (and wider groups) run the
+     * same arithmetic as a second kernel over y.  Not supported by ssd_bwd. */
+    const float *norm_weight;
+    float norm_eps;
 } ssd_fwd_args;
 
 /* ABI version of the loaded library (SSD_ABI_VERSION). */

@@ -67,6 +67,7 @@ class SsdFwdArgs(ctypes.Structure):
         ("y_dtype", ctypes.c_int32), ("ops", ctypes.c_int32), ("plan", ctypes.c_int32),
         ("dt_softplus", ctypes.c_int32), ("dt_min", ctypes.c_float), ("dt_max", ctypes.c_float),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+        ("norm_weight", ctypes.c_void_p), ("norm_eps", ctypes.c_float),
     ]
 
 
@@ -172,7 +173,8 @@ def _stream_handle(device=None):
 
 def make_args(x, dt, A, B, C, chunk_size, *, y=None, final_state=None, D=None, z=None,
               dt_bias=None, initial_states=None, dt_softplus=False,
-              dt_limit=(0.0, math.inf), ops=None, plan="auto", workspace=None) -> SsdFwdArgs:
+              dt_limit=(0.0, math.inf), ops=None, plan="auto", workspace=None, norm_weight=None,
+              norm_eps=1e-5) -> SsdFwdArgs:
     """Fill an ``ssd_fwd_args`` from tensors (device or host; no copies)."""
     Bb, L, H, P = x.shape
     G, N = B.shape[2], B.shape[3]
@@ -196,6 +198,7 @@ def make_args(x, dt, A, B, C, chunk_size, *, y=None, final_state=None, D=None, z
     a.dt_min, a.dt_max = float(dt_limit[0]), float(dt_limit[1])
     if workspace is not None:
         a.workspace, a.workspace_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
+    a.norm_weight, a.norm_eps = _ptr(norm_weight), float(norm_eps)
     return a
 
 
@@ -320,16 +323,17 @@ def ssd_state_fold(log_decay, states, out, stream=None):
 
 def mamba2_ssd_fwd(x, dt, A, B, C, chunk_size, dt_softplus=False, return_final_state=False, *,
                    D=None, z=None, dt_bias=None, dt_limit=(0.0, math.inf), initial_states=None,
-                   ops=None, plan="auto", workspace=None, out=None):
+                   ops=None, plan="auto", workspace=None, out=None, norm_weight=None, norm_eps=1e-5):
     """SSD forward on the GPU.  Returns ``out`` or ``(out, final_state)``.
 
     x [B,L,H,P], dt [B,L,H] fp32, A [H] fp32, B/C [B,L,G,N], D [H] fp32,
     z [B,L,H,P], dt_bias [H] fp32, initial_states [B,H,P,N] fp32; x, B, C, z
     share a dtype (fp32, fp16 or bf16) and the output takes it.  ``ops``
     ("f32" | "f16" | "bf16") is the operand precision of the contractions
-    (default: that of x).  Allocation of out, final_state and the workspace is
-    done here with torch; all compute runs in libssd_gb300.so on the current
-    stream.
+    (default: that of x).  With ``norm_weight`` (fp32 [H*P], z required) the
+    output is the gated RMSNorm of the SSD, groups of (H/G)*P channels.
+    Allocation of out, final_state and the workspace is done here with torch;
+    all compute runs in libssd_gb300.so on the current stream.
     """
     if not x.is_cuda:
         raise ValueError("mamba2_ssd_fwd takes CUDA tensors; use ssd_fwd_host for host buffers")
@@ -340,7 +344,7 @@ def mamba2_ssd_fwd(x, dt, A, B, C, chunk_size, dt_softplus=False, return_final_s
         fin = torch.empty((Bb, H, P, B.shape[3]), device=x.device, dtype=torch.float32)
     args = make_args(x, dt, A, B, C, chunk_size, y=y, final_state=fin, D=D, z=z, dt_bias=dt_bias,
                      initial_states=initial_states, dt_softplus=dt_softplus, dt_limit=dt_limit,
-                     ops=ops, plan=plan)
+                     ops=ops, plan=plan, norm_weight=norm_weight, norm_eps=norm_eps)
     if workspace is None:
         nbytes = ssd_fwd_workspace_size(args)
         workspace = torch.empty(max(nbytes, 256), device=x.device, dtype=torch.uint8)
@@ -397,11 +401,12 @@ def mamba2_ssd_decode(x, dt, A, B, C, state, dt_softplus=False, *, D=None, z=Non
 
 def mamba2_ssd_fwd_varlen(x, dt, A, B, C, chunk_size, cu_seqlens, dt_softplus=False, return_final_state=False,
                           *, D=None, z=None, dt_bias=None, dt_limit=(0.0, math.inf), initial_states=None,
-                          ops=None, plan="auto", out=None):
+                          ops=None, plan="auto", out=None, norm_weight=None, norm_eps=1e-5):
     """Packed variable-length SSD forward on the GPU: x [1,T,H,P], dt [1,T,H],
     B/C [1,T,G,N], z like x; sequence s holds tokens [cu_seqlens[s],
     cu_seqlens[s+1]) and starts from initial_states[s] (or 0).  Returns y, or
-    (y, final_state [nseq,H,P,N]).  All compute runs in libssd_gb300.so."""
+    (y, final_state [nseq,H,P,N]); ``norm_weight`` as in ``mamba2_ssd_fwd``.
+    All compute runs in libssd_gb300.so."""
     if not x.is_cuda:
         raise ValueError("mamba2_ssd_fwd_varlen takes CUDA tensors")
     cu, nseq = _cu_host(cu_seqlens)
@@ -411,7 +416,7 @@ def mamba2_ssd_fwd_varlen(x, dt, A, B, C, chunk_size, cu_seqlens, dt_softplus=Fa
         fin = torch.empty((nseq, x.shape[2], x.shape[3], B.shape[3]), device=x.device, dtype=torch.float32)
     args = make_args(x, dt, A, B, C, chunk_size, y=y, final_state=fin, D=D, z=z, dt_bias=dt_bias,
                      initial_states=initial_states, dt_softplus=dt_softplus, dt_limit=dt_limit, ops=ops,
-                     plan=plan)
+                     plan=plan, norm_weight=norm_weight, norm_eps=norm_eps)
     nbytes = ssd_fwd_varlen_workspace_size(args, cu)
     ws = torch.empty(max(nbytes, 256), device=x.device, dtype=torch.uint8)
     args.workspace, args.workspace_bytes = ws.data_ptr(), ws.numel()

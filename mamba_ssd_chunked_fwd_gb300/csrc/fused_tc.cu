@@ -101,6 +101,20 @@ constexpr uint32_t BOX_BYTES = 8192;
 constexpr uint32_t OFF_VEC = 221184;  // 3 x ChunkVec
 constexpr uint32_t VEC_BYTES = 2064;
 constexpr uint32_t SMEM_BYTES = OFF_VEC + 3 * VEC_BYTES + 1024;  // + alignment slack
+// The gated instantiations (ZM 1: y * silu(z); ZM 2: then the gated RMSNorm)
+// load each chunk's z tile by TMA into the y staging tile, where the epilogue
+// reads z at the address it then writes y to; an mbarrier after the decay
+// vectors marks its arrival.  ZM 2 adds the exchange of per-token sums of
+// squares between the CTAs of a cluster that hold the head pairs of one norm
+// group (a B/C group).
+constexpr int kNormMaxRanks = 4;
+constexpr uint32_t OFF_NORM = OFF_VEC + 3 * VEC_BYTES;
+constexpr uint32_t NORM_LPART = 0;     // [4 warpgroups][4 warps][16 tokens] fp32: per-warp sums
+constexpr uint32_t NORM_RECV = 1024;   // [2 slots][kNormMaxRanks][64 tokens] fp32: per-CTA sums
+constexpr uint32_t NORM_BARS = NORM_RECV + 2 * kNormMaxRanks * 64 * 4;  // [2 slots][4 warpgroups] mbarriers
+constexpr uint32_t NORM_ZBAR = NORM_BARS + 2 * 4 * 8;                    // z tile arrived
+constexpr uint32_t SMEM_BYTES_NORM = OFF_NORM + NORM_ZBAR + 16 + 1024;
+static_assert(OFF_NORM % 16 == 0 && SMEM_BYTES_NORM + 512 <= 232448, "norm exchange fits in shared memory");
 
 // TMEM columns (512 allocated)
 constexpr uint32_t TM_G = 0, TM_DS = 64, TM_COLS = 512;
@@ -117,7 +131,7 @@ enum {
 // TMA descriptors of x [B,L,H*P] and B, C [B,L,G*N] as 3-D tensors
 // (innermost first: features, tokens, batch), boxes of 128 bytes x 64 tokens.
 struct TmaMaps {
-    CUtensorMap x, b, c, y;
+    CUtensorMap x, b, c, y, z;  // z: gated instantiations only
 };
 
 // 16-byte aligned so that consecutive slots keep their float4 reads aligned
@@ -250,13 +264,28 @@ __device__ __forceinline__ void decay_vectors(const Params &p, int h, int hh, in
     if (lane == 0) V.a[hh] = expf(last);
 }
 
+// One value of an unswizzled staging tile (fp32, or fp16 / bf16 bits).
+template <int IO>
+__device__ __forceinline__ float ld_stage(uint32_t a) {
+    if (IO == IO_F32) {
+        float v;
+        asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
+        return v;
+    } else {
+        uint16_t hb;
+        asm volatile("ld.shared.b16 %0, [%1];" : "=h"(hb) : "r"(a));
+        if (IO == IO_BF16) return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(&hb));
+        return __half2float(*reinterpret_cast<const __half *>(&hb));
+    }
+}
+
 // y for one (head, p) and 8 consecutive tokens from tok_base, read from the
 // TMEM accumulators of buffer bp and written into the y staging tile (rows of
 // 128 bytes per box; the TMA store drops rows past L).  For packed sequences
 // (VARLEN) tokens count from t0 in batch row 0, the sequence ends at len, and
 // in its last chunk (`direct`) y goes straight to global memory for the
 // tokens inside the sequence, since the rows past its end belong to the next.
-template <int IO, bool VARLEN>
+template <int IO, bool VARLEN, int ZM = 0>
 __device__ __forceinline__ void epilogue8(const Params &p, const Dims &dm, const ChunkVec &V, uint32_t tlane,
                                           int bp, int col, int b, int h0, int my_h, int my_p, int tok_base,
                                           uint32_t ystage, int t0, int len, bool direct) {
@@ -287,7 +316,13 @@ __device__ __forceinline__ void epilogue8(const Params &p, const Dims &dm, const
 #pragma unroll
         for (int ii = 0; ii < 8; ++ii) v[ii] = fmaf(Dh, xv[ii], v[ii]);
     }
-    if (p.z) {
+    if constexpr (ZM > 0) {  // z staged where y goes
+        const int f = my_h * kP + my_p;
+        const uint32_t a0 = IO == IO_F32 ? ystage + (f >> 5) * BOX_BYTES + i0 * 128 + (f & 31) * 4
+                                         : ystage + (f >> 6) * BOX_BYTES + i0 * 128 + (f & 63) * 2;
+#pragma unroll
+        for (int ii = 0; ii < 8; ++ii) v[ii] *= silu_f(ld_stage<IO>(a0 + ii * 128));
+    } else if (p.z) {
         float zv[8];
 #pragma unroll
         for (int ii = 0; ii < 8; ++ii)
@@ -324,10 +359,142 @@ __device__ __forceinline__ void epilogue8(const Params &p, const Dims &dm, const
     tc::fence_smem_to_async();
 }
 
-template <int IO, bool BF16, bool VARLEN>
+// Shared-memory addresses of the norm exchange and this CTA's place in it.
+struct NormCtx {
+    uint32_t lpart, recv, rbar;
+    int cs, rank;  // CTAs per norm group (the cluster), this CTA's rank (= its head pair)
+};
+
+// NORM epilogue: y of this thread's feature for the 16 tokens col0 .. col0+15
+// of the chunk (as epilogue8, gate included), then the gated RMSNorm of the
+// ops-transformer MambaV2 article, section 4.6: every token is divided by the
+// root mean square of its cs * 128 gated features (the group's heads) and
+// multiplied by the feature's weight.  The sum of squares runs over the warp's
+// 32 features (shuffles), the warpgroup's 4 warps (shared memory), then the
+// cs CTAs of the cluster (remote stores + an mbarrier per warpgroup and slot;
+// two slots alternate by chunk).  Every CTA adds the cs partial sums in rank
+// order, so all features of a group use bitwise the same scale.
+template <int IO>
+__device__ __forceinline__ void epilogue_norm(const Params &p, const Dims &dm, const ChunkVec &V, uint32_t tlane,
+                                              int bp, int col0, int b, int h0, int my_h, int my_p, int tok_base,
+                                              uint32_t ystage, const NormCtx &nc, uint32_t gp, int wg, int quarter,
+                                              int lane, float Dh, float wf, bool &timed_out) {
+    const int h = h0 + my_h;
+    const int f = my_h * kP + my_p;  // feature within the pair's 128
+    auto stage_addr = [&](int ib) {  // token row ib of the staging tile, this feature
+        return IO == IO_F32 ? ystage + (f >> 5) * BOX_BYTES + ib * 128 + (f & 31) * 4
+                            : ystage + (f >> 6) * BOX_BYTES + ib * 128 + (f & 63) * 2;
+    };
+    const size_t step = (size_t)dm.H * kP;
+    const size_t off0 = (((size_t)b * dm.L + tok_base) * dm.H + h) * kP + my_p;
+    float v[16];
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+        float yo[8], yi[8];
+        tc::tmem_ld8(tlane + tm_yoff(bp) + col0 + 8 * hf, yo);
+        tc::tmem_ld8(tlane + tm_yint(bp) + col0 + 8 * hf, yi);
+        const float4 e0 = *reinterpret_cast<const float4 *>(&V.ecs[my_h][col0 + 8 * hf]);
+        const float4 e1 = *reinterpret_cast<const float4 *>(&V.ecs[my_h][col0 + 8 * hf + 4]);
+        const float ev[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
+#pragma unroll
+        for (int ii = 0; ii < 8; ++ii) v[8 * hf + ii] = fmaf(ev[ii], yo[ii], yi[ii]);
+    }
+    tc::fence_before_sync();
+    if (p.D) {
+#pragma unroll
+        for (int ii = 0; ii < 16; ++ii)
+            v[ii] = fmaf(Dh, (tok_base + ii < dm.L) ? ld_io<IO>(p.x, off0 + ii * step) : 0.f, v[ii]);
+    }
+#pragma unroll
+    for (int ii = 0; ii < 16; ++ii) v[ii] *= silu_f(ld_stage<IO>(stage_addr(col0 + ii)));  // z staged where y goes
+    // per-token sum of squares over the warp's 32 features: halve the token set
+    // at each shuffle step; lane l ends with token tk(l) (bits 4..1 of l), l and
+    // l ^ 1 holding the same sum
+    float e;
+    {
+        float a8[8], a4[4], a2[2];
+        const bool u4 = lane & 16, u3 = lane & 8, u2 = lane & 4, u1 = lane & 2;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float lo = v[j] * v[j], hi = v[8 + j] * v[8 + j];
+            a8[j] = (u4 ? hi : lo) + __shfl_xor_sync(0xffffffffu, u4 ? lo : hi, 16);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) a4[j] = (u3 ? a8[4 + j] : a8[j]) + __shfl_xor_sync(0xffffffffu, u3 ? a8[j] : a8[4 + j], 8);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) a2[j] = (u2 ? a4[2 + j] : a4[j]) + __shfl_xor_sync(0xffffffffu, u2 ? a4[j] : a4[2 + j], 4);
+        e = (u1 ? a2[1] : a2[0]) + __shfl_xor_sync(0xffffffffu, u1 ? a2[0] : a2[1], 2);
+        e += __shfl_xor_sync(0xffffffffu, e, 1);
+    }
+    const int tk = ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
+    if (!(lane & 1)) asm volatile("st.shared.f32 [%0], %1;" ::"r"(nc.lpart + ((wg * 4 + quarter) * 16 + tk) * 4), "f"(e));
+    tc::named_barrier(1 + wg, 128);
+    const uint32_t slot = gp & 1u;
+    const uint32_t rbar = nc.rbar + (slot * 4 + wg) * 8;
+    if (quarter == 0 && lane < 16) {  // this CTA's sum for token `lane` of the warpgroup
+        float sum = 0.f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            float t;
+            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(t) : "r"(nc.lpart + ((wg * 4 + q) * 16 + lane) * 4));
+            sum += t;
+        }
+        const uint32_t mine = nc.recv + ((slot * kNormMaxRanks + nc.rank) * 64 + wg * 16 + lane) * 4;
+        asm volatile("st.shared.f32 [%0], %1;" ::"r"(mine), "f"(sum));
+        for (int r = 0; r < nc.cs; ++r) {
+            if (r == nc.rank) continue;
+            tc::st_cluster_f32(tc::mapa_shared(mine, r), sum);
+            tc::mbar_arrive_cluster(tc::mapa_shared(rbar, r));
+        }
+    }
+    tc::named_barrier(1 + wg, 128);
+    if (nc.cs > 1 && !timed_out && !tc::mbar_wait_cluster(rbar, (gp >> 1) & 1u, kWaitNs)) timed_out = true;
+    float tot[16];
+#pragma unroll
+    for (int ii = 0; ii < 16; ++ii) tot[ii] = 0.f;
+    for (int r = 0; r < nc.cs; ++r) {
+        const uint32_t base = nc.recv + ((slot * kNormMaxRanks + r) * 64 + wg * 16) * 4;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint4 t4 = tc::ld_shared_v4(base + 16 * q);
+            tot[4 * q] += __uint_as_float(t4.x);
+            tot[4 * q + 1] += __uint_as_float(t4.y);
+            tot[4 * q + 2] += __uint_as_float(t4.z);
+            tot[4 * q + 3] += __uint_as_float(t4.w);
+        }
+    }
+    const float inv_n = 1.f / (float)(nc.cs * 2 * kP);
+#pragma unroll
+    for (int ii = 0; ii < 16; ++ii) v[ii] *= rsqrtf(fmaf(tot[ii], inv_n, p.norm_eps)) * wf;
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+        const uint32_t a0 = stage_addr(col0 + 8 * hf);
+#pragma unroll
+        for (int ii = 0; ii < 8; ++ii) {
+            const uint32_t a = a0 + ii * 128;
+            const float val = v[8 * hf + ii];
+            if (IO == IO_F32) {
+                asm volatile("st.shared.f32 [%0], %1;" ::"r"(a), "f"(val));
+            } else {
+                uint16_t hbits;
+                if (IO == IO_BF16) {
+                    __nv_bfloat16 hv = __float2bfloat16_rn(val);
+                    hbits = *reinterpret_cast<uint16_t *>(&hv);
+                } else {
+                    __half hv = __float2half_rn(val);
+                    hbits = *reinterpret_cast<uint16_t *>(&hv);
+                }
+                asm volatile("st.shared.b16 [%0], %1;" ::"r"(a), "h"(hbits));
+            }
+        }
+    }
+    tc::fence_smem_to_async();
+}
+
+template <int IO, bool BF16, bool VARLEN, int ZM>
 __global__ void __launch_bounds__(kThreads, 1)
 ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMaps tm, int n_units,
-                 unsigned int *err) {
+                 unsigned int *err, int norm_cs) {
     extern __shared__ unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t bars[NBARS];
     __shared__ uint32_t tmem_slot;
@@ -356,6 +523,11 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
             tc::mbar_init(bar(BAR_VEC_FULL0 + i), 2);
             tc::mbar_init(bar(BAR_VEC_EMPTY0 + i), kComputeWarps);
         }
+        if constexpr (ZM > 0) tc::mbar_init(sbase + OFF_NORM + NORM_ZBAR, 1);
+        if constexpr (ZM == 2) {
+            if (norm_cs > 1)
+                for (int i = 0; i < 8; ++i) tc::mbar_init(sbase + OFF_NORM + NORM_BARS + 8 * i, (norm_cs - 1) * 16);
+        }
         tc::mbar_init_fence();
     }
     if (warp == kMmaWarp) {
@@ -371,6 +543,9 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
+    if constexpr (ZM == 2) {  // the partners' exchange barriers are initialised before any remote arrive
+        if (norm_cs > 1) tc::cluster_sync();
+    }
     const uint32_t tmem = tmem_slot;
     const int pairs = dm.hpg >> 1;
     bool timed_out = false;
@@ -432,6 +607,7 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
             tc::prefetch_tensormap(&tm.b);
             tc::prefetch_tensormap(&tm.c);
             tc::prefetch_tensormap(&tm.y);
+            if constexpr (ZM > 0) tc::prefetch_tensormap(&tm.z);
             constexpr int bw = IO == IO_F32 ? 32 : 64;  // features per 128-byte box
             constexpr uint32_t kStageBytes = (IO == IO_F32 ? 8u : 4u) * BOX_BYTES;
             // The same loop twice: packed sequences walk per-unit spans, the regular
@@ -514,8 +690,26 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                         tc::tma_load_3d(sbase + OFF_STG_C + bx * BOX_BYTES, &tm.c, g * kN + bx * bw, k * kQ, b,
                                         bar(BAR_STAGE_FULL));
                     }
+                    if constexpr (ZM > 0) {  // this chunk's z into L2, ahead of its load into the y tile
+#pragma unroll
+                        for (int bx = 0; bx < 128 / bw; ++bx) tc::tma_prefetch_3d(&tm.z, h0 * kP + bx * bw, k * kQ, b);
+                    }
                 };
                 uint32_t yt = 0;  // y tiles stored so far
+                // gated instantiations: the z tile of chunk k of a unit into the (free) y staging tile
+                auto load_z = [&](int unit, int k) {
+                    if constexpr (ZM > 0) {
+                        const int pair = unit % pairs, bg = unit / pairs;
+                        const int g = bg % dm.G, b = bg / dm.G;
+                        const int h0 = g * dm.hpg + 2 * pair;
+                        const uint32_t zbar = sbase + OFF_NORM + NORM_ZBAR;
+                        tc::mbar_arrive_expect_tx(zbar, (IO == IO_F32 ? 4u : 2u) * BOX_BYTES);
+#pragma unroll
+                        for (int bx = 0; bx < 128 / bw; ++bx)
+                            tc::tma_load_3d(sbase + OFF_STG_Y + bx * BOX_BYTES, &tm.z, h0 * kP + bx * bw, k * kQ, b,
+                                            zbar);
+                    }
+                };
                 // the y tile of chunk k of (b, head pair from h0), once the compute warps staged it
                 auto store_y = [&](int b, int h0, int k) {
                     wait(BAR_Y_STAGED, yt & 1u);
@@ -527,7 +721,10 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                     tc::mbar_arrive(bar(BAR_Y_FREE));
                     ++yt;
                 };
-                if ((int)blockIdx.x < n_units) stage(blockIdx.x, 0);
+                if ((int)blockIdx.x < n_units) {
+                    stage(blockIdx.x, 0);
+                    load_z(blockIdx.x, 0);
+                }
                 uint32_t gk = 0;
                 for (int unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
                     const int pair = unit % pairs, bg = unit / pairs;
@@ -537,9 +734,13 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                         wait(BAR_OPS_FULL, gk & 1u);  // the compute warps are done with the staging area
                         if (k + 1 < dm.nchunks) stage(unit, k + 1);
                         else if (unit + (int)gridDim.x < n_units) stage(unit + gridDim.x, 0);
-                        if (k > 0) store_y(b, h0, k - 1);
+                        if (k > 0) {
+                            store_y(b, h0, k - 1);
+                            load_z(unit, k);  // the next tile the compute warps stage
+                        }
                     }
                     store_y(b, h0, dm.nchunks - 1);
+                    if (unit + (int)gridDim.x < n_units) load_z(unit + gridDim.x, 0);
                 }
                 tc::bulk_wait_all();
             }
@@ -571,6 +772,15 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
         const uint32_t tlane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
         uint32_t gk = 0;
         uint32_t yt = 0;  // y tiles staged so far
+        NormCtx nc{};
+        float norm_wf = 0.f, norm_dh = 0.f;  // per unit: this feature's norm weight, its head's D
+        if constexpr (ZM == 2) {
+            nc.lpart = sbase + OFF_NORM + NORM_LPART;
+            nc.recv = sbase + OFF_NORM + NORM_RECV;
+            nc.rbar = sbase + OFF_NORM + NORM_BARS;
+            nc.cs = norm_cs;
+            nc.rank = norm_cs > 1 ? (int)tc::cluster_ctarank() : 0;
+        }
         // epilogue of global chunk gp (chunk kk of the unit) into the y staging tile
         // (the last chunk of a packed sequence straight into y)
         auto epilogue = [&](uint32_t gp, int kk, int b, int h0, int t0, int len) {
@@ -578,11 +788,19 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
             const bool direct = VARLEN && (kk + 1) * kQ > len;
             if (yt > 0) wait(BAR_Y_FREE, (yt - 1) & 1u);  // the TMA unit has read the previous tile
             wait(bp ? BAR_Y_DONE1 : BAR_Y_DONE0, (gp >> 1) & 1u);
+            if constexpr (ZM > 0) {  // this tile's z is in the staging tile
+                if (!timed_out && !tc::mbar_wait(sbase + OFF_NORM + NORM_ZBAR, yt & 1u, kWaitNs)) timed_out = true;
+            }
             tc::fence_after_sync();
+            if constexpr (ZM == 2) {
+                epilogue_norm<IO>(p, dm, Vbuf[gp % kVecSlots], tlane, bp, col0, b, h0, my_h, my_p, kk * kQ + col0,
+                                  sbase + OFF_STG_Y, nc, gp, wg, quarter, lane, norm_dh, norm_wf, timed_out);
+            } else {
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf)
-                epilogue8<IO, VARLEN>(p, dm, Vbuf[gp % kVecSlots], tlane, bp, col0 + 8 * hf, b, h0, my_h, my_p,
-                                      kk * kQ + col0 + 8 * hf, sbase + OFF_STG_Y, t0, len, direct);
+                for (int hf = 0; hf < 2; ++hf)
+                    epilogue8<IO, VARLEN, ZM>(p, dm, Vbuf[gp % kVecSlots], tlane, bp, col0 + 8 * hf, b, h0, my_h,
+                                              my_p, kk * kQ + col0 + 8 * hf, sbase + OFF_STG_Y, t0, len, direct);
+            }
             __syncwarp();
             if (lane == 0) {
                 tc::mbar_arrive(bar(BAR_Y_STAGED));
@@ -606,6 +824,10 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                 b = bg / dm.G;
                 h0 = g * dm.hpg + 2 * pair;
                 sb = b;
+            }
+            if constexpr (ZM == 2) {
+                norm_wf = __ldg(p.norm_w + (size_t)(h0 + my_h) * kP + my_p);
+                norm_dh = p.D ? __ldg(p.D + h0 + my_h) : 0.f;
             }
 
             // state of (head my_h, row my_p), columns n = col0 .. col0+kCols-1
@@ -758,6 +980,9 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
     __syncthreads();
     tc::fence_after_sync();
     if (warp == kMmaWarp) tc::tmem_dealloc(tmem, TM_COLS);
+    if constexpr (ZM == 2) {  // no CTA leaves while a partner may still write into its shared memory
+        if (norm_cs > 1) tc::cluster_sync();
+    }
 }
 
 int g_num_sms = 0;
@@ -815,19 +1040,57 @@ cudaError_t encode_map(CUtensorMap *m, const void *base, int io, int64_t feats, 
 
 template <int IO, bool BF16>
 cudaError_t launch_typed(const Params &p, int units, unsigned int *err, cudaStream_t s) {
-    // packed variable-length sequences get their own instantiation, so that the
-    // regular layout pays nothing for per-sequence offsets
-    auto kern = p.cu ? ssd_fused_kernel<IO, BF16, true> : ssd_fused_kernel<IO, BF16, false>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    // packed variable-length sequences and the fused norm get their own
+    // instantiations, so that the regular layout pays nothing for them
+    // z on the regular layout: staged by TMA through the y tile (ZM 1), with the norm (ZM 2)
+    const bool norm = p.norm_w && !p.cu;
+    const bool gated = p.z && !p.cu;
+    auto kern = p.cu    ? ssd_fused_kernel<IO, BF16, true, 0>
+                : norm  ? ssd_fused_kernel<IO, BF16, false, 2>
+                : gated ? ssd_fused_kernel<IO, BF16, false, 1>
+                        : ssd_fused_kernel<IO, BF16, false, 0>;
+    const uint32_t smem = gated ? SMEM_BYTES_NORM : SMEM_BYTES;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     TmaMaps tm;
     if ((e = encode_map(&tm.x, p.x, IO, (int64_t)p.H * kP, p.L, p.B)) != cudaSuccess) return e;
     if ((e = encode_map(&tm.b, p.Bm, IO, (int64_t)p.G * kN, p.L, p.B)) != cudaSuccess) return e;
     if ((e = encode_map(&tm.c, p.Cm, IO, (int64_t)p.G * kN, p.L, p.B)) != cudaSuccess) return e;
     if ((e = encode_map(&tm.y, p.y, IO, (int64_t)p.H * kP, p.L, p.B, false)) != cudaSuccess) return e;
+    if (gated && (e = encode_map(&tm.z, p.z, IO, (int64_t)p.H * kP, p.L, p.B, false)) != cudaSuccess) return e;
     // one CTA per SM: its shared memory and 512 TMEM columns fill the SM
-    const int grid = units < num_sms() ? units : num_sms();
-    kern<<<grid, kThreads, SMEM_BYTES, s>>>(p, tm, units, err);
+    if (!norm) {
+        const int grid = units < num_sms() ? units : num_sms();
+        kern<<<grid, kThreads, smem, s>>>(p, tm, units, err, 1);
+        return cudaGetLastError();
+    }
+    // fused norm: the head pairs of a group run in one cluster of cs CTAs, in
+    // step (unit u goes to the CTA of rank u % cs, and the grid is a multiple of cs)
+    const int cs = p.hpg / 2;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = cs > 1 ? 1 : 0;
+    int clusters = num_sms() / cs;
+    if (cs > 1) {
+        cfg.gridDim = dim3((unsigned)(clusters * cs));
+        int active = 0;
+        if (cudaOccupancyMaxActiveClusters(&active, kern, &cfg) == cudaSuccess && active > 0 && active < clusters)
+            clusters = active;
+        (void)cudaGetLastError();
+    }
+    int grid = clusters * cs;
+    if (grid > units) grid = units;  // units is a multiple of cs
+    cfg.gridDim = dim3((unsigned)grid);
+    e = cudaLaunchKernelEx(&cfg, kern, p, tm, units, err, cs);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -841,10 +1104,15 @@ const char *fused_unsupported_reason(const ssd_fwd_args *a) {
     for (const void *ptr : {static_cast<const void *>(a->x), static_cast<const void *>(a->Bm),
                             static_cast<const void *>(a->Cm), static_cast<const void *>(a->y)})
         if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return "needs 16-byte aligned x, B, C and y";
+    if (a->z && reinterpret_cast<uintptr_t>(a->z) % 16 != 0) return "needs a 16-byte aligned z (its tiles come by TMA)";
     return nullptr;
 }
 
 bool fused_supported(const ssd_fwd_args *a) { return fused_unsupported_reason(a) == nullptr; }
+
+bool fused_norm_supported(const ssd_fwd_args *a) {
+    return fused_supported(a) && a->z && (a->H / a->G) / 2 <= kNormMaxRanks;
+}
 
 bool fused_preferred(const ssd_fwd_args *a) { return fused_units(a) >= num_sms(); }
 
@@ -863,6 +1131,8 @@ Params fused_params(const ssd_fwd_args *a) {
     p.dt_softplus = a->dt_softplus ? 1 : 0;
     p.has_limit = !(a->dt_min == 0.f && isinf(a->dt_max) && a->dt_max > 0.f);
     p.dt_min = a->dt_min; p.dt_max = a->dt_max;
+    p.norm_w = a->norm_weight;
+    p.norm_eps = a->norm_eps;
     return p;
 }
 

@@ -84,6 +84,9 @@ ssd_status check_pointers(const ssd_fwd_args *a, bool need_y) {
         return fail(SSD_ERR_INVALID_ARG, "initial_state must be 16-byte aligned");
     if (a->final_state && !aligned(a->final_state, 16))
         return fail(SSD_ERR_INVALID_ARG, "final_state must be 16-byte aligned");
+    if (a->norm_weight && !a->z) return fail(SSD_ERR_INVALID_ARG, "the gated RMSNorm (norm_weight) needs z");
+    if (a->norm_weight && !(a->norm_eps >= 0.f && a->norm_eps < INFINITY))
+        return fail(SSD_ERR_INVALID_ARG, "norm_eps must be finite and >= 0");
     return SSD_OK;
 }
 
@@ -168,6 +171,27 @@ ssd_status run_chunked(const ssd_fwd_args *a, cudaStream_t s) {
     if ((e = launch_state_step(a, p, dtp, cs, states, err, s)) != cudaSuccess) return cuda_fail(e, "chunk_state");
     if ((e = ssd::launch_state_passing(p, cs, states, s)) != cudaSuccess) return cuda_fail(e, "state_passing");
     if ((e = launch_scan_step(a, p, dtp, cs, states, err, s)) != cudaSuccess) return cuda_fail(e, "chunk_scan");
+    return ok();
+}
+
+// The gated RMSNorm runs inside the fused kernel when it can; otherwise the
+// forward runs without its z gate and a second kernel normalises y in place
+// over `rows` tokens (the gate included).
+bool norm_in_kernel(const ssd_fwd_args *a, int32_t plan) {
+    return a->norm_weight && plan == SSD_PLAN_FUSED && ssd::fused_norm_supported(a);
+}
+
+ssd_fwd_args without_norm(const ssd_fwd_args *a) {
+    ssd_fwd_args o = *a;
+    o.z = nullptr;
+    o.norm_weight = nullptr;
+    return o;
+}
+
+ssd_status norm_after(const ssd_fwd_args *a, int64_t rows, cudaStream_t s) {
+    cudaError_t e = ssd::launch_gated_rmsnorm(rows, (int)(a->H * a->P), (int)a->G, a->norm_eps, a->x_dtype, a->y,
+                                              a->z, a->norm_weight, a->y, s);
+    if (e != cudaSuccess) return cuda_fail(e, "gated_rmsnorm");
     return ok();
 }
 
@@ -261,6 +285,7 @@ ssd_status check_bwd(const ssd_bwd_args *b) {
     const ssd_fwd_args *a = &b->fwd;
     ssd_status st = check_shape(a);
     if (st != SSD_OK) return st;
+    if (a->norm_weight) return fail(SSD_ERR_UNSUPPORTED, "the backward does not take the gated RMSNorm");
     if (a->chunk > 64 || a->P > 64 || a->N > 64)
         return fail(SSD_ERR_UNSUPPORTED, "the backward needs chunk, P, N <= 64 (chunk=%lld P=%lld N=%lld)",
                     (long long)a->chunk, (long long)a->P, (long long)a->N);
@@ -323,15 +348,16 @@ ssd_status ssd_fwd_describe(const ssd_fwd_args *a, char *out, size_t cap) {
     ssd_status st = ssd_fwd_resolve_plan(a, &plan);
     if (st != SSD_OK) return st;
     if (!out || cap == 0) return fail(SSD_ERR_INVALID_ARG, "out buffer required");
+    const char *norm = a->norm_weight && !norm_in_kernel(a, plan) ? ",gated_rmsnorm" : "";
     if (plan == SSD_PLAN_FUSED) {
-        snprintf(out, cap, "ssd_fused_kernel");
+        snprintf(out, cap, "ssd_fused_kernel%s", norm);
         return ok();
     }
     const ssd::Params p = make_params(a);
     const bool tc_state = ssd::chunk_tc_state_supported(p, a->ops) && tc_ok(a);
     const bool tc_scan = ssd::chunk_tc_scan_supported(p, a->ops) && tc_ok(a);
-    snprintf(out, cap, "chunk_cumsum,%s,state_passing,%s", tc_state ? "chunk_state_tc" : "chunk_state",
-             tc_scan ? "chunk_scan_tc" : "chunk_scan");
+    snprintf(out, cap, "chunk_cumsum,%s,state_passing,%s%s", tc_state ? "chunk_state_tc" : "chunk_state",
+             tc_scan ? "chunk_scan_tc" : "chunk_scan", norm);
     return ok();
 }
 
@@ -346,6 +372,16 @@ ssd_status ssd_fwd(const ssd_fwd_args *a, void *stream) {
                     a->workspace ? a->workspace_bytes : (size_t)0);
     if (!aligned(a->workspace, kAlign)) return fail(SSD_ERR_WORKSPACE, "workspace must be 256-byte aligned");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (a->norm_weight && !norm_in_kernel(a, plan)) {  // the forward without its gate, then the norm
+        const ssd_fwd_args o = without_norm(a);
+        if (plan == SSD_PLAN_FUSED) {
+            cudaError_t e = ssd::run_fused(&o, s);
+            if (e != cudaSuccess) return cuda_fail(e, "fused kernel");
+        } else if ((st = run_chunked(&o, s)) != SSD_OK) {
+            return st;
+        }
+        return norm_after(a, a->B * a->L, s);
+    }
     if (plan == SSD_PLAN_FUSED) {
         cudaError_t e = ssd::run_fused(a, s);
         if (e != cudaSuccess) return cuda_fail(e, "fused kernel");
@@ -367,6 +403,12 @@ ssd_status ssd_fwd_varlen(const ssd_fwd_args *a, const int64_t *cu, int64_t nseq
     int64_t mx = 0;
     ssd_status st = check_varlen(a, cu, nseq, &mx);
     if (st != SSD_OK) return st;
+    if (a->norm_weight) {  // the packed forward without its gate, then the norm over every token
+        if ((st = check_pointers(a, true)) != SSD_OK) return st;
+        const ssd_fwd_args o = without_norm(a);
+        if ((st = ssd_fwd_varlen(&o, cu, nseq, stream)) != SSD_OK) return st;
+        return norm_after(a, a->L, static_cast<cudaStream_t>(stream));
+    }
     if (a->plan == SSD_PLAN_FUSED && !varlen_fused(a, nseq))
         return fail(SSD_ERR_UNSUPPORTED, "the fused plan does not support this shape: %s",
                     ssd::fused_unsupported_reason(a) ? ssd::fused_unsupported_reason(a) : "too many units");
@@ -595,7 +637,7 @@ ssd_status ssd_chunk_scan(const ssd_fwd_args *a, const float *dtp, const float *
 namespace {
 
 struct HostLayout {
-    size_t fwd_ws, x, dt, A, Bm, Cm, D, z, dt_bias, h0, y, fin, total;
+    size_t fwd_ws, x, dt, A, Bm, Cm, D, z, dt_bias, h0, y, fin, nw, total;
 };
 
 HostLayout host_layout(const ssd_fwd_args *a, int32_t plan) {
@@ -618,6 +660,7 @@ HostLayout host_layout(const ssd_fwd_args *a, int32_t plan) {
     l.h0 = take(a->initial_state ? nst * 4 : 0);
     l.y = take(nx * io);
     l.fin = take(a->final_state ? nst * 4 : 0);
+    l.nw = take(a->norm_weight ? (size_t)a->H * a->P * 4 : 0);
     l.total = off;
     return l;
 }
@@ -705,6 +748,7 @@ ssd_status ssd_fwd_host(const ssd_fwd_args *a, void *stream) {
     d.initial_state = a->initial_state ? reinterpret_cast<const float *>(ws + l.h0) : nullptr;
     d.y = ws + l.y;
     d.final_state = a->final_state ? reinterpret_cast<float *>(ws + l.fin) : nullptr;
+    d.norm_weight = a->norm_weight ? reinterpret_cast<const float *>(ws + l.nw) : nullptr;
     d.workspace = ws + l.fwd_ws;
     d.workspace_bytes = workspace_for(a, plan);
     d.plan = plan;
@@ -745,6 +789,7 @@ ssd_status ssd_fwd_host(const ssd_fwd_args *a, void *stream) {
     h2d(ws + l.A, a->A, (size_t)a->H * 4);
     h2d(ws + l.D, a->D, (size_t)a->H * 4);
     h2d(ws + l.dt_bias, a->dt_bias, (size_t)a->H * 4);
+    h2d(ws + l.nw, a->norm_weight, (size_t)a->H * a->P * 4);
     ssd_status st2 = SSD_OK;
     for (int64_t b0 = 0; b0 < a->B && e == cudaSuccess && st2 == SSD_OK; b0 += per) {
         const int64_t nb = a->B - b0 < per ? a->B - b0 : per;

@@ -10,6 +10,9 @@
 namespace ssd {
 
 bool fused_supported(const ssd_fwd_args *a);
+// The fused kernel can apply the gated RMSNorm in its store stage: z given and
+// at most 8 heads per group (a cluster of up to 4 CTAs, one per head pair).
+bool fused_norm_supported(const ssd_fwd_args *a);
 const char *fused_unsupported_reason(const ssd_fwd_args *a);
 bool fused_preferred(const ssd_fwd_args *a);
 size_t fused_workspace_size(const ssd_fwd_args *a);

@@ -35,6 +35,9 @@ struct Params {
     // packed sequences: the unit at walk position i (CTA i % grid, its
     // (i / grid)-th unit), from the host's schedule
     const int *sched_units = nullptr;
+    // gated RMSNorm of the output (fused plan), NULL otherwise
+    const float *norm_w = nullptr;
+    float norm_eps = 0.f;
 };
 
 enum IoType { IO_F32 = SSD_F32, IO_F16 = SSD_F16, IO_BF16 = SSD_BF16 };

@@ -24,7 +24,7 @@ def test_library_exports_every_declared_symbol():
     assert "ssd_fwd" in names and "ssd_chunk_scan" in names
     for name in names:
         assert hasattr(lib, name), f"missing export {name}"
-    assert lib.ssd_abi_version() == 2
+    assert lib.ssd_abi_version() == 3
 
 
 def test_status_strings():
@@ -107,6 +107,25 @@ def test_misaligned_state_rejected():
     a = _args()
     a.final_state = 8  # not 16-byte aligned
     assert lib.ssd_fwd(ctypes.byref(a), None) == 1
+
+
+def test_norm_needs_z_and_a_finite_eps():
+    lib = ssd.load_library()
+    a = _args()
+    a.norm_weight, a.norm_eps, a.z = 4096, 1e-5, None
+    assert lib.ssd_fwd(ctypes.byref(a), None) == 1
+    assert b"needs z" in lib.ssd_last_error_detail()
+    a = _args()
+    a.norm_weight, a.norm_eps, a.z = 4096, float("nan"), 4096
+    assert lib.ssd_fwd(ctypes.byref(a), None) == 1
+
+
+def test_backward_rejects_the_norm():
+    lib = ssd.load_library()
+    b = ssd.SsdBwdArgs()
+    b.fwd = _args()
+    b.fwd.norm_weight, b.fwd.z = 4096, 4096
+    assert lib.ssd_bwd(ctypes.byref(b), None) == 2
 
 
 def test_python_binding_raises_with_detail():
