@@ -35,7 +35,7 @@ causal_conv1d_kernel(int S, int D, int W, const void *x, const float *__restrict
     __shared__ __align__(16) float xs[kConvRows][kPad + kConvTile];
     const int s0 = blockIdx.x * kConvTile, d0 = blockIdx.y * kConvRows, b = blockIdx.z;
     const int halo = W - 1;
-    // tiles: xs[r][kPad + i] = x[t = s0 + i], xs[r][kPad - m] = x[s0 - m] (halo)
+    // tiles: xs[r][kPad + i] = x[t = s0 + i], xs[r][kPad - m] = x[s0 - m] for m <= W-1 (halo), 0 before
 #pragma unroll
     for (int r = 0; r < kConvRows; ++r) {
         const int d = d0 + r;
@@ -53,9 +53,9 @@ causal_conv1d_kernel(int S, int D, int W, const void *x, const float *__restrict
                 xs[r][kPad + j] = t < S ? ld_io<IO>(x, row + t) : 0.f;
             }
         }
-        if (threadIdx.x < halo) {
-            const int t = s0 - halo + threadIdx.x;
-            xs[r][kPad - halo + threadIdx.x] = t >= 0 ? ld_io<IO>(x, row + t) : 0.f;
+        if (threadIdx.x < kPad) {  // the whole pad: the halo, zeros in front of it (read with zero taps)
+            const int m = threadIdx.x, t = s0 - kPad + m;
+            xs[r][m] = (m >= kPad - halo && t >= 0) ? ld_io<IO>(x, row + t) : 0.f;
         }
     }
     __syncthreads();
@@ -64,21 +64,44 @@ causal_conv1d_kernel(int S, int D, int W, const void *x, const float *__restrict
         const int d = d0 + r;
         if (d >= D) break;
         const size_t row = ((size_t)b * D + d) * S;
-        float wk[kMaxW];
-#pragma unroll
-        for (int k = 0; k < kMaxW; ++k) wk[k] = k < W ? __ldg(w + (size_t)d * W + k) : 0.f;
         const float bv = bias ? __ldg(bias + d) : 0.f;
         float o[kConvPer];
+        if (VEC) {
+            // The thread's 4 consecutive outputs need x[t - (W-1) .. t + 3]: three aligned float4
+            // cover xs[r][4 tid .. 4 tid + 11] (bank-conflict free).  The taps sit right-aligned
+            // in 8 slots (wr[j] = w[j - (8 - W)], zeros before), so output i is
+            // sum_j wr[j] win[1 + i + j] with compile-time indices.
+            float wr[kMaxW];
 #pragma unroll
-        for (int i = 0; i < kConvPer; ++i) {
-            // VEC: the thread's 4 outputs are consecutive; else strided by the block
-            const int j = VEC ? 4 * threadIdx.x + i : threadIdx.x + kConvThreads * i;
-            float acc = bv;
+            for (int j = 0; j < kMaxW; ++j) wr[j] = j >= kMaxW - W ? __ldg(w + (size_t)d * W + j - (kMaxW - W)) : 0.f;
+            float win[12];
 #pragma unroll
-            for (int k = 0; k < kMaxW; ++k)
-                if (k < W) acc = fmaf(wk[k], xs[r][kPad - halo + j + k], acc);  // x[t - (W-1) + k]
-            if (silu) acc = acc / (1.f + expf(-acc));
-            o[i] = acc;
+            for (int q = 0; q < 3; ++q) {
+                const float4 v = *reinterpret_cast<const float4 *>(&xs[r][4 * threadIdx.x + 4 * q]);
+                win[4 * q] = v.x; win[4 * q + 1] = v.y; win[4 * q + 2] = v.z; win[4 * q + 3] = v.w;
+            }
+#pragma unroll
+            for (int i = 0; i < kConvPer; ++i) {
+                float acc = bv;
+#pragma unroll
+                for (int j = 0; j < kMaxW; ++j) acc = fmaf(wr[j], win[1 + i + j], acc);
+                if (silu) acc = acc / (1.f + expf(-acc));
+                o[i] = acc;
+            }
+        } else {
+            float wk[kMaxW];
+#pragma unroll
+            for (int k = 0; k < kMaxW; ++k) wk[k] = k < W ? __ldg(w + (size_t)d * W + k) : 0.f;
+#pragma unroll
+            for (int i = 0; i < kConvPer; ++i) {
+                const int j = threadIdx.x + kConvThreads * i;  // outputs strided by the block
+                float acc = bv;
+#pragma unroll
+                for (int k = 0; k < kMaxW; ++k)
+                    if (k < W) acc = fmaf(wk[k], xs[r][kPad - halo + j + k], acc);  // x[t - (W-1) + k]
+                if (silu) acc = acc / (1.f + expf(-acc));
+                o[i] = acc;
+            }
         }
         if (VEC) {
             const int t = s0 + 4 * threadIdx.x;
