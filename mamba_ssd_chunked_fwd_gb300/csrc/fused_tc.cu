@@ -321,7 +321,7 @@ __device__ __forceinline__ void epilogue8(const Params &p, const Dims &dm, const
         const uint32_t a0 = IO == IO_F32 ? ystage + (f >> 5) * BOX_BYTES + i0 * 128 + (f & 31) * 4
                                          : ystage + (f >> 6) * BOX_BYTES + i0 * 128 + (f & 63) * 2;
 #pragma unroll
-        for (int ii = 0; ii < 8; ++ii) v[ii] *= silu_f(ld_stage<IO>(a0 + ii * 128));
+        for (int ii = 0; ii < 8; ++ii) v[ii] *= silu_fast(ld_stage<IO>(a0 + ii * 128));
     } else if (p.z) {
         float zv[8];
 #pragma unroll
@@ -406,7 +406,7 @@ __device__ __forceinline__ void epilogue_norm(const Params &p, const Dims &dm, c
             v[ii] = fmaf(Dh, (tok_base + ii < dm.L) ? ld_io<IO>(p.x, off0 + ii * step) : 0.f, v[ii]);
     }
 #pragma unroll
-    for (int ii = 0; ii < 16; ++ii) v[ii] *= silu_f(ld_stage<IO>(stage_addr(col0 + ii)));  // z staged where y goes
+    for (int ii = 0; ii < 16; ++ii) v[ii] *= silu_fast(ld_stage<IO>(stage_addr(col0 + ii)));  // z staged where y goes
     // per-token sum of squares over the warp's 32 features: halve the token set
     // at each shuffle step; lane l ends with token tk(l) (bits 4..1 of l), l and
     // l ^ 1 holding the same sum

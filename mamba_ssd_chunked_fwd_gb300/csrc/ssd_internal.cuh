@@ -96,6 +96,10 @@ __device__ __forceinline__ float dt_processed(const Params &p, float raw, int h)
 }
 
 __device__ __forceinline__ float silu_f(float v) { return v / (1.f + expf(-v)); }
+// The same with the fast exponential and division intrinsics (a few ulp),
+// for kernels whose operands are already fp16 / bf16 (the fused kernel).
+// For v < -87 the denominator is +inf and the quotient 0, the function's limit.
+__device__ __forceinline__ float silu_fast(float v) { return __fdividef(v, 1.f + __expf(-v)); }
 
 // One decode step (decode.cu): the shape of ssd_decode_args in device form.
 struct DecodeParams {
