@@ -186,6 +186,13 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+def step_quantiles(per_step):
+    """Median, 20th and 80th percentile of the per-step event times (ms)."""
+    v = sorted(per_step)
+    q = lambda f: v[min(len(v) - 1, int(round(f * (len(v) - 1))))]
+    return {"median": round(q(0.5), 5), "p20": round(q(0.2), 5), "p80": round(q(0.8), 5)}
+
+
 def traffic_for(kernel: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, when the kernel's
     source is unchanged since the counters were taken (else None)."""
@@ -316,6 +323,7 @@ def run_gpu(args):
                           else f"inputs {in_bytes / 1e9:.2f} GB > 129 MB L2, no flush"),
                    "path_roofline_ms": round(path_roofline_ms, 4),
                    "path_frac_of_roofline": round(path_roofline_ms / ms, 4),
+                   "step_ms_quantiles": step_quantiles(per_step),
                    "parallelism": f"replica x{world}" if world > 1 else "1 GPU"},
         "roofline": roofline,
         "kernels": kernels,

@@ -307,7 +307,7 @@ __device__ __forceinline__ void epilogue8(const Params &p, const Dims &dm, const
     float v[8];
 #pragma unroll
     for (int ii = 0; ii < 8; ++ii) v[ii] = fmaf(ev[ii], yo[ii], yi[ii]);
-    if (p.D) {
+    if (ZM == 0 && p.D && !(VARLEN && p.z)) {  // (with z, D x is in the intra-chunk product)
         const float Dh = __ldg(p.D + h);
         float xv[8];
 #pragma unroll
@@ -328,7 +328,7 @@ __device__ __forceinline__ void epilogue8(const Params &p, const Dims &dm, const
         for (int ii = 0; ii < 8; ++ii)
             zv[ii] = (tok_base + ii < len) ? ld_io<IO>(p.z, off0 + ii * step) : 0.f;
 #pragma unroll
-        for (int ii = 0; ii < 8; ++ii) v[ii] *= silu_f(zv[ii]);
+        for (int ii = 0; ii < 8; ++ii) v[ii] *= silu_fast(zv[ii]);
     }
     if (VARLEN && direct) {
 #pragma unroll
@@ -366,7 +366,8 @@ struct NormCtx {
 };
 
 // NORM epilogue: y of this thread's feature for the 16 tokens col0 .. col0+15
-// of the chunk (as epilogue8, gate included), then the gated RMSNorm of the
+// of the chunk (as epilogue8 with z staged; D x is already in the intra-chunk
+// product), then the gated RMSNorm of the
 // ops-transformer MambaV2 article, section 4.6: every token is divided by the
 // root mean square of its cs * 128 gated features (the group's heads) and
 // multiplied by the feature's weight.  The sum of squares runs over the warp's
@@ -378,15 +379,12 @@ template <int IO>
 __device__ __forceinline__ void epilogue_norm(const Params &p, const Dims &dm, const ChunkVec &V, uint32_t tlane,
                                               int bp, int col0, int b, int h0, int my_h, int my_p, int tok_base,
                                               uint32_t ystage, const NormCtx &nc, uint32_t gp, int wg, int quarter,
-                                              int lane, float Dh, float wf, bool &timed_out) {
-    const int h = h0 + my_h;
+                                              int lane, float wf, bool &timed_out) {
     const int f = my_h * kP + my_p;  // feature within the pair's 128
     auto stage_addr = [&](int ib) {  // token row ib of the staging tile, this feature
         return IO == IO_F32 ? ystage + (f >> 5) * BOX_BYTES + ib * 128 + (f & 31) * 4
                             : ystage + (f >> 6) * BOX_BYTES + ib * 128 + (f & 63) * 2;
     };
-    const size_t step = (size_t)dm.H * kP;
-    const size_t off0 = (((size_t)b * dm.L + tok_base) * dm.H + h) * kP + my_p;
     float v[16];
 #pragma unroll
     for (int hf = 0; hf < 2; ++hf) {
@@ -399,12 +397,7 @@ __device__ __forceinline__ void epilogue_norm(const Params &p, const Dims &dm, c
 #pragma unroll
         for (int ii = 0; ii < 8; ++ii) v[8 * hf + ii] = fmaf(ev[ii], yo[ii], yi[ii]);
     }
-    tc::fence_before_sync();
-    if (p.D) {
-#pragma unroll
-        for (int ii = 0; ii < 16; ++ii)
-            v[ii] = fmaf(Dh, (tok_base + ii < dm.L) ? ld_io<IO>(p.x, off0 + ii * step) : 0.f, v[ii]);
-    }
+    tc::fence_before_sync();  // (D x is in the intra-chunk product)
 #pragma unroll
     for (int ii = 0; ii < 16; ++ii) v[ii] *= silu_fast(ld_stage<IO>(stage_addr(col0 + ii)));  // z staged where y goes
     // per-token sum of squares over the warp's 32 features: halve the token set
@@ -773,7 +766,7 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
         uint32_t gk = 0;
         uint32_t yt = 0;  // y tiles staged so far
         NormCtx nc{};
-        float norm_wf = 0.f, norm_dh = 0.f;  // per unit: this feature's norm weight, its head's D
+        float norm_wf = 0.f;  // per unit: this feature's norm weight
         if constexpr (ZM == 2) {
             nc.lpart = sbase + OFF_NORM + NORM_LPART;
             nc.recv = sbase + OFF_NORM + NORM_RECV;
@@ -794,7 +787,7 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
             tc::fence_after_sync();
             if constexpr (ZM == 2) {
                 epilogue_norm<IO>(p, dm, Vbuf[gp % kVecSlots], tlane, bp, col0, b, h0, my_h, my_p, kk * kQ + col0,
-                                  sbase + OFF_STG_Y, nc, gp, wg, quarter, lane, norm_dh, norm_wf, timed_out);
+                                  sbase + OFF_STG_Y, nc, gp, wg, quarter, lane, norm_wf, timed_out);
             } else {
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf)
@@ -827,7 +820,6 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
             }
             if constexpr (ZM == 2) {
                 norm_wf = __ldg(p.norm_w + (size_t)(h0 + my_h) * kP + my_p);
-                norm_dh = p.D ? __ldg(p.D + h0 + my_h) : 0.f;
             }
 
             // state of (head my_h, row my_p), columns n = col0 .. col0+kCols-1
@@ -908,6 +900,13 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                 {
                     const int i = row & 63, h = row >> 6;
                     const float csi = V.cs2[h][i];
+                    // gated instantiations: D x_i as D on the diagonal of the intra-chunk matrix (the
+                    // diagonal's decay is exp(0) = 1), on the tensor core with x's operand rounding
+                    // (packed sequences do the same when z is given, so that both layouts give the same bits)
+                    float diag_d = 0.f;
+                    if constexpr (ZM > 0 || VARLEN) {
+                        if (ZM > 0 || p.z) diag_d = p.D ? __ldg(p.D + h0 + h) : 0.f;
+                    }
                     wait(BAR_G_DONE, ph);
                     tc::fence_after_sync();
                     const uint32_t mc = sbase + OFF_MC;
@@ -927,6 +926,7 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                         for (int e = 0; e < 8; ++e) {
                             const float v = gv[e] * ex2_approx(csi - cj[e]) * dj[e];
                             m[e] = (j0 + e <= i) ? v : 0.f;
+                            if constexpr (ZM > 0 || VARLEN) m[e] += (j0 + e == i) ? diag_d : 0.f;
                         }
                         const int kg = 8 * h + (j0 >> 3);
                         store8(mc + (kg * 8 + (i >> 3)) * 128 + (i & 7) * 16, m, BF16);
