@@ -307,15 +307,7 @@ __device__ __forceinline__ void epilogue8(const Params &p, const Dims &dm, const
     float v[8];
 #pragma unroll
     for (int ii = 0; ii < 8; ++ii) v[ii] = fmaf(ev[ii], yo[ii], yi[ii]);
-    if (ZM == 0 && p.D && !(VARLEN && p.z)) {  // (with z, D x is in the intra-chunk product)
-        const float Dh = __ldg(p.D + h);
-        float xv[8];
-#pragma unroll
-        for (int ii = 0; ii < 8; ++ii)
-            xv[ii] = (tok_base + ii < len) ? ld_io<IO>(p.x, off0 + ii * step) : 0.f;
-#pragma unroll
-        for (int ii = 0; ii < 8; ++ii) v[ii] = fmaf(Dh, xv[ii], v[ii]);
-    }
+    // (D x is in the intra-chunk product)
     if constexpr (ZM > 0) {  // z staged where y goes
         const int f = my_h * kP + my_p;
         const uint32_t a0 = IO == IO_F32 ? ystage + (f >> 5) * BOX_BYTES + i0 * 128 + (f & 31) * 4
@@ -900,13 +892,9 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                 {
                     const int i = row & 63, h = row >> 6;
                     const float csi = V.cs2[h][i];
-                    // gated instantiations: D x_i as D on the diagonal of the intra-chunk matrix (the
-                    // diagonal's decay is exp(0) = 1), on the tensor core with x's operand rounding
-                    // (packed sequences do the same when z is given, so that both layouts give the same bits)
-                    float diag_d = 0.f;
-                    if constexpr (ZM > 0 || VARLEN) {
-                        if (ZM > 0 || p.z) diag_d = p.D ? __ldg(p.D + h0 + h) : 0.f;
-                    }
+                    // D x_i as D on the diagonal of the intra-chunk matrix (the diagonal's decay is
+                    // exp(0) = 1): on the tensor core with x's operand rounding, no x loads in the epilogue
+                    const float diag_d = p.D ? __ldg(p.D + h0 + h) : 0.f;
                     wait(BAR_G_DONE, ph);
                     tc::fence_after_sync();
                     const uint32_t mc = sbase + OFF_MC;
@@ -926,7 +914,7 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                         for (int e = 0; e < 8; ++e) {
                             const float v = gv[e] * ex2_approx(csi - cj[e]) * dj[e];
                             m[e] = (j0 + e <= i) ? v : 0.f;
-                            if constexpr (ZM > 0 || VARLEN) m[e] += (j0 + e == i) ? diag_d : 0.f;
+                            m[e] += (j0 + e == i) ? diag_d : 0.f;
                         }
                         const int kg = 8 * h + (j0 >> 3);
                         store8(mc + (kg * 8 + (i >> 3)) * 128 + (i & 7) * 16, m, BF16);
