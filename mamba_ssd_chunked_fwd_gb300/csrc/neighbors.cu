@@ -27,8 +27,9 @@ constexpr int kConvRows = 4;  // channels per CTA
 constexpr int kMaxW = 8;
 constexpr int kPad = 8;       // the halo slot in front of each channel's tile (>= W-1, keeps float4 alignment)
 
-// VEC: fp32 rows with S % 4 == 0 (16-byte aligned rows): float4 loads and stores.
-template <int IO, bool VEC>
+// VEC: fp32 rows with S % 4 == 0 (16-byte aligned rows): float4 loads and stores,
+// the taps in KT (4 or 8, >= W) slots.
+template <int IO, bool VEC, int KT = kMaxW>
 __global__ void __launch_bounds__(kConvThreads)
 causal_conv1d_kernel(int S, int D, int W, const void *x, const float *__restrict__ w, const float *__restrict__ bias,
                      int silu, void *out) {
@@ -67,25 +68,25 @@ causal_conv1d_kernel(int S, int D, int W, const void *x, const float *__restrict
         const float bv = bias ? __ldg(bias + d) : 0.f;
         float o[kConvPer];
         if (VEC) {
-            // The thread's 4 consecutive outputs need x[t - (W-1) .. t + 3]: three aligned float4
-            // cover xs[r][4 tid .. 4 tid + 11] (bank-conflict free).  The taps sit right-aligned
-            // in 8 slots (wr[j] = w[j - (8 - W)], zeros before), so output i is
+            // The thread's 4 consecutive outputs need x[t - (W-1) .. t + 3]: the (KT + 4) / 4
+            // aligned float4 from xs[r][4 tid + 8 - KT] on (bank-conflict free).  The taps sit
+            // right-aligned in KT slots (wr[j] = w[j - (KT - W)], zeros before), so output i is
             // sum_j wr[j] win[1 + i + j] with compile-time indices.
-            float wr[kMaxW];
+            float wr[KT];
 #pragma unroll
-            for (int j = 0; j < kMaxW; ++j) wr[j] = j >= kMaxW - W ? __ldg(w + (size_t)d * W + j - (kMaxW - W)) : 0.f;
-            float win[12];
+            for (int j = 0; j < KT; ++j) wr[j] = j >= KT - W ? __ldg(w + (size_t)d * W + j - (KT - W)) : 0.f;
+            float win[KT + 4];
 #pragma unroll
-            for (int q = 0; q < 3; ++q) {
-                const float4 v = *reinterpret_cast<const float4 *>(&xs[r][4 * threadIdx.x + 4 * q]);
+            for (int q = 0; q < (KT + 4) / 4; ++q) {
+                const float4 v = *reinterpret_cast<const float4 *>(&xs[r][4 * threadIdx.x + kPad - KT + 4 * q]);
                 win[4 * q] = v.x; win[4 * q + 1] = v.y; win[4 * q + 2] = v.z; win[4 * q + 3] = v.w;
             }
 #pragma unroll
             for (int i = 0; i < kConvPer; ++i) {
                 float acc = bv;
 #pragma unroll
-                for (int j = 0; j < kMaxW; ++j) acc = fmaf(wr[j], win[1 + i + j], acc);
-                if (silu) acc = acc / (1.f + expf(-acc));
+                for (int j = 0; j < KT; ++j) acc = fmaf(wr[j], win[1 + i + j], acc);
+                if (silu) acc = __fdividef(acc, 1.f + __expf(-acc));  // a few ulp; 0 below -87 (the limit)
                 o[i] = acc;
             }
         } else {
@@ -118,7 +119,8 @@ causal_conv1d_kernel(int S, int D, int W, const void *x, const float *__restrict
 }
 
 // PER: values each lane keeps in registers (PER * 32 >= the group size), 0 for
-// groups wider than 512 channels (second pass).
+// groups wider than 512 channels (second pass).  The gate uses the fast
+// exponential and division (a few ulp; 0 for z below -87, the limit).
 template <int IO, int PER>
 __global__ void __launch_bounds__(256)
 gated_rmsnorm_kernel(long long rows, int D, int groups, float eps, const void *x, const void *z,
@@ -139,7 +141,7 @@ gated_rmsnorm_kernel(long long rows, int D, int groups, float eps, const void *x
             v[k] = 0.f;
             if (i < gs) {
                 const float zv = ld_io<IO>(z, base + i);
-                v[k] = ld_io<IO>(x, base + i) * (zv / (1.f + expf(-zv)));
+                v[k] = ld_io<IO>(x, base + i) * __fdividef(zv, 1.f + __expf(-zv));
             }
         }
 #pragma unroll
@@ -155,7 +157,7 @@ gated_rmsnorm_kernel(long long rows, int D, int groups, float eps, const void *x
     } else {
         for (int i = lane; i < gs; i += 32) {
             const float zv = ld_io<IO>(z, base + i);
-            const float v = ld_io<IO>(x, base + i) * (zv / (1.f + expf(-zv)));
+            const float v = ld_io<IO>(x, base + i) * __fdividef(zv, 1.f + __expf(-zv));
             ss = fmaf(v, v, ss);
         }
 #pragma unroll
@@ -163,7 +165,7 @@ gated_rmsnorm_kernel(long long rows, int D, int groups, float eps, const void *x
         const float inv = rsqrtf(ss / (float)gs + eps);
         for (int i = lane; i < gs; i += 32) {  // second pass, from L1/L2
             const float zv = ld_io<IO>(z, base + i);
-            const float v = ld_io<IO>(x, base + i) * (zv / (1.f + expf(-zv)));
+            const float v = ld_io<IO>(x, base + i) * __fdividef(zv, 1.f + __expf(-zv));
             st_io<IO>(out, base + i, v * inv * __ldg(w + g * gs + i));
         }
     }
@@ -178,7 +180,10 @@ cudaError_t launch_causal_conv1d(int B, int D, int S, int W, int io, const void 
     const bool vec = S % 4 == 0 && reinterpret_cast<uintptr_t>(x) % 16 == 0 && reinterpret_cast<uintptr_t>(out) % 16 == 0;
     switch (io) {
         case IO_F32:
-            if (vec) causal_conv1d_kernel<IO_F32, true><<<grid, kConvThreads, 0, s>>>(S, D, W, x, w, bias, silu, out);
+            if (vec && W <= 4)
+                causal_conv1d_kernel<IO_F32, true, 4><<<grid, kConvThreads, 0, s>>>(S, D, W, x, w, bias, silu, out);
+            else if (vec)
+                causal_conv1d_kernel<IO_F32, true, 8><<<grid, kConvThreads, 0, s>>>(S, D, W, x, w, bias, silu, out);
             else causal_conv1d_kernel<IO_F32, false><<<grid, kConvThreads, 0, s>>>(S, D, W, x, w, bias, silu, out);
             break;
         case IO_F16: causal_conv1d_kernel<IO_F16, false><<<grid, kConvThreads, 0, s>>>(S, D, W, x, w, bias, silu, out); break;
