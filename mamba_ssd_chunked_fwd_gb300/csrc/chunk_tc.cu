@@ -395,7 +395,7 @@ chunk_scan_tc_kernel(const __grid_constant__ Params p, const float *__restrict__
             const int tb = k * Q + i0 + ic;
             float ev[16];
 #pragma unroll
-            for (int ii = 0; ii < 16; ++ii) ev[ii] = expf(cs_s[h * kMaxQ + i0 + ic + ii]);
+            for (int ii = 0; ii < 16; ++ii) ev[ii] = __expf(cs_s[h * kMaxQ + i0 + ic + ii]);  // cs <= 0
             const size_t off0 = (((size_t)b * L + tb) * H + h0 + h) * kP + pp;
             float v[16];
 #pragma unroll
@@ -408,7 +408,7 @@ chunk_scan_tc_kernel(const __grid_constant__ Params p, const float *__restrict__
             if (p.z) {
 #pragma unroll
                 for (int ii = 0; ii < 16; ++ii)
-                    if (tb + ii < L) v[ii] *= silu_f(ld_io<IO>(p.z, off0 + ii * step));
+                    if (tb + ii < L) v[ii] *= silu_fast(ld_io<IO>(p.z, off0 + ii * step));
             }
 #pragma unroll
             for (int ii = 0; ii < 16; ++ii)
