@@ -171,6 +171,45 @@ gated_rmsnorm_kernel(long long rows, int D, int groups, float eps, const void *x
     }
 }
 
+// Groups of 32, 64 or 128 channels: one warp covers GPW groups (256 channels,
+// PER = group size / 32 values per lane and group), so that a warp keeps 2 KB
+// of loads in flight; each group's sum of squares reduces over the warp as in
+// the kernel above (per-lane partial, then the xor tree).
+template <int IO, int PER, int GPW>
+__global__ void __launch_bounds__(256)
+gated_rmsnorm_multi_kernel(long long rows, int D, int groups, float eps, const void *x, const void *z,
+                           const float *__restrict__ w, void *out) {
+    constexpr int kGs = 32 * PER, kVpl = PER * GPW;
+    const long long wid = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);  // (row, block of GPW groups)
+    const int lane = threadIdx.x & 31;
+    const int spans = groups / GPW;
+    if (wid >= rows * spans) return;
+    const long long r = wid / spans;
+    const int g0 = (int)(wid % spans) * GPW;
+    const size_t base = (size_t)r * D + (size_t)g0 * kGs;
+    float v[kVpl];
+#pragma unroll
+    for (int k = 0; k < kVpl; ++k) {  // every load first
+        const float zv = ld_io<IO>(z, base + lane + 32 * k);
+        v[k] = ld_io<IO>(x, base + lane + 32 * k) * __fdividef(zv, 1.f + __expf(-zv));
+    }
+    float inv[GPW];
+#pragma unroll
+    for (int j = 0; j < GPW; ++j) {
+        float ss = 0.f;
+#pragma unroll
+        for (int k = j * PER; k < (j + 1) * PER; ++k) ss = fmaf(v[k], v[k], ss);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        inv[j] = rsqrtf(ss / (float)kGs + eps);
+    }
+#pragma unroll
+    for (int k = 0; k < kVpl; ++k) {
+        const int i = lane + 32 * k;
+        st_io<IO>(out, base + i, v[k] * inv[k / PER] * __ldg(w + (size_t)g0 * kGs + i));
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_causal_conv1d(int B, int D, int S, int W, int io, const void *x, const float *w,
@@ -195,9 +234,26 @@ cudaError_t launch_causal_conv1d(int B, int D, int S, int W, int io, const void 
 
 cudaError_t launch_gated_rmsnorm(long long rows, int D, int groups, float eps, int io, const void *x, const void *z,
                                  const float *w, void *out, cudaStream_t s) {
+    const int gs = D / groups;
+    const int gpw = (gs == 32 || gs == 64 || gs == 128) ? 256 / gs : 1;
+    if (gpw > 1 && groups % gpw == 0) {  // several groups per warp
+        const long long mwarps = rows * (groups / gpw);
+        const unsigned mblocks = (unsigned)((mwarps + 7) / 8);
+#define SSD_RMS_MULTI(PER, GPW)                                                                                   \
+    switch (io) {                                                                                                 \
+        case IO_F32: gated_rmsnorm_multi_kernel<IO_F32, PER, GPW><<<mblocks, 256, 0, s>>>(rows, D, groups, eps, x, z, w, out); break; \
+        case IO_F16: gated_rmsnorm_multi_kernel<IO_F16, PER, GPW><<<mblocks, 256, 0, s>>>(rows, D, groups, eps, x, z, w, out); break; \
+        case IO_BF16: gated_rmsnorm_multi_kernel<IO_BF16, PER, GPW><<<mblocks, 256, 0, s>>>(rows, D, groups, eps, x, z, w, out); break; \
+        default: return cudaErrorInvalidValue;                                                                    \
+    }
+        if (gs == 32) { SSD_RMS_MULTI(1, 8) }
+        else if (gs == 64) { SSD_RMS_MULTI(2, 4) }
+        else { SSD_RMS_MULTI(4, 2) }
+#undef SSD_RMS_MULTI
+        return cudaGetLastError();
+    }
     const long long warps = rows * groups;
     const unsigned blocks = (unsigned)((warps + 7) / 8);
-    const int gs = D / groups;
 #define SSD_RMS_LAUNCH(PER)                                                                                  \
     switch (io) {                                                                                            \
         case IO_F32: gated_rmsnorm_kernel<IO_F32, PER><<<blocks, 256, 0, s>>>(rows, D, groups, eps, x, z, w, out); break; \

@@ -31,9 +31,11 @@ def test_causal_conv1d(oracle_mod, shape, dtype, feats):
     assert_close(oracle_mod, out.double().cpu().numpy(), ref, dtype, f"conv1d {shape} {dtype}")
 
 
-# group sizes 256, 32, 4096 (two passes), 25, 512, 500, 128, 60
+# group sizes 256, 32, 4096 (two passes), 25, 512, 500, 128, 60; then 32, 64, 128 with the groups
+# a multiple of 8, 4, 2 (several groups per warp)
 @pytest.mark.parametrize("shape", [(2, 512, 16384, 64), (3, 7, 96, 3), (1, 5, 4096, 1), (4, 33, 200, 8),
-                                   (2, 9, 1024, 2), (1, 3, 1000, 2), (1, 17, 384, 3), (2, 11, 300, 5)])
+                                   (2, 9, 1024, 2), (1, 3, 1000, 2), (1, 17, 384, 3), (2, 11, 300, 5),
+                                   (2, 9, 512, 16), (1, 13, 512, 8), (3, 5, 512, 4)])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_gated_rmsnorm(oracle_mod, shape, dtype):
     import mamba_ssd_chunked_fwd_gb300 as ssd
