@@ -119,7 +119,7 @@ typedef struct ssd_fwd_args {
      * where ssd is the output above without its own z gate and rmsnorm_g
      * divides each run of (H/G)*P consecutive channels (the heads of one B/C
      * group) by sqrt(mean of squares + norm_eps).  The fused plan does it in
-     * its store stage when H/G <= 8; other plans (and wider groups) run the
+     * its store stage when H/G <= 4; other plans (and wider groups) run the
      * same arithmetic as a second kernel over y.  Not supported by ssd_bwd. */
     const float *norm_weight;
     float norm_eps;

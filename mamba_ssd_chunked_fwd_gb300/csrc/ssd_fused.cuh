@@ -11,7 +11,7 @@ namespace ssd {
 
 bool fused_supported(const ssd_fwd_args *a);
 // The fused kernel can apply the gated RMSNorm in its store stage: z given and
-// at most 8 heads per group (a cluster of up to 4 CTAs, one per head pair).
+// at most 4 heads per group (a cluster of up to 2 CTAs, one per head pair).
 bool fused_norm_supported(const ssd_fwd_args *a);
 const char *fused_unsupported_reason(const ssd_fwd_args *a);
 bool fused_preferred(const ssd_fwd_args *a);
