@@ -117,29 +117,29 @@ bwd_chunk_adjoint_kernel(Params p, const float *__restrict__ cs, const float *__
                          float *__restrict__ adj) {
     __shared__ __align__(16) float ds[kMax * kMax];  // exp(cs_i) dyp_i, [i][p] (N)
     __shared__ __align__(16) float cc[kMax * kMax];  // C, [i][n] (N)
+    __shared__ float e_s[kMax];                      // exp(cs_i)
     const int k = blockIdx.y, bh = blockIdx.x;
     const int b = bh / p.H, h = bh % p.H, g = h / p.hpg;
     const int P = p.P, N = p.N, Q = p.Q, L = p.L, tid = threadIdx.x;
     const size_t crow = (((size_t)b * p.H + h) * p.nchunks + k) * Q;
-    {
-        // every global load issued before the shared-memory stores; 0 outside (Q, P, N) and past L
-        constexpr int kPer = kMax * kMax / kThreads;
-        const int col = tid & (kMax - 1), rb = tid >> 6;
-        float rd[kPer], rc[kPer], re[kPer];
+    if (tid < kMax) e_s[tid] = tid < Q ? expf(__ldg(cs + crow + tid)) : 0.f;
+    // every global load issued before the shared-memory stores; 0 outside (Q, P, N) and past L
+    constexpr int kPer = kMax * kMax / kThreads;
+    const int col = tid & (kMax - 1), rb = tid >> 6;
+    float rd[kPer], rc[kPer];
 #pragma unroll
-        for (int q = 0; q < kPer; ++q) {
-            const int i = rb * kPer + q, t = k * Q + i;
-            const bool row_in = i < Q && t < L;
-            rd[q] = row_in && col < P ? __ldg(dyp + (((size_t)b * L + t) * p.H + h) * P + col) : 0.f;
-            rc[q] = row_in && col < N ? ld_io<IO>(p.Cm, (((size_t)b * L + t) * p.G + g) * N + col) : 0.f;
-            re[q] = row_in ? __ldg(cs + crow + i) : 0.f;
-        }
+    for (int q = 0; q < kPer; ++q) {
+        const int i = rb * kPer + q, t = k * Q + i;
+        const bool row_in = i < Q && t < L;
+        rd[q] = row_in && col < P ? __ldg(dyp + (((size_t)b * L + t) * p.H + h) * P + col) : 0.f;
+        rc[q] = row_in && col < N ? ld_io<IO>(p.Cm, (((size_t)b * L + t) * p.G + g) * N + col) : 0.f;
+    }
+    __syncthreads();  // e_s
 #pragma unroll
-        for (int q = 0; q < kPer; ++q) {
-            const int i = rb * kPer + q;
-            ds[i * kMax + col] = rd[q] * expf(re[q]);
-            cc[i * kMax + col] = rc[q];
-        }
+    for (int q = 0; q < kPer; ++q) {
+        const int i = rb * kPer + q;
+        ds[i * kMax + col] = rd[q] * e_s[i];
+        cc[i * kMax + col] = rc[q];
     }
     __syncthreads();
     const int r0 = tid >> 4, c0 = tid & 15;
