@@ -91,7 +91,7 @@ __device__ __forceinline__ float f4(const float4 &v, int i) { return i == 0 ? v.
 // return the float4s; k1 - k0 is a multiple of 4.
 template <class FA, class FB>
 __device__ __forceinline__ void tile4v(float (&acc)[4][4], int k0, int k1, FA fa, FB fb) {
-#pragma unroll 4
+#pragma unroll 8
     for (int k = k0; k < k1; ++k) {
         const float4 av = fa(k), bv = fb(k);
         const float ar[4] = {av.x, av.y, av.z, av.w}, br[4] = {bv.x, bv.y, bv.z, bv.w};
