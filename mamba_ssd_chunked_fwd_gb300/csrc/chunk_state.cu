@@ -151,7 +151,7 @@ chunk_state64_kernel(Params p, const float *__restrict__ dtp, const float *__res
     for (int a = 0; a < 4; ++a)
 #pragma unroll
         for (int c = 0; c < 4; ++c) acc[a][c] = 0.f;
-#pragma unroll 4
+#pragma unroll 8
     for (int i = 0; i < Q; ++i) {
         const float4 x4 = *reinterpret_cast<const float4 *>(&xs[i][4 * tp]);
         const float4 b4 = *reinterpret_cast<const float4 *>(&bs[i][4 * tn]);
