@@ -453,26 +453,46 @@ bwd_chunk_kernel(Params p, const float *__restrict__ dtp, const float *__restric
         sm.u[tid] = f;
     }
     __syncthreads();
-    if (tid == 0) {
-        float wsum = 0.f;
-        for (int j = 0; j < Q; ++j) wsum += sm.w[j];
-        sm.dcs[Q - 1] += expf(cs_last) * gs + wsum;
-        // reverse cumsum; dd, dA, dbias (fixed order)
-        float run = 0.f, sA = 0.f, sBias = 0.f, sD = 0.f;
-        for (int t = Q - 1; t >= 0; --t) {
-            run += sm.dcs[t];
-            sm.dcs[t] = run;
+    if (warp == 0) {
+        // tokens 2 lane and 2 lane + 1 (Q is even): the last token's extra terms, the reverse
+        // cumulative sum of dcs (a shuffle scan of the pair sums), then dA, dD, dbias partials;
+        // every sum in a fixed order
+        const int t0 = 2 * lane, t1 = t0 + 1;
+        const bool q0 = t0 < Q, q1 = t1 < Q;
+        float wsum = (q0 ? sm.w[t0] : 0.f) + (q1 ? sm.w[t1] : 0.f);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
+        const float d0 = q0 ? sm.dcs[t0] : 0.f;
+        float d1 = q1 ? sm.dcs[t1] : 0.f;
+        if (t1 == Q - 1) d1 += expf(cs_last) * gs + wsum;
+        const float pr = d0 + d1;
+        float S = pr;  // sum of the pair sums of lanes >= this one
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float o = __shfl_down_sync(0xffffffffu, S, off);
+            if (lane + off < 32) S += o;
         }
-        for (int t = 0; t < Q; ++t) {
-            sD += sm.dxd[t];
-            if (k * Q + t >= L) continue;
-            sA = fmaf(sm.d[t], sm.dcs[t], sA);
-            sBias = fmaf(fmaf(A, sm.dcs[t], sm.dd1[t]), sm.u[t], sBias);
+        float excl = __shfl_down_sync(0xffffffffu, S, 1);  // lanes > this one
+        if (lane == 31) excl = 0.f;
+        const float R1 = d1 + excl, R0 = d0 + R1;
+        if (q0) sm.dcs[t0] = R0;
+        if (q1) sm.dcs[t1] = R1;
+        const bool in0 = q0 && k * Q + t0 < L, in1 = q1 && k * Q + t1 < L;
+        float sA = (in0 ? sm.d[t0] * R0 : 0.f) + (in1 ? sm.d[t1] * R1 : 0.f);
+        float sBias = (in0 ? fmaf(A, R0, sm.dd1[t0]) * sm.u[t0] : 0.f) + (in1 ? fmaf(A, R1, sm.dd1[t1]) * sm.u[t1] : 0.f);
+        float sD = (q0 ? sm.dxd[t0] : 0.f) + (q1 ? sm.dxd[t1] : 0.f);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            sA += __shfl_xor_sync(0xffffffffu, sA, off);
+            sBias += __shfl_xor_sync(0xffffffffu, sBias, off);
+            sD += __shfl_xor_sync(0xffffffffu, sD, off);
         }
-        const size_t pi = ((size_t)b * p.nchunks + k) * p.H + h;
-        partA[pi] = sA;
-        partD[pi] = sD;
-        partBias[pi] = sBias;
+        if (lane == 0) {
+            const size_t pi = ((size_t)b * p.nchunks + k) * p.H + h;
+            partA[pi] = sA;
+            partD[pi] = sD;
+            partBias[pi] = sBias;
+        }
     }
     __syncthreads();
     for (int t = tid; t < Q; t += kThreads)
