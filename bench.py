@@ -293,14 +293,19 @@ def run_gpu(args):
     if plan == ssd.SSD_PLAN_FUSED:
         kname, kbytes, kms = "ssd_fused_kernel", ab["total"], ms
         launches_per_step = 1
+        scope = "one launch = the whole step"
     else:
-        kname, kbytes, kms, stages = stage_timing(ssd, a, w, dev, sh, stream, args, kernels)
-        launches_per_step = 4
+        # several launches per step: the fraction is the path's algorithmic
+        # bytes (public I/O only) over the whole step, the dominant stage named
+        kname, _, _, stages = stage_timing(ssd, a, w, dev, sh, stream, args, kernels)
+        kbytes, kms = ab["total"], ms
+        launches_per_step = len(kernels)
+        scope = f"whole step ({launches_per_step} launches; dominant stage {kname}, see stages)"
     achieved = kbytes / (kms * 1e-3) / 1e9
     roofline = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1), "peak": hbm,
                 "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / hbm, 4),
-                "traffic": traffic_for(kname, args.workload), "alg_bytes_per_launch": kbytes,
-                "launch_ms": round(kms, 5)}
+                "traffic": traffic_for(kname, args.workload) if plan == ssd.SSD_PLAN_FUSED else None,
+                "alg_bytes_per_launch": kbytes, "launch_ms": round(kms, 5), "scope": scope}
     path_roofline_ms = ab["total"] / (hbm * 1e9) * 1e3
 
     e2e = e2e_timing(ssd, inp, w, dev, args) if not args.no_e2e else None
@@ -750,45 +755,67 @@ def e2e_timing(ssd, inp, w, dev, args):
     for _ in range(2):
         ssd.ssd_fwd_host(a, sh)
     torch.cuda.synchronize(dev)
-    steps = max(2, min(args.steps, 5))
-    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s.record(stream)
-    for _ in range(steps):
+    steps = max(3, args.steps)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        starts[i].record(stream)
         ssd.ssd_fwd_host(a, sh)
-    e.record(stream)
+        ends[i].record(stream)
     torch.cuda.synchronize(dev)
-    ms = s.elapsed_time(e) / steps
+    per_step = [st.elapsed_time(en) for st, en in zip(starts, ends)]
+    ms = sum(per_step) / len(per_step)
     h2d = sum(v.numel() * v.element_size() for k, v in h.items()
               if isinstance(v, torch.Tensor))
     d2h = y.numel() * y.element_size() + (fin.numel() * 4 if fin is not None else 0)
     return {"value": round(w.tokens / (ms * 1e-3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
+            "steps": steps, "step_ms_quantiles": step_quantiles(per_step),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
 
 # ---- the CPU oracle (cpu_baseline and --impl reference) --------------------------------
 
-def oracle_sample(w, inp, seconds, *, nthreads=0):
-    """Time the float64 oracle on a bounded sample of the workload: whole
-    (batch, head) sequences over the full L, as many as fit in ~``seconds``."""
+def _oracle_problem(inp):
     import oracle
     oracle.build()
-    prob = oracle.Problem(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], D=inp["D"], z=inp["z"],
+    return oracle.Problem(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], D=inp["D"], z=inp["z"],
                           dt_bias=inp["dt_bias"], initial_states=inp["initial_states"],
                           dt_softplus=inp["dt_softplus"])
+
+
+def oracle_sample_size(w, prob, seconds, *, nthreads=0):
+    """How many whole (batch, head) sequences of the workload the float64
+    oracle finishes in about ``seconds`` (from one timed calibration run over
+    one sequence per core)."""
+    import oracle
     cores = nthreads or oracle.threads()
     total = w.B * w.H
     n = min(total, max(1, cores))
     t0 = time.perf_counter()
     oracle.recurrence(prob, [(i // w.H, i % w.H) for i in range(n)], nthreads=nthreads)
-    dt = time.perf_counter() - t0
-    per_pair = dt / n
-    n2 = int(min(total, max(n, seconds / max(per_pair, 1e-9))))
-    if n2 > n:
-        pairs = [(i // w.H, i % w.H) for i in range(n2)]
-        t0 = time.perf_counter()
-        oracle.recurrence(prob, pairs, nthreads=nthreads)
-        dt = time.perf_counter() - t0
-        n = n2
+    per_pair = (time.perf_counter() - t0) / n
+    return int(min(total, max(n, seconds / max(per_pair, 1e-9)))), cores
+
+
+def oracle_timed(w, prob, n, *, nthreads=0, offset=0):
+    """One timed oracle run over n whole sequences (starting at sequence
+    ``offset``, wrapping around): (wall seconds, tokens processed, counted
+    as the workload's tokens B*L times the share of its B*H sequences run)."""
+    import oracle
+    total = w.B * w.H
+    pairs = [((offset + i) % total // w.H, (offset + i) % total % w.H) for i in range(n)]
+    t0 = time.perf_counter()
+    oracle.recurrence(prob, pairs, nthreads=nthreads)
+    return time.perf_counter() - t0, w.tokens * n / total
+
+
+def oracle_sample(w, inp, seconds, *, nthreads=0):
+    """Time the float64 oracle on a bounded sample of the workload: whole
+    (batch, head) sequences over the full L, as many as fit in ~``seconds``."""
+    prob = _oracle_problem(inp)
+    n, cores = oracle_sample_size(w, prob, seconds, nthreads=nthreads)
+    dt, _ = oracle_timed(w, prob, n, nthreads=nthreads)
+    total = w.B * w.H
     frac = n / total
     tok_s = w.tokens * frac / dt
     return {"value": round(tok_s, 1), "unit": "tokens/s", "cores": cores, "kind": "oracle",
@@ -802,16 +829,32 @@ def cpu_baseline(w, inp, seconds):
 
 
 def run_reference(args):
+    """The float64 oracle as the reference arm.  Each step is one bounded
+    sample of the workload (the same number of whole (batch, head) sequences
+    every step, sized in the warm-up so that all steps take about
+    --cpu-seconds); ms_per_step is a step's own measured wall time, and value
+    is the tokens those steps processed over their total wall time."""
     rank, world, _ = rank_info()
     if rank != 0:
         return
     w = ssd_inputs.WORKLOADS[args.workload]
     inp = ssd_inputs.make(w)
-    per_step = max(1.0, args.cpu_seconds / max(1, args.steps))
-    samples = [oracle_sample(w, inp, per_step) for _ in range(args.warmup and 1 or 0)]
-    samples = [oracle_sample(w, inp, per_step) for _ in range(args.steps)]
-    value = statistics.median(s["value"] for s in samples)
-    ms = w.tokens / value * 1e3
+    prob = _oracle_problem(inp)
+    per_step = max(0.5, args.cpu_seconds / max(1, args.steps))
+    n, cores = oracle_sample_size(w, prob, per_step)
+    for i in range(args.warmup and 1 or 0):
+        oracle_timed(w, prob, n, offset=i * n)
+    walls, tokens = [], 0
+    for i in range(args.steps):
+        dt, tk = oracle_timed(w, prob, n, offset=i * n)
+        walls.append(dt)
+        tokens += tk
+    value = tokens / sum(walls)
+    ms = sum(walls) / len(walls) * 1e3
+    total = w.B * w.H
+    sample = (f"each step: {n} of {total} (batch, head) sequences over the full L={w.L} "
+              f"({n / total * 100:.2f}% of the workload's tokens); {len(walls)} steps, "
+              f"{sum(walls):.2f} s wall in total")
     line = {
         "impl": "reference",
         "metric": METRIC if args.workload == "large_training" else f"SSD fwd tokens/s ({args.workload})",
@@ -819,9 +862,12 @@ def run_reference(args):
         "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": f"{args.workload} {w.shape_tuple()} [B,L,H,P,N,chunk,G]",
-                   "what": "float64 CPU oracle (token-by-token recurrence), bounded sample per step"},
-        "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": samples[0]["cores"],
-                         "kind": "oracle", "sample": samples[0]["sample"]},
+                   "what": "float64 CPU oracle (token-by-token recurrence), one bounded sample per step",
+                   "tokens_per_step": round(w.tokens * n / total, 1),
+                   "projected_full_workload_ms": round(w.tokens / value * 1e3, 1),
+                   "step_ms_quantiles": step_quantiles([x * 1e3 for x in walls])},
+        "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": cores,
+                         "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

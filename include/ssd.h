@@ -363,6 +363,22 @@ ssd_status ssd_causal_conv1d(int64_t B, int64_t D, int64_t S, int64_t W, int32_t
 ssd_status ssd_gated_rmsnorm(int64_t rows, int64_t D, int64_t groups, float eps, int32_t dtype, const void *x,
                              const void *z, const float *w, void *out, void *stream);
 
+/* Self-test of the bounded device-side waits (no counterpart on the pages;
+ * the pages' kernels report errors only as exceptions on the host).  Every
+ * mbarrier wait in the tensor-core kernels gives up after a time limit
+ * instead of hanging, records the timeout in the workspace error word and
+ * lets the kernel finish; ssd_check_device_error then returns
+ * SSD_ERR_TIMEOUT.  This call exercises that path on purpose: it clears the
+ * first 256 bytes of `workspace` (device, 256-byte aligned, caller-owned,
+ * at least 256 bytes) and launches one CTA whose thread waits, through the
+ * same bounded wait, on an mbarrier that nothing arrives on, for
+ * timeout_us microseconds (1 .. 1e6).  With `arrive` nonzero the thread
+ * arrives first, so the wait succeeds and the word stays clear.  Nothing else
+ * (no copy, no tensor-core operation) is in flight.  Asynchronous on `stream`;
+ * read the outcome with ssd_check_device_error on args whose workspace is
+ * this buffer.  Returns SSD_OK, SSD_ERR_INVALID_ARG or SSD_ERR_CUDA. */
+ssd_status ssd_selftest_wait_timeout(void *workspace, uint32_t timeout_us, int32_t arrive, void *stream);
+
 /* Synchronises `stream`, then reads the device error word the last ssd_fwd
  * on this workspace left behind (bounded waits that gave up set it).
  * Returns SSD_OK or SSD_ERR_TIMEOUT (or SSD_ERR_CUDA). */

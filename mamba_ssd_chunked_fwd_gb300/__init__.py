@@ -110,6 +110,7 @@ _SIGS = {
     "ssd_fwd_host_workspace_size": [_P, ctypes.POINTER(ctypes.c_size_t)],
     "ssd_fwd_host": [_P, ctypes.c_void_p],
     "ssd_check_device_error": [_P, ctypes.c_void_p],
+    "ssd_selftest_wait_timeout": [ctypes.c_void_p, ctypes.c_uint32, ctypes.c_int32, ctypes.c_void_p],
     "ssd_fwd_describe": [_P, ctypes.c_char_p, ctypes.c_size_t],
     "ssd_fwd_noalloc": [_P, ctypes.c_void_p],
     "ssd_decode_step": [ctypes.POINTER(SsdDecodeArgs), ctypes.c_void_p],
@@ -276,6 +277,17 @@ def ssd_fwd_host(args: SsdFwdArgs, stream=None):
 def ssd_check_device_error(args: SsdFwdArgs, stream=None):
     s = stream if stream is not None else _stream_handle()
     _check(load_library().ssd_check_device_error(ctypes.byref(args), s), "ssd_check_device_error")
+
+
+def ssd_selftest_wait_timeout(workspace, timeout_us: int, arrive: bool = False, stream=None):
+    """Run the bounded-wait self-test into ``workspace`` (a CUDA uint8 tensor
+    of at least 256 bytes): one bounded mbarrier wait that nothing releases
+    (or, with ``arrive``, one that completes at once)."""
+    s = stream if stream is not None else _stream_handle()
+    if workspace.numel() * workspace.element_size() < 256:
+        raise ValueError("the self-test needs a workspace of at least 256 bytes")
+    _check(load_library().ssd_selftest_wait_timeout(_ptr(workspace), int(timeout_us), int(bool(arrive)), s),
+           "ssd_selftest_wait_timeout")
 
 
 def _cu_host(cu_seqlens):

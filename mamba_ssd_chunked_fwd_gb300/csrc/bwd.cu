@@ -453,6 +453,8 @@ bwd_chunk_kernel(Params p, const float *__restrict__ dtp, const float *__restric
         sm.u[tid] = f;
     }
     __syncthreads();
+    // the tail below gives each of the 32 lanes two tokens: it needs Q <= 64 and an even Q
+    static_assert(kMax <= 64 && kMax % 2 == 0, "the one-warp tail covers at most 2 x 32 tokens");
     if (warp == 0) {
         // tokens 2 lane and 2 lane + 1 (Q is even): the last token's extra terms, the reverse
         // cumulative sum of dcs (a shuffle scan of the pair sums), then dA, dD, dbias partials;

@@ -58,6 +58,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <mutex>
 #include <vector>
 
 #include "ssd_fused.cuh"
@@ -975,16 +976,29 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
     }
 }
 
-int g_num_sms = 0;
+// SM count of the current device, looked up once per device index (plan
+// choice and the persistent grids depend on it).
+constexpr int kMaxDevices = 64;
+std::mutex g_sms_mu;
+int g_num_sms[kMaxDevices] = {};
 
 int num_sms() {
-    if (g_num_sms == 0) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
-        if (g_num_sms <= 0) g_num_sms = 1;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
+        (void)cudaGetLastError();
+        dev = 0;
     }
-    return g_num_sms;
+    int n = 0;
+    if (dev >= kMaxDevices) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) (void)cudaGetLastError();
+        return n > 0 ? n : 1;
+    }
+    std::lock_guard<std::mutex> lock(g_sms_mu);
+    if (g_num_sms[dev] == 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) (void)cudaGetLastError();
+        g_num_sms[dev] = n > 0 ? n : 1;
+    }
+    return g_num_sms[dev];
 }
 
 int64_t fused_units(const ssd_fwd_args *a) { return a->B * a->G * ((a->H / a->G) / 2); }

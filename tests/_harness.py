@@ -84,3 +84,57 @@ def workload_inputs(name):
     """Inputs of a named workload (cached: the large ones take seconds to draw)."""
     w = ssd_inputs.WORKLOADS[name]
     return w, ssd_inputs.make(w)
+
+
+def stream_compare(oracle, prob, outs, B, H, *, block=64, want_final=True):
+    """Compare GPU outputs with the oracle over EVERY (batch, head) sequence,
+    recomputing the oracle block by block (``block`` sequences at a time, in
+    float64) so that host memory stays bounded.
+
+    ``outs`` maps a label to (y [B,L,H,P], final_state [B,H,P,N] or None),
+    torch tensors on the GPU.  Returns {label: {"y": metrics, "final_state":
+    metrics}} with the global rel-L2 and max|diff|/max|ref| over all elements,
+    accumulated exactly as ``oracle.compare`` would over the whole tensors."""
+    views = {}
+    for k, (y, fin) in outs.items():
+        Bq, L, Hq, P = y.shape
+        yv = y.permute(0, 2, 1, 3).reshape(Bq * Hq, L, P)  # pair-major copy on the GPU
+        fv = fin.reshape(Bq * Hq, fin.shape[2], fin.shape[3]) if (fin is not None and want_final) else None
+        views[k] = (yv, fv)
+    acc = {k: {w: [0.0, 0.0, 0.0, 0.0, True] for w in ("y", "final_state")} for k in outs}
+    total = B * H
+    for i0 in range(0, total, block):
+        i1 = min(total, i0 + block)
+        pairs = [(i // H, i % H) for i in range(i0, i1)]
+        ref = oracle.recurrence(prob, pairs, want_final=want_final)
+        for k, (yv, fv) in views.items():
+            for what, got_t, r in (("y", yv, ref["y"]), ("final_state", fv, ref["final_state"])):
+                if got_t is None or r is None:
+                    continue
+                g = got_t[i0:i1].double().cpu().numpy()
+                d = g - r
+                a = acc[k][what]
+                a[0] += float(np.sum(d * d))
+                a[1] += float(np.sum(r * r))
+                a[2] = max(a[2], float(np.max(np.abs(d))) if d.size else 0.0)
+                a[3] = max(a[3], float(np.max(np.abs(r))) if r.size else 0.0)
+                a[4] = a[4] and bool(np.all(np.isfinite(g)))
+    res = {}
+    for k in outs:
+        res[k] = {}
+        for what, a in acc[k].items():
+            if a[1] == 0.0 and a[3] == 0.0 and a[0] == 0.0:
+                continue
+            nd, nr = math.sqrt(a[0]), math.sqrt(a[1])
+            res[k][what] = {"rel_l2": nd / nr if nr > 0 else nd,
+                            "max_abs_rel": a[2] / a[3] if a[3] > 0 else a[2],
+                            "max_abs": a[2], "finite": a[4]}
+    return res
+
+
+def assert_metrics(m, mode, what=""):
+    tol = TOL[mode]
+    assert m["finite"], f"{what}: non-finite output"
+    assert m["rel_l2"] <= tol["rel_l2"], f"{what}: rel_l2 {m['rel_l2']:.3e} > {tol['rel_l2']}"
+    assert m["max_abs_rel"] <= tol["max_abs_rel"], \
+        f"{what}: max_abs_rel {m['max_abs_rel']:.3e} > {tol['max_abs_rel']}"

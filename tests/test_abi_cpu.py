@@ -231,3 +231,17 @@ def test_neighbour_validation_without_a_gpu():
     assert lib.ssd_gated_rmsnorm(4, 10, 3, 1e-5, 0, fake, fake, fake, fake, None) == 1
     assert lib.ssd_gated_rmsnorm(4, 12, 3, -1.0, 0, fake, fake, fake, fake, None) == 1
     assert lib.ssd_gated_rmsnorm(4, 12, 3, 1e-5, 0, fake, None, fake, fake, None) == 1
+
+
+def test_selftest_validation_without_a_gpu():
+    """The bounded-wait self-test rejects a missing or misaligned workspace and
+    an out-of-range limit before anything is enqueued."""
+    import ctypes
+    lib = ssd.load_library()
+    assert lib.ssd_selftest_wait_timeout(None, 1000, 0, None) == 1
+    buf = ctypes.create_string_buffer(512)
+    base = ctypes.addressof(buf)
+    aligned = (base + 255) // 256 * 256
+    assert lib.ssd_selftest_wait_timeout(ctypes.c_void_p(aligned + 4), 1000, 0, None) == 1
+    assert lib.ssd_selftest_wait_timeout(ctypes.c_void_p(aligned), 0, 0, None) == 1
+    assert lib.ssd_selftest_wait_timeout(ctypes.c_void_p(aligned), 2000000, 0, None) == 1

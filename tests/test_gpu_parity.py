@@ -2,8 +2,9 @@
 oracle on the same seeded inputs.
 
 Small shapes are compared element by element in full (several chunks and a
-ragged tail); the five named workloads run at full size and are compared on
-sampled (batch, head) sequences the oracle recomputes one by one.
+ragged tail); the five named workloads run at full size and are compared
+element by element over every (batch, head) sequence, the oracle recomputing
+them block by block.
 """
 import math
 
@@ -12,8 +13,8 @@ import pytest
 import torch
 
 import ssd_inputs
-from _harness import (TOL, assert_close, gather_pairs, oracle_problem, pick_pairs, run_gpu,
-                      to_device, workload_inputs)
+from _harness import (TOL, assert_close, assert_metrics, gather_pairs, oracle_problem, pick_pairs,
+                      run_gpu, stream_compare, to_device, workload_inputs)
 
 pytestmark = pytest.mark.gpu
 
@@ -34,22 +35,27 @@ def _full_compare(oracle_mod, inp, y, fin, mode, what):
 
 @pytest.mark.parametrize("name", ["tiny", "same_device", "large_training", "long_sequence",
                                   "gated_prefill"])
-@pytest.mark.parametrize("plan", ["auto", "chunked"])
-def test_named_workload(oracle_mod, name, plan):
+def test_named_workload(oracle_mod, name):
+    """Each named workload at full size on both plans (auto, and the chunked
+    plan forced), compared with the oracle over every (batch, head) sequence
+    and every element of y and final_state."""
     w, inp = workload_inputs(name)
-    y, fin = run_gpu(inp, ops=w.ops, plan=plan)
-    assert y.dtype == inp["x"].dtype
+    outs = {}
+    for plan in ("auto", "chunked"):
+        y, fin = run_gpu(inp, ops=w.ops, plan=plan)
+        assert y.dtype == inp["x"].dtype
+        outs[plan] = (y, fin)
     if name == "tiny":
-        _full_compare(oracle_mod, inp, y, fin, _mode(w.ops), name)
+        for plan, (y, fin) in outs.items():
+            _full_compare(oracle_mod, inp, y, fin, _mode(w.ops), f"{name} {plan}")
         return
-    pairs = pick_pairs(w.B, w.H, 6, seed=w.seed)
     prob = oracle_problem(oracle_mod, inp)
-    ref = oracle_mod.recurrence(prob, pairs, want_final=w.return_final_state)
-    ys, fs = gather_pairs(y, fin, pairs)
-    assert_close(oracle_mod, ys, ref["y"], _mode(w.ops), f"{name} y")
-    if w.return_final_state:
-        assert_close(oracle_mod, fs, ref["final_state"], _mode(w.ops), f"{name} final_state")
-    assert torch.isfinite(y.float()).all()
+    res = stream_compare(oracle_mod, prob, outs, w.B, w.H, want_final=w.return_final_state)
+    for plan, r in res.items():
+        assert "y" in r
+        assert_metrics(r["y"], _mode(w.ops), f"{name} {plan} y (all {w.B * w.H} sequences)")
+        if w.return_final_state:
+            assert_metrics(r["final_state"], _mode(w.ops), f"{name} {plan} final_state")
 
 
 # ---- small shapes, every feature, element by element ----------------------------

@@ -501,3 +501,49 @@ def test_gated_rmsnorm_closed_forms(oracle_mod):
     v = x * z / (1.0 + np.exp(-z))
     one = v / np.sqrt(np.mean(v * v, axis=-1, keepdims=True) + 1e-5) * w
     assert np.allclose(oracle_mod.gated_rmsnorm(x, z, w, 1, 1e-5), one, rtol=1e-12)
+
+
+def test_gated_rmsnorm_groups_are_runs_of_consecutive_channels(oracle_mod):
+    """The article's grouped norm (ops-transformer MambaV2 article, section 4.6)
+    normalises each of G runs of D/G consecutive channels on its own.  A row
+    whose k-th run holds one constant c_k (distinct magnitudes) must come out as
+    sign(c_k) * w channel by channel when eps = 0: a strided grouping (channel d
+    in group d mod G) mixes the constants and fails, and so does a transposed
+    reshape."""
+    D, G = 12, 3
+    c = np.array([0.5, -3.0, 7.0])
+    x = np.repeat(c, D // G)[None, :]            # [c0 c0 c0 c0 c1 c1 ... c2]
+    z = np.full((1, D), 40.0)                    # silu(40) = 40 to 4e-18
+    w = np.linspace(0.25, 3.0, D)
+    out = oracle_mod.gated_rmsnorm(x, z, w, G, 0.0)
+    assert np.allclose(out[0], np.repeat(np.sign(c), D // G) * w, rtol=1e-12, atol=0)
+    # the strided reading would give c_k / rms(c) * w, which differs for every run here
+    strided_rms = np.sqrt(np.mean(c ** 2))
+    assert not np.allclose(out[0], np.repeat(c / strided_rms, D // G) * w, rtol=1e-3)
+
+
+def test_gated_rmsnorm_eps_inside_the_root_and_the_gate(oracle_mod):
+    """eps sits inside the root: a run of equal gated values v gives
+    v / sqrt(v^2 + eps) * w (with eps outside it would be v / (|v| + eps) * w,
+    which differs at the values chosen).  With runs of one channel the gate is
+    visible on its own: z = 1 gives silu(1) = 1 / (1 + e^-1) =
+    0.7310585786300049 (the logistic function at 1), z = 0 gives 0, so the
+    output is 0 there whatever x is."""
+    D, G = 8, 2
+    x = np.full((1, D), 0.01)
+    z = np.full((1, D), 40.0)
+    w = np.linspace(0.5, 2.0, D)
+    eps = 0.1
+    v = 0.4                                       # 0.01 * silu(40)
+    out = oracle_mod.gated_rmsnorm(x, z, w, G, eps)
+    assert np.allclose(out[0], v / np.sqrt(v * v + eps) * w, rtol=1e-12)
+    assert not np.allclose(out[0], v / (v + eps) * w, rtol=1e-3)
+    # groups of one channel: out = v / sqrt(v^2 + eps) * w with v = x silu(z)
+    x1 = np.array([[2.0, -1.5, 3.0, 0.7]])
+    z1 = np.array([[1.0, 1.0, 0.0, 1.0]])
+    w1 = np.array([1.0, 2.0, 3.0, 4.0])
+    s1 = 0.7310585786300049
+    v1 = x1[0] * np.array([s1, s1, 0.0, s1])
+    out1 = oracle_mod.gated_rmsnorm(x1, z1, w1, 4, 1e-3)
+    assert np.allclose(out1[0], v1 / np.sqrt(v1 * v1 + 1e-3) * w1, rtol=1e-12, atol=1e-300)
+    assert out1[0, 2] == 0.0

@@ -12,15 +12,15 @@ import pytest
 import torch
 
 import ssd_inputs
-from _harness import TOL, to_device
+from _harness import TOL, oracle_problem, to_device
 
 pytestmark = pytest.mark.gpu
 
 CASES = [
-    # (B, L, H, P, N, G, chunk), ops, public dtype
-    ((1, 200, 2, 64, 128, 1, 128), "f32", "f32"),    # chunked plan, CUDA-core kernels, ragged tail
-    ((2, 384, 8, 64, 128, 2, 128), "bf16", "f32"),   # chunked plan, tensor-core kernels
-    ((2, 256, 8, 64, 64, 2, 64), "bf16", "bf16"),    # fused plan
+    # (B, L, H, P, N, G, chunk), ops, public dtype, plan, a kernel the plan must launch
+    ((1, 200, 2, 64, 128, 1, 128), "f32", "f32", "chunked", "chunk_scan"),    # CUDA-core kernels, ragged tail
+    ((2, 384, 8, 64, 128, 2, 128), "bf16", "f32", "chunked", "chunk_scan_tc"),  # tensor-core kernels
+    ((2, 256, 8, 64, 64, 2, 64), "bf16", "bf16", "fused", "ssd_fused_kernel"),       # fused plan
 ]
 
 
@@ -32,14 +32,15 @@ def _metrics(got, ref):
             float(np.max(np.abs(d)) / max(np.max(np.abs(r)), 1e-300)))
 
 
-def _run(ssd, inp, Q, ops, noalloc):
+def _run(ssd, inp, Q, ops, plan, kernel, noalloc):
     d = to_device(inp)
     B, L, H, P = d["x"].shape
     y = torch.full_like(d["x"], float("nan"))
     fin = torch.full((B, H, P, d["B"].shape[3]), float("nan"), device="cuda")
     args = ssd.make_args(d["x"], d["dt"], d["A"], d["B"], d["C"], Q, y=y, final_state=fin, D=d["D"],
                          z=d["z"], dt_bias=d["dt_bias"], initial_states=d["initial_states"],
-                         dt_softplus=True, ops=ops)
+                         dt_softplus=True, ops=ops, plan=plan)
+    assert kernel in ssd.ssd_fwd_describe(args), ssd.ssd_fwd_describe(args)
     if noalloc:
         ssd.ssd_fwd_noalloc(args)
     else:
@@ -50,20 +51,30 @@ def _run(ssd, inp, Q, ops, noalloc):
     return y, fin
 
 
-@pytest.mark.parametrize("shape,ops,io", CASES)
-def test_noalloc_matches_ssd_fwd_on_consecutive_calls(shape, ops, io):
+@pytest.mark.parametrize("shape,ops,io,plan,kernel", CASES)
+def test_noalloc_matches_ssd_fwd_on_consecutive_calls(oracle_mod, shape, ops, io, plan, kernel):
+    """Two calls in a row with different inputs: each must equal ssd_fwd with a
+    caller-owned workspace bit for bit (both run the same deterministic
+    kernels, so any scratch left over from the previous call would show), and
+    match the float64 oracle within the operand mode's tolerance."""
     import mamba_ssd_chunked_fwd_gb300 as ssd
     B, L, H, P, N, G, Q = shape
     for seed in (101, 202):  # two calls in a row, different inputs, same built-in scratch
         _, inp = ssd_inputs.custom(B, L, H, P, N, G, Q, seed=seed, x_dtype=io, ops=ops, D=True, z=True,
                                    dt_bias=True, h0=True)
-        y_ref, f_ref = _run(ssd, inp, Q, ops, noalloc=False)
-        y, f = _run(ssd, inp, Q, ops, noalloc=True)
-        tol = TOL[ops]
+        y_ref, f_ref = _run(ssd, inp, Q, ops, plan, kernel, noalloc=False)
+        y, f = _run(ssd, inp, Q, ops, plan, kernel, noalloc=True)
         for got, ref, what in ((y, y_ref, "y"), (f, f_ref, "final_state")):
             assert torch.isfinite(got.float()).all(), what
-            rel, mabs = _metrics(got, ref)
-            assert rel <= tol["rel_l2"] and mabs <= tol["max_abs_rel"], (what, seed, rel, mabs)
+            if not torch.equal(got, ref):
+                rel, mabs = _metrics(got, ref)
+                raise AssertionError(f"{what} (seed {seed}) differs from ssd_fwd: rel_l2 {rel:.3e}, "
+                                     f"max_abs_rel {mabs:.3e}")
+        yr, fr = oracle_mod.forward(oracle_problem(oracle_mod, inp))
+        tol = TOL[ops]
+        for got, ref, what in ((y, yr, "y"), (f, fr, "final_state")):
+            m = oracle_mod.compare(got.double().cpu().numpy(), ref)
+            assert m["rel_l2"] <= tol["rel_l2"] and m["max_abs_rel"] <= tol["max_abs_rel"], (what, seed, m)
 
 
 def test_noalloc_rejects_calls_larger_than_its_buffer():
