@@ -649,6 +649,8 @@ def run_neighbor(args):
     torch.cuda.set_device(dev)
     g = torch.Generator().manual_seed(17)
     w = ssd_inputs.WORKLOADS[args.workload]
+    if args.batch:
+        w = w.with_(B=args.batch)
     if args.path == "conv1d":
         B, D, S, W = 1, 10240, 1024, 4
         x = torch.randn((B, D, S), generator=g).to(dev)
