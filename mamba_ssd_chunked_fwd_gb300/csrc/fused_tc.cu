@@ -65,43 +65,23 @@
 #include "ssd_internal.cuh"
 #include "tc_operands.cuh"
 #include "tc_ptx.cuh"
+#include "tc_stage.cuh"
 
 namespace ssd {
 
 namespace {
 
-constexpr int kQ = 64, kN = 64, kP = 64;
+constexpr int kQ = 64, kP = 64;
 constexpr int kComputeWarps = 16;
 constexpr int kComputeThreads = kComputeWarps * 32;
 constexpr int kMmaWarp = kComputeWarps;           // warp 16
 constexpr int kTmaWarp = kComputeWarps + 1;       // warp 17
 constexpr int kDecayWarp0 = kComputeWarps + 2;    // warps 18, 19
 constexpr int kThreads = kComputeThreads + 4 * 32;  // 640
-constexpr int kCols = 16;                         // columns of each TMEM region per thread
 constexpr int kVecSlots = 3;
 constexpr uint64_t kWaitNs = 2000000000ull;       // an mbarrier wait gives up after 2 s
-
-// shared-memory layout, bytes from a 1024-aligned base
-constexpr uint32_t OFF_CB2 = 0;       // C twice (rows 0-63, 64-127), K-major, 16 KB
-constexpr uint32_t OFF_BB = 16384;    // B blocks (j, n), 8 KB: K-major for G, MN-major for dS
-constexpr uint32_t OFF_XT = 24576;    // Xw^T, MN-major, 128 (h,p) x 64 j, 16 KB
-constexpr uint32_t OFF_XC = 40960;    // 2 x [X_h0 | 0 | X_h1], MN-major, 192 rows x 64 j, 24 KB each
-constexpr uint32_t XC_BYTES = 24576;
-constexpr uint32_t OFF_MC = 90112;    // Mcat, K-major B operand, 64 i x 128 (h', j), 16 KB
-constexpr uint32_t OFF_S = 106496;    // S, K-major, 128 (h,p) x 64 n, 16 KB
-// TMA staging, boxes of 64 token rows x 128 bytes (8 KB each): one chunk's y
-// tile on its way out (4 boxes fp32, 2 16-bit; not swizzled, the epilogue
-// writes whole rows), and the next chunk's x, B, C tiles on their way in
-// (x 4 or 2 boxes, B and C 2 or 1; 128-byte swizzled for conflict-free
-// column reads)
-constexpr uint32_t OFF_STG_Y = 122880;
-constexpr uint32_t OFF_STG_X = 155648;
-constexpr uint32_t OFF_STG_B = 188416;
-constexpr uint32_t OFF_STG_C = 204800;
-constexpr uint32_t BOX_BYTES = 8192;
-constexpr uint32_t OFF_VEC = 221184;  // 3 x ChunkVec
+constexpr uint32_t XC_BYTES = 24576;              // [X_h0 | 0 | X_h1], MN-major, 192 rows x 64 j
 constexpr uint32_t VEC_BYTES = 2064;
-constexpr uint32_t SMEM_BYTES = OFF_VEC + 3 * VEC_BYTES + 1024;  // + alignment slack
 // The gated instantiations (ZM 1: y * silu(z); ZM 2: then the gated RMSNorm)
 // load each chunk's z tile by TMA into the y staging tile, where the epilogue
 // reads z at the address it then writes y to; an mbarrier after the decay
@@ -111,18 +91,66 @@ constexpr uint32_t SMEM_BYTES = OFF_VEC + 3 * VEC_BYTES + 1024;  // + alignment 
 // Clusters of up to 2: at 8 heads per group (4 CTAs) the forward plus the
 // standalone norm kernel measured faster (2.19 vs 2.39 ms at the large shape).
 constexpr int kNormMaxRanks = 2;
-constexpr uint32_t OFF_NORM = OFF_VEC + 3 * VEC_BYTES;
 constexpr uint32_t NORM_LPART = 0;     // [4 warpgroups][4 warps][16 tokens] fp32: per-warp sums
 constexpr uint32_t NORM_RECV = 1024;   // [2 slots][kNormMaxRanks][64 tokens] fp32: per-CTA sums
 constexpr uint32_t NORM_BARS = NORM_RECV + 2 * kNormMaxRanks * 64 * 4;  // [2 slots][4 warpgroups] mbarriers
 constexpr uint32_t NORM_ZBAR = NORM_BARS + 2 * 4 * 8;                    // z tile arrived
-constexpr uint32_t SMEM_BYTES_NORM = OFF_NORM + NORM_ZBAR + 16 + 1024;
-static_assert(OFF_NORM % 16 == 0 && SMEM_BYTES_NORM + 512 <= 232448, "norm exchange fits in shared memory");
 
-// TMEM columns (512 allocated)
+// Shared-memory layout, bytes from a 1024-aligned base, for state width NN
+// (64 or 128) and public dtype IO:
+//   CB2    C twice (rows 0-63, 64-127), K-major, 128 x NN
+//   BB     B blocks (j, n), 64 x NN: K-major for G, MN-major for dS
+//   XT     Xw^T, MN-major, 128 (h,p) x 64 j, 16 KB
+//   XC     kXcBufs x [X_h0 | 0 | X_h1], MN-major, 192 rows x 64 j
+//   MC     Mcat, K-major B operand, 64 i x 128 (h', j), 16 KB
+//   S      bf16 copy of the state, K-major, 128 (h,p) x NN (NN = 64 only)
+//   TMA staging, boxes of 64 token rows x 128 bytes (8 KB each): one chunk's y
+//   tile on its way out (not swizzled, the epilogue writes whole rows), and the
+//   next chunk's x, B, C tiles on their way in (128-byte swizzled for
+//   conflict-free column reads)
+//   VEC    3 x ChunkVec, then the norm exchange (gated instantiations)
+// At NN = 128 the state lives in TMEM (an fp32 accumulator and the bf16 copy
+// that is the A operand of S C^T), and with fp32 I/O y is staged in the C
+// staging tile and Xcat has one buffer: the layout then fits in 227 KB.
+// NN = 64 keeps the layout the large training shape was tuned on.
+template <int NN, int IO>
+struct Smem {
+    static constexpr bool kStateTmem = NN == 128;
+    static constexpr bool kAliasY = NN == 128 && IO == IO_F32;
+    static constexpr int kXcBufs = kAliasY ? 1 : 2;
+    static constexpr uint32_t CB2 = 0;
+    static constexpr uint32_t BB = CB2 + 256 * NN;
+    static constexpr uint32_t XT = BB + 128 * NN;
+    static constexpr uint32_t XC = XT + 16384;
+    static constexpr uint32_t MC = XC + kXcBufs * XC_BYTES;
+    static constexpr uint32_t S = MC + 16384;
+    static constexpr uint32_t STG_Y = S + (kStateTmem ? 0 : 256 * NN);
+    static constexpr uint32_t Y_BYTES = NN == 64 ? 32768 : kAliasY ? 0 : (IO == IO_F32 ? 32768 : 16384);
+    static constexpr uint32_t STG_X = STG_Y + Y_BYTES;
+    static constexpr uint32_t X_BYTES = NN == 64 ? 32768 : (IO == IO_F32 ? 32768 : 16384);
+    static constexpr uint32_t STG_B = STG_X + X_BYTES;
+    static constexpr uint32_t BC_BYTES = NN == 64 ? 16384 : 64 * NN * (IO == IO_F32 ? 4 : 2);
+    static constexpr uint32_t STG_C = STG_B + BC_BYTES;
+    static constexpr uint32_t YSTAGE = kAliasY ? STG_C : STG_Y;  // where the epilogue stages y (and z)
+    static constexpr uint32_t VEC = STG_C + BC_BYTES;
+    static constexpr uint32_t NORM = VEC + 3 * VEC_BYTES;
+    static constexpr uint32_t BYTES = NORM + 1024;                    // + alignment slack
+    static constexpr uint32_t BYTES_NORM = NORM + NORM_ZBAR + 16 + 1024;
+    static_assert(STG_X % 1024 == 0 && STG_B % 1024 == 0 && STG_C % 1024 == 0, "swizzled TMA boxes need 1 KB");
+    static_assert(NORM % 16 == 0 && BYTES_NORM + 512 <= 232448, "the layout fits in shared memory");
+};
+static_assert(Smem<64, IO_F32>::VEC == 221184 && Smem<64, IO_BF16>::STG_C == 204800, "N = 64 layout unchanged");
+
+// TMEM columns (512 allocated).  NN = 64: G 0-63, dS 64-127, Yoff / Yint in
+// two buffers from 128.  NN = 128: G 0-63, the fp32 state 64-191 (dS is
+// accumulated onto the decayed state there), Yoff 192 / 256, Yint 320 / 384,
+// the bf16 state (A operand of S C^T, two values per column) 448-511.
 constexpr uint32_t TM_G = 0, TM_DS = 64, TM_COLS = 512;
-__device__ __forceinline__ uint32_t tm_yoff(int buf) { return 128u + 128u * buf; }
-__device__ __forceinline__ uint32_t tm_yint(int buf) { return 192u + 128u * buf; }
+constexpr uint32_t TM_S32 = 64, TM_SBF = 448;
+template <int NN>
+__device__ __forceinline__ uint32_t tm_yoff(int buf) { return NN == 64 ? 128u + 128u * buf : 192u + 64u * buf; }
+template <int NN>
+__device__ __forceinline__ uint32_t tm_yint(int buf) { return NN == 64 ? 192u + 128u * buf : 320u + 64u * buf; }
 
 // mbarriers
 enum {
@@ -151,6 +179,8 @@ using tcop::ex2_approx;
 using tcop::pack2;
 using tcop::st_shared_v4;
 using tcop::store8;
+using tcstage::BOX_BYTES;
+using tcstage::stage_read8;
 
 // Shapes of one call, held in registers by every thread.
 struct Dims {
@@ -159,15 +189,18 @@ struct Dims {
 
 // Tokens of one work unit: tensor batch b, state index sb (b, or the sequence
 // for packed variable-length input), group g, first head h0, token offset t0
-// and length len within the batch row, and its number of chunks.
+// and length len within the batch row, its number of chunks, and its segment
+// (segmented walks, else 0).
 struct Span {
-    int b, sb, g, h0, t0, len, nch;
+    int b, sb, g, h0, t0, len, nch, seg;
 };
 
 // `unit` is the walk position: every CTA walks positions blockIdx.x,
 // blockIdx.x + gridDim.x, ...; for packed sequences the host's schedule maps a
-// position to the unit it runs there.
-template <bool VARLEN>
+// position to the unit it runs there.  Segmented walks (SEG) order the units
+// (batch, segment, group, head pair) with the head pair fastest, so that the
+// CTAs running side by side share their B and C tiles in L2.
+template <bool VARLEN, bool SEG = false>
 __device__ __forceinline__ Span unit_span(const Params &p, const Dims &dm, int unit) {
     if (VARLEN) unit = p.sched_units[unit];
     const int pairs = dm.hpg >> 1;
@@ -177,10 +210,17 @@ __device__ __forceinline__ Span unit_span(const Params &p, const Dims &dm, int u
     u.h0 = u.g * dm.hpg + 2 * pair;
     const int q = bg / dm.G;
     u.sb = q;
+    u.seg = 0;
     if (VARLEN) {
         u.b = 0;
         u.t0 = (int)p.cu[q];
         u.len = (int)(p.cu[q + 1] - p.cu[q]);
+        u.nch = (u.len + kQ - 1) / kQ;
+    } else if (SEG) {
+        u.seg = q % p.nseg;
+        u.b = u.sb = q / p.nseg;
+        u.t0 = u.seg * p.seg_len;
+        u.len = min(p.seg_len, dm.L - u.t0);
         u.nch = (u.len + kQ - 1) / kQ;
     } else {
         u.b = q;
@@ -202,39 +242,6 @@ __device__ __forceinline__ void load_dt(const Params &p, const Dims &dm, const S
     const float *row = p.dt + ((size_t)u.b * dm.L + u.t0) * dm.H + h;
     r.dt0 = t0 < u.len ? __ldg(row + (size_t)t0 * dm.H) : 0.f;
     r.dt1 = t1 < u.len ? __ldg(row + (size_t)t1 * dm.H) : 0.f;
-}
-
-// 16-byte chunk c of row r in a 128-byte-swizzled TMA box (chunk index XOR row % 8)
-__device__ __forceinline__ uint32_t swz(uint32_t box, int r, int c) {
-    return box + r * 128 + ((c ^ (r & 7)) << 4);
-}
-
-__device__ __forceinline__ void unpack8(uint4 u, bool bf16, float (&v)[8]) {
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        float2 f;
-        if (bf16) f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[i]));
-        else f = __half22float2(*reinterpret_cast<const __half2 *>(&w[i]));
-        v[2 * i] = f.x; v[2 * i + 1] = f.y;
-    }
-}
-
-// 8 consecutive features [8c8, 8c8+8) of token row r from a staged tile whose
-// rows hold `row_feats` features split over boxes of 128 bytes.
-template <int IO>
-__device__ __forceinline__ void stage_read8(uint32_t base, int r, int c8, float (&v)[8]) {
-    if (IO == IO_F32) {  // 32 features per box, 8 floats = 2 chunks
-        const uint32_t box = base + (c8 >> 2) * BOX_BYTES;
-        const int c = 2 * (c8 & 3);
-        const uint4 a = tc::ld_shared_v4(swz(box, r, c)), b = tc::ld_shared_v4(swz(box, r, c + 1));
-        v[0] = __uint_as_float(a.x); v[1] = __uint_as_float(a.y); v[2] = __uint_as_float(a.z);
-        v[3] = __uint_as_float(a.w); v[4] = __uint_as_float(b.x); v[5] = __uint_as_float(b.y);
-        v[6] = __uint_as_float(b.z); v[7] = __uint_as_float(b.w);
-    } else {  // 64 features per box, 8 values = 1 chunk
-        const uint32_t box = base + (c8 >> 3) * BOX_BYTES;
-        unpack8(tc::ld_shared_v4(swz(box, r, c8 & 7)), IO == IO_BF16, v);
-    }
 }
 
 // Decay vectors of one chunk for head hh (one warp): processed step, the
@@ -288,17 +295,17 @@ __device__ __forceinline__ float ld_stage(uint32_t a) {
 // (VARLEN) tokens count from t0 in batch row 0, the sequence ends at len, and
 // in its last chunk (`direct`) y goes straight to global memory for the
 // tokens inside the sequence, since the rows past its end belong to the next.
-template <int IO, bool VARLEN, int ZM = 0>
+template <int IO, bool VARLEN, int ZM = 0, int NN = 64, bool SEG = false>
 __device__ __forceinline__ void epilogue8(const Params &p, const Dims &dm, const ChunkVec &V, uint32_t tlane,
                                           int bp, int col, int b, int h0, int my_h, int my_p, int tok_base,
                                           uint32_t ystage, int t0, int len, bool direct) {
-    if (!VARLEN) {
+    if (!VARLEN && !SEG) {
         t0 = 0;
         len = dm.L;
     }
     float yo[8], yi[8];
-    tc::tmem_ld8(tlane + tm_yoff(bp) + col, yo);
-    tc::tmem_ld8(tlane + tm_yint(bp) + col, yi);
+    tc::tmem_ld8(tlane + tm_yoff<NN>(bp) + col, yo);
+    tc::tmem_ld8(tlane + tm_yint<NN>(bp) + col, yi);
     tc::fence_before_sync();
     const int i0 = tok_base % kQ;
     const float4 e0 = *reinterpret_cast<const float4 *>(&V.ecs[my_h][i0]);
@@ -384,8 +391,8 @@ __device__ __forceinline__ void epilogue_norm(const Params &p, const Dims &dm, c
 #pragma unroll
     for (int hf = 0; hf < 2; ++hf) {
         float yo[8], yi[8];
-        tc::tmem_ld8(tlane + tm_yoff(bp) + col0 + 8 * hf, yo);
-        tc::tmem_ld8(tlane + tm_yint(bp) + col0 + 8 * hf, yi);
+        tc::tmem_ld8(tlane + tm_yoff<64>(bp) + col0 + 8 * hf, yo);
+        tc::tmem_ld8(tlane + tm_yint<64>(bp) + col0 + 8 * hf, yi);
         const float4 e0 = *reinterpret_cast<const float4 *>(&V.ecs[my_h][col0 + 8 * hf]);
         const float4 e1 = *reinterpret_cast<const float4 *>(&V.ecs[my_h][col0 + 8 * hf + 4]);
         const float ev[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
@@ -479,17 +486,29 @@ __device__ __forceinline__ void epilogue_norm(const Params &p, const Dims &dm, c
     tc::fence_smem_to_async();
 }
 
-template <int IO, bool BF16, bool VARLEN, int ZM>
+// NN = 128 (N = 128) walks segments of the sequence (SEG: unit = (batch,
+// segment, group, head pair), the state entering a segment from the segment
+// passes, the final state from the last segment) with the state in TMEM; it
+// takes neither packed sequences nor the fused norm.
+template <int IO, bool BF16, bool VARLEN, int ZM, int NN = 64>
 __global__ void __launch_bounds__(kThreads, 1)
 ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMaps tm, int n_units,
                  unsigned int *err, int norm_cs) {
+    using L = Smem<NN, IO>;
+    constexpr bool SEG = NN == 128;
+    constexpr bool kAliasY = L::kAliasY;
+    static_assert(NN == 64 || NN == 128, "state width 64 or 128");
+    static_assert(NN == 64 || (!VARLEN && ZM < 2), "N = 128: no packed sequences, no fused norm");
+    static_assert(!kAliasY || ZM == 0, "with y staged in the C tile there is no room for a z tile");
+    constexpr int kGCols = 16;      // this thread's columns of each 64-column region (G, Yoff, Yint)
+    constexpr int kSCols = NN / 4;  // this thread's state columns
     extern __shared__ unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t bars[NBARS];
     __shared__ uint32_t tmem_slot;
     const uint32_t raw = tc::smem_addr(smem_raw);
     unsigned char *sm = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
     const uint32_t sbase = tc::smem_addr(sm);
-    ChunkVec *Vbuf = reinterpret_cast<ChunkVec *>(sm + OFF_VEC);
+    ChunkVec *Vbuf = reinterpret_cast<ChunkVec *>(sm + L::VEC);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const Dims dm{p.L, p.H, p.G, p.hpg, p.nchunks};
@@ -511,10 +530,10 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
             tc::mbar_init(bar(BAR_VEC_FULL0 + i), 2);
             tc::mbar_init(bar(BAR_VEC_EMPTY0 + i), kComputeWarps);
         }
-        if constexpr (ZM > 0) tc::mbar_init(sbase + OFF_NORM + NORM_ZBAR, 1);
+        if constexpr (ZM > 0) tc::mbar_init(sbase + L::NORM + NORM_ZBAR, 1);
         if constexpr (ZM == 2) {
             if (norm_cs > 1)
-                for (int i = 0; i < 8; ++i) tc::mbar_init(sbase + OFF_NORM + NORM_BARS + 8 * i, (norm_cs - 1) * 16);
+                for (int i = 0; i < 8; ++i) tc::mbar_init(sbase + L::NORM + NORM_BARS + 8 * i, (norm_cs - 1) * 16);
         }
         tc::mbar_init_fence();
     }
@@ -522,11 +541,13 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
         tc::tmem_alloc(tc::smem_addr(&tmem_slot), TM_COLS);
         tc::tmem_relinquish();
     }
-    // the zero block between the two heads' x tiles (MN groups 8..15), both buffers
-    for (int e = tid; e < 2 * 8 * 8 * 8; e += kThreads) {
+    // the zero block between the two heads' x tiles (MN groups 8..15), every buffer
+    for (int e = tid; e < L::kXcBufs * 8 * 8 * 8; e += kThreads) {
         const int buf = e >> 9, jg = (e >> 6) & 7, mg = 8 + ((e >> 3) & 7), rr = e & 7;
-        st_shared_v4(sbase + OFF_XC + buf * XC_BYTES + (jg * 24 + mg) * 128 + rr * 16, 0u, 0u, 0u, 0u);
+        st_shared_v4(sbase + L::XC + buf * XC_BYTES + (jg * 24 + mg) * 128 + rr * 16, 0u, 0u, 0u, 0u);
     }
+    // Mcat starts zero: the blocks above the diagonal that no warp writes stay so
+    for (int e = tid; e < 16384 / 16; e += kThreads) st_shared_v4(sbase + L::MC + 16 * e, 0u, 0u, 0u, 0u);
     tc::fence_smem_to_async();
     tc::fence_before_sync();
     __syncthreads();
@@ -547,40 +568,52 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
         // ---------------- MMA issue (one thread) ----------------
         if (lane == 0) {
             constexpr uint32_t ID_KK = tc::idesc_f16(128, 64, BF16, false, false);
-            constexpr uint32_t ID_MNMN = tc::idesc_f16(128, 64, BF16, true, true);
+            constexpr uint32_t ID_MNMN = tc::idesc_f16(128, NN, BF16, true, true);
             constexpr uint32_t ID_MNK = tc::idesc_f16(128, 64, BF16, true, false);
             uint32_t gk = 0;
             for (int unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
-                const int nch = unit_span<VARLEN>(p, dm, unit).nch;
+                const int nch = unit_span<VARLEN, SEG>(p, dm, unit).nch;
                 for (int k = 0; k < nch; ++k, ++gk) {
                     const uint32_t ph = gk & 1u;
                     const int buf = gk & 1;
+                    const int xbuf = L::kXcBufs == 2 ? buf : 0;
                     wait(BAR_OPS_FULL, ph);
                     tc::fence_after_sync();
 #pragma unroll
-                    for (int ks = 0; ks < kN / 16; ++ks)  // G = C B^T, K = n
-                        tc::mma_f16(tmem + TM_G, tc::desc(sbase + OFF_CB2 + ks * 4096, 2048, 128),
-                                    tc::desc(sbase + OFF_BB + ks * 2048, 1024, 128), ID_KK, ks > 0);
+                    for (int ks = 0; ks < NN / 16; ++ks)  // G = C B^T, K = n
+                        tc::mma_f16(tmem + TM_G, tc::desc(sbase + L::CB2 + ks * 4096, 2048, 128),
+                                    tc::desc(sbase + L::BB + ks * 2048, 1024, 128), ID_KK, ks > 0);
                     tc::commit(bar(BAR_G_DONE));
                     wait(BAR_S_FULL, ph);
                     tc::fence_after_sync();
+                    if constexpr (NN == 64) {
 #pragma unroll
-                    for (int ks = 0; ks < kQ / 16; ++ks)  // dS = Xw^T B, K = j
-                        tc::mma_f16(tmem + TM_DS, tc::desc(sbase + OFF_XT + ks * 4096, 2048, 128),
-                                    tc::desc(sbase + OFF_BB + ks * 256, 128, 1024), ID_MNMN, ks > 0);
+                        for (int ks = 0; ks < kQ / 16; ++ks)  // dS = Xw^T B, K = j
+                            tc::mma_f16(tmem + TM_DS, tc::desc(sbase + L::XT + ks * 4096, 2048, 128),
+                                        tc::desc(sbase + L::BB + ks * 256, 128, 1024), ID_MNMN, ks > 0);
 #pragma unroll
-                    for (int ks = 0; ks < kN / 16; ++ks)  // Yoff = S C^T, K = n
-                        tc::mma_f16(tmem + tm_yoff(buf), tc::desc(sbase + OFF_S + ks * 4096, 2048, 128),
-                                    tc::desc(sbase + OFF_CB2 + ks * 4096, 2048, 128), ID_KK, ks > 0);
+                        for (int ks = 0; ks < NN / 16; ++ks)  // Yoff = S C^T, K = n
+                            tc::mma_f16(tmem + tm_yoff<NN>(buf), tc::desc(sbase + L::S + ks * 4096, 2048, 128),
+                                        tc::desc(sbase + L::CB2 + ks * 4096, 2048, 128), ID_KK, ks > 0);
+                    } else {
+#pragma unroll
+                        for (int ks = 0; ks < kQ / 16; ++ks)  // S += Xw^T B onto the decayed state, K = j
+                            tc::mma_f16(tmem + TM_S32, tc::desc(sbase + L::XT + ks * 4096, 2048, 128),
+                                        tc::desc(sbase + L::BB + ks * 256, 128, 1024), ID_MNMN, 1u);
+#pragma unroll
+                        for (int ks = 0; ks < NN / 16; ++ks)  // Yoff = S C^T, S from TMEM, K = n
+                            tc::mma_f16_ts(tmem + tm_yoff<NN>(buf), tmem + TM_SBF + ks * 8,
+                                           tc::desc(sbase + L::CB2 + ks * 4096, 2048, 128), ID_KK, ks > 0);
+                    }
                     tc::commit(bar(BAR_DS_DONE));
                     wait(BAR_MCAT_FULL, ph);
                     tc::fence_after_sync();
-                    const uint32_t xc = sbase + OFF_XC + buf * XC_BYTES, mc = sbase + OFF_MC;
+                    const uint32_t xc = sbase + L::XC + xbuf * XC_BYTES, mc = sbase + L::MC;
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
                         for (int ks = 0; ks < kQ / 16; ++ks)
-                            tc::mma_f16(tmem + tm_yint(buf), tc::desc(xc + hh * 1024 + ks * 6144, 3072, 128),
+                            tc::mma_f16(tmem + tm_yint<NN>(buf), tc::desc(xc + hh * 1024 + ks * 6144, 3072, 128),
                                         tc::desc(mc + hh * 8192 + ks * 2048, 1024, 128), ID_MNK,
                                         (hh | ks) != 0);
                     tc::commit(bar(buf ? BAR_Y_DONE1 : BAR_Y_DONE0));
@@ -598,10 +631,10 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
             if constexpr (ZM > 0) tc::prefetch_tensormap(&tm.z);
             constexpr int bw = IO == IO_F32 ? 32 : 64;  // features per 128-byte box
             constexpr uint32_t kStageBytes = (IO == IO_F32 ? 8u : 4u) * BOX_BYTES;
-            // The same loop twice: packed sequences walk per-unit spans, the regular
-            // layout keeps plain index arithmetic (measured 0.8 % faster than the
-            // span version at the large training shape).
-            if (VARLEN) {
+            // The same loop three times: packed sequences and segmented walks take
+            // per-unit spans, the regular layout keeps plain index arithmetic
+            // (measured 0.8 % faster than the span version at the large training shape).
+            if constexpr (VARLEN) {
                 // the public x, B, C tiles of chunk k of a unit into the staging area
                 // (rows past the sequence's end are read but enter with d = 0)
                 auto stage = [&](const Span &u, int k) {
@@ -609,13 +642,13 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                     tc::mbar_arrive_expect_tx(bar(BAR_STAGE_FULL), kStageBytes);
 #pragma unroll
                     for (int bx = 0; bx < 128 / bw; ++bx)
-                        tc::tma_load_3d(sbase + OFF_STG_X + bx * BOX_BYTES, &tm.x, u.h0 * kP + bx * bw, tok, u.b,
+                        tc::tma_load_3d(sbase + L::STG_X + bx * BOX_BYTES, &tm.x, u.h0 * kP + bx * bw, tok, u.b,
                                         bar(BAR_STAGE_FULL));
 #pragma unroll
-                    for (int bx = 0; bx < 64 / bw; ++bx) {
-                        tc::tma_load_3d(sbase + OFF_STG_B + bx * BOX_BYTES, &tm.b, u.g * kN + bx * bw, tok, u.b,
+                    for (int bx = 0; bx < NN / bw; ++bx) {
+                        tc::tma_load_3d(sbase + L::STG_B + bx * BOX_BYTES, &tm.b, u.g * NN + bx * bw, tok, u.b,
                                         bar(BAR_STAGE_FULL));
-                        tc::tma_load_3d(sbase + OFF_STG_C + bx * BOX_BYTES, &tm.c, u.g * kN + bx * bw, tok, u.b,
+                        tc::tma_load_3d(sbase + L::STG_C + bx * BOX_BYTES, &tm.c, u.g * NN + bx * bw, tok, u.b,
                                         bar(BAR_STAGE_FULL));
                     }
                 };
@@ -632,7 +665,7 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                     if (!(VARLEN && (k + 1) * kQ > u.len)) {
 #pragma unroll
                         for (int bx = 0; bx < 128 / bw; ++bx)
-                            tc::tma_store_3d(&tm.y, sbase + OFF_STG_Y + bx * BOX_BYTES, u.h0 * kP + bx * bw,
+                            tc::tma_store_3d(&tm.y, sbase + L::STG_Y + bx * BOX_BYTES, u.h0 * kP + bx * bw,
                                              u.t0 + k * kQ, u.b);
                         tc::bulk_commit();
                         tc::bulk_wait_read();
@@ -660,6 +693,97 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                     if (u.nch > 0) store_y(u, u.nch - 1);
                 }
                 tc::bulk_wait_all();
+            } else if constexpr (SEG) {
+                // x and B of chunk k of a unit into the staging area, expecting C too
+                // (its copy is issued by load_c: with y staged in the C tile it has to
+                // wait until the previous y tile has left)
+                constexpr uint32_t kXBytes = (128 / bw) * BOX_BYTES, kBCBytes = (NN / bw) * BOX_BYTES;
+                auto load_xb = [&](const Span &u, int k) {
+                    const int tok = u.t0 + k * kQ;
+                    tc::mbar_arrive_expect_tx(bar(BAR_STAGE_FULL), kXBytes + 2 * kBCBytes);
+#pragma unroll
+                    for (int bx = 0; bx < 128 / bw; ++bx)
+                        tc::tma_load_3d(sbase + L::STG_X + bx * BOX_BYTES, &tm.x, u.h0 * kP + bx * bw, tok, u.b,
+                                        bar(BAR_STAGE_FULL));
+#pragma unroll
+                    for (int bx = 0; bx < NN / bw; ++bx) {
+                        tc::tma_load_3d(sbase + L::STG_B + bx * BOX_BYTES, &tm.b, u.g * NN + bx * bw, tok, u.b,
+                                        bar(BAR_STAGE_FULL));
+                        if constexpr (kAliasY) tc::tma_prefetch_3d(&tm.c, u.g * NN + bx * bw, tok, u.b);
+                    }
+                };
+                auto load_c = [&](const Span &u, int k) {
+                    const int tok = u.t0 + k * kQ;
+#pragma unroll
+                    for (int bx = 0; bx < NN / bw; ++bx)
+                        tc::tma_load_3d(sbase + L::STG_C + bx * BOX_BYTES, &tm.c, u.g * NN + bx * bw, tok, u.b,
+                                        bar(BAR_STAGE_FULL));
+                    if constexpr (ZM > 0) {  // this chunk's z into L2, ahead of its load into the y tile
+#pragma unroll
+                        for (int bx = 0; bx < 128 / bw; ++bx) tc::tma_prefetch_3d(&tm.z, u.h0 * kP + bx * bw, tok, u.b);
+                    }
+                };
+                // gated instantiation: the z tile of chunk k into the (free) y staging tile
+                auto load_z = [&](const Span &u, int k) {
+                    if constexpr (ZM > 0) {
+                        const uint32_t zbar = sbase + L::NORM + NORM_ZBAR;
+                        tc::mbar_arrive_expect_tx(zbar, (128 / bw) * BOX_BYTES);
+#pragma unroll
+                        for (int bx = 0; bx < 128 / bw; ++bx)
+                            tc::tma_load_3d(sbase + L::YSTAGE + bx * BOX_BYTES, &tm.z, u.h0 * kP + bx * bw,
+                                            u.t0 + k * kQ, u.b, zbar);
+                    }
+                };
+                uint32_t yt = 0;  // y tiles stored so far
+                auto store_y = [&](const Span &u, int k) {
+                    wait(BAR_Y_STAGED, yt & 1u);
+#pragma unroll
+                    for (int bx = 0; bx < 128 / bw; ++bx)
+                        tc::tma_store_3d(&tm.y, sbase + L::YSTAGE + bx * BOX_BYTES, u.h0 * kP + bx * bw,
+                                         u.t0 + k * kQ, u.b);
+                    tc::bulk_commit();
+                    tc::bulk_wait_read();
+                    tc::mbar_arrive(bar(BAR_Y_FREE));
+                    ++yt;
+                };
+                if ((int)blockIdx.x < n_units) {
+                    const Span u0 = unit_span<false, true>(p, dm, blockIdx.x);
+                    load_xb(u0, 0);
+                    load_c(u0, 0);
+                    load_z(u0, 0);
+                }
+                uint32_t gk = 0;
+                for (int unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
+                    const Span u = unit_span<false, true>(p, dm, unit);
+                    const bool more = unit + (int)gridDim.x < n_units;
+                    const Span nu = unit_span<false, true>(p, dm, more ? unit + gridDim.x : unit);
+                    for (int k = 0; k < u.nch; ++k, ++gk) {
+                        wait(BAR_OPS_FULL, gk & 1u);  // the compute warps are done with the staging area
+                        const bool next_here = k + 1 < u.nch;
+                        if (next_here) load_xb(u, k + 1);
+                        else if (more) load_xb(nu, 0);
+                        // the C tile is free once the compute warps converted it; when y is
+                        // staged there, only once y of the previous chunk has left too, and
+                        // the next unit's first C then waits for this unit's last y
+                        if constexpr (!kAliasY) {
+                            if (next_here) load_c(u, k + 1);
+                            else if (more) load_c(nu, 0);
+                        }
+                        if (k > 0) {
+                            store_y(u, k - 1);
+                            if constexpr (ZM > 0) load_z(u, k);  // the next tile the compute warps stage
+                        }
+                        if constexpr (kAliasY) {
+                            if (next_here) load_c(u, k + 1);
+                        }
+                    }
+                    store_y(u, u.nch - 1);
+                    if (more) {
+                        if constexpr (kAliasY) load_c(nu, 0);
+                        load_z(nu, 0);
+                    }
+                }
+                tc::bulk_wait_all();
             } else {
                 // the public x, B, C tiles of chunk k of a unit into the staging area
                 auto stage = [&](int unit, int k) {
@@ -669,13 +793,13 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                     tc::mbar_arrive_expect_tx(bar(BAR_STAGE_FULL), kStageBytes);
 #pragma unroll
                     for (int bx = 0; bx < 128 / bw; ++bx)
-                        tc::tma_load_3d(sbase + OFF_STG_X + bx * BOX_BYTES, &tm.x, h0 * kP + bx * bw, k * kQ, b,
+                        tc::tma_load_3d(sbase + L::STG_X + bx * BOX_BYTES, &tm.x, h0 * kP + bx * bw, k * kQ, b,
                                         bar(BAR_STAGE_FULL));
 #pragma unroll
-                    for (int bx = 0; bx < 64 / bw; ++bx) {
-                        tc::tma_load_3d(sbase + OFF_STG_B + bx * BOX_BYTES, &tm.b, g * kN + bx * bw, k * kQ, b,
+                    for (int bx = 0; bx < NN / bw; ++bx) {
+                        tc::tma_load_3d(sbase + L::STG_B + bx * BOX_BYTES, &tm.b, g * NN + bx * bw, k * kQ, b,
                                         bar(BAR_STAGE_FULL));
-                        tc::tma_load_3d(sbase + OFF_STG_C + bx * BOX_BYTES, &tm.c, g * kN + bx * bw, k * kQ, b,
+                        tc::tma_load_3d(sbase + L::STG_C + bx * BOX_BYTES, &tm.c, g * NN + bx * bw, k * kQ, b,
                                         bar(BAR_STAGE_FULL));
                     }
                     if constexpr (ZM > 0) {  // this chunk's z into L2, ahead of its load into the y tile
@@ -690,11 +814,11 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                         const int pair = unit % pairs, bg = unit / pairs;
                         const int g = bg % dm.G, b = bg / dm.G;
                         const int h0 = g * dm.hpg + 2 * pair;
-                        const uint32_t zbar = sbase + OFF_NORM + NORM_ZBAR;
+                        const uint32_t zbar = sbase + L::NORM + NORM_ZBAR;
                         tc::mbar_arrive_expect_tx(zbar, (IO == IO_F32 ? 4u : 2u) * BOX_BYTES);
 #pragma unroll
                         for (int bx = 0; bx < 128 / bw; ++bx)
-                            tc::tma_load_3d(sbase + OFF_STG_Y + bx * BOX_BYTES, &tm.z, h0 * kP + bx * bw, k * kQ, b,
+                            tc::tma_load_3d(sbase + L::STG_Y + bx * BOX_BYTES, &tm.z, h0 * kP + bx * bw, k * kQ, b,
                                             zbar);
                     }
                 };
@@ -703,7 +827,7 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                     wait(BAR_Y_STAGED, yt & 1u);
 #pragma unroll
                     for (int bx = 0; bx < 128 / bw; ++bx)
-                        tc::tma_store_3d(&tm.y, sbase + OFF_STG_Y + bx * BOX_BYTES, h0 * kP + bx * bw, k * kQ, b);
+                        tc::tma_store_3d(&tm.y, sbase + L::STG_Y + bx * BOX_BYTES, h0 * kP + bx * bw, k * kQ, b);
                     tc::bulk_commit();
                     tc::bulk_wait_read();
                     tc::mbar_arrive(bar(BAR_Y_FREE));
@@ -739,7 +863,7 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
         const int hh = warp - kDecayWarp0;
         uint32_t gd = 0;
         for (int unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
-            const Span u = unit_span<VARLEN>(p, dm, unit);
+            const Span u = unit_span<VARLEN, SEG>(p, dm, unit);
             const int h = u.h0 + hh;
             for (int k = 0; k < u.nch; ++k, ++gd) {
                 DtRegs r;
@@ -756,16 +880,17 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
         const int wg = warp >> 2, quarter = warp & 3;
         const int row = quarter * 32 + lane;  // TMEM lane owned by this thread
         const int my_h = row >> 6, my_p = row & 63;
-        const int col0 = wg * kCols;          // this thread's columns of each 64-column region
+        const int col0 = wg * kGCols;         // this thread's columns of each 64-column region
+        const int scol0 = wg * kSCols;        // this thread's state columns
         const uint32_t tlane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
         uint32_t gk = 0;
         uint32_t yt = 0;  // y tiles staged so far
         NormCtx nc{};
         float norm_wf = 0.f;  // per unit: this feature's norm weight
         if constexpr (ZM == 2) {
-            nc.lpart = sbase + OFF_NORM + NORM_LPART;
-            nc.recv = sbase + OFF_NORM + NORM_RECV;
-            nc.rbar = sbase + OFF_NORM + NORM_BARS;
+            nc.lpart = sbase + L::NORM + NORM_LPART;
+            nc.recv = sbase + L::NORM + NORM_RECV;
+            nc.rbar = sbase + L::NORM + NORM_BARS;
             nc.cs = norm_cs;
             nc.rank = norm_cs > 1 ? (int)tc::cluster_ctarank() : 0;
         }
@@ -777,17 +902,18 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
             if (yt > 0) wait(BAR_Y_FREE, (yt - 1) & 1u);  // the TMA unit has read the previous tile
             wait(bp ? BAR_Y_DONE1 : BAR_Y_DONE0, (gp >> 1) & 1u);
             if constexpr (ZM > 0) {  // this tile's z is in the staging tile
-                if (!timed_out && !tc::mbar_wait(sbase + OFF_NORM + NORM_ZBAR, yt & 1u, kWaitNs)) timed_out = true;
+                if (!timed_out && !tc::mbar_wait(sbase + L::NORM + NORM_ZBAR, yt & 1u, kWaitNs)) timed_out = true;
             }
             tc::fence_after_sync();
             if constexpr (ZM == 2) {
                 epilogue_norm<IO>(p, dm, Vbuf[gp % kVecSlots], tlane, bp, col0, b, h0, my_h, my_p, kk * kQ + col0,
-                                  sbase + OFF_STG_Y, nc, gp, wg, quarter, lane, norm_wf, timed_out);
+                                  sbase + L::STG_Y, nc, gp, wg, quarter, lane, norm_wf, timed_out);
             } else {
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf)
-                    epilogue8<IO, VARLEN, ZM>(p, dm, Vbuf[gp % kVecSlots], tlane, bp, col0 + 8 * hf, b, h0, my_h,
-                                              my_p, kk * kQ + col0 + 8 * hf, sbase + OFF_STG_Y, t0, len, direct);
+                    epilogue8<IO, VARLEN, ZM, NN, SEG>(p, dm, Vbuf[gp % kVecSlots], tlane, bp, col0 + 8 * hf, b, h0,
+                                                       my_h, my_p, kk * kQ + col0 + 8 * hf, sbase + L::YSTAGE, t0,
+                                                       len, direct);
             }
             __syncwarp();
             if (lane == 0) {
@@ -796,14 +922,37 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
             }
             ++yt;
         };
+        // NN = 128: the state S (this thread's kSCols columns of row (head, p))
+        // goes to TMEM twice before the products of a chunk: decayed by the
+        // chunk's exp(cs_last) as the fp32 accumulator that S += Xw^T B adds to,
+        // and as the bf16 A operand of Yoff = S C^T
+        auto publish_state = [&](const float (&Sv)[kSCols], float a) {
+            if constexpr (NN == 128) {
+                uint32_t r[16];
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(a * Sv[16 * hf + i]);
+                    tc::tmem_st16(tlane + TM_S32 + scol0 + 16 * hf, r);
+                }
+#pragma unroll
+                for (int i = 0; i < 16; ++i) r[i] = pack2(Sv[2 * i], Sv[2 * i + 1], BF16);
+                tc::tmem_st16(tlane + TM_SBF + scol0 / 2, r);
+                tc::tmem_wait_st();
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(bar(BAR_S_FULL));
+            }
+        };
 
         for (int unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
             // b: batch row, h0: first head, sb: state index (b, or the packed
-            // sequence), t0 / len: the sequence's tokens in its row, nch: its chunks
-            int b, h0, sb, t0 = 0, len = 0, nch = dm.nchunks;
-            if (VARLEN) {
-                const Span u = unit_span<true>(p, dm, unit);
-                b = u.b; h0 = u.h0; sb = u.sb; t0 = u.t0; len = u.len; nch = u.nch;
+            // sequence), t0 / len: the unit's tokens in its row, nch: its chunks,
+            // seg: its segment (segmented walks)
+            int b, h0, sb, t0 = 0, len = 0, nch = dm.nchunks, seg = 0;
+            if (VARLEN || SEG) {
+                const Span u = unit_span<VARLEN, SEG>(p, dm, unit);
+                b = u.b; h0 = u.h0; sb = u.sb; t0 = u.t0; len = u.len; nch = u.nch; seg = u.seg;
             } else {
                 const int pairs = dm.hpg >> 1;
                 const int pair = unit % pairs;
@@ -817,41 +966,56 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                 norm_wf = __ldg(p.norm_w + (size_t)(h0 + my_h) * kP + my_p);
             }
 
-            // state of (head my_h, row my_p), columns n = col0 .. col0+kCols-1
-            float S[kCols];
-            if (p.h0) {
-                const float4 *src = reinterpret_cast<const float4 *>(
-                    p.h0 + (((size_t)sb * dm.H + h0 + my_h) * kP + my_p) * kN + col0);
+            // state of (head my_h, row my_p), columns n = scol0 .. scol0+kSCols-1: the
+            // initial state, or for a later segment the state the segment passes left
+            float S[kSCols];
+            {
+                const float *src = nullptr;
+                if (SEG && seg > 0)
+                    src = p.seg_states + ((((size_t)b * p.nseg + seg) * dm.H + h0 + my_h) * kP + my_p) * NN + scol0;
+                else if (p.h0)
+                    src = p.h0 + (((size_t)sb * dm.H + h0 + my_h) * kP + my_p) * NN + scol0;
+                if (src) {
+                    const float4 *s4 = reinterpret_cast<const float4 *>(src);
 #pragma unroll
-                for (int q = 0; q < kCols / 4; ++q) {
-                    const float4 v = __ldg(src + q);
-                    S[4 * q] = v.x; S[4 * q + 1] = v.y; S[4 * q + 2] = v.z; S[4 * q + 3] = v.w;
+                    for (int q = 0; q < kSCols / 4; ++q) {
+                        const float4 v = __ldg(s4 + q);
+                        S[4 * q] = v.x; S[4 * q + 1] = v.y; S[4 * q + 2] = v.z; S[4 * q + 3] = v.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int n = 0; n < kSCols; ++n) S[n] = 0.f;
                 }
-            } else {
-#pragma unroll
-                for (int n = 0; n < kCols; ++n) S[n] = 0.f;
             }
+            if constexpr (NN == 64) {
 #pragma unroll
-            for (int q = 0; q < kCols / 8; ++q) {
-                float v[8];
+                for (int q = 0; q < kSCols / 8; ++q) {
+                    float v[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) v[e] = S[8 * q + e];
-                const int ng = (col0 >> 3) + q;
-                store8(sbase + OFF_S + (ng * 16 + (row >> 3)) * 128 + (row & 7) * 16, v, BF16);
+                    for (int e = 0; e < 8; ++e) v[e] = S[8 * q + e];
+                    const int ng = (scol0 >> 3) + q;
+                    store8(sbase + L::S + (ng * 16 + (row >> 3)) * 128 + (row & 7) * 16, v, BF16);
+                }
+                tc::fence_smem_to_async();
+                __syncwarp();
+                // (a packed sequence without tokens has no chunk to consume this state)
+                if (lane == 0 && (!VARLEN || nch > 0)) tc::mbar_arrive(bar(BAR_S_FULL));
             }
-            tc::fence_smem_to_async();
-            __syncwarp();
-            // (a packed sequence without tokens has no chunk to consume this state)
-            if (lane == 0 && (!VARLEN || nch > 0)) tc::mbar_arrive(bar(BAR_S_FULL));
 
             for (int k = 0; k < nch; ++k, ++gk) {
                 const int buf = gk & 1;
+                const int xbuf = L::kXcBufs == 2 ? buf : 0;
                 const uint32_t ph = gk & 1u;
                 ChunkVec &V = Vbuf[gk % kVecSlots];
                 wait(BAR_VEC_FULL0 + gk % kVecSlots, (gk / kVecSlots) & 1u);  // decay vectors of chunk k
+                if constexpr (NN == 128) {
+                    if (k == 0) publish_state(S, V.a[my_h]);
+                }
 
                 // ---- A: operands of chunk k into shared memory ----
                 wait(BAR_STAGE_FULL, ph);
+                // one Xcat buffer: the previous chunk's intra product has read it
+                if (L::kXcBufs == 1 && gk > 0) wait((gk - 1) & 1 ? BAR_Y_DONE1 : BAR_Y_DONE0, ((gk - 1) >> 1) & 1u);
                 {
                     float wv[2];
 #pragma unroll
@@ -860,7 +1024,7 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                         const int jl = e & 7, c16 = (e >> 3) & 15, jg = e >> 7;
                         wv[it] = V.w[c16 >> 3][jg * 8 + jl];
                     }
-                    const uint32_t xc = sbase + OFF_XC + buf * XC_BYTES;
+                    const uint32_t xc = sbase + L::XC + xbuf * XC_BYTES;
 #pragma unroll
                     for (int it = 0; it < 2; ++it) {
                         const int e = tid + kComputeThreads * it;
@@ -868,31 +1032,38 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                         const int h = c16 >> 3, po = c16 & 7;
                         const int mgc = h ? 16 + po : po;
                         float xv[8];
-                        stage_read8<IO>(sbase + OFF_STG_X, jg * 8 + jl, c16, xv);
+                        stage_read8<IO>(sbase + L::STG_X, jg * 8 + jl, c16, xv);
                         store8(xc + (jg * 24 + mgc) * 128 + jl * 16, xv, BF16);
                         float xs[8];
 #pragma unroll
                         for (int q = 0; q < 8; ++q) xs[q] = xv[q] * wv[it];
-                        store8(sbase + OFF_XT + (jg * 16 + 8 * h + po) * 128 + jl * 16, xs, BF16);
+                        store8(sbase + L::XT + (jg * 16 + 8 * h + po) * 128 + jl * 16, xs, BF16);
                     }
-                    const int e = tid;
-                    const int jl = e & 7, ng = (e >> 3) & 7, jg = e >> 6;
-                    float bv[8], cv[8];
-                    stage_read8<IO>(sbase + OFF_STG_B, jg * 8 + jl, ng, bv);
-                    stage_read8<IO>(sbase + OFF_STG_C, jg * 8 + jl, ng, cv);
-                    store8(sbase + OFF_BB + (ng * 8 + jg) * 128 + jl * 16, bv, BF16);
-                    store8(sbase + OFF_CB2 + (ng * 16 + jg) * 128 + jl * 16, cv, BF16);
-                    store8(sbase + OFF_CB2 + (ng * 16 + jg + 8) * 128 + jl * 16, cv, BF16);
+#pragma unroll
+                    for (int it = 0; it < NN / 64; ++it) {
+                        const int e = tid + kComputeThreads * it;
+                        const int jl = e & 7, ng = (e >> 3) & (NN / 8 - 1), jg = e / NN;
+                        float bv[8], cv[8];
+                        stage_read8<IO>(sbase + L::STG_B, jg * 8 + jl, ng, bv);
+                        stage_read8<IO>(sbase + L::STG_C, jg * 8 + jl, ng, cv);
+                        store8(sbase + L::BB + (ng * 8 + jg) * 128 + jl * 16, bv, BF16);
+                        store8(sbase + L::CB2 + (ng * 16 + jg) * 128 + jl * 16, cv, BF16);
+                        store8(sbase + L::CB2 + (ng * 16 + jg + 8) * 128 + jl * 16, cv, BF16);
+                    }
                 }
                 tc::fence_smem_to_async();
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(bar(BAR_OPS_FULL));
+                // y staged in the C tile: every compute warp has read chunk k's C first
+                if constexpr (kAliasY) tc::named_barrier(5, kComputeThreads);
 
                 // ---- D: epilogue of the previous chunk (overlaps the G MMA) ----
                 if (k > 0) epilogue(gk - 1, k - 1, b, h0, t0, len);
 
                 // ---- B: masked, decayed C B^T -> Mcat ----
-                {
+                // A warp whose rows are 0-31 and columns 32-63 holds only blocks above the
+                // diagonal: they stay as zeroed at start, and the warp skips the phase.
+                if (!((quarter & 1) == 0 && wg >= 2)) {
                     const int i = row & 63, h = row >> 6;
                     const float csi = V.cs2[h][i];
                     // D x_i as D on the diagonal of the intra-chunk matrix (the diagonal's decay is
@@ -900,9 +1071,9 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                     const float diag_d = p.D ? __ldg(p.D + h0 + h) : 0.f;
                     wait(BAR_G_DONE, ph);
                     tc::fence_after_sync();
-                    const uint32_t mc = sbase + OFF_MC;
+                    const uint32_t mc = sbase + L::MC;
 #pragma unroll
-                    for (int q = 0; q < kCols / 8; ++q) {
+                    for (int q = 0; q < kGCols / 8; ++q) {
                         const int j0 = col0 + 8 * q;
                         float gv[8];
                         tc::tmem_ld8(tlane + TM_G + j0, gv);
@@ -929,38 +1100,56 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                 if (lane == 0) tc::mbar_arrive(bar(BAR_MCAT_FULL));
 
                 // ---- C: state update S <- exp(cs_last) S + dS ----
-                {
+                if constexpr (NN == 64) {
                     const float a = V.a[my_h];
                     wait(BAR_DS_DONE, ph);
                     tc::fence_after_sync();
-                    float ds[kCols];
-                    tc::tmem_ld16(tlane + TM_DS + col0, ds);
+                    float ds[kSCols];
+                    tc::tmem_ld16(tlane + TM_DS + scol0, ds);
                     tc::fence_before_sync();
 #pragma unroll
-                    for (int n = 0; n < kCols; ++n) S[n] = fmaf(a, S[n], ds[n]);
+                    for (int n = 0; n < kSCols; ++n) S[n] = fmaf(a, S[n], ds[n]);
                     if (k + 1 < nch) {
 #pragma unroll
-                        for (int q = 0; q < kCols / 8; ++q) {
+                        for (int q = 0; q < kSCols / 8; ++q) {
                             float v[8];
 #pragma unroll
                             for (int e = 0; e < 8; ++e) v[e] = S[8 * q + e];
-                            const int ng = (col0 >> 3) + q;
-                            store8(sbase + OFF_S + (ng * 16 + (row >> 3)) * 128 + (row & 7) * 16, v, BF16);
+                            const int ng = (scol0 >> 3) + q;
+                            store8(sbase + L::S + (ng * 16 + (row >> 3)) * 128 + (row & 7) * 16, v, BF16);
                         }
                         tc::fence_smem_to_async();
                         __syncwarp();
                         if (lane == 0) tc::mbar_arrive(bar(BAR_S_FULL));
+                    }
+                } else {
+                    // the tensor core added dS onto the decayed state: read S back, and
+                    // publish it for the next chunk, decayed by that chunk's exp(cs_last)
+                    wait(BAR_DS_DONE, ph);
+                    tc::fence_after_sync();
+                    float s16[16];
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        tc::tmem_ld16(tlane + TM_S32 + scol0 + 16 * hf, s16);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) S[16 * hf + i] = s16[i];
+                    }
+                    tc::fence_before_sync();
+                    if (k + 1 < nch) {
+                        const uint32_t gn = gk + 1;
+                        wait(BAR_VEC_FULL0 + gn % kVecSlots, (gn / kVecSlots) & 1u);
+                        publish_state(S, Vbuf[gn % kVecSlots].a[my_h]);
                     }
                 }
             }
 
             // ---- drain: epilogue of the unit's last chunk, final state ----
             if (!VARLEN || nch > 0) epilogue(gk - 1, nch - 1, b, h0, t0, len);
-            if (p.final_state) {
+            if (p.final_state && (!SEG || seg == p.nseg - 1)) {
                 float4 *dst = reinterpret_cast<float4 *>(
-                    p.final_state + (((size_t)sb * dm.H + h0 + my_h) * kP + my_p) * kN + col0);
+                    p.final_state + (((size_t)sb * dm.H + h0 + my_h) * kP + my_p) * NN + scol0);
 #pragma unroll
-                for (int q = 0; q < kCols / 4; ++q)
+                for (int q = 0; q < kSCols / 4; ++q)
                     dst[q] = make_float4(S[4 * q], S[4 * q + 1], S[4 * q + 2], S[4 * q + 3]);
             }
         }
@@ -1021,10 +1210,10 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// [batch, tokens, features] tensor, boxes of 128 bytes x 64 tokens x 1 (128-byte
-// swizzle or none), zero fill past the end of the sequence.
-cudaError_t encode_map(CUtensorMap *m, const void *base, int io, int64_t feats, int64_t L, int64_t B,
-                       bool swizzle = true) {
+}  // namespace
+
+cudaError_t encode_tile_map(CUtensorMap *m, const void *base, int io, int64_t feats, int64_t L, int64_t B,
+                            bool swizzle) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return cudaErrorNotSupported;
     const size_t esz = io == IO_F32 ? 4 : 2;
@@ -1042,26 +1231,35 @@ cudaError_t encode_map(CUtensorMap *m, const void *base, int io, int64_t feats, 
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int IO, bool BF16>
+namespace {
+
+template <int IO, bool BF16, int NN>
 cudaError_t launch_typed(const Params &p, int units, unsigned int *err, cudaStream_t s) {
+    using L = Smem<NN, IO>;
     // packed variable-length sequences and the fused norm get their own
-    // instantiations, so that the regular layout pays nothing for them
-    // z on the regular layout: staged by TMA through the y tile (ZM 1), with the norm (ZM 2)
-    const bool norm = p.norm_w && !p.cu;
-    const bool gated = p.z && !p.cu;
-    auto kern = p.cu    ? ssd_fused_kernel<IO, BF16, true, 0>
-                : norm  ? ssd_fused_kernel<IO, BF16, false, 2>
-                : gated ? ssd_fused_kernel<IO, BF16, false, 1>
-                        : ssd_fused_kernel<IO, BF16, false, 0>;
-    const uint32_t smem = gated ? SMEM_BYTES_NORM : SMEM_BYTES;
+    // instantiations, so that the regular layout pays nothing for them;
+    // z is staged by TMA through the y tile (ZM 1; with the norm, ZM 2),
+    // except where y itself is staged in the C tile (fp32 I/O at N = 128):
+    // the epilogue then loads z from global memory
+    const bool norm = NN == 64 && p.norm_w && !p.cu;
+    const bool gated = p.z && !p.cu && !L::kAliasY;
+    auto kern = ssd_fused_kernel<IO, BF16, false, 0, NN>;
+    if constexpr (NN == 64) {
+        if (p.cu) kern = ssd_fused_kernel<IO, BF16, true, 0>;
+        else if (norm) kern = ssd_fused_kernel<IO, BF16, false, 2>;
+        else if (gated) kern = ssd_fused_kernel<IO, BF16, false, 1>;
+    } else if constexpr (!L::kAliasY) {
+        if (gated) kern = ssd_fused_kernel<IO, BF16, false, 1, NN>;
+    }
+    const uint32_t smem = gated ? L::BYTES_NORM : L::BYTES;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     TmaMaps tm;
-    if ((e = encode_map(&tm.x, p.x, IO, (int64_t)p.H * kP, p.L, p.B)) != cudaSuccess) return e;
-    if ((e = encode_map(&tm.b, p.Bm, IO, (int64_t)p.G * kN, p.L, p.B)) != cudaSuccess) return e;
-    if ((e = encode_map(&tm.c, p.Cm, IO, (int64_t)p.G * kN, p.L, p.B)) != cudaSuccess) return e;
-    if ((e = encode_map(&tm.y, p.y, IO, (int64_t)p.H * kP, p.L, p.B, false)) != cudaSuccess) return e;
-    if (gated && (e = encode_map(&tm.z, p.z, IO, (int64_t)p.H * kP, p.L, p.B, false)) != cudaSuccess) return e;
+    if ((e = encode_tile_map(&tm.x, p.x, IO, (int64_t)p.H * kP, p.L, p.B, true)) != cudaSuccess) return e;
+    if ((e = encode_tile_map(&tm.b, p.Bm, IO, (int64_t)p.G * NN, p.L, p.B, true)) != cudaSuccess) return e;
+    if ((e = encode_tile_map(&tm.c, p.Cm, IO, (int64_t)p.G * NN, p.L, p.B, true)) != cudaSuccess) return e;
+    if ((e = encode_tile_map(&tm.y, p.y, IO, (int64_t)p.H * kP, p.L, p.B, false)) != cudaSuccess) return e;
+    if (gated && (e = encode_tile_map(&tm.z, p.z, IO, (int64_t)p.H * kP, p.L, p.B, false)) != cudaSuccess) return e;
     // one CTA per SM: its shared memory and 512 TMEM columns fill the SM
     if (!norm) {
         const int grid = units < num_sms() ? units : num_sms();
@@ -1098,13 +1296,60 @@ cudaError_t launch_typed(const Params &p, int units, unsigned int *err, cudaStre
     return cudaGetLastError();
 }
 
+size_t up256(size_t v) { return (v + 255) / 256 * 256; }
+
+// How a walk at N = 128 is cut into segments: nseg segments of seg_len tokens
+// (a multiple of 64, the last one possibly shorter), chosen by a cost model
+// in microseconds from measurements on GB300: rounds of (batch, group, head
+// pair, segment) units over the SMs, each a segment's 64-token steps (about
+// 7 us each at N = 128) plus about 3 us to start a unit; with more than one
+// segment, the pre-pass re-reading x and B and writing the segment states,
+// and the fold (a dependent step of about 1 us per segment, and the states
+// read and written), at about 6 TB/s, plus two more launches.
+struct SegPlan {
+    int nseg, seg_len;
+};
+
+SegPlan seg_plan(const ssd_fwd_args *a) {
+    const int64_t units0 = fused_units(a);
+    const int64_t nsub = (a->L + kQ - 1) / kQ;
+    const int64_t sms = num_sms();
+    const double io = a->x_dtype == SSD_F32 ? 4.0 : 2.0;
+    constexpr double kStepUs = 7.0, kUnitUs = 3.0, kFoldStepUs = 1.0, kLaunchUs = 6.0, kBytesPerUs = 6.0e6;
+    const double reread_us = (double)a->B * a->L * (a->H * a->P + a->G * a->N) * io / kBytesPerUs;
+    const double states_us = (double)a->B * a->H * a->P * a->N * 4.0 / kBytesPerUs;  // one segment boundary
+    SegPlan best{1, (int)(nsub * kQ)};
+    double best_cost = (double)((units0 + sms - 1) / sms) * (nsub * kStepUs + kUnitUs);
+    for (int64_t want = 2; want <= nsub && want <= 256; ++want) {
+        const int64_t steps = (nsub + want - 1) / want;
+        const int64_t nseg = (nsub + steps - 1) / steps;
+        const int seg_len = (int)(steps * kQ);
+        if (nseg < 2 || !segment_smem_fits(a->x_dtype, seg_len)) continue;
+        const double walk = (double)((units0 * nseg + sms - 1) / sms) * (steps * kStepUs + kUnitUs);
+        const double pre = reread_us * (double)(nseg - 1) / nseg + states_us * (nseg - 1);
+        const double fold = kFoldStepUs * nseg + 2.0 * states_us * (nseg - 1);
+        const double cost = walk + pre + fold + kLaunchUs;
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = {(int)nseg, seg_len};
+        }
+    }
+    return best;
+}
+
+size_t seg_states_bytes(const ssd_fwd_args *a, int nseg) {
+    return up256((size_t)a->B * nseg * a->H * a->P * a->N * sizeof(float));
+}
+
 }  // namespace
 
 const char *fused_unsupported_reason(const ssd_fwd_args *a) {
-    if (a->P != kP || a->N != kN || a->chunk != kQ) return "needs P = N = chunk = 64";
+    if (a->P != kP) return "needs P = 64";
+    if (a->N != 64 && a->N != 128) return "needs N = 64 or 128";
+    if (a->chunk % kQ != 0) return "needs a chunk size that is a multiple of 64 (it walks each chunk in 64-token steps)";
     if ((a->H / a->G) % 2 != 0) return "needs an even number of heads per group";
     if (a->ops == SSD_OPS_F32) return "needs fp16 or bf16 operands (the fp32 path is the chunked plan)";
-    if (fused_units(a) > 0x7fffffffLL) return "too many (batch, group, head pair) units";
+    if (fused_units(a) * ((a->L + kQ - 1) / kQ) > 0x7fffffffLL) return "too many (batch, group, head pair) units";
     for (const void *ptr : {static_cast<const void *>(a->x), static_cast<const void *>(a->Bm),
                             static_cast<const void *>(a->Cm), static_cast<const void *>(a->y)})
         if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return "needs 16-byte aligned x, B, C and y";
@@ -1114,21 +1359,32 @@ const char *fused_unsupported_reason(const ssd_fwd_args *a) {
 
 bool fused_supported(const ssd_fwd_args *a) { return fused_unsupported_reason(a) == nullptr; }
 
+bool fused_varlen_supported(const ssd_fwd_args *a) { return fused_supported(a) && a->N == 64; }
+
 bool fused_norm_supported(const ssd_fwd_args *a) {
-    return fused_supported(a) && a->z && (a->H / a->G) / 2 <= kNormMaxRanks;
+    return fused_supported(a) && a->N == 64 && a->z && (a->H / a->G) / 2 <= kNormMaxRanks;
 }
 
-bool fused_preferred(const ssd_fwd_args *a) { return fused_units(a) >= num_sms(); }
+// N = 64: the unit-sequential walk needs as many units as SMs; at N = 128 the
+// segmented walk fills the GPU by itself.
+bool fused_preferred(const ssd_fwd_args *a) { return a->N == 128 || fused_units(a) >= num_sms(); }
 
-size_t fused_workspace_size(const ssd_fwd_args *) { return 256; }
+int fused_segments(const ssd_fwd_args *a) { return a->N == 128 ? seg_plan(a).nseg : 1; }
+
+size_t fused_workspace_size(const ssd_fwd_args *a) {
+    if (a->N != 128) return 256;
+    const SegPlan sp = seg_plan(a);
+    if (sp.nseg < 2) return 256;
+    return 256 + seg_states_bytes(a, sp.nseg) + up256((size_t)a->B * a->H * sp.nseg * sizeof(float));
+}
 
 namespace {
 
 Params fused_params(const ssd_fwd_args *a) {
     Params p;
     p.B = (int)a->B; p.L = (int)a->L; p.H = (int)a->H; p.P = (int)a->P; p.N = (int)a->N;
-    p.G = (int)a->G; p.Q = (int)a->chunk;
-    p.nchunks = (int)((a->L + a->chunk - 1) / a->chunk);
+    p.G = (int)a->G; p.Q = kQ;  // every chunk is walked in 64-token steps
+    p.nchunks = (int)((a->L + kQ - 1) / kQ);
     p.hpg = (int)(a->H / a->G);
     p.x = a->x; p.dt = a->dt; p.A = a->A; p.Bm = a->Bm; p.Cm = a->Cm; p.D = a->D; p.z = a->z;
     p.dt_bias = a->dt_bias; p.h0 = a->initial_state; p.y = a->y; p.final_state = a->final_state;
@@ -1140,24 +1396,50 @@ Params fused_params(const ssd_fwd_args *a) {
     return p;
 }
 
+// The fused kernel (the error word at err cleared by the caller).
 cudaError_t launch(const ssd_fwd_args *a, const Params &p, int units, unsigned int *err, cudaStream_t s) {
-    cudaError_t e = cudaMemsetAsync(err, 0, 256, s);
-    if (e != cudaSuccess) return e;
     const bool bf16 = a->ops == SSD_OPS_BF16;
+    if (a->N == 128) {
+        switch (a->x_dtype) {
+            case SSD_F32: return bf16 ? launch_typed<IO_F32, true, 128>(p, units, err, s) : launch_typed<IO_F32, false, 128>(p, units, err, s);
+            case SSD_F16: return bf16 ? launch_typed<IO_F16, true, 128>(p, units, err, s) : launch_typed<IO_F16, false, 128>(p, units, err, s);
+            case SSD_BF16: return bf16 ? launch_typed<IO_BF16, true, 128>(p, units, err, s) : launch_typed<IO_BF16, false, 128>(p, units, err, s);
+        }
+        return cudaErrorInvalidValue;
+    }
     switch (a->x_dtype) {
-        case SSD_F32: return bf16 ? launch_typed<IO_F32, true>(p, units, err, s) : launch_typed<IO_F32, false>(p, units, err, s);
-        case SSD_F16: return bf16 ? launch_typed<IO_F16, true>(p, units, err, s) : launch_typed<IO_F16, false>(p, units, err, s);
-        case SSD_BF16: return bf16 ? launch_typed<IO_BF16, true>(p, units, err, s) : launch_typed<IO_BF16, false>(p, units, err, s);
+        case SSD_F32: return bf16 ? launch_typed<IO_F32, true, 64>(p, units, err, s) : launch_typed<IO_F32, false, 64>(p, units, err, s);
+        case SSD_F16: return bf16 ? launch_typed<IO_F16, true, 64>(p, units, err, s) : launch_typed<IO_F16, false, 64>(p, units, err, s);
+        case SSD_BF16: return bf16 ? launch_typed<IO_BF16, true, 64>(p, units, err, s) : launch_typed<IO_BF16, false, 64>(p, units, err, s);
     }
     return cudaErrorInvalidValue;
 }
 
-size_t up256(size_t v) { return (v + 255) / 256 * 256; }
-
 }  // namespace
 
 cudaError_t run_fused(const ssd_fwd_args *a, cudaStream_t s) {
-    return launch(a, fused_params(a), (int)fused_units(a), static_cast<unsigned int *>(a->workspace), s);
+    unsigned int *err = static_cast<unsigned int *>(a->workspace);
+    cudaError_t e = cudaMemsetAsync(err, 0, 256, s);
+    if (e != cudaSuccess) return e;
+    Params p = fused_params(a);
+    int64_t units = fused_units(a);
+    if (a->N == 128) {
+        // the walk in segments: the segment passes leave the state entering
+        // each later segment in the workspace
+        const SegPlan sp = seg_plan(a);
+        p.nseg = sp.nseg;
+        p.seg_len = sp.seg_len;
+        units *= sp.nseg;
+        if (sp.nseg > 1) {
+            char *ws = static_cast<char *>(a->workspace);
+            float *states = reinterpret_cast<float *>(ws + 256);
+            float *decay = reinterpret_cast<float *>(ws + 256 + seg_states_bytes(a, sp.nseg));
+            p.seg_states = states;
+            e = launch_segment_passes(p, a->x_dtype, a->ops == SSD_OPS_BF16, states, decay, err, s);
+            if (e != cudaSuccess) return e;
+        }
+    }
+    return launch(a, p, (int)units, err, s);
 }
 
 size_t fused_varlen_workspace_size(const ssd_fwd_args *a, int64_t nseq) {
@@ -1192,7 +1474,9 @@ cudaError_t run_fused_varlen(const ssd_fwd_args *a, const int64_t *cu, int nseq,
         sched[i] = order[base + ((round & 1) ? m - 1 - c : c)];
     }
     char *ws = static_cast<char *>(a->workspace);
-    cudaError_t e = cudaMemcpyAsync(ws + o_cu, host.data(), host.size(), cudaMemcpyHostToDevice, s);
+    cudaError_t e = cudaMemsetAsync(ws, 0, 256, s);
+    if (e != cudaSuccess) return e;
+    e = cudaMemcpyAsync(ws + o_cu, host.data(), host.size(), cudaMemcpyHostToDevice, s);
     if (e != cudaSuccess) return e;
     Params p = fused_params(a);
     p.cu = reinterpret_cast<const long long *>(ws + o_cu);

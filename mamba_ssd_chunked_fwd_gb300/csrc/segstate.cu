@@ -1,0 +1,296 @@
+// segstate.cu -- the segment passes that let the fused plan walk one sequence
+// in parallel at state width N = 128, where (batch x group x head pair) alone
+// is too few units for the GPU.  The sequence is cut into nseg segments of
+// seg_len tokens (a multiple of 64); the fused kernel walks each segment from
+// the state entering it, and these two kernels provide that state.  It is the
+// chunked algorithm's inter-chunk recurrence (ops-transformer MambaV2 article,
+// sections 4.3 and 4.4: chunk_state, then chunk_state_passing) taken over
+// segments instead of chunks: the pages' chunk-parallel lesson (MindSpeed-Ops
+// PR #101 page, the "aux" path for shapes whose batch x heads cannot fill
+// the device) with the states of only nseg - 1 boundaries materialised.
+//
+// Pre-pass, one CTA per (batch b, group g, head pair, segment s < nseg - 1):
+//     E_s[(h,p), n] = sum_{t in s} exp(sum_{t' in s, t' > t} d_t' A_h) d_t x_t[h,p] B_t[n]
+//     a_s[h]        = sum_{t in s} d_t A_h
+// E_s is the state segment s produces from a zero start; it is one tcgen05
+// accumulation (M = 128 rows (head, p), N = 128, K = the segment's tokens in
+// 64-token blocks) of bf16 / fp16 operands into an fp32 TMEM accumulator.
+// The decay weight of every token is an exclusive suffix sum of d A taken
+// backwards over the segment, so no large cumulative sums are subtracted.
+// Warps 0-7 convert the TMA-staged x and B tiles into operands (warps 0 and 1
+// first compute the weights of one head each), warp 8 issues the TMA copies
+// into a two-stage ring, warp 9 issues the MMAs; every handoff is an mbarrier
+// whose wait gives up after 2 s (recorded in the workspace error word).
+//
+// Fold, one thread per 4 state elements of one (b, h):
+//     S_in(0) = h0 (or 0),   S_in(s + 1) = exp(a_s) S_in(s) + E_s,
+// written over E in place: seg_states[b, s] holds the state entering segment s.
+#include "ssd_fused.cuh"
+#include "ssd_internal.cuh"
+#include "tc_operands.cuh"
+#include "tc_ptx.cuh"
+#include "tc_stage.cuh"
+
+namespace ssd {
+
+namespace {
+
+using tcop::store8;
+using tcstage::BOX_BYTES;
+using tcstage::stage_read8;
+
+constexpr int kNN = 128, kP = 64;
+constexpr int kConvWarps = 8;
+constexpr int kConvThreads = kConvWarps * 32;
+constexpr int kTmaWarp = kConvWarps, kMmaWarp = kConvWarps + 1;
+constexpr int kThreads = kConvThreads + 64;
+constexpr uint64_t kWaitNs = 2000000000ull;
+
+// shared memory (bytes from a 1024-aligned base): two staging stages of x
+// (128 features) and B (128 features), two operand buffers of Xw^T (MN-major,
+// 128 (h,p) x 64 j) and B (MN-major, 64 j x 128 n), then the weights w[2][seg_len]
+template <int IO>
+struct PreSmem {
+    static constexpr uint32_t STG_BYTES = (IO == IO_F32 ? 4u : 2u) * BOX_BYTES;  // x or B of one block
+    static constexpr uint32_t STG = 0;                          // stage i: x at STG + 2 i STG_BYTES, B after it
+    static constexpr uint32_t XT = 4 * STG_BYTES;               // operand buffer i at XT + i OP_BYTES
+    static constexpr uint32_t OP_BYTES = 16384 + 16384;         // Xw^T, then B
+    static constexpr uint32_t W = XT + 2 * OP_BYTES;
+    static constexpr uint32_t bytes(int seg_len) { return W + 2u * seg_len * 4u + 1024u; }
+};
+
+enum { PB_FULL0 = 0, PB_EMPTY0 = 2, PB_OPS0 = 4, PB_DONE0 = 6, PB_N = 8 };
+
+template <int IO, bool BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+segment_state_kernel(const __grid_constant__ Params p, const __grid_constant__ SegMaps tm, float *seg_states,
+                     float *seg_decay, unsigned int *err) {
+    using SM = PreSmem<IO>;
+    extern __shared__ unsigned char smem_raw[];
+    __shared__ __align__(8) uint64_t bars[PB_N];
+    __shared__ uint32_t tmem_slot;
+    const uint32_t raw = tc::smem_addr(smem_raw);
+    unsigned char *sm = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    const uint32_t sbase = tc::smem_addr(sm);
+    float *w_s = reinterpret_cast<float *>(sm + SM::W);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int pairs = p.hpg >> 1, nsg = p.nseg - 1;  // the last segment needs no pre-pass
+    int q = blockIdx.x;
+    const int pair = q % pairs;
+    q /= pairs;
+    const int g = q % p.G;
+    q /= p.G;
+    const int s = q % nsg, b = q / nsg;
+    const int h0 = g * p.hpg + 2 * pair;
+    const int t0 = s * p.seg_len, nblk = p.seg_len / 64;
+    const uint32_t bar0 = tc::smem_addr(&bars[0]);
+    auto bar = [bar0](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
+    bool timed_out = false;
+    auto wait = [&](int i, uint32_t parity) {
+        if (!timed_out && !tc::mbar_wait(bar(i), parity, kWaitNs)) timed_out = true;
+    };
+
+    if (tid == 0) {
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(bar(PB_FULL0 + i), 1);
+            tc::mbar_init(bar(PB_EMPTY0 + i), kConvWarps);
+            tc::mbar_init(bar(PB_OPS0 + i), kConvWarps);
+            tc::mbar_init(bar(PB_DONE0 + i), 1);
+        }
+        tc::mbar_init_fence();
+    }
+    if (warp == kMmaWarp) {
+        tc::tmem_alloc(tc::smem_addr(&tmem_slot), kNN);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = tmem_slot;
+    constexpr int bw = IO == IO_F32 ? 32 : 64;  // features per 128-byte box
+
+    if (warp == kTmaWarp) {
+        if (lane == 0) {
+            tc::prefetch_tensormap(&tm.x);
+            tc::prefetch_tensormap(&tm.b);
+            for (int j = 0; j < nblk; ++j) {
+                const int st = j & 1;
+                if (j >= 2) wait(PB_EMPTY0 + st, ((j - 2) >> 1) & 1u);
+                const uint32_t xdst = sbase + SM::STG + 2 * st * SM::STG_BYTES, bdst = xdst + SM::STG_BYTES;
+                tc::mbar_arrive_expect_tx(bar(PB_FULL0 + st), 2 * SM::STG_BYTES);
+#pragma unroll
+                for (int bx = 0; bx < 128 / bw; ++bx) {
+                    tc::tma_load_3d(xdst + bx * BOX_BYTES, &tm.x, h0 * kP + bx * bw, t0 + 64 * j, b, bar(PB_FULL0 + st));
+                    tc::tma_load_3d(bdst + bx * BOX_BYTES, &tm.b, g * kNN + bx * bw, t0 + 64 * j, b, bar(PB_FULL0 + st));
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == kMmaWarp) {
+        if (lane == 0) {
+            constexpr uint32_t ID = tc::idesc_f16(128, kNN, BF16, true, true);
+            for (int j = 0; j < nblk; ++j) {
+                const int ob = j & 1;
+                wait(PB_OPS0 + ob, (j >> 1) & 1u);
+                tc::fence_after_sync();
+                const uint32_t xt = sbase + SM::XT + ob * SM::OP_BYTES, bb = xt + 16384;
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)  // E += Xw^T B, K = 16 tokens per step
+                    tc::mma_f16(tmem, tc::desc(xt + ks * 4096, 2048, 128), tc::desc(bb + ks * 256, 128, 1024), ID,
+                                (j | ks) != 0);
+                tc::commit(bar(PB_DONE0 + ob));
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---- weights: the segment's processed steps d (all loads in flight at
+        // once), then one head per warp, backwards over the segment ----
+        for (int e = tid; e < 2 * p.seg_len; e += kConvThreads) {
+            const int hh = e / p.seg_len, t = t0 + e % p.seg_len;
+            w_s[e] = dt_processed(p, __ldg(p.dt + ((size_t)b * p.L + t) * p.H + h0 + hh), h0 + hh);
+        }
+        tc::named_barrier(1, kConvThreads);
+        if (warp < 2) {
+            const int h = h0 + warp;
+            const float A = __ldg(p.A + h);
+            float carry = 0.f;  // sum of d A over the tokens after the current 32-token block
+            for (int blk = p.seg_len / 32 - 1; blk >= 0; --blk) {
+                const float d = w_s[warp * p.seg_len + 32 * blk + lane];
+                const float v = d * A;
+                float incl = v;  // sum over this lane and the lanes after it
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const float o = __shfl_down_sync(0xffffffffu, incl, off);
+                    if (lane + off < 32) incl += o;
+                }
+                float excl = __shfl_down_sync(0xffffffffu, incl, 1);
+                if (lane == 31) excl = 0.f;
+                w_s[warp * p.seg_len + 32 * blk + lane] = expf(carry + excl) * d;
+                carry += __shfl_sync(0xffffffffu, incl, 0);
+            }
+            if (lane == 0) seg_decay[((size_t)b * p.H + h) * p.nseg + s] = carry;
+        }
+        tc::named_barrier(1, kConvThreads);
+
+        // ---- operands: block j of x (scaled by w) and B, from the staging ring ----
+        for (int j = 0; j < nblk; ++j) {
+            const int st = j & 1, ob = j & 1;
+            wait(PB_FULL0 + st, (j >> 1) & 1u);
+            if (j >= 2) wait(PB_DONE0 + ob, ((j - 2) >> 1) & 1u);  // the MMA of block j - 2 read this buffer
+            const uint32_t xsrc = sbase + SM::STG + 2 * st * SM::STG_BYTES, bsrc = xsrc + SM::STG_BYTES;
+            const uint32_t xt = sbase + SM::XT + ob * SM::OP_BYTES, bb = xt + 16384;
+#pragma unroll
+            for (int it = 0; it < 4; ++it) {  // 64 tokens x 16 groups of 8 features, for x and for B
+                const int e = tid + kConvThreads * it;
+                const int jl = e & 7, c16 = (e >> 3) & 15, jg = e >> 7;
+                const int r = jg * 8 + jl;
+                float v[8];
+                stage_read8<IO>(xsrc, r, c16, v);
+                const float wv = w_s[(c16 >> 3) * p.seg_len + 64 * j + r];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v[i] *= wv;
+                store8(xt + (jg * 16 + c16) * 128 + jl * 16, v, BF16);  // row (h, p) = 8 c16 + ..
+                stage_read8<IO>(bsrc, r, c16, v);
+                store8(bb + (c16 * 8 + jg) * 128 + jl * 16, v, BF16);
+            }
+            tc::fence_smem_to_async();
+            __syncwarp();
+            if (lane == 0) {
+                tc::mbar_arrive(bar(PB_EMPTY0 + st));
+                tc::mbar_arrive(bar(PB_OPS0 + ob));
+            }
+        }
+
+        // ---- E_s out of TMEM: warp w reads lanes 32 (w % 4) .. + 31, columns 64 (w / 4) .. + 63 ----
+        wait(PB_DONE0 + ((nblk - 1) & 1), ((nblk - 1) >> 1) & 1u);
+        tc::fence_after_sync();
+        const int quarter = warp & 3, half = warp >> 2;
+        const int row = quarter * 32 + lane, h = row >> 6, pp = row & 63;
+        float *dst = seg_states + ((((size_t)b * p.nseg + s + 1) * p.H + h0 + h) * kP + pp) * kNN + 64 * half;
+        const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + 64 * half;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            float v[16];
+            tc::tmem_ld16(tl + 16 * c, v);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                reinterpret_cast<float4 *>(dst + 16 * c)[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        }
+    }
+
+    if (timed_out) atomicOr(err, 4u);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (warp == kMmaWarp) tc::tmem_dealloc(tmem, kNN);
+}
+
+// S_in(s + 1) = exp(a_s) S_in(s) + E_s over s = 0 .. nseg - 2, in place
+__global__ void __launch_bounds__(256)
+segment_fold_kernel(const Params p, const float *__restrict__ seg_decay, float *seg_states) {
+    const int bh = blockIdx.x, b = bh / p.H, h = bh % p.H;
+    const int PN = kP * kNN;
+    const int e = (blockIdx.y * 256 + threadIdx.x) * 4;
+    if (e >= PN) return;
+    const size_t sstride = (size_t)p.H * PN;  // distance between segments
+    float *base = seg_states + ((size_t)b * p.nseg * p.H + h) * PN + e;
+    float4 st = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (p.h0) st = __ldg(reinterpret_cast<const float4 *>(p.h0 + ((size_t)b * p.H + h) * PN + e));
+    const float *a = seg_decay + ((size_t)b * p.H + h) * p.nseg;
+    float4 nxt = *reinterpret_cast<const float4 *>(base + sstride);
+    for (int s = 1; s < p.nseg; ++s) {
+        const float4 loc = nxt;
+        if (s + 1 < p.nseg) nxt = *reinterpret_cast<const float4 *>(base + (size_t)(s + 1) * sstride);
+        const float ea = expf(__ldg(a + s - 1));
+        st.x = fmaf(ea, st.x, loc.x);
+        st.y = fmaf(ea, st.y, loc.y);
+        st.z = fmaf(ea, st.z, loc.z);
+        st.w = fmaf(ea, st.w, loc.w);
+        *reinterpret_cast<float4 *>(base + (size_t)s * sstride) = st;
+    }
+}
+
+template <int IO, bool BF16>
+cudaError_t launch_pre(const Params &p, float *seg_states, float *seg_decay, unsigned int *err, cudaStream_t s) {
+    SegMaps tm;
+    cudaError_t e;
+    if ((e = encode_tile_map(&tm.x, p.x, IO, (int64_t)p.H * kP, p.L, p.B, true)) != cudaSuccess) return e;
+    if ((e = encode_tile_map(&tm.b, p.Bm, IO, (int64_t)p.G * kNN, p.L, p.B, true)) != cudaSuccess) return e;
+    const uint32_t smem = PreSmem<IO>::bytes(p.seg_len);
+    auto kern = segment_state_kernel<IO, BF16>;
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
+        return e;
+    const int ctas = p.B * p.G * (p.hpg / 2) * (p.nseg - 1);
+    kern<<<ctas, kThreads, smem, s>>>(p, tm, seg_states, seg_decay, err);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int segment_max_len() { return 2048; }
+
+bool segment_smem_fits(int io, int seg_len) {
+    const uint32_t need = io == IO_F32 ? PreSmem<IO_F32>::bytes(seg_len) : PreSmem<IO_BF16>::bytes(seg_len);
+    return seg_len % 64 == 0 && seg_len <= segment_max_len() && need <= 232448u - 256u;
+}
+
+cudaError_t launch_segment_passes(const Params &p, int io, bool bf16, float *seg_states, float *seg_decay,
+                                  unsigned int *err, cudaStream_t s) {
+    if (p.nseg < 2) return cudaSuccess;
+    cudaError_t e;
+    switch (io) {
+        case IO_F32: e = bf16 ? launch_pre<IO_F32, true>(p, seg_states, seg_decay, err, s)
+                              : launch_pre<IO_F32, false>(p, seg_states, seg_decay, err, s); break;
+        case IO_F16: e = bf16 ? launch_pre<IO_F16, true>(p, seg_states, seg_decay, err, s)
+                              : launch_pre<IO_F16, false>(p, seg_states, seg_decay, err, s); break;
+        default: e = bf16 ? launch_pre<IO_BF16, true>(p, seg_states, seg_decay, err, s)
+                          : launch_pre<IO_BF16, false>(p, seg_states, seg_decay, err, s); break;
+    }
+    if (e != cudaSuccess) return e;
+    dim3 grid(p.B * p.H, (kP * kNN / 4 + 255) / 256);
+    segment_fold_kernel<<<grid, 256, 0, s>>>(p, seg_decay, seg_states);
+    return cudaGetLastError();
+}
+
+}  // namespace ssd

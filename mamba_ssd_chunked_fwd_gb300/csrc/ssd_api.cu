@@ -217,7 +217,7 @@ ssd_status check_varlen(const ssd_fwd_args *a, const int64_t *cu, int64_t nseq, 
 }
 
 bool varlen_fused(const ssd_fwd_args *a, int64_t nseq) {
-    if (a->plan == SSD_PLAN_CHUNKED || !ssd::fused_supported(a)) return false;
+    if (a->plan == SSD_PLAN_CHUNKED || !ssd::fused_varlen_supported(a)) return false;
     // the host builds a schedule over the units: keep it small
     return (int64_t)nseq * a->G * ((a->H / a->G) / 2) <= (1LL << 24);
 }
@@ -350,7 +350,8 @@ ssd_status ssd_fwd_describe(const ssd_fwd_args *a, char *out, size_t cap) {
     if (!out || cap == 0) return fail(SSD_ERR_INVALID_ARG, "out buffer required");
     const char *norm = a->norm_weight && !norm_in_kernel(a, plan) ? ",gated_rmsnorm" : "";
     if (plan == SSD_PLAN_FUSED) {
-        snprintf(out, cap, "ssd_fused_kernel%s", norm);
+        const bool seg = ssd::fused_segments(a) > 1;
+        snprintf(out, cap, "%sssd_fused_kernel%s", seg ? "segment_state_kernel,segment_fold_kernel," : "", norm);
         return ok();
     }
     const ssd::Params p = make_params(a);
@@ -411,7 +412,9 @@ ssd_status ssd_fwd_varlen(const ssd_fwd_args *a, const int64_t *cu, int64_t nseq
     }
     if (a->plan == SSD_PLAN_FUSED && !varlen_fused(a, nseq))
         return fail(SSD_ERR_UNSUPPORTED, "the fused plan does not support this shape: %s",
-                    ssd::fused_unsupported_reason(a) ? ssd::fused_unsupported_reason(a) : "too many units");
+                    ssd::fused_unsupported_reason(a)  ? ssd::fused_unsupported_reason(a)
+                    : !ssd::fused_varlen_supported(a) ? "packed sequences take it at N = 64 only"
+                                                      : "too many units");
     if ((st = check_pointers(a, true)) != SSD_OK) return st;
     const size_t need = varlen_workspace(a, nseq, mx);
     if (!a->workspace || a->workspace_bytes < need)

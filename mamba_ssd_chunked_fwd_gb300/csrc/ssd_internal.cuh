@@ -38,6 +38,11 @@ struct Params {
     // gated RMSNorm of the output (fused plan), NULL otherwise
     const float *norm_w = nullptr;
     float norm_eps = 0.f;
+    // fused plan at N = 128: each sequence is cut into nseg segments of
+    // seg_len tokens (a multiple of 64) walked in parallel; seg_states
+    // [B, nseg, H, P, N] holds the state entering segment s >= 1
+    int seg_len = 0, nseg = 1;
+    const float *seg_states = nullptr;
 };
 
 enum IoType { IO_F32 = SSD_F32, IO_F16 = SSD_F16, IO_BF16 = SSD_BF16 };

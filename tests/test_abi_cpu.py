@@ -147,15 +147,17 @@ def test_fused_plan_request_is_checked():
 
 
 def test_describe_names_the_kernels_each_workload_runs():
-    """The named workloads run on the tensor cores (fused kernel or the
-    tensor-core chunk steps); only the fp32 tiny workload uses CUDA cores."""
+    """The named workloads run on the tensor cores (the fused kernel, at N = 128
+    after the segment passes when it cuts the walk into segments); only the
+    fp32 tiny workload uses the CUDA-core chunk steps.  Without a GPU the SM
+    count reads as 1, so no walk is cut into segments here."""
     import ssd_inputs
     expect = {
         "tiny": ["chunk_cumsum", "chunk_state", "state_passing", "chunk_scan"],
-        "same_device": ["chunk_cumsum", "chunk_state_tc", "state_passing", "chunk_scan_tc"],
+        "same_device": ["ssd_fused_kernel"],
         "large_training": ["ssd_fused_kernel"],
-        "long_sequence": ["chunk_cumsum", "chunk_state_tc", "state_passing", "chunk_scan_tc"],
-        "gated_prefill": ["chunk_cumsum", "chunk_state_tc", "state_passing", "chunk_scan_tc"],
+        "long_sequence": ["ssd_fused_kernel"],
+        "gated_prefill": ["ssd_fused_kernel"],
     }
     dt_of = {"f32": torch.float32, "bf16": torch.bfloat16}
     for name, w in ssd_inputs.WORKLOADS.items():

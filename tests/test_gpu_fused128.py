@@ -1,0 +1,102 @@
+"""The fused plan at state width N = 128 (chunks of 64, 128 or 256 tokens
+walked in 64-token steps): the walk cut into segments, the segment pre-pass
+and fold, the state held in TMEM, and with fp32 I/O y staged in the C tile.
+Every case is compared element by element with the float64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import ssd_inputs
+from _harness import assert_close, oracle_problem, run_gpu, to_device
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = [
+    # B, L, H, P, N, G, chunk
+    (1, 64, 2, 64, 128, 1, 64),        # one step, one unit
+    (2, 384, 8, 64, 128, 2, 128),      # several segments and units
+    (1, 513, 4, 64, 128, 1, 256),      # ragged tail one token past a chunk
+    (2, 1000, 8, 64, 128, 4, 128),     # two heads per group, ragged
+    (1, 4096, 32, 64, 128, 1, 256),    # many segments, more units than CTAs
+]
+
+
+def _describe(inp, ops, plan="fused"):
+    import mamba_ssd_chunked_fwd_gb300 as ssd
+    d = to_device(inp)
+    a = ssd.make_args(d["x"], d["dt"], d["A"], d["B"], d["C"], inp["chunk_size"], ops=ops, plan=plan,
+                      y=torch.empty_like(d["x"]))
+    return ssd.ssd_fwd_describe(a)
+
+
+def _full(oracle_mod, inp, y, fin, mode, what):
+    yr, fr = oracle_mod.forward(oracle_problem(oracle_mod, inp))
+    assert_close(oracle_mod, y.double().cpu().numpy(), yr, mode, what + " y")
+    if fin is not None:
+        assert_close(oracle_mod, fin.double().cpu().numpy(), fr, mode, what + " final_state")
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+@pytest.mark.parametrize("feat", ["plain", "all"])
+@pytest.mark.parametrize("io,ops", [("f32", "bf16"), ("f32", "f16"), ("bf16", "bf16")])
+def test_fused128(oracle_mod, shape, feat, io, ops):
+    B, L, H, P, N, G, Q = shape
+    f = dict(D=True, z=True, dt_bias=True, h0=True) if feat == "all" else {}
+    _, inp = ssd_inputs.custom(B, L, H, P, N, G, Q, seed=11 + L + H, x_dtype=io, ops=ops, **f)
+    assert _describe(inp, ops)[-1] == "ssd_fused_kernel"
+    y, fin = run_gpu(inp, ops=ops, plan="fused")
+    _full(oracle_mod, inp, y, fin, ops, f"fused N=128 {shape} {feat} {io}/{ops}")
+
+
+def test_fused128_walk_is_cut_into_segments():
+    """Few units: the plan runs the segment passes before the walk."""
+    _, inp = ssd_inputs.custom(1, 4096, 32, 64, 128, 1, 256, seed=3, ops="bf16")
+    assert _describe(inp, "bf16") == ["segment_state_kernel", "segment_fold_kernel", "ssd_fused_kernel"]
+
+
+def test_fused128_one_segment_many_units(oracle_mod):
+    """Units enough to fill the GPU: one segment per sequence (no passes), each
+    CTA walks several units in turn; initial state, D and z."""
+    _, inp = ssd_inputs.custom(4, 320, 128, 64, 128, 8, 256, seed=5, ops="bf16", x_dtype="bf16",
+                               D=True, z=True, h0=True)
+    assert _describe(inp, "bf16") == ["ssd_fused_kernel"]
+    y, fin = run_gpu(inp, ops="bf16", plan="fused")
+    _full(oracle_mod, inp, y, fin, "bf16", "fused N=128 one segment")
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_fused128_steep_decay(oracle_mod, io):
+    """Decay rates from gentle to steep (|d A| up to ~24 per token) across many
+    segments: segment decays far below fp32's range next to ones that barely
+    decay."""
+    _, inp = ssd_inputs.custom(1, 3000, 8, 64, 128, 2, 128, seed=83, ops="bf16", x_dtype=io,
+                               dt_dist=("uniform", -3.0, 3.0), A_dist=("neg_uniform", 0.25, 8.0),
+                               D=True, dt_bias=True, h0=True)
+    y, fin = run_gpu(inp, ops="bf16", plan="fused")
+    _full(oracle_mod, inp, y, fin, "bf16", f"fused N=128 steep decay {io}")
+
+
+def test_fused128_matches_chunked_plan_and_is_deterministic():
+    """The same inputs through both plans agree to the operand tolerance, and
+    two fused runs agree bit for bit."""
+    _, inp = ssd_inputs.custom(2, 2048, 16, 64, 128, 4, 128, seed=91, ops="f16", D=True, h0=True)
+    y1, f1 = run_gpu(inp, ops="f16", plan="fused")
+    y2, f2 = run_gpu(inp, ops="f16", plan="fused")
+    assert torch.equal(y1, y2) and torch.equal(f1, f2)
+    yc, fc = run_gpu(inp, ops="f16", plan="chunked")
+    d = (y1.double() - yc.double()).norm() / yc.double().norm()
+    assert float(d) < 5e-3
+
+
+def test_fused128_reports_no_device_error():
+    import mamba_ssd_chunked_fwd_gb300 as ssd
+    _, inp = ssd_inputs.custom(1, 4096, 32, 64, 128, 1, 256, seed=93, ops="bf16")
+    d = to_device(inp)
+    y = torch.empty_like(d["x"])
+    args = ssd.make_args(d["x"], d["dt"], d["A"], d["B"], d["C"], 256, y=y, dt_softplus=True, ops="bf16",
+                         plan="fused")
+    ws = torch.full((ssd.ssd_fwd_workspace_size(args),), 255, dtype=torch.uint8, device="cuda")
+    args.workspace, args.workspace_bytes = ws.data_ptr(), ws.numel()
+    ssd.ssd_fwd(args)
+    ssd.ssd_check_device_error(args)
+    assert torch.isfinite(y).all()

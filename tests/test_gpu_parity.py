@@ -396,7 +396,7 @@ def test_fused_plan_reports_no_device_error():
 
 def test_fused_plan_rejects_unsupported_shape():
     import mamba_ssd_chunked_fwd_gb300 as ssd
-    _, inp = ssd_inputs.custom(1, 128, 2, 64, 128, 1, 64, seed=79, ops="bf16")
+    _, inp = ssd_inputs.custom(1, 128, 2, 64, 96, 1, 64, seed=79, ops="bf16")  # N = 96
     with pytest.raises(ssd.SsdError) as ei:
         run_gpu(inp, ops="bf16", plan="fused")
     assert ei.value.status == 2

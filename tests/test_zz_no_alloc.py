@@ -21,6 +21,7 @@ CASES = [
     ((1, 200, 2, 64, 128, 1, 128), "f32", "f32", "chunked", "chunk_scan"),    # CUDA-core kernels, ragged tail
     ((2, 384, 8, 64, 128, 2, 128), "bf16", "f32", "chunked", "chunk_scan_tc"),  # tensor-core kernels
     ((2, 256, 8, 64, 64, 2, 64), "bf16", "bf16", "fused", "ssd_fused_kernel"),       # fused plan
+    ((1, 2048, 16, 64, 128, 1, 256), "bf16", "f32", "fused", "segment_state_kernel"),  # N = 128, segments
 ]
 
 
