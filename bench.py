@@ -707,6 +707,101 @@ def run_neighbor(args):
     print(json.dumps(line), flush=True)
 
 
+def run_conv_ssd(args):
+    """The causal conv1d + SiLU in front of the SSD (a Mamba-2 block's x, B, C
+    before their convolution, width 4 with bias): the forward that convolves in
+    its load stage, one ``ssd_fwd`` per step, against the two-kernel route
+    (token-major conv kernels for x, B and C into separate buffers, then the
+    forward on them) timed the same way on the same inputs.  Prints its own
+    JSON line; its value is the one-call forward."""
+    import mamba_ssd_chunked_fwd_gb300 as ssd
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    w = ssd_inputs.WORKLOADS[args.workload]
+    if args.batch:
+        w = w.with_(B=args.batch)
+    inp = ssd_inputs.make(w)
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    g = torch.Generator().manual_seed(23)
+    W = 4
+    cw = [(torch.randn((ch, W), generator=g) * 0.5).to(dev) for ch in (w.H * w.P, w.G * w.N, w.G * w.N)]
+    cb = [(torch.randn(ch, generator=g) * 0.2).to(dev) for ch in (w.H * w.P, w.G * w.N, w.G * w.N)]
+    conv = (cw[0], cb[0], cw[1], cb[1], cw[2], cb[2])
+    y = torch.empty_like(d["x"])
+    fin = torch.empty((w.B, w.H, w.P, w.N), device=dev) if w.return_final_state else None
+    ops = args.ops or w.ops
+
+    def make(x, Bm, Cm, conv_arg):
+        a = ssd.make_args(x, d["dt"], d["A"], Bm, Cm, w.chunk, y=y, final_state=fin, D=d["D"], z=d["z"],
+                          dt_bias=d["dt_bias"], initial_states=d["initial_states"], dt_softplus=w.dt_softplus,
+                          ops=ops, plan=args.plan, conv=conv_arg)
+        ws = torch.zeros(max(ssd.ssd_fwd_workspace_size(a), 256), dtype=torch.uint8, device=dev)
+        a.workspace, a.workspace_bytes = ws.data_ptr(), ws.numel()
+        return a, ws
+
+    fused_args, ws1 = make(d["x"], d["B"], d["C"], conv)
+    xc, Bc, Cc = torch.empty_like(d["x"]), torch.empty_like(d["B"]), torch.empty_like(d["C"])
+    plain_args, ws2 = make(xc, Bc, Cc, None)
+    sh = ssd._stream_handle(dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def fused_step():
+        ssd.ssd_fwd(fused_args, sh)
+
+    def two_kernel_step():
+        ssd.ssd_causal_conv1d_tokens(d["x"].view(w.B, w.L, -1), cw[0], cb[0], xc.view(w.B, w.L, -1), True, sh)
+        ssd.ssd_causal_conv1d_tokens(d["B"].view(w.B, w.L, -1), cw[1], cb[1], Bc.view(w.B, w.L, -1), True, sh)
+        ssd.ssd_causal_conv1d_tokens(d["C"].view(w.B, w.L, -1), cw[2], cb[2], Cc.view(w.B, w.L, -1), True, sh)
+        ssd.ssd_fwd(plain_args, sh)
+
+    def timed(step):
+        for _ in range(args.warmup):
+            step()
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        torch.cuda.synchronize(dev)
+        for i in range(args.steps):
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+        return [st.elapsed_time(en) for st, en in zip(starts, ends)]
+
+    with ClockSampler(dev.index, enabled=not args.no_clocks) as clk:
+        per_two = timed(two_kernel_step)
+        per_fused = timed(fused_step)
+        if not args.no_clocks:
+            extra_until = time.time() + 0.5
+            while time.time() < extra_until:
+                fused_step()
+            torch.cuda.synchronize(dev)
+    ms = sum(per_fused) / len(per_fused)
+    ms_two = sum(per_two) / len(per_two)
+    ab = algorithmic_bytes(w)
+    nbytes = ab["total"] + sum(t.numel() * 4 for t in cw + cb)
+    hbm, peak_kind = peaks()
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    kernels = ssd.ssd_fwd_describe(fused_args)
+    line = {
+        "metric": f"SSD fwd with the causal conv1d in front, tokens/s ({args.workload})",
+        "value": round(w.tokens / (ms * 1e-3), 1), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": ops, "data": "synthetic (seeded, pages' distributions; conv width 4)",
+        "config": {"workload": f"{args.workload} {w.shape_tuple()} [B,L,H,P,N,chunk,G] + conv1d W=4",
+                   "step_ms_quantiles": step_quantiles(per_fused),
+                   "two_kernel_ms": round(ms_two, 5), "two_kernel_quantiles": step_quantiles(per_two),
+                   "speedup_over_two_kernels": round(ms_two / ms, 3),
+                   "l2": f"inputs {(ab['x'] + ab['B'] + ab['C']) / 1e9:.2f} GB > 129 MB L2, no flush"},
+        "roofline": {"bound": "hbm", "kernel": kernels[-1], "achieved": round(achieved, 1), "peak": hbm,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": None,
+                     "alg_bytes_per_launch": nbytes, "launch_ms": round(ms, 5)},
+        "kernels": kernels,
+        "clocks": clk.summary(),
+        "gpu_launches": len(kernels) * args.steps,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def stage_timing(ssd, a, w, dev, sh, stream, args, kernels):
     """Time the four chunked-plan kernels one by one (events between launches)
     and return the dominant one with its algorithmic bytes, plus every stage's
@@ -891,12 +986,15 @@ def main():
     ap.add_argument("--no-clocks", action="store_true", help="skip the nvidia-smi clock sampler")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch size (a smaller case of the same shape)")
-    ap.add_argument("--path", choices=["forward", "decode", "varlen", "bwd", "conv1d", "rmsnorm", "norm"],
+    ap.add_argument("--path", choices=["forward", "decode", "varlen", "bwd", "conv1d", "rmsnorm", "norm",
+                                       "conv_ssd"],
                     default="forward",
                     help="forward (default): the whole SSD forward; decode: one decode step per "
                          "sequence from a carried state; varlen: the forward over packed sequences "
                          "of random lengths; bwd: the backward; conv1d, rmsnorm: the neighbours alone; "
-                         "norm: the forward with the gated RMSNorm of its output")
+                         "norm: the forward with the gated RMSNorm of its output; conv_ssd: the forward "
+                         "with the causal conv1d of x, B, C in front (in its load stage) against conv "
+                         "kernels plus the forward")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
@@ -919,6 +1017,9 @@ def main():
         return
     if args.path in ("conv1d", "rmsnorm"):
         run_neighbor(args)
+        return
+    if args.path == "conv_ssd":
+        run_conv_ssd(args)
         return
     run_gpu(args)
 

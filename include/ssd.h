@@ -40,7 +40,7 @@
 extern "C" {
 #endif
 
-#define SSD_ABI_VERSION 3
+#define SSD_ABI_VERSION 4
 
 /* Element types of the public tensors. */
 typedef enum { SSD_F32 = 0, SSD_F16 = 1, SSD_BF16 = 2 } ssd_dtype;
@@ -123,6 +123,23 @@ typedef struct ssd_fwd_args {
      * same arithmetic as a second kernel over y.  Not supported by ssd_bwd. */
     const float *norm_weight;
     float norm_eps;
+    /* Optional causal depthwise conv1d + SiLU in front of the SSD
+     * (ops-transformer MambaV2 article, sections 1.4 and 4.1: the step before
+     * chunk_cumsum in a Mamba-2 block).  When conv_width > 0, x, Bm and Cm hold
+     * the activations BEFORE the convolution and the SSD runs on
+     *   x'[b,t,c] = silu(conv_x_bias[c] + sum_{k<W} conv_x_weight[c,k] x[b,t-(W-1)+k,c])
+     * with x = 0 before t = 0, and likewise B' and C' with their own weights;
+     * c runs over the H*P (x) or G*N (B, C) channels of a token, W = conv_width
+     * (1..4).  Weights fp32 [channels, W] (all three required), biases fp32
+     * [channels] or NULL.  The fused plan at N = 64 convolves the tiles it
+     * stages, in the kernel; other plans convolve x, B and C into the
+     * workspace first (ssd_causal_conv1d_tokens), then run the SSD.  Not
+     * supported by ssd_fwd_host, ssd_fwd_varlen or ssd_bwd (SSD_ERR_UNSUPPORTED);
+     * x, B and C must be 16-byte aligned. */
+    const float *conv_x_weight, *conv_x_bias;
+    const float *conv_b_weight, *conv_b_bias;
+    const float *conv_c_weight, *conv_c_bias;
+    int32_t conv_width;
 } ssd_fwd_args;
 
 /* ABI version of the loaded library (SSD_ABI_VERSION). */
@@ -355,6 +372,15 @@ ssd_status ssd_state_fold(int64_t nseg, int64_t B, int64_t H, int64_t P, int64_t
  */
 ssd_status ssd_causal_conv1d(int64_t B, int64_t D, int64_t S, int64_t W, int32_t dtype, const void *x,
                              const float *w, const float *bias, int32_t silu, void *out, void *stream);
+
+/* The same convolution over token-major activations, the layout of a
+ * Mamba-2 block's x, B and C (and of ssd_fwd_args.conv_*):
+ *   out[b,t,c] = silu(bias[c] + sum_{k<W} w[c,k] x[b,t-(W-1)+k,c])  (SiLU if silu)
+ * x, out [B, S, C] (dtype, contiguous); w [C, W] fp32 (1 <= W <= 4); bias [C]
+ * fp32 or NULL; C % 4 == 0 and 16-byte aligned x and out.  out must not
+ * overlap x. */
+ssd_status ssd_causal_conv1d_tokens(int64_t B, int64_t S, int64_t C, int64_t W, int32_t dtype, const void *x,
+                                    const float *w, const float *bias, int32_t silu, void *out, void *stream);
 
 /* Gated grouped RMSNorm: v = x * silu(z), normalised by the root mean square
  * of v over each of `groups` runs of D/groups consecutive channels (eps inside

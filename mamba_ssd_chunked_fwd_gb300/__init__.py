@@ -68,6 +68,10 @@ class SsdFwdArgs(ctypes.Structure):
         ("dt_softplus", ctypes.c_int32), ("dt_min", ctypes.c_float), ("dt_max", ctypes.c_float),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
         ("norm_weight", ctypes.c_void_p), ("norm_eps", ctypes.c_float),
+        ("conv_x_weight", ctypes.c_void_p), ("conv_x_bias", ctypes.c_void_p),
+        ("conv_b_weight", ctypes.c_void_p), ("conv_b_bias", ctypes.c_void_p),
+        ("conv_c_weight", ctypes.c_void_p), ("conv_c_bias", ctypes.c_void_p),
+        ("conv_width", ctypes.c_int32),
     ]
 
 
@@ -121,6 +125,9 @@ _SIGS = {
     "ssd_causal_conv1d": [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
                           ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
                           ctypes.c_void_p],
+    "ssd_causal_conv1d_tokens": [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
+                                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
+                                 ctypes.c_void_p],
     "ssd_gated_rmsnorm": [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_float, ctypes.c_int32,
                           ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p],
     "ssd_fwd_varlen": [_P, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p],
@@ -175,8 +182,13 @@ def _stream_handle(device=None):
 def make_args(x, dt, A, B, C, chunk_size, *, y=None, final_state=None, D=None, z=None,
               dt_bias=None, initial_states=None, dt_softplus=False,
               dt_limit=(0.0, math.inf), ops=None, plan="auto", workspace=None, norm_weight=None,
-              norm_eps=1e-5) -> SsdFwdArgs:
-    """Fill an ``ssd_fwd_args`` from tensors (device or host; no copies)."""
+              norm_eps=1e-5, conv=None) -> SsdFwdArgs:
+    """Fill an ``ssd_fwd_args`` from tensors (device or host; no copies).
+
+    ``conv``: optional (x_weight, x_bias, B_weight, B_bias, C_weight, C_bias)
+    of the causal conv1d + SiLU in front of the SSD (weights [channels, W]
+    fp32, biases [channels] fp32 or None); x, B and C are then the
+    activations before the convolution."""
     Bb, L, H, P = x.shape
     G, N = B.shape[2], B.shape[3]
     io = _DTYPE_CODES.get(x.dtype)
@@ -200,6 +212,12 @@ def make_args(x, dt, A, B, C, chunk_size, *, y=None, final_state=None, D=None, z
     if workspace is not None:
         a.workspace, a.workspace_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
     a.norm_weight, a.norm_eps = _ptr(norm_weight), float(norm_eps)
+    if conv is not None:
+        wx, bx, wb, bb, wc, bc = conv
+        a.conv_x_weight, a.conv_x_bias = _ptr(wx), _ptr(bx)
+        a.conv_b_weight, a.conv_b_bias = _ptr(wb), _ptr(bb)
+        a.conv_c_weight, a.conv_c_bias = _ptr(wc), _ptr(bc)
+        a.conv_width = int(wx.shape[-1])
     return a
 
 
@@ -335,7 +353,8 @@ def ssd_state_fold(log_decay, states, out, stream=None):
 
 def mamba2_ssd_fwd(x, dt, A, B, C, chunk_size, dt_softplus=False, return_final_state=False, *,
                    D=None, z=None, dt_bias=None, dt_limit=(0.0, math.inf), initial_states=None,
-                   ops=None, plan="auto", workspace=None, out=None, norm_weight=None, norm_eps=1e-5):
+                   ops=None, plan="auto", workspace=None, out=None, norm_weight=None, norm_eps=1e-5,
+                   conv=None):
     """SSD forward on the GPU.  Returns ``out`` or ``(out, final_state)``.
 
     x [B,L,H,P], dt [B,L,H] fp32, A [H] fp32, B/C [B,L,G,N], D [H] fp32,
@@ -344,6 +363,10 @@ def mamba2_ssd_fwd(x, dt, A, B, C, chunk_size, dt_softplus=False, return_final_s
     ("f32" | "f16" | "bf16") is the operand precision of the contractions
     (default: that of x).  With ``norm_weight`` (fp32 [H*P], z required) the
     output is the gated RMSNorm of the SSD, groups of (H/G)*P channels.
+    With ``conv`` = (x_weight, x_bias, B_weight, B_bias, C_weight, C_bias)
+    (weights [channels, W] fp32, W <= 4; biases or None), x, B and C are the
+    activations before the causal conv1d + SiLU of a Mamba-2 block, which runs
+    in front of the SSD.
     Allocation of out, final_state and the workspace is done here with torch;
     all compute runs in libssd_gb300.so on the current stream.
     """
@@ -356,7 +379,7 @@ def mamba2_ssd_fwd(x, dt, A, B, C, chunk_size, dt_softplus=False, return_final_s
         fin = torch.empty((Bb, H, P, B.shape[3]), device=x.device, dtype=torch.float32)
     args = make_args(x, dt, A, B, C, chunk_size, y=y, final_state=fin, D=D, z=z, dt_bias=dt_bias,
                      initial_states=initial_states, dt_softplus=dt_softplus, dt_limit=dt_limit,
-                     ops=ops, plan=plan, norm_weight=norm_weight, norm_eps=norm_eps)
+                     ops=ops, plan=plan, norm_weight=norm_weight, norm_eps=norm_eps, conv=conv)
     if workspace is None:
         nbytes = ssd_fwd_workspace_size(args)
         workspace = torch.empty(max(nbytes, 256), device=x.device, dtype=torch.uint8)
@@ -492,6 +515,15 @@ def ssd_causal_conv1d(x, w, bias, out, silu=True, stream=None):
     s = stream if stream is not None else _stream_handle()
     _check(load_library().ssd_causal_conv1d(Bb, D, S, w.shape[1], _DTYPE_CODES[x.dtype], _ptr(x), _ptr(w),
                                             _ptr(bias), 1 if silu else 0, _ptr(out), s), "ssd_causal_conv1d")
+
+
+def ssd_causal_conv1d_tokens(x, w, bias, out, silu=True, stream=None):
+    """C entry: token-major x, out [B,S,C]; w [C,W] fp32; bias [C] fp32 or None."""
+    Bb, S, C = x.shape
+    s = stream if stream is not None else _stream_handle()
+    _check(load_library().ssd_causal_conv1d_tokens(Bb, S, C, w.shape[1], _DTYPE_CODES[x.dtype], _ptr(x), _ptr(w),
+                                                   _ptr(bias), 1 if silu else 0, _ptr(out), s),
+           "ssd_causal_conv1d_tokens")
 
 
 def ssd_gated_rmsnorm(x, z, w, groups, eps, out, stream=None):

@@ -78,6 +78,10 @@ constexpr int kMmaWarp = kComputeWarps;           // warp 16
 constexpr int kTmaWarp = kComputeWarps + 1;       // warp 17
 constexpr int kDecayWarp0 = kComputeWarps + 2;    // warps 18, 19
 constexpr int kThreads = kComputeThreads + 4 * 32;  // 640
+// the conv1d instantiation adds 4 warps that convolve the staged x, B, C tiles
+constexpr int kConvWarp0 = kComputeWarps + 4;     // warps 20-23
+constexpr int kConvWarps = 4;
+constexpr int kThreadsConv = kThreads + kConvWarps * 32;  // 768
 constexpr int kVecSlots = 3;
 constexpr uint64_t kWaitNs = 2000000000ull;       // an mbarrier wait gives up after 2 s
 constexpr uint32_t XC_BYTES = 24576;              // [X_h0 | 0 | X_h1], MN-major, 192 rows x 64 j
@@ -113,18 +117,26 @@ constexpr uint32_t NORM_ZBAR = NORM_BARS + 2 * 4 * 8;                    // z ti
 // that is the A operand of S C^T), and with fp32 I/O y is staged in the C
 // staging tile and Xcat has one buffer: the layout then fits in 227 KB.
 // NN = 64 keeps the layout the large training shape was tuned on.
-template <int NN, int IO>
+// The conv1d instantiation (CV, N = 64) adds POST: the convolved x, B, C of a
+// chunk in the operand dtype, laid out like 16-bit TMA staging tiles (x 2
+// boxes, B and C one each), which the compute warps read while the next
+// chunk's raw tiles land in the staging area; to make room its bf16 state copy
+// lives in TMEM and Xcat has one buffer.
+template <int NN, int IO, bool CV = false>
 struct Smem {
     static constexpr bool kStateTmem = NN == 128;
+    static constexpr bool kStateBfTmem = NN == 128 || CV;  // the bf16 copy of the state in TMEM
     static constexpr bool kAliasY = NN == 128 && IO == IO_F32;
-    static constexpr int kXcBufs = kAliasY ? 1 : 2;
+    static constexpr int kXcBufs = (kAliasY || CV) ? 1 : 2;
     static constexpr uint32_t CB2 = 0;
     static constexpr uint32_t BB = CB2 + 256 * NN;
     static constexpr uint32_t XT = BB + 128 * NN;
     static constexpr uint32_t XC = XT + 16384;
     static constexpr uint32_t MC = XC + kXcBufs * XC_BYTES;
-    static constexpr uint32_t S = MC + 16384;
-    static constexpr uint32_t STG_Y = S + (kStateTmem ? 0 : 256 * NN);
+    static constexpr uint32_t POST = MC + 16384;                 // x at POST, B at POST_B, C at POST_C
+    static constexpr uint32_t POST_B = POST + 2 * 8192, POST_C = POST_B + 8192;
+    static constexpr uint32_t S = POST + (CV ? 4 * 8192 : 0);
+    static constexpr uint32_t STG_Y = S + (kStateBfTmem ? 0 : 256 * NN);
     static constexpr uint32_t Y_BYTES = NN == 64 ? 32768 : kAliasY ? 0 : (IO == IO_F32 ? 32768 : 16384);
     static constexpr uint32_t STG_X = STG_Y + Y_BYTES;
     static constexpr uint32_t X_BYTES = NN == 64 ? 32768 : (IO == IO_F32 ? 32768 : 16384);
@@ -136,7 +148,8 @@ struct Smem {
     static constexpr uint32_t NORM = VEC + 3 * VEC_BYTES;
     static constexpr uint32_t BYTES = NORM + 1024;                    // + alignment slack
     static constexpr uint32_t BYTES_NORM = NORM + NORM_ZBAR + 16 + 1024;
-    static_assert(STG_X % 1024 == 0 && STG_B % 1024 == 0 && STG_C % 1024 == 0, "swizzled TMA boxes need 1 KB");
+    static_assert(STG_X % 1024 == 0 && STG_B % 1024 == 0 && STG_C % 1024 == 0 && POST % 1024 == 0,
+                  "swizzled TMA boxes need 1 KB");
     static_assert(NORM % 16 == 0 && BYTES_NORM + 512 <= 232448, "the layout fits in shared memory");
 };
 static_assert(Smem<64, IO_F32>::VEC == 221184 && Smem<64, IO_BF16>::STG_C == 204800, "N = 64 layout unchanged");
@@ -146,7 +159,7 @@ static_assert(Smem<64, IO_F32>::VEC == 221184 && Smem<64, IO_BF16>::STG_C == 204
 // accumulated onto the decayed state there), Yoff 192 / 256, Yint 320 / 384,
 // the bf16 state (A operand of S C^T, two values per column) 448-511.
 constexpr uint32_t TM_G = 0, TM_DS = 64, TM_COLS = 512;
-constexpr uint32_t TM_S32 = 64, TM_SBF = 448;
+constexpr uint32_t TM_S32 = 64, TM_SBF = 448;  // (the conv1d instantiation at N = 64 keeps its bf16 state at 448 too)
 template <int NN>
 __device__ __forceinline__ uint32_t tm_yoff(int buf) { return NN == 64 ? 128u + 128u * buf : 192u + 64u * buf; }
 template <int NN>
@@ -156,7 +169,7 @@ __device__ __forceinline__ uint32_t tm_yint(int buf) { return NN == 64 ? 192u + 
 enum {
     BAR_OPS_FULL = 0, BAR_MCAT_FULL, BAR_S_FULL, BAR_G_DONE, BAR_DS_DONE, BAR_Y_DONE0, BAR_Y_DONE1,
     BAR_STAGE_FULL, BAR_Y_STAGED, BAR_Y_FREE, BAR_VEC_FULL0, BAR_VEC_EMPTY0 = BAR_VEC_FULL0 + kVecSlots,
-    NBARS = BAR_VEC_EMPTY0 + kVecSlots
+    BAR_CONV_DONE = BAR_VEC_EMPTY0 + kVecSlots, BAR_STG_FREE, NBARS
 };
 
 // TMA descriptors of x [B,L,H*P] and B, C [B,L,G*N] as 3-D tensors
@@ -490,18 +503,29 @@ __device__ __forceinline__ void epilogue_norm(const Params &p, const Dims &dm, c
 // segment, group, head pair), the state entering a segment from the segment
 // passes, the final state from the last segment) with the state in TMEM; it
 // takes neither packed sequences nor the fused norm.
-template <int IO, bool BF16, bool VARLEN, int ZM, int NN = 64>
-__global__ void __launch_bounds__(kThreads, 1)
+// CV (N = 64, regular layout): x, B and C arrive before their causal conv1d +
+// SiLU (ops-transformer MambaV2 article, sections 1.4 and 4.1), and 4 more
+// warps convolve each staged tile in place before the compute warps read it.
+// A conv thread owns two channels for the whole walk of a unit, so the W-1
+// tokens before a chunk (the conv's halo) stay in its registers from the
+// previous chunk, and the taps too; a unit starts from zeros (no tokens before
+// t = 0).  The results are rounded to the staging tile's dtype.
+template <int IO, bool BF16, bool VARLEN, int ZM, int NN = 64, bool CV = false>
+__global__ void __launch_bounds__(CV ? kThreadsConv : kThreads, 1)
 ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMaps tm, int n_units,
                  unsigned int *err, int norm_cs) {
-    using L = Smem<NN, IO>;
+    using L = Smem<NN, IO, CV>;
     constexpr bool SEG = NN == 128;
     constexpr bool kAliasY = L::kAliasY;
     static_assert(NN == 64 || NN == 128, "state width 64 or 128");
     static_assert(NN == 64 || (!VARLEN && ZM < 2), "N = 128: no packed sequences, no fused norm");
+    static_assert(!CV || (NN == 64 && !VARLEN && ZM < 2), "the in-kernel conv1d: N = 64, regular layout, no norm");
     static_assert(!kAliasY || ZM == 0, "with y staged in the C tile there is no room for a z tile");
     constexpr int kGCols = 16;      // this thread's columns of each 64-column region (G, Yoff, Yint)
     constexpr int kSCols = NN / 4;  // this thread's state columns
+    // dtype of the tiles the operand stage reads: the staging tiles, or with the
+    // conv1d the convolved tiles in POST (in the operand dtype)
+    constexpr int SIO = CV ? (BF16 ? IO_BF16 : IO_F16) : IO;
     extern __shared__ unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t bars[NBARS];
     __shared__ uint32_t tmem_slot;
@@ -530,6 +554,8 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
             tc::mbar_init(bar(BAR_VEC_FULL0 + i), 2);
             tc::mbar_init(bar(BAR_VEC_EMPTY0 + i), kComputeWarps);
         }
+        tc::mbar_init(bar(BAR_CONV_DONE), kConvWarps);
+        tc::mbar_init(bar(BAR_STG_FREE), kConvWarps);
         if constexpr (ZM > 0) tc::mbar_init(sbase + L::NORM + NORM_ZBAR, 1);
         if constexpr (ZM == 2) {
             if (norm_cs > 1)
@@ -542,12 +568,12 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
         tc::tmem_relinquish();
     }
     // the zero block between the two heads' x tiles (MN groups 8..15), every buffer
-    for (int e = tid; e < L::kXcBufs * 8 * 8 * 8; e += kThreads) {
+    for (int e = tid; e < L::kXcBufs * 8 * 8 * 8; e += blockDim.x) {
         const int buf = e >> 9, jg = (e >> 6) & 7, mg = 8 + ((e >> 3) & 7), rr = e & 7;
         st_shared_v4(sbase + L::XC + buf * XC_BYTES + (jg * 24 + mg) * 128 + rr * 16, 0u, 0u, 0u, 0u);
     }
     // Mcat starts zero: the blocks above the diagonal that no warp writes stay so
-    for (int e = tid; e < 16384 / 16; e += kThreads) st_shared_v4(sbase + L::MC + 16 * e, 0u, 0u, 0u, 0u);
+    for (int e = tid; e < 16384 / 16; e += blockDim.x) st_shared_v4(sbase + L::MC + 16 * e, 0u, 0u, 0u, 0u);
     tc::fence_smem_to_async();
     tc::fence_before_sync();
     __syncthreads();
@@ -592,9 +618,14 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                             tc::mma_f16(tmem + TM_DS, tc::desc(sbase + L::XT + ks * 4096, 2048, 128),
                                         tc::desc(sbase + L::BB + ks * 256, 128, 1024), ID_MNMN, ks > 0);
 #pragma unroll
-                        for (int ks = 0; ks < NN / 16; ++ks)  // Yoff = S C^T, K = n
-                            tc::mma_f16(tmem + tm_yoff<NN>(buf), tc::desc(sbase + L::S + ks * 4096, 2048, 128),
-                                        tc::desc(sbase + L::CB2 + ks * 4096, 2048, 128), ID_KK, ks > 0);
+                        for (int ks = 0; ks < NN / 16; ++ks) {  // Yoff = S C^T, K = n
+                            if constexpr (L::kStateBfTmem)
+                                tc::mma_f16_ts(tmem + tm_yoff<NN>(buf), tmem + TM_SBF + ks * 8,
+                                               tc::desc(sbase + L::CB2 + ks * 4096, 2048, 128), ID_KK, ks > 0);
+                            else
+                                tc::mma_f16(tmem + tm_yoff<NN>(buf), tc::desc(sbase + L::S + ks * 4096, 2048, 128),
+                                            tc::desc(sbase + L::CB2 + ks * 4096, 2048, 128), ID_KK, ks > 0);
+                        }
                     } else {
 #pragma unroll
                         for (int ks = 0; ks < kQ / 16; ++ks)  // S += Xw^T B onto the decayed state, K = j
@@ -843,7 +874,9 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                     const int g = bg % dm.G, b = bg / dm.G;
                     const int h0 = g * dm.hpg + 2 * pair;
                     for (int k = 0; k < dm.nchunks; ++k, ++gk) {
-                        wait(BAR_OPS_FULL, gk & 1u);  // the compute warps are done with the staging area
+                        // the staging area is free: the compute warps (or, with the conv1d,
+                        // the conv warps) have read it
+                        wait(CV ? BAR_STG_FREE : BAR_OPS_FULL, gk & 1u);
                         if (k + 1 < dm.nchunks) stage(unit, k + 1);
                         else if (unit + (int)gridDim.x < n_units) stage(unit + gridDim.x, 0);
                         if (k > 0) {
@@ -858,6 +891,85 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
             }
         }
         __syncwarp();
+    } else if (CV && warp >= kConvWarp0) {
+        // ---------------- causal conv1d + SiLU, staging tile -> POST ----------------
+        // thread ct: x features 2ct, 2ct+1 of the pair (ct < 64), else B (ct < 96) or C
+        // features 2 (ct % 32), 2 (ct % 32) + 1 of the group.  A chunk is convolved as
+        // soon as its raw tiles land and the compute warps have read the previous
+        // chunk's POST; the staging area is then released to the TMA unit.
+        const int ct = (warp - kConvWarp0) * 32 + lane;
+        const int kind = ct < 64 ? 0 : ct < 96 ? 1 : 2;
+        const int f = kind == 0 ? 2 * ct : 2 * (ct & 31);
+        const uint32_t src = sbase + (kind == 0 ? L::STG_X : kind == 1 ? L::STG_B : L::STG_C);
+        const uint32_t dst = sbase + (kind == 0 ? L::POST : kind == 1 ? L::POST_B : L::POST_C);
+        const float *wsrc = kind == 0 ? p.conv_wx : kind == 1 ? p.conv_wb : p.conv_wc;
+        const float *bsrc = kind == 0 ? p.conv_bx : kind == 1 ? p.conv_bb : p.conv_bc;
+        constexpr int esz = IO == IO_F32 ? 4 : 2, bw = 128 / esz;  // features per 128-byte staging box
+        const uint32_t sbox = src + (f / bw) * BOX_BYTES;
+        const int sc16 = (f % bw) * esz / 16, swithin = (f % bw) * esz % 16;
+        const uint32_t dbox = dst + (f / 64) * BOX_BYTES;               // POST: 64 16-bit features per box
+        const int dc16 = (f % 64) / 8, dwithin = (f % 8) * 2;
+        const int W = p.conv_w;
+        uint32_t gc = 0;
+        for (int unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
+            const Span u = unit_span<false>(p, dm, unit);
+            const int cg = kind == 0 ? u.h0 * kP + f : u.g * NN + f;  // the channel in the public tensor
+            float w0[4], w1[4];  // taps right-aligned: slot 3 multiplies the current token
+#pragma unroll
+            for (int sl = 0; sl < 4; ++sl) {
+                const int k = sl - (4 - W);
+                w0[sl] = k >= 0 ? __ldg(wsrc + (size_t)cg * W + k) : 0.f;
+                w1[sl] = k >= 0 ? __ldg(wsrc + (size_t)(cg + 1) * W + k) : 0.f;
+            }
+            const float b0 = bsrc ? __ldg(bsrc + cg) : 0.f, b1 = bsrc ? __ldg(bsrc + cg + 1) : 0.f;
+            float h0[3] = {0.f, 0.f, 0.f}, h1[3] = {0.f, 0.f, 0.f};  // tokens t-3, t-2, t-1
+            for (int k = 0; k < u.nch; ++k, ++gc) {
+                wait(BAR_STAGE_FULL, gc & 1u);
+                if (gc > 0) wait(BAR_OPS_FULL, (gc - 1) & 1u);  // the compute warps have read POST
+                // 8 rows at a time: their loads first (independent), then the taps and
+                // SiLU of 8 rows, then 8 stores, so the latencies overlap
+                for (int r0 = 0; r0 < kQ; r0 += 8) {
+                    float v0[8], v1[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int r = r0 + i;
+                        const uint32_t sa = sbox + r * 128 + ((sc16 ^ (r & 7)) << 4) + swithin;
+                        if (IO == IO_F32) {
+                            asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v0[i]), "=f"(v1[i]) : "r"(sa));
+                        } else {
+                            uint32_t wv;
+                            asm volatile("ld.shared.b32 %0, [%1];" : "=r"(wv) : "r"(sa));
+                            float2 fv;
+                            if (IO == IO_BF16) fv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&wv));
+                            else fv = __half22float2(*reinterpret_cast<const __half2 *>(&wv));
+                            v0[i] = fv.x; v1[i] = fv.y;
+                        }
+                    }
+                    uint32_t out[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float o0 =
+                            fmaf(w0[3], v0[i], fmaf(w0[2], h0[2], fmaf(w0[1], h0[1], fmaf(w0[0], h0[0], b0))));
+                        const float o1 =
+                            fmaf(w1[3], v1[i], fmaf(w1[2], h1[2], fmaf(w1[1], h1[1], fmaf(w1[0], h1[0], b1))));
+                        h0[0] = h0[1]; h0[1] = h0[2]; h0[2] = v0[i];
+                        h1[0] = h1[1]; h1[1] = h1[2]; h1[2] = v1[i];
+                        out[i] = pack2(silu_fast(o0), silu_fast(o1), BF16);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int r = r0 + i;
+                        const uint32_t da = dbox + r * 128 + ((dc16 ^ (r & 7)) << 4) + dwithin;
+                        asm volatile("st.shared.b32 [%0], %1;" ::"r"(da), "r"(out[i]) : "memory");
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    tc::mbar_arrive(bar(BAR_CONV_DONE));
+                    tc::mbar_arrive(bar(BAR_STG_FREE));
+                }
+            }
+        }
     } else if (warp >= kDecayWarp0) {
         // ---------------- decay vectors, one head per warp ----------------
         const int hh = warp - kDecayWarp0;
@@ -921,6 +1033,32 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                 tc::mbar_arrive(bar(BAR_VEC_EMPTY0 + gp % kVecSlots));
             }
             ++yt;
+        };
+        // NN = 64: the bf16 copy of the state S (the A operand of Yoff = S C^T) into
+        // shared memory, or into TMEM in the conv1d instantiation; the caller arrives
+        // on S_FULL
+        auto publish_bf16_state = [&](const float (&Sv)[kSCols]) {
+            if constexpr (NN == 64) {
+                if constexpr (L::kStateBfTmem) {
+                    uint32_t r[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) r[i] = pack2(Sv[2 * i], Sv[2 * i + 1], BF16);
+                    tc::tmem_st8(tlane + TM_SBF + scol0 / 2, r);
+                    tc::tmem_wait_st();
+                    tc::fence_before_sync();
+                } else {
+#pragma unroll
+                    for (int q = 0; q < kSCols / 8; ++q) {
+                        float v[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) v[e] = Sv[8 * q + e];
+                        const int ng = (scol0 >> 3) + q;
+                        store8(sbase + L::S + (ng * 16 + (row >> 3)) * 128 + (row & 7) * 16, v, BF16);
+                    }
+                    tc::fence_smem_to_async();
+                }
+                __syncwarp();
+            }
         };
         // NN = 128: the state S (this thread's kSCols columns of row (head, p))
         // goes to TMEM twice before the products of a chunk: decayed by the
@@ -988,16 +1126,7 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                 }
             }
             if constexpr (NN == 64) {
-#pragma unroll
-                for (int q = 0; q < kSCols / 8; ++q) {
-                    float v[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) v[e] = S[8 * q + e];
-                    const int ng = (scol0 >> 3) + q;
-                    store8(sbase + L::S + (ng * 16 + (row >> 3)) * 128 + (row & 7) * 16, v, BF16);
-                }
-                tc::fence_smem_to_async();
-                __syncwarp();
+                publish_bf16_state(S);
                 // (a packed sequence without tokens has no chunk to consume this state)
                 if (lane == 0 && (!VARLEN || nch > 0)) tc::mbar_arrive(bar(BAR_S_FULL));
             }
@@ -1013,7 +1142,7 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                 }
 
                 // ---- A: operands of chunk k into shared memory ----
-                wait(BAR_STAGE_FULL, ph);
+                wait(CV ? BAR_CONV_DONE : BAR_STAGE_FULL, ph);  // with the conv1d: once it has run
                 // one Xcat buffer: the previous chunk's intra product has read it
                 if (L::kXcBufs == 1 && gk > 0) wait((gk - 1) & 1 ? BAR_Y_DONE1 : BAR_Y_DONE0, ((gk - 1) >> 1) & 1u);
                 {
@@ -1032,7 +1161,7 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                         const int h = c16 >> 3, po = c16 & 7;
                         const int mgc = h ? 16 + po : po;
                         float xv[8];
-                        stage_read8<IO>(sbase + L::STG_X, jg * 8 + jl, c16, xv);
+                        stage_read8<SIO>(sbase + (CV ? L::POST : L::STG_X), jg * 8 + jl, c16, xv);
                         store8(xc + (jg * 24 + mgc) * 128 + jl * 16, xv, BF16);
                         float xs[8];
 #pragma unroll
@@ -1044,8 +1173,8 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                         const int e = tid + kComputeThreads * it;
                         const int jl = e & 7, ng = (e >> 3) & (NN / 8 - 1), jg = e / NN;
                         float bv[8], cv[8];
-                        stage_read8<IO>(sbase + L::STG_B, jg * 8 + jl, ng, bv);
-                        stage_read8<IO>(sbase + L::STG_C, jg * 8 + jl, ng, cv);
+                        stage_read8<SIO>(sbase + (CV ? L::POST_B : L::STG_B), jg * 8 + jl, ng, bv);
+                        stage_read8<SIO>(sbase + (CV ? L::POST_C : L::STG_C), jg * 8 + jl, ng, cv);
                         store8(sbase + L::BB + (ng * 8 + jg) * 128 + jl * 16, bv, BF16);
                         store8(sbase + L::CB2 + (ng * 16 + jg) * 128 + jl * 16, cv, BF16);
                         store8(sbase + L::CB2 + (ng * 16 + jg + 8) * 128 + jl * 16, cv, BF16);
@@ -1110,16 +1239,7 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
 #pragma unroll
                     for (int n = 0; n < kSCols; ++n) S[n] = fmaf(a, S[n], ds[n]);
                     if (k + 1 < nch) {
-#pragma unroll
-                        for (int q = 0; q < kSCols / 8; ++q) {
-                            float v[8];
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) v[e] = S[8 * q + e];
-                            const int ng = (scol0 >> 3) + q;
-                            store8(sbase + L::S + (ng * 16 + (row >> 3)) * 128 + (row & 7) * 16, v, BF16);
-                        }
-                        tc::fence_smem_to_async();
-                        __syncwarp();
+                        publish_bf16_state(S);
                         if (lane == 0) tc::mbar_arrive(bar(BAR_S_FULL));
                     }
                 } else {
@@ -1241,17 +1361,23 @@ cudaError_t launch_typed(const Params &p, int units, unsigned int *err, cudaStre
     // z is staged by TMA through the y tile (ZM 1; with the norm, ZM 2),
     // except where y itself is staged in the C tile (fp32 I/O at N = 128):
     // the epilogue then loads z from global memory
+    // (the in-kernel conv1d, N = 64 only, has instantiations of its own with 4 more warps)
     const bool norm = NN == 64 && p.norm_w && !p.cu;
     const bool gated = p.z && !p.cu && !L::kAliasY;
+    const bool conv = NN == 64 && p.conv_w > 0 && !p.cu && !norm;
     auto kern = ssd_fused_kernel<IO, BF16, false, 0, NN>;
     if constexpr (NN == 64) {
         if (p.cu) kern = ssd_fused_kernel<IO, BF16, true, 0>;
+        else if (conv) kern = gated ? ssd_fused_kernel<IO, BF16, false, 1, 64, true>
+                                    : ssd_fused_kernel<IO, BF16, false, 0, 64, true>;
         else if (norm) kern = ssd_fused_kernel<IO, BF16, false, 2>;
         else if (gated) kern = ssd_fused_kernel<IO, BF16, false, 1>;
     } else if constexpr (!L::kAliasY) {
         if (gated) kern = ssd_fused_kernel<IO, BF16, false, 1, NN>;
     }
-    const uint32_t smem = gated ? L::BYTES_NORM : L::BYTES;
+    const int threads = conv ? kThreadsConv : kThreads;
+    using LC = Smem<64, IO, true>;  // (the conv1d instantiation exists at N = 64 only)
+    const uint32_t smem = conv ? (gated ? LC::BYTES_NORM : LC::BYTES) : gated ? L::BYTES_NORM : L::BYTES;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     TmaMaps tm;
@@ -1263,7 +1389,7 @@ cudaError_t launch_typed(const Params &p, int units, unsigned int *err, cudaStre
     // one CTA per SM: its shared memory and 512 TMEM columns fill the SM
     if (!norm) {
         const int grid = units < num_sms() ? units : num_sms();
-        kern<<<grid, kThreads, smem, s>>>(p, tm, units, err, 1);
+        kern<<<grid, threads, smem, s>>>(p, tm, units, err, 1);
         return cudaGetLastError();
     }
     // fused norm: the head pairs of a group run in one cluster of cs CTAs, in
@@ -1361,6 +1487,8 @@ bool fused_supported(const ssd_fwd_args *a) { return fused_unsupported_reason(a)
 
 bool fused_varlen_supported(const ssd_fwd_args *a) { return fused_supported(a) && a->N == 64; }
 
+bool fused_conv_supported(const ssd_fwd_args *a) { return fused_supported(a) && a->N == 64; }
+
 bool fused_norm_supported(const ssd_fwd_args *a) {
     return fused_supported(a) && a->N == 64 && a->z && (a->H / a->G) / 2 <= kNormMaxRanks;
 }
@@ -1393,6 +1521,10 @@ Params fused_params(const ssd_fwd_args *a) {
     p.dt_min = a->dt_min; p.dt_max = a->dt_max;
     p.norm_w = a->norm_weight;
     p.norm_eps = a->norm_eps;
+    p.conv_wx = a->conv_x_weight; p.conv_bx = a->conv_x_bias;
+    p.conv_wb = a->conv_b_weight; p.conv_bb = a->conv_b_bias;
+    p.conv_wc = a->conv_c_weight; p.conv_bc = a->conv_c_bias;
+    p.conv_w = a->conv_width;
     return p;
 }
 

@@ -6,7 +6,10 @@
 //   gated RMSNorm          v = x * silu(z);  out = v / sqrt(mean_group(v^2) + eps) * w
 //                          over `groups` runs of D/groups consecutive channels
 //
-// Both are HBM-bound elementwise-plus-reduction passes, fp32 arithmetic.
+// Both are HBM-bound elementwise-plus-reduction passes, fp32 arithmetic.  The
+// conv1d also exists for token-major activations ([B, S, C], the layout of a
+// Mamba-2 block's x, B and C), which the SSD forward uses when it runs the
+// convolution in front of itself outside the fused kernel.
 //   conv1d: one CTA per (1024-token tile, 4 channels, batch); each channel's
 //           tile and its W-1 token halo go through shared memory, loads and
 //           stores are coalesced along the sequence (16 bytes per thread when
@@ -210,7 +213,111 @@ gated_rmsnorm_multi_kernel(long long rows, int D, int groups, float eps, const v
     }
 }
 
+// 4 consecutive channels of one token row as floats (16 bytes fp32, 8 bytes 16-bit).
+template <int IO>
+__device__ __forceinline__ void load4(const void *base, size_t i, float (&v)[4]) {
+    if (IO == IO_F32) {
+        const float4 a = __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(base) + i));
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    } else {
+        const uint2 u = __ldg(reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(base) + i));
+        const uint32_t wd[2] = {u.x, u.y};
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            float2 f;
+            if (IO == IO_BF16) f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&wd[q]));
+            else f = __half22float2(*reinterpret_cast<const __half2 *>(&wd[q]));
+            v[2 * q] = f.x; v[2 * q + 1] = f.y;
+        }
+    }
+}
+
+template <int IO>
+__device__ __forceinline__ void store4(void *base, size_t i, const float (&v)[4]) {
+    if (IO == IO_F32) {
+        *reinterpret_cast<float4 *>(static_cast<float *>(base) + i) = make_float4(v[0], v[1], v[2], v[3]);
+    } else {
+        uint2 u;
+        if (IO == IO_BF16) {
+            __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]), b = __floats2bfloat162_rn(v[2], v[3]);
+            u.x = *reinterpret_cast<uint32_t *>(&a); u.y = *reinterpret_cast<uint32_t *>(&b);
+        } else {
+            __half2 a = __floats2half2_rn(v[0], v[1]), b = __floats2half2_rn(v[2], v[3]);
+            u.x = *reinterpret_cast<uint32_t *>(&a); u.y = *reinterpret_cast<uint32_t *>(&b);
+        }
+        *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(base) + i) = u;
+    }
+}
+
+// Token-major causal conv1d + SiLU, the layout of a Mamba-2 block's x, B and C:
+//   out[b,t,c] = silu(bias[c] + sum_{k<W} w[c,k] x[b,t-(W-1)+k,c]).
+// A thread owns 4 consecutive channels over kTokRun consecutive tokens: it
+// reads the 3 tokens before its run once and slides the window in registers.
+// A warp's 32 threads cover 128 channels of one token row, so every load and
+// store is coalesced.  Taps sit right-aligned in 4 slots (slot 3 = the current
+// token), so every register index is a constant.
+constexpr int kTokRun = 16;
+template <int IO>
+__global__ void __launch_bounds__(256)
+conv_tokens_kernel(int S, int C, int W, const void *x, const float *__restrict__ w, const float *__restrict__ bias,
+                   int silu, void *out) {
+    const int c = (blockIdx.x * 256 + threadIdx.x) * 4;
+    if (c >= C) return;
+    const int t0 = blockIdx.y * kTokRun;
+    const size_t row0 = (size_t)blockIdx.z * S;
+    float wk[4][4], bj[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+#pragma unroll
+        for (int sl = 0; sl < 4; ++sl) {
+            const int k = sl - (4 - W);
+            wk[sl][j] = k >= 0 ? __ldg(w + (size_t)(c + j) * W + k) : 0.f;
+        }
+        bj[j] = bias ? __ldg(bias + c + j) : 0.f;
+    }
+    float win[3][4];  // tokens t-3, t-2, t-1 of the current output token t
+#pragma unroll
+    for (int m = 0; m < 3; ++m) {
+        const int t = t0 - 3 + m;
+        if (t >= 0) load4<IO>(x, (row0 + t) * C + c, win[m]);
+        else win[m][0] = win[m][1] = win[m][2] = win[m][3] = 0.f;
+    }
+#pragma unroll 4
+    for (int i = 0; i < kTokRun; ++i) {
+        const int t = t0 + i;
+        if (t >= S) break;
+        float v[4], o[4];
+        load4<IO>(x, (row0 + t) * C + c, v);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            float a = bj[j];
+            a = fmaf(wk[0][j], win[0][j], a);
+            a = fmaf(wk[1][j], win[1][j], a);
+            a = fmaf(wk[2][j], win[2][j], a);
+            a = fmaf(wk[3][j], v[j], a);
+            o[j] = silu ? silu_fast(a) : a;
+            win[0][j] = win[1][j];
+            win[1][j] = win[2][j];
+            win[2][j] = v[j];
+        }
+        store4<IO>(out, (row0 + t) * C + c, o);
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_conv_tokens(int B, int S, int C, int W, int io, const void *x, const float *w, const float *bias,
+                               int silu, void *out, cudaStream_t s) {
+    if (C % 4 != 0 || W < 1 || W > 4) return cudaErrorInvalidValue;
+    const dim3 grid((unsigned)((C / 4 + 255) / 256), (unsigned)((S + kTokRun - 1) / kTokRun), (unsigned)B);
+    switch (io) {
+        case IO_F32: conv_tokens_kernel<IO_F32><<<grid, 256, 0, s>>>(S, C, W, x, w, bias, silu, out); break;
+        case IO_F16: conv_tokens_kernel<IO_F16><<<grid, 256, 0, s>>>(S, C, W, x, w, bias, silu, out); break;
+        case IO_BF16: conv_tokens_kernel<IO_BF16><<<grid, 256, 0, s>>>(S, C, W, x, w, bias, silu, out); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
 
 cudaError_t launch_causal_conv1d(int B, int D, int S, int W, int io, const void *x, const float *w,
                                  const float *bias, int silu, void *out, cudaStream_t s) {

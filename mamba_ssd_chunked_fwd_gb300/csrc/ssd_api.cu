@@ -73,6 +73,8 @@ ssd_status check_shape(const ssd_fwd_args *a) {
         return fail(SSD_ERR_INVALID_ARG, "unknown plan %d", a->plan);
     if (!(a->dt_min <= a->dt_max) || isnan(a->dt_min) || isnan(a->dt_max))
         return fail(SSD_ERR_INVALID_ARG, "dt_limit must satisfy dt_min <= dt_max");
+    if (a->conv_width < 0 || a->conv_width > 4)
+        return fail(SSD_ERR_UNSUPPORTED, "conv_width must be 0 (no convolution) or 1..4 (got %d)", a->conv_width);
     return SSD_OK;
 }
 
@@ -87,6 +89,19 @@ ssd_status check_pointers(const ssd_fwd_args *a, bool need_y) {
     if (a->norm_weight && !a->z) return fail(SSD_ERR_INVALID_ARG, "the gated RMSNorm (norm_weight) needs z");
     if (a->norm_weight && !(a->norm_eps >= 0.f && a->norm_eps < INFINITY))
         return fail(SSD_ERR_INVALID_ARG, "norm_eps must be finite and >= 0");
+    if (a->conv_width > 0) {
+        if (!a->conv_x_weight || !a->conv_b_weight || !a->conv_c_weight)
+            return fail(SSD_ERR_INVALID_ARG, "the conv1d (conv_width > 0) needs conv_x_weight, conv_b_weight and "
+                                             "conv_c_weight");
+        for (const void *ptr : {a->x, a->Bm, a->Cm})
+            if (!aligned(ptr, 16)) return fail(SSD_ERR_UNSUPPORTED, "the conv1d needs 16-byte aligned x, B and C");
+    }
+    return SSD_OK;
+}
+
+// Entry points that take no convolution in front of the SSD.
+ssd_status reject_conv(const ssd_fwd_args *a, const char *entry) {
+    if (a && a->conv_width != 0) return fail(SSD_ERR_UNSUPPORTED, "%s does not take the conv1d (conv_width)", entry);
     return SSD_OK;
 }
 
@@ -127,9 +142,35 @@ int32_t resolve_plan(const ssd_fwd_args *a) {
     return SSD_PLAN_CHUNKED;
 }
 
-size_t workspace_for(const ssd_fwd_args *a, int32_t plan) {
+size_t plan_workspace(const ssd_fwd_args *a, int32_t plan) {
     if (plan == SSD_PLAN_FUSED) return ssd::fused_workspace_size(a);
     return chunked_layout(a).total;
+}
+
+// The causal conv1d in front of the SSD runs inside the fused kernel (N = 64);
+// otherwise x, B and C are convolved into the workspace, after the plan's own
+// part, by three launches of the token-major conv kernel.
+bool conv_in_kernel(const ssd_fwd_args *a, int32_t plan) {
+    return a->conv_width > 0 && plan == SSD_PLAN_FUSED && ssd::fused_conv_supported(a);
+}
+
+struct ConvLayout {
+    size_t x, b, c, total;
+};
+
+ConvLayout conv_layout(const ssd_fwd_args *a, int32_t plan) {
+    const size_t io = io_size(a->x_dtype);
+    ConvLayout l;
+    l.x = align_up(plan_workspace(a, plan));
+    l.b = l.x + align_up((size_t)a->B * a->L * a->H * a->P * io);
+    l.c = l.b + align_up((size_t)a->B * a->L * a->G * a->N * io);
+    l.total = l.c + align_up((size_t)a->B * a->L * a->G * a->N * io);
+    return l;
+}
+
+size_t workspace_for(const ssd_fwd_args *a, int32_t plan) {
+    if (a->conv_width > 0 && !conv_in_kernel(a, plan)) return conv_layout(a, plan).total;
+    return plan_workspace(a, plan);
 }
 
 // Steps 2 and 4 run on the tensor cores when the operands are fp16 / bf16 and
@@ -178,7 +219,7 @@ ssd_status run_chunked(const ssd_fwd_args *a, cudaStream_t s) {
 // forward runs without its z gate and a second kernel normalises y in place
 // over `rows` tokens (the gate included).
 bool norm_in_kernel(const ssd_fwd_args *a, int32_t plan) {
-    return a->norm_weight && plan == SSD_PLAN_FUSED && ssd::fused_norm_supported(a);
+    return a->norm_weight && plan == SSD_PLAN_FUSED && ssd::fused_norm_supported(a) && a->conv_width == 0;
 }
 
 ssd_fwd_args without_norm(const ssd_fwd_args *a) {
@@ -286,6 +327,7 @@ ssd_status check_bwd(const ssd_bwd_args *b) {
     ssd_status st = check_shape(a);
     if (st != SSD_OK) return st;
     if (a->norm_weight) return fail(SSD_ERR_UNSUPPORTED, "the backward does not take the gated RMSNorm");
+    if ((st = reject_conv(a, "ssd_bwd")) != SSD_OK) return st;
     if (a->chunk > 64 || a->P > 64 || a->N > 64)
         return fail(SSD_ERR_UNSUPPORTED, "the backward needs chunk, P, N <= 64 (chunk=%lld P=%lld N=%lld)",
                     (long long)a->chunk, (long long)a->P, (long long)a->N);
@@ -349,15 +391,19 @@ ssd_status ssd_fwd_describe(const ssd_fwd_args *a, char *out, size_t cap) {
     if (st != SSD_OK) return st;
     if (!out || cap == 0) return fail(SSD_ERR_INVALID_ARG, "out buffer required");
     const char *norm = a->norm_weight && !norm_in_kernel(a, plan) ? ",gated_rmsnorm" : "";
+    const char *conv = a->conv_width > 0 && !conv_in_kernel(a, plan)
+                           ? "conv_tokens_kernel,conv_tokens_kernel,conv_tokens_kernel,"
+                           : "";
     if (plan == SSD_PLAN_FUSED) {
         const bool seg = ssd::fused_segments(a) > 1;
-        snprintf(out, cap, "%sssd_fused_kernel%s", seg ? "segment_state_kernel,segment_fold_kernel," : "", norm);
+        snprintf(out, cap, "%s%sssd_fused_kernel%s", conv, seg ? "segment_state_kernel,segment_fold_kernel," : "",
+                 norm);
         return ok();
     }
     const ssd::Params p = make_params(a);
     const bool tc_state = ssd::chunk_tc_state_supported(p, a->ops) && tc_ok(a);
     const bool tc_scan = ssd::chunk_tc_scan_supported(p, a->ops) && tc_ok(a);
-    snprintf(out, cap, "chunk_cumsum,%s,state_passing,%s%s", tc_state ? "chunk_state_tc" : "chunk_state",
+    snprintf(out, cap, "%schunk_cumsum,%s,state_passing,%s%s", conv, tc_state ? "chunk_state_tc" : "chunk_state",
              tc_scan ? "chunk_scan_tc" : "chunk_scan", norm);
     return ok();
 }
@@ -373,6 +419,25 @@ ssd_status ssd_fwd(const ssd_fwd_args *a, void *stream) {
                     a->workspace ? a->workspace_bytes : (size_t)0);
     if (!aligned(a->workspace, kAlign)) return fail(SSD_ERR_WORKSPACE, "workspace must be 256-byte aligned");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (a->conv_width > 0 && !conv_in_kernel(a, plan)) {  // convolve x, B, C into the workspace, then the SSD
+        const ConvLayout cl = conv_layout(a, plan);
+        char *ws = static_cast<char *>(a->workspace);
+        const int B = (int)a->B, L = (int)a->L, W = a->conv_width;
+        cudaError_t e;
+        if ((e = ssd::launch_conv_tokens(B, L, (int)(a->H * a->P), W, a->x_dtype, a->x, a->conv_x_weight,
+                                         a->conv_x_bias, 1, ws + cl.x, s)) != cudaSuccess ||
+            (e = ssd::launch_conv_tokens(B, L, (int)(a->G * a->N), W, a->x_dtype, a->Bm, a->conv_b_weight,
+                                         a->conv_b_bias, 1, ws + cl.b, s)) != cudaSuccess ||
+            (e = ssd::launch_conv_tokens(B, L, (int)(a->G * a->N), W, a->x_dtype, a->Cm, a->conv_c_weight,
+                                         a->conv_c_bias, 1, ws + cl.c, s)) != cudaSuccess)
+            return cuda_fail(e, "conv1d");
+        ssd_fwd_args o = *a;
+        o.x = ws + cl.x;
+        o.Bm = ws + cl.b;
+        o.Cm = ws + cl.c;
+        o.conv_width = 0;
+        return ssd_fwd(&o, stream);
+    }
     if (a->norm_weight && !norm_in_kernel(a, plan)) {  // the forward without its gate, then the norm
         const ssd_fwd_args o = without_norm(a);
         if (plan == SSD_PLAN_FUSED) {
@@ -393,7 +458,9 @@ ssd_status ssd_fwd(const ssd_fwd_args *a, void *stream) {
 
 ssd_status ssd_fwd_varlen_workspace_size(const ssd_fwd_args *a, const int64_t *cu, int64_t nseq, size_t *bytes) {
     int64_t mx = 0;
-    ssd_status st = check_varlen(a, cu, nseq, &mx);
+    ssd_status st = reject_conv(a, "ssd_fwd_varlen");
+    if (st != SSD_OK) return st;
+    st = check_varlen(a, cu, nseq, &mx);
     if (st != SSD_OK) return st;
     if (!bytes) return fail(SSD_ERR_INVALID_ARG, "bytes is NULL");
     *bytes = varlen_workspace(a, nseq, mx);
@@ -402,7 +469,9 @@ ssd_status ssd_fwd_varlen_workspace_size(const ssd_fwd_args *a, const int64_t *c
 
 ssd_status ssd_fwd_varlen(const ssd_fwd_args *a, const int64_t *cu, int64_t nseq, void *stream) {
     int64_t mx = 0;
-    ssd_status st = check_varlen(a, cu, nseq, &mx);
+    ssd_status st = reject_conv(a, "ssd_fwd_varlen");
+    if (st != SSD_OK) return st;
+    st = check_varlen(a, cu, nseq, &mx);
     if (st != SSD_OK) return st;
     if (a->norm_weight) {  // the packed forward without its gate, then the norm over every token
         if ((st = check_pointers(a, true)) != SSD_OK) return st;
@@ -496,6 +565,25 @@ ssd_status ssd_bwd(const ssd_bwd_args *b, void *stream) {
     w.partD = reinterpret_cast<float *>(ws + l.partD);
     w.partBias = reinterpret_cast<float *>(ws + l.partBias);
     if ((e = ssd::launch_bwd(p, a->x_dtype, w, s)) != cudaSuccess) return cuda_fail(e, "backward");
+    return ok();
+}
+
+ssd_status ssd_causal_conv1d_tokens(int64_t B, int64_t S, int64_t C, int64_t W, int32_t dtype, const void *x,
+                                    const float *w, const float *bias, int32_t silu, void *out, void *stream) {
+    if (B <= 0 || S <= 0 || C <= 0 || W <= 0)
+        return fail(SSD_ERR_INVALID_ARG, "B, S, C, W must be > 0 (B=%lld S=%lld C=%lld W=%lld)", (long long)B,
+                    (long long)S, (long long)C, (long long)W);
+    if (W > 4) return fail(SSD_ERR_UNSUPPORTED, "W must be <= 4 (got %lld)", (long long)W);
+    if (C % 4 != 0) return fail(SSD_ERR_UNSUPPORTED, "C must be a multiple of 4 (got %lld)", (long long)C);
+    if (B > 65535 || (S + 15) / 16 > 65535 || C > 0x7fffffffLL || B * S * C > 0x7fffffffffffLL)
+        return fail(SSD_ERR_UNSUPPORTED, "B <= 65535, S <= 1048560 and C < 2^31 required");
+    if (dtype != SSD_F32 && dtype != SSD_F16 && dtype != SSD_BF16)
+        return fail(SSD_ERR_INVALID_ARG, "unknown dtype code %d", dtype);
+    if (!x || !w || !out) return fail(SSD_ERR_INVALID_ARG, "x, w and out are required");
+    if (!aligned(x, 16) || !aligned(out, 16)) return fail(SSD_ERR_UNSUPPORTED, "x and out must be 16-byte aligned");
+    cudaError_t e = ssd::launch_conv_tokens((int)B, (int)S, (int)C, (int)W, dtype, x, w, bias, silu, out,
+                                            static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "causal_conv1d_tokens");
     return ok();
 }
 
@@ -715,7 +803,9 @@ int64_t host_slice_batch(const ssd_fwd_args *a) {
 
 ssd_status ssd_fwd_host_workspace_size(const ssd_fwd_args *a, size_t *bytes) {
     int32_t plan = 0;
-    ssd_status st = ssd_fwd_resolve_plan(a, &plan);
+    ssd_status st = reject_conv(a, "ssd_fwd_host");
+    if (st != SSD_OK) return st;
+    st = ssd_fwd_resolve_plan(a, &plan);
     if (st != SSD_OK) return st;
     if (!bytes) return fail(SSD_ERR_INVALID_ARG, "bytes is NULL");
     *bytes = host_layout(a, plan).total;
@@ -724,7 +814,9 @@ ssd_status ssd_fwd_host_workspace_size(const ssd_fwd_args *a, size_t *bytes) {
 
 ssd_status ssd_fwd_host(const ssd_fwd_args *a, void *stream) {
     int32_t plan = 0;
-    ssd_status st = ssd_fwd_resolve_plan(a, &plan);
+    ssd_status st = reject_conv(a, "ssd_fwd_host");
+    if (st != SSD_OK) return st;
+    st = ssd_fwd_resolve_plan(a, &plan);
     if (st != SSD_OK) return st;
     if ((st = check_pointers(a, true)) != SSD_OK) return st;
     const HostLayout l = host_layout(a, plan);

@@ -31,6 +31,8 @@ cudaError_t launch_segment_passes(const Params &p, int io, bool bf16, float *seg
 bool fused_supported(const ssd_fwd_args *a);
 // Packed sequences take the fused plan at N = 64 only.
 bool fused_varlen_supported(const ssd_fwd_args *a);
+// The causal conv1d in front of the SSD runs inside the fused kernel at N = 64.
+bool fused_conv_supported(const ssd_fwd_args *a);
 // Segments the fused walk cuts each sequence into (1 at N = 64).
 int fused_segments(const ssd_fwd_args *a);
 // The fused kernel can apply the gated RMSNorm in its store stage: z given and

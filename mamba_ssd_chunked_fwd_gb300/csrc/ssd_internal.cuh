@@ -43,6 +43,12 @@ struct Params {
     // [B, nseg, H, P, N] holds the state entering segment s >= 1
     int seg_len = 0, nseg = 1;
     const float *seg_states = nullptr;
+    // causal conv1d + SiLU of the staged x, B, C tiles (fused plan, N = 64):
+    // weights [channels, conv_w], biases [channels] or NULL; conv_w = 0: none
+    const float *conv_wx = nullptr, *conv_bx = nullptr;
+    const float *conv_wb = nullptr, *conv_bb = nullptr;
+    const float *conv_wc = nullptr, *conv_bc = nullptr;
+    int conv_w = 0;
 };
 
 enum IoType { IO_F32 = SSD_F32, IO_F16 = SSD_F16, IO_BF16 = SSD_BF16 };
@@ -145,6 +151,8 @@ cudaError_t launch_bwd(const Params &p, int io, const BwdBuffers &w, cudaStream_
 // The SSD's neighbours (neighbors.cu).
 cudaError_t launch_causal_conv1d(int B, int D, int S, int W, int io, const void *x, const float *w,
                                  const float *bias, int silu, void *out, cudaStream_t s);
+cudaError_t launch_conv_tokens(int B, int S, int C, int W, int io, const void *x, const float *w, const float *bias,
+                               int silu, void *out, cudaStream_t s);
 cudaError_t launch_gated_rmsnorm(long long rows, int D, int groups, float eps, int io, const void *x, const void *z,
                                  const float *w, void *out, cudaStream_t s);
 

@@ -24,7 +24,7 @@ def test_library_exports_every_declared_symbol():
     assert "ssd_fwd" in names and "ssd_chunk_scan" in names
     for name in names:
         assert hasattr(lib, name), f"missing export {name}"
-    assert lib.ssd_abi_version() == 3
+    assert lib.ssd_abi_version() == 4
 
 
 def test_status_strings():
@@ -247,3 +247,24 @@ def test_selftest_validation_without_a_gpu():
     assert lib.ssd_selftest_wait_timeout(ctypes.c_void_p(aligned + 4), 1000, 0, None) == 1
     assert lib.ssd_selftest_wait_timeout(ctypes.c_void_p(aligned), 0, 0, None) == 1
     assert lib.ssd_selftest_wait_timeout(ctypes.c_void_p(aligned), 2000000, 0, None) == 1
+
+
+def test_conv_arguments_are_validated_without_a_gpu():
+    """The conv1d in front of the SSD: width 0..4, the three weights required,
+    16-byte aligned x, B, C; the host-buffer, packed and backward entries do
+    not take it."""
+    import ctypes
+    lib = ssd.load_library()
+    a = _args()
+    a.conv_width = 5
+    assert lib.ssd_fwd(ctypes.byref(a), None) == 2
+    a.conv_width = 4
+    assert lib.ssd_fwd(ctypes.byref(a), None) == 1   # no weights
+    a.conv_x_weight = a.conv_b_weight = a.conv_c_weight = 1 << 20
+    size = ctypes.c_size_t(0)
+    assert lib.ssd_fwd_host_workspace_size(ctypes.byref(a), ctypes.byref(size)) == 2
+    assert lib.ssd_fwd_host(ctypes.byref(a), None) == 2
+    cu = (ctypes.c_int64 * 2)(0, a.L)
+    assert lib.ssd_fwd_varlen(ctypes.byref(a), cu, 1, None) == 2
+    assert lib.ssd_causal_conv1d_tokens(1, 8, 6, 4, 0, 1 << 20, 1 << 20, None, 1, 1 << 21, None) == 2  # C % 4
+    assert lib.ssd_causal_conv1d_tokens(1, 8, 8, 5, 0, 1 << 20, 1 << 20, None, 1, 1 << 21, None) == 2  # W > 4
