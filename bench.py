@@ -292,8 +292,9 @@ def run_gpu(args):
     stages = None
     if plan == ssd.SSD_PLAN_FUSED:
         kname, kbytes, kms = "ssd_fused_kernel", ab["total"], ms
-        launches_per_step = 1
-        scope = "one launch = the whole step"
+        launches_per_step = len(kernels)
+        scope = ("one launch = the whole step" if launches_per_step == 1 else
+                 f"whole step ({launches_per_step} launches: {', '.join(kernels)})")
     else:
         # several launches per step: the fraction is the path's algorithmic
         # bytes (public I/O only) over the whole step, the dominant stage named
@@ -304,7 +305,7 @@ def run_gpu(args):
     achieved = kbytes / (kms * 1e-3) / 1e9
     roofline = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1), "peak": hbm,
                 "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / hbm, 4),
-                "traffic": traffic_for(kname, args.workload) if plan == ssd.SSD_PLAN_FUSED else None,
+                "traffic": traffic_for(kname, args.workload) if launches_per_step == 1 else None,
                 "alg_bytes_per_launch": kbytes, "launch_ms": round(kms, 5), "scope": scope}
     path_roofline_ms = ab["total"] / (hbm * 1e9) * 1e3
 

@@ -302,6 +302,13 @@ __device__ __forceinline__ float ld_stage(uint32_t a) {
     }
 }
 
+// The z gate silu(z) of the staged-z epilogues: with a 16-bit y the one-MUFU
+// form (its error is below y's rounding), with fp32 y the two-MUFU form.
+template <int IO>
+__device__ __forceinline__ float gate(float z) {
+    return IO == IO_F32 ? silu_fast(z) : silu_tanh(z);
+}
+
 // y for one (head, p) and 8 consecutive tokens from tok_base, read from the
 // TMEM accumulators of buffer bp and written into the y staging tile (rows of
 // 128 bytes per box; the TMA store drops rows past L).  For packed sequences
@@ -336,14 +343,14 @@ __device__ __forceinline__ void epilogue8(const Params &p, const Dims &dm, const
         const uint32_t a0 = IO == IO_F32 ? ystage + (f >> 5) * BOX_BYTES + i0 * 128 + (f & 31) * 4
                                          : ystage + (f >> 6) * BOX_BYTES + i0 * 128 + (f & 63) * 2;
 #pragma unroll
-        for (int ii = 0; ii < 8; ++ii) v[ii] *= silu_fast(ld_stage<IO>(a0 + ii * 128));
+        for (int ii = 0; ii < 8; ++ii) v[ii] *= gate<IO>(ld_stage<IO>(a0 + ii * 128));
     } else if (p.z) {
         float zv[8];
 #pragma unroll
         for (int ii = 0; ii < 8; ++ii)
             zv[ii] = (tok_base + ii < len) ? ld_io<IO>(p.z, off0 + ii * step) : 0.f;
 #pragma unroll
-        for (int ii = 0; ii < 8; ++ii) v[ii] *= silu_fast(zv[ii]);
+        for (int ii = 0; ii < 8; ++ii) v[ii] *= gate<IO>(zv[ii]);
     }
     if (VARLEN && direct) {
 #pragma unroll
@@ -414,7 +421,7 @@ __device__ __forceinline__ void epilogue_norm(const Params &p, const Dims &dm, c
     }
     tc::fence_before_sync();  // (D x is in the intra-chunk product)
 #pragma unroll
-    for (int ii = 0; ii < 16; ++ii) v[ii] *= silu_fast(ld_stage<IO>(stage_addr(col0 + ii)));  // z staged where y goes
+    for (int ii = 0; ii < 16; ++ii) v[ii] *= gate<IO>(ld_stage<IO>(stage_addr(col0 + ii)));  // z staged where y goes
     // per-token sum of squares over the warp's 32 features: halve the token set
     // at each shuffle step; lane l ends with token tk(l) (bits 4..1 of l), l and
     // l ^ 1 holding the same sum
@@ -905,10 +912,12 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
         const float *wsrc = kind == 0 ? p.conv_wx : kind == 1 ? p.conv_wb : p.conv_wc;
         const float *bsrc = kind == 0 ? p.conv_bx : kind == 1 ? p.conv_bb : p.conv_bc;
         constexpr int esz = IO == IO_F32 ? 4 : 2, bw = 128 / esz;  // features per 128-byte staging box
-        const uint32_t sbox = src + (f / bw) * BOX_BYTES;
-        const int sc16 = (f % bw) * esz / 16, swithin = (f % bw) * esz % 16;
-        const uint32_t dbox = dst + (f / 64) * BOX_BYTES;               // POST: 64 16-bit features per box
-        const int dc16 = (f % 64) / 8, dwithin = (f % 8) * 2;
+        // row r's address: box + r 128 + ((c16 ^ (r % 8)) << 4) + within; rows go 8 at a
+        // time from a multiple of 8, so (c16 ^ i) << 4 = (c16 << 4) ^ (i << 4) with i a constant
+        const uint32_t sbox = src + (f / bw) * BOX_BYTES + (f % bw) * esz % 16;
+        const uint32_t sc16 = (uint32_t)((f % bw) * esz / 16) << 4;
+        const uint32_t dbox = dst + (f / 64) * BOX_BYTES + (f % 8) * 2;  // POST: 64 16-bit features per box
+        const uint32_t dc16 = (uint32_t)((f % 64) / 8) << 4;
         const int W = p.conv_w;
         uint32_t gc = 0;
         for (int unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
@@ -932,8 +941,7 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                     float v0[8], v1[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
-                        const int r = r0 + i;
-                        const uint32_t sa = sbox + r * 128 + ((sc16 ^ (r & 7)) << 4) + swithin;
+                        const uint32_t sa = sbox + (r0 + i) * 128 + (sc16 ^ (i << 4));
                         if (IO == IO_F32) {
                             asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v0[i]), "=f"(v1[i]) : "r"(sa));
                         } else {
@@ -954,12 +962,11 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                             fmaf(w1[3], v1[i], fmaf(w1[2], h1[2], fmaf(w1[1], h1[1], fmaf(w1[0], h1[0], b1))));
                         h0[0] = h0[1]; h0[1] = h0[2]; h0[2] = v0[i];
                         h1[0] = h1[1]; h1[1] = h1[2]; h1[2] = v1[i];
-                        out[i] = pack2(silu_fast(o0), silu_fast(o1), BF16);
+                        out[i] = pack2(silu_tanh(o0), silu_tanh(o1), BF16);
                     }
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
-                        const int r = r0 + i;
-                        const uint32_t da = dbox + r * 128 + ((dc16 ^ (r & 7)) << 4) + dwithin;
+                        const uint32_t da = dbox + (r0 + i) * 128 + (dc16 ^ (i << 4));
                         asm volatile("st.shared.b32 [%0], %1;" ::"r"(da), "r"(out[i]) : "memory");
                     }
                 }

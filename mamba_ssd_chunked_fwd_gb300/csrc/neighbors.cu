@@ -295,7 +295,8 @@ conv_tokens_kernel(int S, int C, int W, const void *x, const float *__restrict__
             a = fmaf(wk[1][j], win[1][j], a);
             a = fmaf(wk[2][j], win[2][j], a);
             a = fmaf(wk[3][j], v[j], a);
-            o[j] = silu ? silu_fast(a) : a;
+            // 16-bit outputs: the one-MUFU SiLU (its error is below the output's rounding)
+            o[j] = !silu ? a : IO == IO_F32 ? silu_fast(a) : silu_tanh(a);
             win[0][j] = win[1][j];
             win[1][j] = win[2][j];
             win[2][j] = v[j];

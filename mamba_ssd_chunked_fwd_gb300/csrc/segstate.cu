@@ -46,20 +46,25 @@ constexpr int kTmaWarp = kConvWarps, kMmaWarp = kConvWarps + 1;
 constexpr int kThreads = kConvThreads + 64;
 constexpr uint64_t kWaitNs = 2000000000ull;
 
-// shared memory (bytes from a 1024-aligned base): two staging stages of x
-// (128 features) and B (128 features), two operand buffers of Xw^T (MN-major,
-// 128 (h,p) x 64 j) and B (MN-major, 64 j x 128 n), then the weights w[2][seg_len]
+// shared memory (bytes from a 1024-aligned base): kStages staging stages of x
+// (128 features) and B (128 features) of one 64-token block, two operand
+// buffers of Xw^T (MN-major, 128 (h,p) x 64 j) and B (MN-major, 64 j x 128 n),
+// then the weights w[2][seg_len].  The CTA streams its segment, so the stages
+// in flight set its bandwidth: four with 16-bit tensors (32 KB each), two with
+// fp32 (64 KB each; a third does not fit beside the operands).
 template <int IO>
 struct PreSmem {
+    static constexpr int kStages = IO == IO_F32 ? 2 : 4;
     static constexpr uint32_t STG_BYTES = (IO == IO_F32 ? 4u : 2u) * BOX_BYTES;  // x or B of one block
     static constexpr uint32_t STG = 0;                          // stage i: x at STG + 2 i STG_BYTES, B after it
-    static constexpr uint32_t XT = 4 * STG_BYTES;               // operand buffer i at XT + i OP_BYTES
+    static constexpr uint32_t XT = 2 * kStages * STG_BYTES;     // operand buffer i at XT + i OP_BYTES
     static constexpr uint32_t OP_BYTES = 16384 + 16384;         // Xw^T, then B
     static constexpr uint32_t W = XT + 2 * OP_BYTES;
     static constexpr uint32_t bytes(int seg_len) { return W + 2u * seg_len * 4u + 1024u; }
 };
 
-enum { PB_FULL0 = 0, PB_EMPTY0 = 2, PB_OPS0 = 4, PB_DONE0 = 6, PB_N = 8 };
+constexpr int kMaxStages = 4;
+enum { PB_FULL0 = 0, PB_EMPTY0 = kMaxStages, PB_OPS0 = 2 * kMaxStages, PB_DONE0 = PB_OPS0 + 2, PB_N = PB_DONE0 + 2 };
 
 template <int IO, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -91,10 +96,13 @@ segment_state_kernel(const __grid_constant__ Params p, const __grid_constant__ S
         if (!timed_out && !tc::mbar_wait(bar(i), parity, kWaitNs)) timed_out = true;
     };
 
+    constexpr int NS = SM::kStages;
     if (tid == 0) {
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < NS; ++i) {
             tc::mbar_init(bar(PB_FULL0 + i), 1);
             tc::mbar_init(bar(PB_EMPTY0 + i), kConvWarps);
+        }
+        for (int i = 0; i < 2; ++i) {
             tc::mbar_init(bar(PB_OPS0 + i), kConvWarps);
             tc::mbar_init(bar(PB_DONE0 + i), 1);
         }
@@ -115,8 +123,8 @@ segment_state_kernel(const __grid_constant__ Params p, const __grid_constant__ S
             tc::prefetch_tensormap(&tm.x);
             tc::prefetch_tensormap(&tm.b);
             for (int j = 0; j < nblk; ++j) {
-                const int st = j & 1;
-                if (j >= 2) wait(PB_EMPTY0 + st, ((j - 2) >> 1) & 1u);
+                const int st = j % NS;
+                if (j >= NS) wait(PB_EMPTY0 + st, ((j - NS) / NS) & 1u);
                 const uint32_t xdst = sbase + SM::STG + 2 * st * SM::STG_BYTES, bdst = xdst + SM::STG_BYTES;
                 tc::mbar_arrive_expect_tx(bar(PB_FULL0 + st), 2 * SM::STG_BYTES);
 #pragma unroll
@@ -175,8 +183,8 @@ segment_state_kernel(const __grid_constant__ Params p, const __grid_constant__ S
 
         // ---- operands: block j of x (scaled by w) and B, from the staging ring ----
         for (int j = 0; j < nblk; ++j) {
-            const int st = j & 1, ob = j & 1;
-            wait(PB_FULL0 + st, (j >> 1) & 1u);
+            const int st = j % NS, ob = j & 1;
+            wait(PB_FULL0 + st, (j / NS) & 1u);
             if (j >= 2) wait(PB_DONE0 + ob, ((j - 2) >> 1) & 1u);  // the MMA of block j - 2 read this buffer
             const uint32_t xsrc = sbase + SM::STG + 2 * st * SM::STG_BYTES, bsrc = xsrc + SM::STG_BYTES;
             const uint32_t xt = sbase + SM::XT + ob * SM::OP_BYTES, bb = xt + 16384;
