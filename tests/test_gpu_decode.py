@@ -43,6 +43,8 @@ def _oracle_step(oracle_mod, one, state):
     (1, 2, 16, 128, 1),   # widest N
     (4, 8, 64, 64, 8),    # G = H
     (2, 4, 5, 7, 4),      # tiny odd dims
+    (8, 64, 64, 128, 8),  # the streaming kernel, N = 128, more half-blocks than CTAs
+    (2, 8, 64, 32, 4),    # the streaming kernel, N = 32
 ])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("feats", [False, True])
