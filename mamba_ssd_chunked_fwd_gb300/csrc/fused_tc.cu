@@ -193,6 +193,7 @@ using tcop::pack2;
 using tcop::st_shared_v4;
 using tcop::store8;
 using tcstage::BOX_BYTES;
+using tcstage::stage_raw16;
 using tcstage::stage_read8;
 
 // Shapes of one call, held in registers by every thread.
@@ -533,6 +534,9 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
     // dtype of the tiles the operand stage reads: the staging tiles, or with the
     // conv1d the convolved tiles in POST (in the operand dtype)
     constexpr int SIO = CV ? (BF16 ? IO_BF16 : IO_F16) : IO;
+    // those tiles hold the operand dtype already: x (unweighted), B and C are
+    // copied chunk by chunk, only the decay-weighted x is converted
+    constexpr bool kRaw = SIO != IO_F32 && ((SIO == IO_BF16) == BF16);
     extern __shared__ unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t bars[NBARS];
     __shared__ uint32_t tmem_slot;
@@ -1167,9 +1171,16 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                         const int jl = e & 7, c16 = (e >> 3) & 15, jg = e >> 7;
                         const int h = c16 >> 3, po = c16 & 7;
                         const int mgc = h ? 16 + po : po;
+                        const uint32_t xsrc = sbase + (CV ? L::POST : L::STG_X);
                         float xv[8];
-                        stage_read8<SIO>(sbase + (CV ? L::POST : L::STG_X), jg * 8 + jl, c16, xv);
-                        store8(xc + (jg * 24 + mgc) * 128 + jl * 16, xv, BF16);
+                        if constexpr (kRaw) {  // the staged chunk is the operand already
+                            const uint4 raw = stage_raw16(xsrc, jg * 8 + jl, c16);
+                            st_shared_v4(xc + (jg * 24 + mgc) * 128 + jl * 16, raw.x, raw.y, raw.z, raw.w);
+                            tcstage::unpack8(raw, BF16, xv);
+                        } else {
+                            stage_read8<SIO>(xsrc, jg * 8 + jl, c16, xv);
+                            store8(xc + (jg * 24 + mgc) * 128 + jl * 16, xv, BF16);
+                        }
                         float xs[8];
 #pragma unroll
                         for (int q = 0; q < 8; ++q) xs[q] = xv[q] * wv[it];
@@ -1179,12 +1190,24 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                     for (int it = 0; it < NN / 64; ++it) {
                         const int e = tid + kComputeThreads * it;
                         const int jl = e & 7, ng = (e >> 3) & (NN / 8 - 1), jg = e / NN;
-                        float bv[8], cv[8];
-                        stage_read8<SIO>(sbase + (CV ? L::POST_B : L::STG_B), jg * 8 + jl, ng, bv);
-                        stage_read8<SIO>(sbase + (CV ? L::POST_C : L::STG_C), jg * 8 + jl, ng, cv);
-                        store8(sbase + L::BB + (ng * 8 + jg) * 128 + jl * 16, bv, BF16);
-                        store8(sbase + L::CB2 + (ng * 16 + jg) * 128 + jl * 16, cv, BF16);
-                        store8(sbase + L::CB2 + (ng * 16 + jg + 8) * 128 + jl * 16, cv, BF16);
+                        const uint32_t bsrc = sbase + (CV ? L::POST_B : L::STG_B);
+                        const uint32_t csrc = sbase + (CV ? L::POST_C : L::STG_C);
+                        const uint32_t bdst = sbase + L::BB + (ng * 8 + jg) * 128 + jl * 16;
+                        const uint32_t cdst = sbase + L::CB2 + (ng * 16 + jg) * 128 + jl * 16;
+                        if constexpr (kRaw) {  // B and C move as they are
+                            const uint4 rb = stage_raw16(bsrc, jg * 8 + jl, ng);
+                            const uint4 rc = stage_raw16(csrc, jg * 8 + jl, ng);
+                            st_shared_v4(bdst, rb.x, rb.y, rb.z, rb.w);
+                            st_shared_v4(cdst, rc.x, rc.y, rc.z, rc.w);
+                            st_shared_v4(cdst + 8 * 128, rc.x, rc.y, rc.z, rc.w);
+                        } else {
+                            float bv[8], cv[8];
+                            stage_read8<SIO>(bsrc, jg * 8 + jl, ng, bv);
+                            stage_read8<SIO>(csrc, jg * 8 + jl, ng, cv);
+                            store8(bdst, bv, BF16);
+                            store8(cdst, cv, BF16);
+                            store8(cdst + 8 * 128, cv, BF16);
+                        }
                     }
                 }
                 tc::fence_smem_to_async();

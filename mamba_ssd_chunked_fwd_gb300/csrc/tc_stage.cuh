@@ -50,5 +50,11 @@ __device__ __forceinline__ void stage_read8(uint32_t base, int r, int c8, float 
     }
 }
 
+// The 16-byte chunk of 8 consecutive 16-bit features [8c8, 8c8+8) of token row
+// r, as stored (64 features per box).
+__device__ __forceinline__ uint4 stage_raw16(uint32_t base, int r, int c8) {
+    return tc::ld_shared_v4(swz(base + (c8 >> 3) * BOX_BYTES, r, c8 & 7));
+}
+
 }  // namespace tcstage
 }  // namespace ssd
