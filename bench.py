@@ -564,6 +564,30 @@ def run_norm(args):
     print(json.dumps(line), flush=True)
 
 
+def measured_fp32_gemm_tflops(dev, n=8192, reps=3):
+    """fp32 FMA throughput measured on this GPU: cuBLAS SGEMM with TF32 off
+    (torch.matmul at 'highest' precision), n^3 multiply-adds, best of ``reps``
+    CUDA-event timings after a warm-up."""
+    prev = torch.get_float32_matmul_precision()
+    torch.set_float32_matmul_precision("highest")
+    try:
+        a = torch.randn((n, n), device=dev)
+        b = torch.randn((n, n), device=dev)
+        torch.matmul(a, b)
+        torch.cuda.synchronize(dev)
+        best = math.inf
+        for _ in range(reps):
+            s0, e0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s0.record()
+            torch.matmul(a, b)
+            e0.record()
+            torch.cuda.synchronize(dev)
+            best = min(best, s0.elapsed_time(e0))
+        return 2.0 * n ** 3 / (best * 1e-3) / 1e12
+    finally:
+        torch.set_float32_matmul_precision(prev)
+
+
 def run_bwd(args):
     """Backward path: one ``ssd_bwd`` per step at the workload's shape (dy and
     dfinal seeded, all gradients written).  Prints its own JSON line; the
@@ -616,6 +640,7 @@ def run_bwd(args):
     flops = bwd_flops(w)
     tflops = flops / (ms * 1e-3) / 1e12
     alu = fp32_alu_peak_tflops()
+    sgemm = measured_fp32_gemm_tflops(dev)
     has_z = d["z"] is not None
     # recompute 3 (+ chunk_scan with z); the gate (skipped for fp32 dy without z); adjoint, passing,
     # chunk, 2 group sums, head sum
@@ -632,6 +657,8 @@ def run_bwd(args):
                      "peak_kind": "derived: 152 SMs x 128 fp32 lanes x 2 flops x max SM clock",
                      "unit": "TFLOP/s", "frac": round(tflops / alu, 4), "traffic": None,
                      "alg_flops_per_step": flops, "launch_ms": round(ms, 4),
+                     "measured_fp32": {"sgemm_tflops": round(sgemm, 2), "frac": round(tflops / sgemm, 4),
+                                       "how": "cuBLAS SGEMM 8192^3, TF32 off, best of 3, this run"},
                      "hbm_view": {"alg_bytes_per_step": nbytes,
                                   "achieved_gbs": round(nbytes / (ms * 1e-3) / 1e9, 1), "peak_gbs": hbm}},
         "clocks": clk.summary(),

@@ -316,46 +316,57 @@ __device__ __forceinline__ float gate(float z) {
 // (VARLEN) tokens count from t0 in batch row 0, the sequence ends at len, and
 // in its last chunk (`direct`) y goes straight to global memory for the
 // tokens inside the sequence, since the rows past its end belong to the next.
-template <int IO, bool VARLEN, int ZM = 0, int NN = 64, bool SEG = false>
-__device__ __forceinline__ void epilogue8(const Params &p, const Dims &dm, const ChunkVec &V, uint32_t tlane,
-                                          int bp, int col, int b, int h0, int my_h, int my_p, int tok_base,
-                                          uint32_t ystage, int t0, int len, bool direct) {
+// T = 16 reads both accumulators' 16 columns with one wait; T = 8 with two
+// loads and two waits, fewer registers live (same-process A/B: T = 16 is 2.3 %
+// faster at N = 128, 0.6 % slower at N = 64 with its register-resident state).
+template <int IO, bool VARLEN, int ZM = 0, int NN = 64, bool SEG = false, int T = 8>
+__device__ __forceinline__ void epilogue_tokens(const Params &p, const Dims &dm, const ChunkVec &V, uint32_t tlane,
+                                                int bp, int col, int b, int h0, int my_h, int my_p, int tok_base,
+                                                uint32_t ystage, int t0, int len, bool direct) {
+    static_assert(T == 8 || T == 16, "8 or 16 tokens col .. col + T - 1 of the chunk");
     if (!VARLEN && !SEG) {
         t0 = 0;
         len = dm.L;
     }
-    float yo[8], yi[8];
-    tc::tmem_ld8(tlane + tm_yoff<NN>(bp) + col, yo);
-    tc::tmem_ld8(tlane + tm_yint<NN>(bp) + col, yi);
+    float yo[T], yi[T];
+    if constexpr (T == 16) {
+        tc::tmem_ld16x2(tlane + tm_yoff<NN>(bp) + col, tlane + tm_yint<NN>(bp) + col, yo, yi);  // one wait
+    } else {
+        tc::tmem_ld8(tlane + tm_yoff<NN>(bp) + col, yo);
+        tc::tmem_ld8(tlane + tm_yint<NN>(bp) + col, yi);
+    }
     tc::fence_before_sync();
     const int i0 = tok_base % kQ;
-    const float4 e0 = *reinterpret_cast<const float4 *>(&V.ecs[my_h][i0]);
-    const float4 e1 = *reinterpret_cast<const float4 *>(&V.ecs[my_h][i0 + 4]);
-    const float ev[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
+    float ev[T];
+#pragma unroll
+    for (int q = 0; q < T / 4; ++q) {
+        const float4 e = *reinterpret_cast<const float4 *>(&V.ecs[my_h][i0 + 4 * q]);
+        ev[4 * q] = e.x; ev[4 * q + 1] = e.y; ev[4 * q + 2] = e.z; ev[4 * q + 3] = e.w;
+    }
     const int h = h0 + my_h;
     const size_t step = (size_t)dm.H * kP;
     const size_t off0 = (((size_t)b * dm.L + t0 + tok_base) * dm.H + h) * kP + my_p;
-    float v[8];
+    float v[T];
 #pragma unroll
-    for (int ii = 0; ii < 8; ++ii) v[ii] = fmaf(ev[ii], yo[ii], yi[ii]);
+    for (int ii = 0; ii < T; ++ii) v[ii] = fmaf(ev[ii], yo[ii], yi[ii]);
     // (D x is in the intra-chunk product)
     if constexpr (ZM > 0) {  // z staged where y goes
         const int f = my_h * kP + my_p;
         const uint32_t a0 = IO == IO_F32 ? ystage + (f >> 5) * BOX_BYTES + i0 * 128 + (f & 31) * 4
                                          : ystage + (f >> 6) * BOX_BYTES + i0 * 128 + (f & 63) * 2;
 #pragma unroll
-        for (int ii = 0; ii < 8; ++ii) v[ii] *= gate<IO>(ld_stage<IO>(a0 + ii * 128));
+        for (int ii = 0; ii < T; ++ii) v[ii] *= gate<IO>(ld_stage<IO>(a0 + ii * 128));
     } else if (p.z) {
-        float zv[8];
+        float zv[T];
 #pragma unroll
-        for (int ii = 0; ii < 8; ++ii)
+        for (int ii = 0; ii < T; ++ii)
             zv[ii] = (tok_base + ii < len) ? ld_io<IO>(p.z, off0 + ii * step) : 0.f;
 #pragma unroll
-        for (int ii = 0; ii < 8; ++ii) v[ii] *= gate<IO>(zv[ii]);
+        for (int ii = 0; ii < T; ++ii) v[ii] *= gate<IO>(zv[ii]);
     }
     if (VARLEN && direct) {
 #pragma unroll
-        for (int ii = 0; ii < 8; ++ii)
+        for (int ii = 0; ii < T; ++ii)
             if (tok_base + ii < len) st_io<IO>(p.y, off0 + ii * step, v[ii]);
         return;
     }
@@ -363,7 +374,7 @@ __device__ __forceinline__ void epilogue8(const Params &p, const Dims &dm, const
     const uint32_t a0 = IO == IO_F32 ? ystage + (f >> 5) * BOX_BYTES + i0 * 128 + (f & 31) * 4
                                      : ystage + (f >> 6) * BOX_BYTES + i0 * 128 + (f & 63) * 2;
 #pragma unroll
-    for (int ii = 0; ii < 8; ++ii) {
+    for (int ii = 0; ii < T; ++ii) {
         const uint32_t a = a0 + ii * 128;
         if (IO == IO_F32) {
             asm volatile("st.shared.f32 [%0], %1;" ::"r"(a), "f"(v[ii]));
@@ -389,7 +400,7 @@ struct NormCtx {
 };
 
 // NORM epilogue: y of this thread's feature for the 16 tokens col0 .. col0+15
-// of the chunk (as epilogue8 with z staged; D x is already in the intra-chunk
+// of the chunk (as epilogue_tokens with z staged; D x is already in the intra-chunk
 // product), then the gated RMSNorm of the
 // ops-transformer MambaV2 article, section 4.6: every token is divided by the
 // root mean square of its cs * 128 gated features (the group's heads) and
@@ -1031,12 +1042,16 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
             if constexpr (ZM == 2) {
                 epilogue_norm<IO>(p, dm, Vbuf[gp % kVecSlots], tlane, bp, col0, b, h0, my_h, my_p, kk * kQ + col0,
                                   sbase + L::STG_Y, nc, gp, wg, quarter, lane, norm_wf, timed_out);
+            } else if constexpr (NN == 128) {
+                epilogue_tokens<IO, VARLEN, ZM, NN, SEG, 16>(p, dm, Vbuf[gp % kVecSlots], tlane, bp, col0, b, h0,
+                                                             my_h, my_p, kk * kQ + col0, sbase + L::YSTAGE, t0, len,
+                                                             direct);
             } else {
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf)
-                    epilogue8<IO, VARLEN, ZM, NN, SEG>(p, dm, Vbuf[gp % kVecSlots], tlane, bp, col0 + 8 * hf, b, h0,
-                                                       my_h, my_p, kk * kQ + col0 + 8 * hf, sbase + L::YSTAGE, t0,
-                                                       len, direct);
+                    epilogue_tokens<IO, VARLEN, ZM, NN, SEG, 8>(p, dm, Vbuf[gp % kVecSlots], tlane, bp, col0 + 8 * hf,
+                                                                b, h0, my_h, my_p, kk * kQ + col0 + 8 * hf,
+                                                                sbase + L::YSTAGE, t0, len, direct);
             }
             __syncwarp();
             if (lane == 0) {
@@ -1231,11 +1246,21 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                     wait(BAR_G_DONE, ph);
                     tc::fence_after_sync();
                     const uint32_t mc = sbase + L::MC;
+                    // N = 128: the thread's 16 columns with one wait, and no mask on blocks that
+                    // lie wholly below the diagonal; N = 64 keeps two 8-column loads and the mask
+                    // (fewer registers live beside its register-resident state)
+                    float gall[kGCols];
+                    if constexpr (NN == 128) tc::tmem_ld16(tlane + TM_G + col0, gall);
+                    const int rows_lo = 32 * (quarter & 1);  // the warp's first row i
 #pragma unroll
                     for (int q = 0; q < kGCols / 8; ++q) {
                         const int j0 = col0 + 8 * q;
-                        float gv[8];
-                        tc::tmem_ld8(tlane + TM_G + j0, gv);
+                        if constexpr (NN == 64) {
+                            float g8[8];
+                            tc::tmem_ld8(tlane + TM_G + j0, g8);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) gall[8 * q + e] = g8[e];
+                        }
                         const float4 c0 = *reinterpret_cast<const float4 *>(&V.cs2[h][j0]);
                         const float4 c1 = *reinterpret_cast<const float4 *>(&V.cs2[h][j0 + 4]);
                         const float4 d0 = *reinterpret_cast<const float4 *>(&V.d[h][j0]);
@@ -1243,11 +1268,16 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                         const float cj[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
                         const float dj[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
                         float m[8];
+                        if (NN == 128 && j0 + 7 < rows_lo) {  // (warp-uniform) wholly below the diagonal
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const float v = gv[e] * ex2_approx(csi - cj[e]) * dj[e];
-                            m[e] = (j0 + e <= i) ? v : 0.f;
-                            m[e] += (j0 + e == i) ? diag_d : 0.f;
+                            for (int e = 0; e < 8; ++e) m[e] = gall[8 * q + e] * ex2_approx(csi - cj[e]) * dj[e];
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                const float v = gall[8 * q + e] * ex2_approx(csi - cj[e]) * dj[e];
+                                m[e] = (j0 + e <= i) ? v : 0.f;
+                                m[e] += (j0 + e == i) ? diag_d : 0.f;
+                            }
                         }
                         const int kg = 8 * h + (j0 >> 3);
                         store8(mc + (kg * 8 + (i >> 3)) * 128 + (i & 7) * 16, m, BF16);
