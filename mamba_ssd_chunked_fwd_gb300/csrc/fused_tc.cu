@@ -124,7 +124,6 @@ constexpr uint32_t NORM_ZBAR = NORM_BARS + 2 * 4 * 8;                    // z ti
 // lives in TMEM and Xcat has one buffer.
 template <int NN, int IO, bool CV = false>
 struct Smem {
-    static constexpr bool kStateTmem = NN == 128;
     static constexpr bool kStateBfTmem = NN == 128 || CV;  // the bf16 copy of the state in TMEM
     static constexpr bool kAliasY = NN == 128 && IO == IO_F32;
     static constexpr int kXcBufs = (kAliasY || CV) ? 1 : 2;
@@ -1135,8 +1134,12 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
             float S[kSCols];
             {
                 const float *src = nullptr;
-                if (SEG && seg > 0)
+                if (SEG && seg > 0) {
+                    // launched as a programmatic dependent of the fold: its states are
+                    // visible once the fold has completed (a no-op after the first time)
+                    tc::pdl_wait();
                     src = p.seg_states + ((((size_t)b * p.nseg + seg) * dm.H + h0 + my_h) * kP + my_p) * NN + scol0;
+                }
                 else if (p.h0)
                     src = p.h0 + (((size_t)sb * dm.H + h0 + my_h) * kP + my_p) * NN + scol0;
                 if (src) {
@@ -1449,6 +1452,24 @@ cudaError_t launch_typed(const Params &p, int units, unsigned int *err, cudaStre
     // one CTA per SM: its shared memory and 512 TMEM columns fill the SM
     if (!norm) {
         const int grid = units < num_sms() ? units : num_sms();
+        if (p.nseg > 1) {
+            // after the segment passes: a programmatic dependent launch, so that the
+            // walk's CTAs set up (and walk the first segment, which needs no passed
+            // state) while the fold finishes; they wait for it before reading states
+            cudaLaunchConfig_t cfg = {};
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[0].val.programmaticStreamSerializationAllowed = 1;
+            cfg.gridDim = dim3((unsigned)grid);
+            cfg.blockDim = dim3((unsigned)threads);
+            cfg.dynamicSmemBytes = smem;
+            cfg.stream = s;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            e = cudaLaunchKernelEx(&cfg, kern, p, tm, units, err, 1);
+            if (e != cudaSuccess) return e;
+            return cudaGetLastError();
+        }
         kern<<<grid, threads, smem, s>>>(p, tm, units, err, 1);
         return cudaGetLastError();
     }

@@ -115,6 +115,7 @@ segment_state_kernel(const __grid_constant__ Params p, const __grid_constant__ S
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
+    tc::pdl_launch_dependents();  // the fold may be scheduled once every pre-pass CTA is resident
     const uint32_t tmem = tmem_slot;
     constexpr int bw = IO == IO_F32 ? 32 : 64;  // features per 128-byte box
 
@@ -237,6 +238,8 @@ segment_state_kernel(const __grid_constant__ Params p, const __grid_constant__ S
 // S_in(s + 1) = exp(a_s) S_in(s) + E_s over s = 0 .. nseg - 2, in place
 __global__ void __launch_bounds__(256)
 segment_fold_kernel(const Params p, const float *__restrict__ seg_decay, float *seg_states) {
+    tc::pdl_launch_dependents();  // the walk may be scheduled; it waits for this grid before reading states
+    tc::pdl_wait();               // the pre-pass has completed
     const int bh = blockIdx.x, b = bh / p.H, h = bh % p.H;
     const int PN = kP * kNN;
     const int e = (blockIdx.y * 256 + threadIdx.x) * 4;
@@ -296,8 +299,19 @@ cudaError_t launch_segment_passes(const Params &p, int io, bool bf16, float *seg
                           : launch_pre<IO_BF16, false>(p, seg_states, seg_decay, err, s); break;
     }
     if (e != cudaSuccess) return e;
-    dim3 grid(p.B * p.H, (kP * kNN / 4 + 255) / 256);
-    segment_fold_kernel<<<grid, 256, 0, s>>>(p, seg_decay, seg_states);
+    // programmatic dependent launch: the fold starts as the pre-pass's last CTAs
+    // run and waits for it on the device (griddepcontrol.wait)
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(p.B * p.H, (kP * kNN / 4 + 255) / 256);
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, segment_fold_kernel, p, static_cast<const float *>(seg_decay), seg_states);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

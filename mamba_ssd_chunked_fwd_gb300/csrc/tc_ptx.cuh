@@ -115,6 +115,13 @@ __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.w
 // Wait until the committed bulk stores are complete.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// Programmatic dependent launch: let the next kernel on the stream (launched
+// with the programmatic-serialization attribute) start once every CTA of
+// this grid has issued this, and wait until the grids this one depends on
+// have completed with their memory visible (returns at once when there are none).
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Pull a TMA descriptor (a kernel parameter's generic address) into the
 // descriptor cache ahead of its first use.
 __device__ __forceinline__ void prefetch_tensormap(const void *map) {
