@@ -237,6 +237,16 @@ def run_gpu(args):
                       D=d["D"], z=d["z"], dt_bias=d["dt_bias"], initial_states=d["initial_states"],
                       dt_softplus=w.dt_softplus, ops=args.ops or w.ops, plan=args.plan)
     plan = ssd.ssd_fwd_resolve_plan(a)
+    fused_note = "taken"
+    if plan != ssd.SSD_PLAN_FUSED:  # why the one-kernel plan is not running, in the library's words
+        probe = ssd.make_args(d["x"], d["dt"], d["A"], d["B"], d["C"], w.chunk, y=y, final_state=fin, D=d["D"],
+                              z=d["z"], dt_bias=d["dt_bias"], initial_states=d["initial_states"],
+                              dt_softplus=w.dt_softplus, ops=args.ops or w.ops, plan="fused")
+        try:
+            ssd.ssd_fwd_resolve_plan(probe)
+            fused_note = "supported, not chosen" + (" (plan forced)" if args.plan != "auto" else "")
+        except ssd.SsdError as exc:
+            fused_note = "unavailable: " + exc.detail
     nws = ssd.ssd_fwd_workspace_size(a)
     ws = torch.zeros(max(nws, 256), dtype=torch.uint8, device=dev)
     a.workspace, a.workspace_bytes = ws.data_ptr(), nws
@@ -323,7 +333,7 @@ def run_gpu(args):
         "data": "synthetic (seeded, pages' distributions)",
         "config": {"workload": f"{args.workload} {w.shape_tuple()} [B,L,H,P,N,chunk,G]"
                                + (" (batch overridden)" if args.batch else ""),
-                   "plan": {1: "chunked", 2: "fused"}[plan], "ops_requested": ops_name,
+                   "plan": {1: "chunked", 2: "fused"}[plan], "fused_plan": fused_note, "ops_requested": ops_name,
                    "public_dtype": w.x_dtype, "tokens_per_step_per_gpu": w.tokens,
                    "l2": ("flushed between steps (256 MiB write)" if flush is not None
                           else f"inputs {in_bytes / 1e9:.2f} GB > 129 MB L2, no flush"),
@@ -407,9 +417,9 @@ def run_decode(args):
         "config": {"workload": f"decode, {args.workload} [B,H,P,N,G] = {[w.B, w.H, w.P, w.N, w.G]}",
                    "l2": "flushed before every timed step (256 MiB written, then read)",
                    "timing": "median of per-step events"},
-        "roofline": {"bound": "hbm", "kernel": "decode_step_kernel", "achieved": round(achieved, 1),
+        "roofline": {"bound": "hbm", "kernel": "decode_step_stream_kernel", "achieved": round(achieved, 1),
                      "peak": hbm, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / hbm, 4),
-                     "traffic": traffic_for("decode_step_kernel", args.workload),
+                     "traffic": traffic_for("decode_step_stream_kernel", args.workload),
                      "alg_bytes_per_launch": nbytes, "launch_ms": round(ms, 6)},
         "clocks": clk.summary(),
         "gpu_launches": args.steps,
@@ -588,6 +598,28 @@ def measured_fp32_gemm_tflops(dev, n=8192, reps=3):
         torch.set_float32_matmul_precision(prev)
 
 
+def measured_fp32_fma_tflops(dev, iters=32768, reps=5):
+    """fp32 CUDA-core throughput measured on this GPU: the library's
+    FMA-chain kernel (8 independent chains per thread, 8 CTAs of 256 threads
+    per SM), best of ``reps`` CUDA-event timings after a warm-up launch."""
+    import mamba_ssd_chunked_fwd_gb300 as ssd
+    grid = 8 * torch.cuda.get_device_properties(dev).multi_processor_count
+    out = torch.empty(grid * 256, device=dev)
+    sh = ssd._stream_handle(dev)
+    stream = torch.cuda.current_stream(dev)
+    ssd.ssd_selftest_fma_rate(out, iters, grid, sh)
+    torch.cuda.synchronize(dev)
+    best = math.inf
+    for _ in range(reps):
+        s0, e0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        ssd.ssd_selftest_fma_rate(out, iters, grid, sh)
+        e0.record(stream)
+        torch.cuda.synchronize(dev)
+        best = min(best, s0.elapsed_time(e0))
+    return 2.0 * 8 * iters * 256 * grid / (best * 1e-3) / 1e12
+
+
 def run_bwd(args):
     """Backward path: one ``ssd_bwd`` per step at the workload's shape (dy and
     dfinal seeded, all gradients written).  Prints its own JSON line; the
@@ -639,7 +671,8 @@ def run_bwd(args):
     hbm, _ = peaks()
     flops = bwd_flops(w)
     tflops = flops / (ms * 1e-3) / 1e12
-    alu = fp32_alu_peak_tflops()
+    derived = fp32_alu_peak_tflops()
+    alu = measured_fp32_fma_tflops(dev)
     sgemm = measured_fp32_gemm_tflops(dev)
     has_z = d["z"] is not None
     # recompute 3 (+ chunk_scan with z); the gate (skipped for fp32 dy without z); adjoint, passing,
@@ -654,8 +687,10 @@ def run_bwd(args):
                    "workspace_gb": round(nws / 1e9, 2)},
         "roofline": {"bound": "alu", "kernel": f"whole backward ({launches} launches, fp32 CUDA cores)",
                      "achieved": round(tflops, 3), "peak": round(alu, 1),
-                     "peak_kind": "derived: 152 SMs x 128 fp32 lanes x 2 flops x max SM clock",
+                     "peak_kind": "measured: fp32 FMA-chain kernel (ssd_selftest_fma_rate), best of 5, this run",
                      "unit": "TFLOP/s", "frac": round(tflops / alu, 4), "traffic": None,
+                     "derived_peak": {"tflops": round(derived, 1),
+                                      "how": "152 SMs x 128 fp32 lanes x 2 flops x max SM clock"},
                      "alg_flops_per_step": flops, "launch_ms": round(ms, 4),
                      "measured_fp32": {"sgemm_tflops": round(sgemm, 2), "frac": round(tflops / sgemm, 4),
                                        "how": "cuBLAS SGEMM 8192^3, TF32 off, best of 3, this run"},
@@ -877,7 +912,7 @@ def e2e_timing(ssd, inp, w, dev, args):
     a.workspace, a.workspace_bytes = ws.data_ptr(), nws
     sh = ssd._stream_handle(dev)
     stream = torch.cuda.current_stream(dev)
-    for _ in range(2):
+    for _ in range(max(3, args.warmup)):
         ssd.ssd_fwd_host(a, sh)
     torch.cuda.synchronize(dev)
     steps = max(3, args.steps)
@@ -895,6 +930,7 @@ def e2e_timing(ssd, inp, w, dev, args):
     d2h = y.numel() * y.element_size() + (fin.numel() * 4 if fin is not None else 0)
     return {"value": round(w.tokens / (ms * 1e-3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
             "steps": steps, "step_ms_quantiles": step_quantiles(per_step),
+            "slowest_step": {"index": max(range(steps), key=per_step.__getitem__), "ms": round(max(per_step), 4)},
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
 

@@ -405,6 +405,16 @@ ssd_status ssd_gated_rmsnorm(int64_t rows, int64_t D, int64_t groups, float eps,
  * this buffer.  Returns SSD_OK, SSD_ERR_INVALID_ARG or SSD_ERR_CUDA. */
 ssd_status ssd_selftest_wait_timeout(void *workspace, uint32_t timeout_us, int32_t arrive, void *stream);
 
+/* A measurement kernel, not part of the SSD: `grid` CTAs of 256 threads, each
+ * thread running 8 independent fp32 FMA chains of `iters` steps (a multiple
+ * of 8 in [8, 2^22]), 2 * 8 * iters * 256 * grid flops in all, and storing
+ * one float per thread into `out` (device, caller-owned, at least grid * 256
+ * floats; the values carry no meaning).  Timed with CUDA events on `stream`
+ * it gives the GPU's fp32 CUDA-core throughput, the peak against which the
+ * backward (fp32 on the CUDA cores) is reported.  Asynchronous; returns
+ * SSD_OK, SSD_ERR_INVALID_ARG (before anything is enqueued) or SSD_ERR_CUDA. */
+ssd_status ssd_selftest_fma_rate(float *out, int64_t out_count, int32_t iters, int32_t grid, void *stream);
+
 /* Synchronises `stream`, then reads the device error word the last ssd_fwd
  * on this workspace left behind (bounded waits that gave up set it).
  * Returns SSD_OK or SSD_ERR_TIMEOUT (or SSD_ERR_CUDA). */

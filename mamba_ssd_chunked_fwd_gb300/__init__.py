@@ -115,6 +115,7 @@ _SIGS = {
     "ssd_fwd_host": [_P, ctypes.c_void_p],
     "ssd_check_device_error": [_P, ctypes.c_void_p],
     "ssd_selftest_wait_timeout": [ctypes.c_void_p, ctypes.c_uint32, ctypes.c_int32, ctypes.c_void_p],
+    "ssd_selftest_fma_rate": [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p],
     "ssd_fwd_describe": [_P, ctypes.c_char_p, ctypes.c_size_t],
     "ssd_fwd_noalloc": [_P, ctypes.c_void_p],
     "ssd_decode_step": [ctypes.POINTER(SsdDecodeArgs), ctypes.c_void_p],
@@ -306,6 +307,17 @@ def ssd_selftest_wait_timeout(workspace, timeout_us: int, arrive: bool = False, 
         raise ValueError("the self-test needs a workspace of at least 256 bytes")
     _check(load_library().ssd_selftest_wait_timeout(_ptr(workspace), int(timeout_us), int(bool(arrive)), s),
            "ssd_selftest_wait_timeout")
+
+
+def ssd_selftest_fma_rate(out, iters: int, grid: int, stream=None):
+    """Launch the fp32 FMA-chain measurement kernel into ``out`` (a CUDA
+    float32 tensor of at least grid * 256 elements); 4096 * iters * grid
+    flops."""
+    s = stream if stream is not None else _stream_handle()
+    if out.dtype != torch.float32:
+        raise ValueError("out must be float32")
+    _check(load_library().ssd_selftest_fma_rate(_ptr(out), out.numel(), int(iters), int(grid), s),
+           "ssd_selftest_fma_rate")
 
 
 def _cu_host(cu_seqlens):

@@ -247,6 +247,11 @@ def test_selftest_validation_without_a_gpu():
     assert lib.ssd_selftest_wait_timeout(ctypes.c_void_p(aligned + 4), 1000, 0, None) == 1
     assert lib.ssd_selftest_wait_timeout(ctypes.c_void_p(aligned), 0, 0, None) == 1
     assert lib.ssd_selftest_wait_timeout(ctypes.c_void_p(aligned), 2000000, 0, None) == 1
+    # the FMA-rate kernel: null out, iters not a multiple of 8, grid out of range, out too small
+    assert lib.ssd_selftest_fma_rate(None, 256, 64, 1, None) == 1
+    assert lib.ssd_selftest_fma_rate(ctypes.c_void_p(aligned), 256, 60, 1, None) == 1
+    assert lib.ssd_selftest_fma_rate(ctypes.c_void_p(aligned), 256, 64, 0, None) == 1
+    assert lib.ssd_selftest_fma_rate(ctypes.c_void_p(aligned), 255, 64, 1, None) == 1
 
 
 def test_conv_arguments_are_validated_without_a_gpu():

@@ -84,6 +84,33 @@ def test_bwd_mid_size(oracle_mod):
     _compare(oracle_mod, inp, dy, dfinal, got, "f32", "bwd mid")
 
 
+def test_bwd_at_the_large_training_shape_on_sampled_groups(oracle_mod):
+    """The benched backward shape [1,4096,256,64,64,64,64] (the large training
+    shape at batch 1, same seeds as the bench): the GPU runs the whole
+    problem; the oracle runs three groups (first, one inside, last) with all
+    of their heads, which fixes every gradient of those heads and groups
+    exactly (heads interact only through the group sums of dB and dC)."""
+    w = ssd_inputs.WORKLOADS["large_training"].with_(B=1)
+    inp = ssd_inputs.make(w)
+    gen = torch.Generator().manual_seed(w.seed + 300)
+    dy = torch.randn(inp["x"].shape, generator=gen).to(inp["x"].dtype)
+    dfinal = torch.randn((w.B, w.H, w.P, w.N), generator=gen).float()
+    got = _gpu(inp, dy, dfinal, w.chunk)
+    hpg = w.H // w.G
+    groups = [0, 29, w.G - 1]
+    heads = [g * hpg + j for g in groups for j in range(hpg)]
+    sub = dict(inp, x=inp["x"][:, :, heads].contiguous(), dt=inp["dt"][:, :, heads].contiguous(),
+               A=inp["A"][heads].contiguous(), B=inp["B"][:, :, groups].contiguous(),
+               C=inp["C"][:, :, groups].contiguous())
+    ref = oracle_mod.backward(oracle_problem(oracle_mod, sub), dy[:, :, heads].contiguous(),
+                              dfinal[:, heads].contiguous())
+    picks = {"dx": (slice(None), slice(None), heads), "ddt": (slice(None), slice(None), heads),
+             "dA": (heads,), "dB": (slice(None), slice(None), groups), "dC": (slice(None), slice(None), groups),
+             "dh0": (slice(None), heads)}
+    for k, idx in picks.items():
+        assert_close(oracle_mod, got[k][idx], ref[k], "f32", f"bwd large_training b1 {k}")
+
+
 def test_bwd_is_deterministic():
     shape = (2, 256, 8, 64, 64, 2, 64)
     inp, dy, dfinal = _case(shape, seed=13)
