@@ -17,10 +17,12 @@
 // 64-token blocks) of bf16 / fp16 operands into an fp32 TMEM accumulator.
 // The decay weight of every token is an exclusive suffix sum of d A taken
 // backwards over the segment, so no large cumulative sums are subtracted.
-// Warps 0-7 convert the TMA-staged x and B tiles into operands (warps 0 and 1
-// first compute the weights of one head each), warp 8 issues the TMA copies
-// into a two-stage ring, warp 9 issues the MMAs; every handoff is an mbarrier
-// whose wait gives up after 2 s (recorded in the workspace error word).
+// Warps 0-7 first compute the weights (four warps per head, 16 consecutive
+// tokens per thread), then convert the TMA-staged x and B tiles into
+// operands; warp 8 issues the TMA copies into a ring of stages and prefetches
+// the blocks after the ring into L2; warp 9 issues the MMAs.  Every handoff is
+// an mbarrier whose wait gives up after 2 s (recorded in the workspace error
+// word).
 //
 // Fold, one thread per 4 state elements of one (b, h):
 //     S_in(0) = h0 (or 0),   S_in(s + 1) = exp(a_s) S_in(s) + E_s,
@@ -64,6 +66,9 @@ struct PreSmem {
 };
 
 constexpr int kMaxStages = 4;
+constexpr int kPrefetchAhead = 2;
+constexpr int kMaxSegLen = 2048;
+static_assert(kMaxSegLen <= 16 * (kConvThreads / 2), "the weights take at most 16 tokens per thread");  // blocks past the ring's last stage requested into L2
 enum { PB_FULL0 = 0, PB_EMPTY0 = kMaxStages, PB_OPS0 = 2 * kMaxStages, PB_DONE0 = PB_OPS0 + 2, PB_N = PB_DONE0 + 2 };
 
 template <int IO, bool BF16>
@@ -74,6 +79,7 @@ segment_state_kernel(const __grid_constant__ Params p, const __grid_constant__ S
     extern __shared__ unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t bars[PB_N];
     __shared__ uint32_t tmem_slot;
+    __shared__ float warp_total[kConvWarps];
     const uint32_t raw = tc::smem_addr(smem_raw);
     unsigned char *sm = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
     const uint32_t sbase = tc::smem_addr(sm);
@@ -123,9 +129,18 @@ segment_state_kernel(const __grid_constant__ Params p, const __grid_constant__ S
         if (lane == 0) {
             tc::prefetch_tensormap(&tm.x);
             tc::prefetch_tensormap(&tm.b);
+            auto prefetch = [&](int j) {  // block j into L2 only
+#pragma unroll
+                for (int bx = 0; bx < 128 / bw; ++bx) {
+                    tc::tma_prefetch_3d(&tm.x, h0 * kP + bx * bw, t0 + 64 * j, b);
+                    tc::tma_prefetch_3d(&tm.b, g * kNN + bx * bw, t0 + 64 * j, b);
+                }
+            };
+            for (int j = NS; j < NS + kPrefetchAhead && j < nblk; ++j) prefetch(j);
             for (int j = 0; j < nblk; ++j) {
                 const int st = j % NS;
                 if (j >= NS) wait(PB_EMPTY0 + st, ((j - NS) / NS) & 1u);
+                if (j + NS + kPrefetchAhead < nblk) prefetch(j + NS + kPrefetchAhead);
                 const uint32_t xdst = sbase + SM::STG + 2 * st * SM::STG_BYTES, bdst = xdst + SM::STG_BYTES;
                 tc::mbar_arrive_expect_tx(bar(PB_FULL0 + st), 2 * SM::STG_BYTES);
 #pragma unroll
@@ -153,32 +168,52 @@ segment_state_kernel(const __grid_constant__ Params p, const __grid_constant__ S
         }
         __syncwarp();
     } else {
-        // ---- weights: the segment's processed steps d (all loads in flight at
-        // once), then one head per warp, backwards over the segment ----
-        for (int e = tid; e < 2 * p.seg_len; e += kConvThreads) {
-            const int hh = e / p.seg_len, t = t0 + e % p.seg_len;
-            w_s[e] = dt_processed(p, __ldg(p.dt + ((size_t)b * p.L + t) * p.H + h0 + hh), h0 + hh);
-        }
-        tc::named_barrier(1, kConvThreads);
-        if (warp < 2) {
-            const int h = h0 + warp;
-            const float A = __ldg(p.A + h);
-            float carry = 0.f;  // sum of d A over the tokens after the current 32-token block
-            for (int blk = p.seg_len / 32 - 1; blk >= 0; --blk) {
-                const float d = w_s[warp * p.seg_len + 32 * blk + lane];
-                const float v = d * A;
-                float incl = v;  // sum over this lane and the lanes after it
+        // ---- weights: w_t = exp(sum of d A over the segment's tokens after t) d_t.
+        // Threads 128 hh .. 128 hh + 127 take head h0 + hh, 16 consecutive tokens
+        // each (every load issued before the first use); the suffix sums run
+        // within the thread, then over the later lanes of its warp, then over
+        // the later warps of its head, each in a fixed order ----
+        {
+            const int hh = tid >> 7, i = tid & 127, h = h0 + hh;
+            const int per = (p.seg_len + 127) >> 7;  // tokens per thread, at most 16
+            const int tb = i * per;
+            float dv[16], ex[16];
 #pragma unroll
-                for (int off = 1; off < 32; off <<= 1) {
-                    const float o = __shfl_down_sync(0xffffffffu, incl, off);
-                    if (lane + off < 32) incl += o;
-                }
-                float excl = __shfl_down_sync(0xffffffffu, incl, 1);
-                if (lane == 31) excl = 0.f;
-                w_s[warp * p.seg_len + 32 * blk + lane] = expf(carry + excl) * d;
-                carry += __shfl_sync(0xffffffffu, incl, 0);
+            for (int m = 0; m < 16; ++m) {
+                const int t = tb + m;
+                dv[m] = (m < per && t < p.seg_len) ? __ldg(p.dt + ((size_t)b * p.L + t0 + t) * p.H + h) : 0.f;
             }
-            if (lane == 0) seg_decay[((size_t)b * p.H + h) * p.nseg + s] = carry;
+            const float A = __ldg(p.A + h);
+            float run = 0.f;  // sum of d A over this thread's tokens after token m
+#pragma unroll
+            for (int m = 15; m >= 0; --m) {
+                const bool ok = m < per && tb + m < p.seg_len;
+                const float d = ok ? dt_processed(p, dv[m], h) : 0.f;
+                dv[m] = d;
+                ex[m] = run;
+                run += d * A;
+            }
+            float incl = run;  // over this lane and the later lanes of the warp
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float o = __shfl_down_sync(0xffffffffu, incl, off);
+                if (lane + off < 32) incl += o;
+            }
+            float excl = __shfl_down_sync(0xffffffffu, incl, 1);
+            if (lane == 31) excl = 0.f;
+            if (lane == 0) warp_total[warp] = incl;
+            tc::named_barrier(1, kConvThreads);
+            float later = 0.f;  // the later warps of this head, from the segment's end backwards
+            for (int q = 4 * hh + 3; q > warp; --q) later += warp_total[q];
+            const float base = later + excl;
+#pragma unroll
+            for (int m = 0; m < 16; ++m)
+                if (m < per && tb + m < p.seg_len) w_s[hh * p.seg_len + tb + m] = expf(ex[m] + base) * dv[m];
+            if (i == 0) {
+                float total = 0.f;
+                for (int q = 4 * hh + 3; q >= 4 * hh; --q) total += warp_total[q];
+                seg_decay[((size_t)b * p.H + h) * p.nseg + s] = total;
+            }
         }
         tc::named_barrier(1, kConvThreads);
 
@@ -279,7 +314,7 @@ cudaError_t launch_pre(const Params &p, float *seg_states, float *seg_decay, uns
 
 }  // namespace
 
-int segment_max_len() { return 2048; }
+int segment_max_len() { return kMaxSegLen; }
 
 bool segment_smem_fits(int io, int seg_len) {
     const uint32_t need = io == IO_F32 ? PreSmem<IO_F32>::bytes(seg_len) : PreSmem<IO_BF16>::bytes(seg_len);
