@@ -17,10 +17,11 @@
 // 64-token blocks) of bf16 / fp16 operands into an fp32 TMEM accumulator.
 // The decay weight of every token is an exclusive suffix sum of d A taken
 // backwards over the segment, so no large cumulative sums are subtracted.
-// Warps 0-7 first compute the weights (four warps per head, 16 consecutive
+// Warps 0-15 first compute the weights (eight warps per head, 8 consecutive
 // tokens per thread), then convert the TMA-staged x and B tiles into
-// operands; warp 8 issues the TMA copies into a ring of stages and prefetches
-// the blocks after the ring into L2; warp 9 issues the MMAs.  Every handoff is
+// operands (B moves as it is when it already has the operand type); warp 16
+// issues the TMA copies into a ring of stages and prefetches the blocks after
+// the ring into L2; warp 17 issues the MMAs.  Every handoff is
 // an mbarrier whose wait gives up after 2 s (recorded in the workspace error
 // word).
 //
@@ -37,12 +38,13 @@ namespace ssd {
 
 namespace {
 
+using tcop::st_shared_v4;
 using tcop::store8;
 using tcstage::BOX_BYTES;
 using tcstage::stage_read8;
 
 constexpr int kNN = 128, kP = 64;
-constexpr int kConvWarps = 8;
+constexpr int kConvWarps = 16;
 constexpr int kConvThreads = kConvWarps * 32;
 constexpr int kTmaWarp = kConvWarps, kMmaWarp = kConvWarps + 1;
 constexpr int kThreads = kConvThreads + 64;
@@ -68,7 +70,9 @@ struct PreSmem {
 constexpr int kMaxStages = 4;
 constexpr int kPrefetchAhead = 2;
 constexpr int kMaxSegLen = 2048;
-static_assert(kMaxSegLen <= 16 * (kConvThreads / 2), "the weights take at most 16 tokens per thread");  // blocks past the ring's last stage requested into L2
+constexpr int kHeadThreads = kConvThreads / 2;  // weight threads per head
+constexpr int kTokPerThread = kMaxSegLen / kHeadThreads;
+static_assert(kMaxSegLen % kHeadThreads == 0, "whole tokens per weight thread");  // blocks past the ring's last stage requested into L2
 enum { PB_FULL0 = 0, PB_EMPTY0 = kMaxStages, PB_OPS0 = 2 * kMaxStages, PB_DONE0 = PB_OPS0 + 2, PB_N = PB_DONE0 + 2 };
 
 template <int IO, bool BF16>
@@ -169,24 +173,26 @@ segment_state_kernel(const __grid_constant__ Params p, const __grid_constant__ S
         __syncwarp();
     } else {
         // ---- weights: w_t = exp(sum of d A over the segment's tokens after t) d_t.
-        // Threads 128 hh .. 128 hh + 127 take head h0 + hh, 16 consecutive tokens
-        // each (every load issued before the first use); the suffix sums run
-        // within the thread, then over the later lanes of its warp, then over
-        // the later warps of its head, each in a fixed order ----
+        // The first kHeadThreads threads take head h0, the rest h0 + 1, up to
+        // kTokPerThread consecutive tokens each (every load issued before the
+        // first use); the suffix sums run within the thread, then over the later
+        // lanes of its warp, then over the later warps of its head, each in a
+        // fixed order ----
         {
-            const int hh = tid >> 7, i = tid & 127, h = h0 + hh;
-            const int per = (p.seg_len + 127) >> 7;  // tokens per thread, at most 16
+            constexpr int kT = kTokPerThread, kHW = kHeadThreads / 32;  // warps per head
+            const int hh = tid / kHeadThreads, i = tid % kHeadThreads, h = h0 + hh;
+            const int per = (p.seg_len + kHeadThreads - 1) / kHeadThreads;  // tokens per thread
             const int tb = i * per;
-            float dv[16], ex[16];
+            float dv[kT], ex[kT];
 #pragma unroll
-            for (int m = 0; m < 16; ++m) {
+            for (int m = 0; m < kT; ++m) {
                 const int t = tb + m;
                 dv[m] = (m < per && t < p.seg_len) ? __ldg(p.dt + ((size_t)b * p.L + t0 + t) * p.H + h) : 0.f;
             }
             const float A = __ldg(p.A + h);
             float run = 0.f;  // sum of d A over this thread's tokens after token m
 #pragma unroll
-            for (int m = 15; m >= 0; --m) {
+            for (int m = kT - 1; m >= 0; --m) {
                 const bool ok = m < per && tb + m < p.seg_len;
                 const float d = ok ? dt_processed(p, dv[m], h) : 0.f;
                 dv[m] = d;
@@ -204,14 +210,14 @@ segment_state_kernel(const __grid_constant__ Params p, const __grid_constant__ S
             if (lane == 0) warp_total[warp] = incl;
             tc::named_barrier(1, kConvThreads);
             float later = 0.f;  // the later warps of this head, from the segment's end backwards
-            for (int q = 4 * hh + 3; q > warp; --q) later += warp_total[q];
+            for (int q = kHW * hh + kHW - 1; q > warp; --q) later += warp_total[q];
             const float base = later + excl;
 #pragma unroll
-            for (int m = 0; m < 16; ++m)
+            for (int m = 0; m < kT; ++m)
                 if (m < per && tb + m < p.seg_len) w_s[hh * p.seg_len + tb + m] = expf(ex[m] + base) * dv[m];
             if (i == 0) {
                 float total = 0.f;
-                for (int q = 4 * hh + 3; q >= 4 * hh; --q) total += warp_total[q];
+                for (int q = kHW * hh + kHW - 1; q >= kHW * hh; --q) total += warp_total[q];
                 seg_decay[((size_t)b * p.H + h) * p.nseg + s] = total;
             }
         }
@@ -224,8 +230,9 @@ segment_state_kernel(const __grid_constant__ Params p, const __grid_constant__ S
             if (j >= 2) wait(PB_DONE0 + ob, ((j - 2) >> 1) & 1u);  // the MMA of block j - 2 read this buffer
             const uint32_t xsrc = sbase + SM::STG + 2 * st * SM::STG_BYTES, bsrc = xsrc + SM::STG_BYTES;
             const uint32_t xt = sbase + SM::XT + ob * SM::OP_BYTES, bb = xt + 16384;
+            constexpr bool kRawB = IO != IO_F32 && ((IO == IO_BF16) == BF16);  // B is the operand already
 #pragma unroll
-            for (int it = 0; it < 4; ++it) {  // 64 tokens x 16 groups of 8 features, for x and for B
+            for (int it = 0; it < 1024 / kConvThreads; ++it) {  // 64 tokens x 16 groups of 8 features
                 const int e = tid + kConvThreads * it;
                 const int jl = e & 7, c16 = (e >> 3) & 15, jg = e >> 7;
                 const int r = jg * 8 + jl;
@@ -235,8 +242,14 @@ segment_state_kernel(const __grid_constant__ Params p, const __grid_constant__ S
 #pragma unroll
                 for (int i = 0; i < 8; ++i) v[i] *= wv;
                 store8(xt + (jg * 16 + c16) * 128 + jl * 16, v, BF16);  // row (h, p) = 8 c16 + ..
-                stage_read8<IO>(bsrc, r, c16, v);
-                store8(bb + (c16 * 8 + jg) * 128 + jl * 16, v, BF16);
+                const uint32_t bdst = bb + (c16 * 8 + jg) * 128 + jl * 16;
+                if constexpr (kRawB) {
+                    const uint4 u = tcstage::stage_raw16(bsrc, r, c16);
+                    st_shared_v4(bdst, u.x, u.y, u.z, u.w);
+                } else {
+                    stage_read8<IO>(bsrc, r, c16, v);
+                    store8(bdst, v, BF16);
+                }
             }
             tc::fence_smem_to_async();
             __syncwarp();
@@ -246,15 +259,16 @@ segment_state_kernel(const __grid_constant__ Params p, const __grid_constant__ S
             }
         }
 
-        // ---- E_s out of TMEM: warp w reads lanes 32 (w % 4) .. + 31, columns 64 (w / 4) .. + 63 ----
+        // ---- E_s out of TMEM: warp w reads lanes 32 (w % 4) .. + 31, kCols columns from kCols (w / 4) ----
+        constexpr int kCols = kNN / (kConvWarps / 4);
         wait(PB_DONE0 + ((nblk - 1) & 1), ((nblk - 1) >> 1) & 1u);
         tc::fence_after_sync();
-        const int quarter = warp & 3, half = warp >> 2;
+        const int quarter = warp & 3, part = warp >> 2;
         const int row = quarter * 32 + lane, h = row >> 6, pp = row & 63;
-        float *dst = seg_states + ((((size_t)b * p.nseg + s + 1) * p.H + h0 + h) * kP + pp) * kNN + 64 * half;
-        const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + 64 * half;
+        float *dst = seg_states + ((((size_t)b * p.nseg + s + 1) * p.H + h0 + h) * kP + pp) * kNN + kCols * part;
+        const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + kCols * part;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < kCols / 16; ++c) {
             float v[16];
             tc::tmem_ld16(tl + 16 * c, v);
 #pragma unroll
