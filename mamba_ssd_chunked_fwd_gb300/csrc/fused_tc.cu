@@ -1648,7 +1648,7 @@ cudaError_t run_fused(const ssd_fwd_args *a, cudaStream_t s) {
             float *states = reinterpret_cast<float *>(ws + 256);
             float *decay = reinterpret_cast<float *>(ws + 256 + seg_states_bytes(a, sp.nseg));
             p.seg_states = states;
-            e = launch_segment_passes(p, a->x_dtype, a->ops == SSD_OPS_BF16, states, decay, err, s);
+            e = launch_segment_passes(p, a->x_dtype, a->ops == SSD_OPS_BF16, states, decay, err, num_sms(), s);
             if (e != cudaSuccess) return e;
         }
     }

@@ -26,7 +26,7 @@ struct SegMaps {
 int segment_max_len();
 bool segment_smem_fits(int io, int seg_len);
 cudaError_t launch_segment_passes(const Params &p, int io, bool bf16, float *seg_states, float *seg_decay,
-                                  unsigned int *err, cudaStream_t s);
+                                  unsigned int *err, int sms, cudaStream_t s);
 
 bool fused_supported(const ssd_fwd_args *a);
 // Packed sequences take the fused plan at N = 64 only.

@@ -31,6 +31,15 @@ __device__ __forceinline__ uint64_t desc(uint32_t saddr, uint32_t lbo, uint32_t 
     return d;
 }
 
+// The same for a 128-byte-swizzled operand (swizzle mode 2 in bits 61-63), as
+// a TMA tile with 128-byte swizzle lays it out; the start address must sit at
+// a 1024-byte boundary of the swizzle pattern (base offset 0).  For an
+// MN-major operand lbo is the distance between 64-element (128-byte) groups
+// along M / N and sbo the distance between groups of 8 rows along K.
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return desc(saddr, lbo, sbo) | (static_cast<uint64_t>(2) << 61);
+}
+
 // Instruction descriptor of tcgen05.mma kind::f16 with an fp32 accumulator.
 // ab_bf16: operands are bf16 (else fp16).  a_mn / b_mn: operand is MN-major.
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool ab_bf16, bool a_mn, bool b_mn) {
