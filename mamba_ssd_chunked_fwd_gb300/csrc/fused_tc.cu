@@ -859,6 +859,29 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                         for (int bx = 0; bx < 128 / bw; ++bx) tc::tma_prefetch_3d(&tm.z, h0 * kP + bx * bw, k * kQ, b);
                     }
                 };
+                // chunk k of a unit into L2 only, one chunk ahead of its load: the load
+                // (issued when the compute warps release the staging area) then hits L2
+                auto prefetch = [&](int unit, int k) {
+                    const int pair = unit % pairs, bg = unit / pairs;
+                    const int g = bg % dm.G, b = bg / dm.G;
+                    const int h0 = g * dm.hpg + 2 * pair;
+#pragma unroll
+                    for (int bx = 0; bx < 128 / bw; ++bx) tc::tma_prefetch_3d(&tm.x, h0 * kP + bx * bw, k * kQ, b);
+#pragma unroll
+                    for (int bx = 0; bx < NN / bw; ++bx) {
+                        tc::tma_prefetch_3d(&tm.b, g * NN + bx * bw, k * kQ, b);
+                        tc::tma_prefetch_3d(&tm.c, g * NN + bx * bw, k * kQ, b);
+                    }
+                };
+                // the chunk `ahead` chunks after chunk k of `unit` in this CTA's walk, if any
+                auto prefetch_after = [&](int unit, int k, int ahead) {
+                    k += ahead;
+                    while (k >= dm.nchunks) {
+                        k -= dm.nchunks;
+                        unit += gridDim.x;
+                    }
+                    if (unit < n_units) prefetch(unit, k);
+                };
                 uint32_t yt = 0;  // y tiles stored so far
                 // gated instantiations: the z tile of chunk k of a unit into the (free) y staging tile
                 auto load_z = [&](int unit, int k) {
@@ -887,6 +910,7 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                 };
                 if ((int)blockIdx.x < n_units) {
                     stage(blockIdx.x, 0);
+                    prefetch_after(blockIdx.x, 0, 1);
                     load_z(blockIdx.x, 0);
                 }
                 uint32_t gk = 0;
@@ -900,6 +924,7 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                         wait(CV ? BAR_STG_FREE : BAR_OPS_FULL, gk & 1u);
                         if (k + 1 < dm.nchunks) stage(unit, k + 1);
                         else if (unit + (int)gridDim.x < n_units) stage(unit + gridDim.x, 0);
+                        prefetch_after(unit, k, 2);
                         if (k > 0) {
                             store_y(b, h0, k - 1);
                             load_z(unit, k);  // the next tile the compute warps stage
