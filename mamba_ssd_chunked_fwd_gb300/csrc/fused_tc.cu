@@ -709,6 +709,26 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                     while (unit < n_units && unit_span<true>(p, dm, unit).nch == 0) unit += gridDim.x;
                     return unit;
                 };
+                // chunk k + ahead of this CTA's walk (skipping units without chunks) into
+                // L2 only, one chunk ahead of its load
+                auto prefetch_after = [&](int unit, int k, int ahead) {
+                    k += ahead;
+                    Span u = unit_span<true>(p, dm, unit);
+                    while (k >= u.nch) {
+                        k -= u.nch;
+                        unit += gridDim.x;
+                        if (unit >= n_units) return;
+                        u = unit_span<true>(p, dm, unit);
+                    }
+                    const int tok = u.t0 + k * kQ;
+#pragma unroll
+                    for (int bx = 0; bx < 128 / bw; ++bx) tc::tma_prefetch_3d(&tm.x, u.h0 * kP + bx * bw, tok, u.b);
+#pragma unroll
+                    for (int bx = 0; bx < NN / bw; ++bx) {
+                        tc::tma_prefetch_3d(&tm.b, u.g * NN + bx * bw, tok, u.b);
+                        tc::tma_prefetch_3d(&tm.c, u.g * NN + bx * bw, tok, u.b);
+                    }
+                };
                 uint32_t yt = 0;  // y tiles stored so far
                 // the y tile of chunk k of unit u, once the compute warps staged it; the
                 // last chunk of a packed sequence was written straight to y instead
@@ -727,7 +747,10 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                 };
                 {
                     const int first = next_busy(blockIdx.x);
-                    if (first < n_units) stage(unit_span<true>(p, dm, first), 0);
+                    if (first < n_units) {
+                        stage(unit_span<true>(p, dm, first), 0);
+                        prefetch_after(first, 0, 1);
+                    }
                 }
                 uint32_t gk = 0;
                 for (int unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
@@ -740,12 +763,14 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                             const int nu = next_busy(unit + gridDim.x);
                             if (nu < n_units) stage(unit_span<VARLEN>(p, dm, nu), 0);
                         }
+                        prefetch_after(unit, k, 2);
                         if (k > 0) store_y(u, k - 1);
                     }
                     if (u.nch > 0) store_y(u, u.nch - 1);
                 }
                 tc::bulk_wait_all();
             } else if constexpr (SEG) {
+                // (no L2 prefetch of the next chunk here: at N = 128 it measured slower)
                 // x and B of chunk k of a unit into the staging area, expecting C too
                 // (its copy is issued by load_c: with y staged in the C tile it has to
                 // wait until the previous y tile has left)
