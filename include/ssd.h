@@ -200,11 +200,15 @@ ssd_status ssd_chunk_scan(const ssd_fwd_args *args, const float *dtp, const floa
  * memory (pinned for overlap; pageable works but serialises).  The library
  * copies the inputs into the device workspace, runs ssd_fwd there and copies
  * y and final_state back; the host outputs are valid after the caller
- * synchronises `stream`.  The batch is cut into up to 8 slices (one slice when
- * a per-batch stride is not a multiple of 256 bytes): the copies in run on an
- * internal stream, each slice's forward on `stream` once its inputs are in,
- * its copies out on a second internal stream, so both copy directions and the
- * kernels overlap.  Work enqueued on `stream` before the call is ordered before
+ * synchronises `stream`.  The call is cut into slices: with the fused plan at
+ * N = 64 or the chunked plan, along the sequence (up to 16 slices of whole
+ * chunks over every batch row, the fp32 state handed from slice to slice, so
+ * the outputs equal ssd_fwd's bit for bit); otherwise along the batch (up to 8
+ * slices; one when a per-batch stride is not a multiple of 256 bytes).  The
+ * copies in run on an internal stream (one 2-D copy per tensor and sequence
+ * slice), each slice's forward on `stream` once its inputs are in, its copies
+ * out on a second internal stream, so both copy directions and the kernels
+ * overlap.  Work enqueued on `stream` before the call is ordered before
  * it, and the call as a whole is complete on `stream`.  The two internal
  * streams and four events are created once per device on first use and kept
  * until exit; concurrent calls from several threads are serialised while they

@@ -727,36 +727,111 @@ ssd_status ssd_chunk_scan(const ssd_fwd_args *a, const float *dtp, const float *
 
 namespace {
 
-struct HostLayout {
-    size_t fwd_ws, x, dt, A, Bm, Cm, D, z, dt_bias, h0, y, fin, nw, total;
+// How ssd_fwd_host cuts a call into slices.  Along the sequence where the plan
+// splits exactly at chunk boundaries (the fused plan at N = 64, whose state is
+// fp32 throughout, and the chunked plan): every batch row, `ls` tokens of whole
+// chunks per slice (the last may be shorter), the fp32 state handed from slice
+// to slice through final_state / initial_state, so the results equal one
+// ssd_fwd over the whole call bit for bit and every slice has all of the
+// call's work units.  Else (the segmented walks at N = 128 choose their
+// segments from L) along the batch.
+constexpr int64_t kSeqSlices = 16;
+struct HostSlicing {
+    bool seq;
+    int64_t n;      // slices
+    int64_t per_b;  // batch entries per slice (batch slicing)
+    int64_t ls;     // tokens per slice (sequence slicing)
 };
+
+// Batch entries per slice: up to 8 slices, and one slice when a per-batch
+// stride would break the 256-byte alignment of the device copies.
+int64_t host_slice_batch(const ssd_fwd_args *a) {
+    const size_t io = io_size(a->x_dtype);
+    const size_t strides[] = {(size_t)a->L * a->H * a->P * io, (size_t)a->L * a->H * 4,
+                              (size_t)a->L * a->G * a->N * io, (size_t)a->H * a->P * a->N * 4};
+    for (size_t st : strides)
+        if (st % kAlign != 0) return a->B;
+    const int64_t nslices = a->B < 8 ? a->B : 8;
+    return (a->B + nslices - 1) / nslices;
+}
+
+HostSlicing host_slicing(const ssd_fwd_args *a, int32_t plan) {
+    const bool exact = (plan == SSD_PLAN_FUSED && a->N == 64) || plan == SSD_PLAN_CHUNKED;
+    // (a 2-D copy's pitch is a batch entry of x: kept well inside the copy engines' limit)
+    const bool pitch_ok = (size_t)a->L * a->H * a->P * io_size(a->x_dtype) <= ((size_t)1 << 30);
+    if (exact && pitch_ok && a->L >= 2 * (int64_t)a->chunk) {
+        int64_t ls = (a->L + kSeqSlices - 1) / kSeqSlices;
+        ls = (ls + a->chunk - 1) / a->chunk * a->chunk;
+        const int64_t n = (a->L + ls - 1) / ls;
+        if (n >= 2) return {true, n, a->B, ls};
+    }
+    const int64_t per = host_slice_batch(a);
+    return {false, (a->B + per - 1) / per, per, a->L};
+}
+
+// Device copies of the call's tensors in the workspace.  Batch slicing: each
+// tensor whole, in its public layout.  Sequence slicing: per slice a block of
+// its own compact tensors [B, tokens of the slice, ...] at xs + s * slice_bytes
+// (x, dt, B, C, z, y in that order), plus two fp32 states that carry the
+// recurrence from slice to slice.
+struct HostLayout {
+    HostSlicing sl;
+    size_t fwd_ws, x, dt, A, Bm, Cm, D, z, dt_bias, h0, y, fin, nw, total;
+    size_t slice_bytes, sx, sdt, sb, sc, sz, sy;  // sequence slicing: offsets within a slice block
+    size_t st[2];                                 // sequence slicing: the carried states
+};
+
+ssd_fwd_args slice_shape(const ssd_fwd_args *a, int64_t L) {
+    ssd_fwd_args o = *a;
+    o.L = L;
+    return o;
+}
 
 HostLayout host_layout(const ssd_fwd_args *a, int32_t plan) {
     const size_t io = io_size(a->x_dtype);
-    const size_t nx = (size_t)a->B * a->L * a->H * a->P;
-    const size_t nbc = (size_t)a->B * a->L * a->G * a->N;
     const size_t nst = (size_t)a->B * a->H * a->P * a->N;
-    HostLayout l;
+    HostLayout l{};
+    l.sl = host_slicing(a, plan);
     size_t off = 0;
     auto take = [&](size_t bytes) { size_t o = off; off += align_up(bytes); return o; };
-    l.fwd_ws = take(workspace_for(a, plan));
-    l.x = take(nx * io);
-    l.dt = take((size_t)a->B * a->L * a->H * 4);
+    if (l.sl.seq) {
+        const ssd_fwd_args o = slice_shape(a, l.sl.ls);
+        l.fwd_ws = take(workspace_for(&o, plan));
+        const size_t tok = (size_t)a->B * l.sl.ls;  // (batch, token) rows of a full slice
+        size_t so = 0;
+        auto stake = [&](size_t bytes) { size_t r = so; so += align_up(bytes); return r; };
+        l.sx = stake(tok * a->H * a->P * io);
+        l.sdt = stake(tok * a->H * 4);
+        l.sb = stake(tok * a->G * a->N * io);
+        l.sc = stake(tok * a->G * a->N * io);
+        l.sz = stake(a->z ? tok * a->H * a->P * io : 0);
+        l.sy = stake(tok * a->H * a->P * io);
+        l.slice_bytes = so;
+        l.x = take(so * l.sl.n);
+        l.st[0] = take(nst * 4);
+        l.st[1] = take(nst * 4);
+    } else {
+        const size_t nx = (size_t)a->B * a->L * a->H * a->P;
+        const size_t nbc = (size_t)a->B * a->L * a->G * a->N;
+        l.fwd_ws = take(workspace_for(a, plan));
+        l.x = take(nx * io);
+        l.dt = take((size_t)a->B * a->L * a->H * 4);
+        l.Bm = take(nbc * io);
+        l.Cm = take(nbc * io);
+        l.z = take(a->z ? nx * io : 0);
+        l.y = take(nx * io);
+    }
     l.A = take((size_t)a->H * 4);
-    l.Bm = take(nbc * io);
-    l.Cm = take(nbc * io);
     l.D = take(a->D ? (size_t)a->H * 4 : 0);
-    l.z = take(a->z ? nx * io : 0);
     l.dt_bias = take(a->dt_bias ? (size_t)a->H * 4 : 0);
     l.h0 = take(a->initial_state ? nst * 4 : 0);
-    l.y = take(nx * io);
     l.fin = take(a->final_state ? nst * 4 : 0);
     l.nw = take(a->norm_weight ? (size_t)a->H * a->P * 4 : 0);
     l.total = off;
     return l;
 }
 
-// The host-buffer pipeline: batch slices copied in on `in`, computed on the
+// The host-buffer pipeline: slices copied in on `in`, computed on the
 // caller's stream, copied out on `out`, so that the copies in both directions
 // and the kernels of different slices overlap.  One set per device, created on
 // first use; `mu` serialises the enqueue sequences of concurrent callers (the
@@ -787,18 +862,6 @@ cudaError_t host_pipe(HostPipe **out) {
     return cudaSuccess;
 }
 
-// Batch entries per slice: up to 8 slices, and one slice when a per-batch
-// stride would break the 256-byte alignment of the device copies.
-int64_t host_slice_batch(const ssd_fwd_args *a) {
-    const size_t io = io_size(a->x_dtype);
-    const size_t strides[] = {(size_t)a->L * a->H * a->P * io, (size_t)a->L * a->H * 4,
-                              (size_t)a->L * a->G * a->N * io, (size_t)a->H * a->P * a->N * 4};
-    for (size_t st : strides)
-        if (st % kAlign != 0) return a->B;
-    const int64_t nslices = a->B < 8 ? a->B : 8;
-    return (a->B + nslices - 1) / nslices;
-}
-
 }  // namespace
 
 ssd_status ssd_fwd_host_workspace_size(const ssd_fwd_args *a, size_t *bytes) {
@@ -827,45 +890,41 @@ ssd_status ssd_fwd_host(const ssd_fwd_args *a, void *stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     char *ws = static_cast<char *>(a->workspace);
     const size_t io = io_size(a->x_dtype);
-    // per batch entry: elements of x / y / z, of dt, of B / C, of a state
-    const size_t ex = (size_t)a->L * a->H * a->P, edt = (size_t)a->L * a->H, ebc = (size_t)a->L * a->G * a->N;
+    // per (batch, token) row: bytes of x / y / z, of dt, of B / C; per batch entry: elements of a state
+    const size_t rx = (size_t)a->H * a->P * io, rdt = (size_t)a->H * 4, rbc = (size_t)a->G * a->N * io;
     const size_t est = (size_t)a->H * a->P * a->N;
-    // the whole call on the device copies, every slice on the same plan
+    // what every slice shares: per-head vectors, the fwd workspace, the plan
     ssd_fwd_args d = *a;
-    d.x = ws + l.x;
-    d.dt = reinterpret_cast<const float *>(ws + l.dt);
     d.A = reinterpret_cast<const float *>(ws + l.A);
-    d.Bm = ws + l.Bm;
-    d.Cm = ws + l.Cm;
     d.D = a->D ? reinterpret_cast<const float *>(ws + l.D) : nullptr;
-    d.z = a->z ? ws + l.z : nullptr;
     d.dt_bias = a->dt_bias ? reinterpret_cast<const float *>(ws + l.dt_bias) : nullptr;
-    d.initial_state = a->initial_state ? reinterpret_cast<const float *>(ws + l.h0) : nullptr;
-    d.y = ws + l.y;
-    d.final_state = a->final_state ? reinterpret_cast<float *>(ws + l.fin) : nullptr;
     d.norm_weight = a->norm_weight ? reinterpret_cast<const float *>(ws + l.nw) : nullptr;
     d.workspace = ws + l.fwd_ws;
-    d.workspace_bytes = workspace_for(a, plan);
     d.plan = plan;
-    int64_t per = host_slice_batch(a);
-    auto slice = [&](int64_t b0, int64_t nb) {
-        ssd_fwd_args o = d;
-        o.B = nb;
-        o.x = static_cast<const char *>(d.x) + b0 * ex * io;
-        o.dt = d.dt + b0 * edt;
-        o.Bm = static_cast<const char *>(d.Bm) + b0 * ebc * io;
-        o.Cm = static_cast<const char *>(d.Cm) + b0 * ebc * io;
-        if (o.z) o.z = static_cast<const char *>(d.z) + b0 * ex * io;
-        if (o.initial_state) o.initial_state = d.initial_state + b0 * est;
-        o.y = static_cast<char *>(d.y) + b0 * ex * io;
-        if (o.final_state) o.final_state = d.final_state + b0 * est;
-        return o;
-    };
-    if (per < a->B) {  // every slice must take the call's plan
-        const ssd_fwd_args o = slice(0, per);
-        int32_t pl = 0;
-        if (ssd_fwd_resolve_plan(&o, &pl) != SSD_OK || pl != plan) per = a->B;
+    float *h0 = a->initial_state ? reinterpret_cast<float *>(ws + l.h0) : nullptr;
+    float *fin = a->final_state ? reinterpret_cast<float *>(ws + l.fin) : nullptr;
+    int64_t per = l.sl.per_b;
+    if (l.sl.seq) {
+        const ssd_fwd_args o = slice_shape(a, l.sl.ls);
+        d.workspace_bytes = workspace_for(&o, plan);
+    } else {
+        d.x = ws + l.x;
+        d.dt = reinterpret_cast<const float *>(ws + l.dt);
+        d.Bm = ws + l.Bm;
+        d.Cm = ws + l.Cm;
+        d.z = a->z ? ws + l.z : nullptr;
+        d.y = ws + l.y;
+        d.initial_state = h0;
+        d.final_state = fin;
+        d.workspace_bytes = workspace_for(a, plan);
+        if (per < a->B) {  // every slice must take the call's plan
+            ssd_fwd_args o = d;
+            o.B = per;
+            int32_t pl = 0;
+            if (ssd_fwd_resolve_plan(&o, &pl) != SSD_OK || pl != plan) per = a->B;
+        }
     }
+    const int64_t nslices = l.sl.seq ? l.sl.n : (a->B + per - 1) / per;
     std::lock_guard<std::mutex> lock(g_pipe_mu);
     HostPipe *hp = nullptr;
     cudaError_t e = host_pipe(&hp);
@@ -881,28 +940,78 @@ ssd_status ssd_fwd_host(const ssd_fwd_args *a, void *stream) {
     auto d2h = [&](void *dst, const void *src, size_t bytes) {
         if (e == cudaSuccess && dst && bytes) e = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToHost, hp->out);
     };
+    // rows [t0, t0 + n) of every batch entry of a [B, L, row bytes] host tensor <-> a compact
+    // [B, n, row bytes] device block: one 2-D copy, a batch entry per 2-D row
+    auto h2d_rows = [&](void *dst, const void *src, size_t row, int64_t t0, int64_t n) {
+        if (e == cudaSuccess && src && row)
+            e = cudaMemcpy2DAsync(dst, n * row, static_cast<const char *>(src) + t0 * row, (size_t)a->L * row, n * row,
+                                  (size_t)a->B, cudaMemcpyHostToDevice, hp->in);
+    };
+    auto d2h_rows = [&](void *dst, const void *src, size_t row, int64_t t0, int64_t n) {
+        if (e == cudaSuccess && dst && row)
+            e = cudaMemcpy2DAsync(static_cast<char *>(dst) + t0 * row, (size_t)a->L * row, src, n * row, n * row,
+                                  (size_t)a->B, cudaMemcpyDeviceToHost, hp->out);
+    };
     h2d(ws + l.A, a->A, (size_t)a->H * 4);
     h2d(ws + l.D, a->D, (size_t)a->H * 4);
     h2d(ws + l.dt_bias, a->dt_bias, (size_t)a->H * 4);
     h2d(ws + l.nw, a->norm_weight, (size_t)a->H * a->P * 4);
+    h2d(h0, a->initial_state, (size_t)a->B * est * 4);
     ssd_status st2 = SSD_OK;
-    for (int64_t b0 = 0; b0 < a->B && e == cudaSuccess && st2 == SSD_OK; b0 += per) {
-        const int64_t nb = a->B - b0 < per ? a->B - b0 : per;
-        const ssd_fwd_args o = slice(b0, nb);
-        h2d(const_cast<void *>(o.x), static_cast<const char *>(a->x) + b0 * ex * io, nb * ex * io);
-        h2d(const_cast<float *>(o.dt), a->dt + b0 * edt, nb * edt * 4);
-        h2d(const_cast<void *>(o.Bm), static_cast<const char *>(a->Bm) + b0 * ebc * io, nb * ebc * io);
-        h2d(const_cast<void *>(o.Cm), static_cast<const char *>(a->Cm) + b0 * ebc * io, nb * ebc * io);
-        if (a->z) h2d(const_cast<void *>(o.z), static_cast<const char *>(a->z) + b0 * ex * io, nb * ex * io);
-        if (a->initial_state) h2d(const_cast<float *>(o.initial_state), a->initial_state + b0 * est, nb * est * 4);
+    for (int64_t si = 0; si < nslices && e == cudaSuccess && st2 == SSD_OK; ++si) {
+        ssd_fwd_args o = d;
+        int64_t b0 = 0, nb = a->B, t0 = 0, nt = a->L;
+        if (l.sl.seq) {
+            t0 = si * l.sl.ls;
+            nt = a->L - t0 < l.sl.ls ? a->L - t0 : l.sl.ls;
+            char *blk = ws + l.x + si * l.slice_bytes;
+            o.L = nt;
+            o.x = blk + l.sx;
+            o.dt = reinterpret_cast<const float *>(blk + l.sdt);
+            o.Bm = blk + l.sb;
+            o.Cm = blk + l.sc;
+            o.z = a->z ? blk + l.sz : nullptr;
+            o.y = blk + l.sy;
+            // the state entering the slice, and the state it leaves for the next one
+            o.initial_state = si == 0 ? h0 : reinterpret_cast<const float *>(ws + l.st[(si - 1) & 1]);
+            o.final_state = si + 1 == nslices ? fin : reinterpret_cast<float *>(ws + l.st[si & 1]);
+            h2d_rows(const_cast<void *>(o.x), a->x, rx, t0, nt);
+            h2d_rows(const_cast<float *>(o.dt), a->dt, rdt, t0, nt);
+            h2d_rows(const_cast<void *>(o.Bm), a->Bm, rbc, t0, nt);
+            h2d_rows(const_cast<void *>(o.Cm), a->Cm, rbc, t0, nt);
+            if (a->z) h2d_rows(const_cast<void *>(o.z), a->z, rx, t0, nt);
+        } else {
+            b0 = si * per;
+            nb = a->B - b0 < per ? a->B - b0 : per;
+            const size_t ex = (size_t)a->L * rx, edt = (size_t)a->L * rdt, ebc = (size_t)a->L * rbc;
+            o.B = nb;
+            o.x = static_cast<const char *>(d.x) + b0 * ex;
+            o.dt = reinterpret_cast<const float *>(reinterpret_cast<const char *>(d.dt) + b0 * edt);
+            o.Bm = static_cast<const char *>(d.Bm) + b0 * ebc;
+            o.Cm = static_cast<const char *>(d.Cm) + b0 * ebc;
+            if (o.z) o.z = static_cast<const char *>(d.z) + b0 * ex;
+            if (o.initial_state) o.initial_state = d.initial_state + b0 * est;
+            o.y = static_cast<char *>(d.y) + b0 * ex;
+            if (o.final_state) o.final_state = d.final_state + b0 * est;
+            h2d(const_cast<void *>(o.x), static_cast<const char *>(a->x) + b0 * ex, nb * ex);
+            h2d(const_cast<float *>(o.dt), reinterpret_cast<const char *>(a->dt) + b0 * edt, nb * edt);
+            h2d(const_cast<void *>(o.Bm), static_cast<const char *>(a->Bm) + b0 * ebc, nb * ebc);
+            h2d(const_cast<void *>(o.Cm), static_cast<const char *>(a->Cm) + b0 * ebc, nb * ebc);
+            if (a->z) h2d(const_cast<void *>(o.z), static_cast<const char *>(a->z) + b0 * ex, nb * ex);
+        }
         if (e != cudaSuccess) break;
         if ((e = cudaEventRecord(hp->copied, hp->in)) != cudaSuccess) break;
         if ((e = cudaStreamWaitEvent(s, hp->copied, 0)) != cudaSuccess) break;
         if ((st2 = ssd_fwd(&o, stream)) != SSD_OK) break;
         if ((e = cudaEventRecord(hp->computed, s)) != cudaSuccess) break;
         if ((e = cudaStreamWaitEvent(hp->out, hp->computed, 0)) != cudaSuccess) break;
-        d2h(static_cast<char *>(a->y) + b0 * ex * io, o.y, nb * ex * io);
-        if (a->final_state) d2h(a->final_state + b0 * est, o.final_state, nb * est * 4);
+        if (l.sl.seq) {
+            d2h_rows(a->y, o.y, rx, t0, nt);
+            if (si + 1 == nslices) d2h(a->final_state, fin, (size_t)a->B * est * 4);
+        } else {
+            d2h(static_cast<char *>(a->y) + b0 * a->L * rx, o.y, nb * a->L * rx);
+            if (a->final_state) d2h(a->final_state + b0 * est, o.final_state, nb * est * 4);
+        }
     }
     // join: the call is complete on `stream` once both copy streams are
     cudaError_t ej = cudaEventRecord(hp->computed, hp->in);

@@ -290,6 +290,69 @@ def test_host_buffer_pipeline_matches_device_entry(B, L, H, P, G, ops):
     assert torch.equal(y, yd.cpu()) and torch.equal(fin, fd.cpu())
 
 
+def _host_call_plan(ssd, inp, chunk, ops, plan, return_final=True):
+    h = {k: (v.contiguous().pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    y = torch.full_like(h["x"], float("nan")).pin_memory()
+    B, L, H, P = h["x"].shape
+    fin = torch.full((B, H, P, h["B"].shape[3]), float("nan")).pin_memory() if return_final else None
+    args = ssd.make_args(h["x"], h["dt"], h["A"], h["B"], h["C"], chunk, y=y, final_state=fin, D=h["D"], z=h["z"],
+                         dt_bias=h["dt_bias"], initial_states=h["initial_states"], dt_softplus=True, ops=ops,
+                         plan=plan)
+    nws = ssd.ssd_fwd_host_workspace_size(args)
+    ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
+    args.workspace, args.workspace_bytes = ws.data_ptr(), nws
+    ssd.ssd_fwd_host(args)
+    torch.cuda.synchronize()
+    return y, fin
+
+
+@pytest.mark.parametrize("B,L,H,G,ops,ret", [
+    (2, 320, 8, 2, "bf16", True),    # fused plan, 5 sequence slices of 64 tokens
+    (3, 300, 4, 1, "f16", True),     # a ragged last slice (44 tokens), f16 operands
+    (2, 1024, 4, 2, "bf16", False),  # 16 slices; the carried state without a final_state output
+])
+def test_host_buffer_sequence_slices_on_the_fused_plan(B, L, H, G, ops, ret):
+    """The fused plan at N = 64 sliced along the sequence (the fp32 state handed
+    from slice to slice) equals one device call bit for bit."""
+    import mamba_ssd_chunked_fwd_gb300 as ssd
+    _, inp = ssd_inputs.custom(B, L, H, 64, 64, G, 64, seed=B * L + H, ops=ops, h0=True, D=True, z=True,
+                               dt_bias=True)
+    d = to_device(inp)
+    args_probe = ssd.make_args(d["x"], d["dt"], d["A"], d["B"], d["C"], 64, plan="fused", ops=ops)
+    assert "ssd_fused_kernel" in ssd.ssd_fwd_describe(args_probe)
+    res = ssd.mamba2_ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], 64, dt_softplus=True, return_final_state=ret,
+                             D=d["D"], z=d["z"], dt_bias=d["dt_bias"], initial_states=d["initial_states"], ops=ops,
+                             plan="fused")
+    yd, fd = res if ret else (res, None)
+    y, fin = _host_call_plan(ssd, inp, 64, ops, "fused", return_final=ret)
+    assert torch.equal(y, yd.cpu())
+    if ret:
+        assert torch.equal(fin, fd.cpu())
+
+
+def test_host_buffer_batch_slices_when_the_sequence_is_one_chunk():
+    """A sequence of one chunk cannot be cut: the call goes in batch slices."""
+    import mamba_ssd_chunked_fwd_gb300 as ssd
+    _, inp = ssd_inputs.custom(6, 64, 4, 64, 64, 2, 64, seed=66, ops="bf16", h0=True, D=True)
+    d = to_device(inp)
+    yd, fd = ssd.mamba2_ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], 64, dt_softplus=True,
+                                return_final_state=True, D=d["D"], initial_states=d["initial_states"], ops="bf16")
+    y, fin = _host_call_plan(ssd, inp, 64, "bf16", "auto")
+    assert torch.equal(y, yd.cpu()) and torch.equal(fin, fd.cpu())
+
+
+def test_host_buffer_fused_n128_batch_slices(oracle_mod):
+    """N = 128 on the fused plan goes in batch slices (its segments depend on the
+    sequence length); each slice's segmentation differs from a whole-batch call,
+    so it is held to the oracle."""
+    import mamba_ssd_chunked_fwd_gb300 as ssd
+    _, inp = ssd_inputs.custom(3, 1024, 4, 64, 128, 2, 128, seed=67, ops="bf16", h0=True, D=True)
+    y, fin = _host_call_plan(ssd, inp, 128, "bf16", "fused")
+    yr, fr = oracle_mod.forward(oracle_problem(oracle_mod, inp))
+    assert_close(oracle_mod, y.double().numpy(), yr, "bf16", "host N=128 y")
+    assert_close(oracle_mod, fin.double().numpy(), fr, "bf16", "host N=128 final_state")
+
+
 def test_host_buffer_calls_back_to_back_stay_ordered():
     """Two calls on one stream with no synchronisation between them: the
     second call's copies in wait for the first call to finish."""
