@@ -392,8 +392,11 @@ segment_state_kernel(const __grid_constant__ Params p, const __grid_constant__ S
     if (warp == kMmaWarp) tc::tmem_dealloc(tmem, 2 * kNN);
 }
 
-// S_in(s + 1) = exp(a_s) S_in(s) + E_s over s = 0 .. nseg - 2, in place
-__global__ void __launch_bounds__(256)
+// S_in(s + 1) = exp(a_s) S_in(s) + E_s over s = 0 .. nseg - 2, in place.  The
+// E_s of up to kFoldBatch segments (and their decays) are loaded at once, so
+// the chain costs one memory round trip per batch, not one per segment.
+constexpr int kFoldBatch = 8;
+__global__ void __launch_bounds__(256, 4)
 segment_fold_kernel(const Params p, const float *__restrict__ seg_decay, float *seg_states) {
     tc::pdl_launch_dependents();  // the walk may be scheduled; it waits for this grid before reading states
     tc::pdl_wait();               // the pre-pass has completed
@@ -406,16 +409,26 @@ segment_fold_kernel(const Params p, const float *__restrict__ seg_decay, float *
     float4 st = make_float4(0.f, 0.f, 0.f, 0.f);
     if (p.h0) st = __ldg(reinterpret_cast<const float4 *>(p.h0 + ((size_t)b * p.H + h) * PN + e));
     const float *a = seg_decay + ((size_t)b * p.H + h) * p.nseg;
-    float4 nxt = *reinterpret_cast<const float4 *>(base + sstride);
-    for (int s = 1; s < p.nseg; ++s) {
-        const float4 loc = nxt;
-        if (s + 1 < p.nseg) nxt = *reinterpret_cast<const float4 *>(base + (size_t)(s + 1) * sstride);
-        const float ea = expf(__ldg(a + s - 1));
-        st.x = fmaf(ea, st.x, loc.x);
-        st.y = fmaf(ea, st.y, loc.y);
-        st.z = fmaf(ea, st.z, loc.z);
-        st.w = fmaf(ea, st.w, loc.w);
-        *reinterpret_cast<float4 *>(base + (size_t)s * sstride) = st;
+    for (int s0 = 1; s0 < p.nseg; s0 += kFoldBatch) {
+        const int cnt = p.nseg - s0 < kFoldBatch ? p.nseg - s0 : kFoldBatch;
+        float4 loc[kFoldBatch];
+        float ea[kFoldBatch];
+#pragma unroll
+        for (int i = 0; i < kFoldBatch; ++i)
+            if (i < cnt) {
+                loc[i] = *reinterpret_cast<const float4 *>(base + (size_t)(s0 + i) * sstride);
+                ea[i] = __ldg(a + s0 + i - 1);
+            }
+#pragma unroll
+        for (int i = 0; i < kFoldBatch; ++i)
+            if (i < cnt) {
+                const float d = expf(ea[i]);
+                st.x = fmaf(d, st.x, loc[i].x);
+                st.y = fmaf(d, st.y, loc[i].y);
+                st.z = fmaf(d, st.z, loc[i].z);
+                st.w = fmaf(d, st.w, loc[i].w);
+                *reinterpret_cast<float4 *>(base + (size_t)(s0 + i) * sstride) = st;
+            }
     }
 }
 
