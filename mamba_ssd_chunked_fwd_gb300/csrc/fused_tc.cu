@@ -122,14 +122,25 @@ constexpr uint32_t NORM_ZBAR = NORM_BARS + 2 * 4 * 8;                    // z ti
 // boxes, B and C one each), which the compute warps read while the next
 // chunk's raw tiles land in the staging area; to make room its bf16 state copy
 // lives in TMEM and Xcat has one buffer.
-template <int NN, int IO, bool CV = false>
+// DIRECT (N = 128 with 16-bit tensors already in the operand dtype): the
+// products read x, B and C from two staging buffers just as the TMA wrote
+// them (128-byte swizzle), so there are no operand copies of them (CB2, BB,
+// XC) and the staging is double-buffered; buffer i at STGD + i * DStg::BUF:
+//   DX  x of the pair as [head 0 box | zero box | head 1 box] (24 KB): the
+//       intra product's block-diagonal A operand, each head's M half beside zeros
+//   DB  B, two 64-feature boxes (16 KB)
+//   DC  C twice, [c0 | c0 | c1 | c1] (32 KB): 128 rows for C B^T
+struct DStg {
+    static constexpr uint32_t DX = 0, DB = 3 * 8192, DC = DB + 2 * 8192, BUF = DC + 4 * 8192;
+};
+template <int NN, int IO, bool CV = false, bool DIRECT = false>
 struct Smem {
     static constexpr bool kStateBfTmem = NN == 128 || CV;  // the bf16 copy of the state in TMEM
     static constexpr bool kAliasY = NN == 128 && IO == IO_F32;
-    static constexpr int kXcBufs = (kAliasY || CV) ? 1 : 2;
+    static constexpr int kXcBufs = DIRECT ? 0 : (kAliasY || CV) ? 1 : 2;
     static constexpr uint32_t CB2 = 0;
-    static constexpr uint32_t BB = CB2 + 256 * NN;
-    static constexpr uint32_t XT = BB + 128 * NN;
+    static constexpr uint32_t BB = CB2 + (DIRECT ? 0 : 256 * NN);
+    static constexpr uint32_t XT = BB + (DIRECT ? 0 : 128 * NN);
     static constexpr uint32_t XC = XT + 16384;
     static constexpr uint32_t MC = XC + kXcBufs * XC_BYTES;
     static constexpr uint32_t POST = MC + 16384;                 // x at POST, B at POST_B, C at POST_C
@@ -138,20 +149,28 @@ struct Smem {
     static constexpr uint32_t STG_Y = S + (kStateBfTmem ? 0 : 256 * NN);
     static constexpr uint32_t Y_BYTES = NN == 64 ? 32768 : kAliasY ? 0 : (IO == IO_F32 ? 32768 : 16384);
     static constexpr uint32_t STG_X = STG_Y + Y_BYTES;
-    static constexpr uint32_t X_BYTES = NN == 64 ? 32768 : (IO == IO_F32 ? 32768 : 16384);
+    static constexpr uint32_t X_BYTES = DIRECT ? 0 : NN == 64 ? 32768 : (IO == IO_F32 ? 32768 : 16384);
     static constexpr uint32_t STG_B = STG_X + X_BYTES;
-    static constexpr uint32_t BC_BYTES = NN == 64 ? 16384 : 64 * NN * (IO == IO_F32 ? 4 : 2);
+    static constexpr uint32_t BC_BYTES = DIRECT ? 0 : NN == 64 ? 16384 : 64 * NN * (IO == IO_F32 ? 4 : 2);
     static constexpr uint32_t STG_C = STG_B + BC_BYTES;
     static constexpr uint32_t YSTAGE = kAliasY ? STG_C : STG_Y;  // where the epilogue stages y (and z)
-    static constexpr uint32_t VEC = STG_C + BC_BYTES;
+    static constexpr uint32_t STGD = STG_C + BC_BYTES;
+    static constexpr uint32_t VEC = STGD + (DIRECT ? 2 * DStg::BUF : 0);
     static constexpr uint32_t NORM = VEC + 3 * VEC_BYTES;
     static constexpr uint32_t BYTES = NORM + 1024;                    // + alignment slack
     static constexpr uint32_t BYTES_NORM = NORM + NORM_ZBAR + 16 + 1024;
-    static_assert(STG_X % 1024 == 0 && STG_B % 1024 == 0 && STG_C % 1024 == 0 && POST % 1024 == 0,
+    static_assert(STG_X % 1024 == 0 && STG_B % 1024 == 0 && STG_C % 1024 == 0 && POST % 1024 == 0 &&
+                      STGD % 1024 == 0 && DStg::BUF % 1024 == 0,
                   "swizzled TMA boxes need 1 KB");
     static_assert(NORM % 16 == 0 && BYTES_NORM + 512 <= 232448, "the layout fits in shared memory");
 };
 static_assert(Smem<64, IO_F32>::VEC == 221184 && Smem<64, IO_BF16>::STG_C == 204800, "N = 64 layout unchanged");
+// the launch sizes shared memory from the regular layout
+static_assert(Smem<128, IO_BF16, false, true>::BYTES == Smem<128, IO_BF16>::BYTES &&
+                  Smem<128, IO_BF16, false, true>::BYTES_NORM == Smem<128, IO_BF16>::BYTES_NORM &&
+                  Smem<128, IO_F16, false, true>::BYTES == Smem<128, IO_F16>::BYTES &&
+                  Smem<128, IO_F16, false, true>::BYTES_NORM == Smem<128, IO_F16>::BYTES_NORM,
+              "the direct layout takes the same room");
 
 // TMEM columns (512 allocated).  NN = 64: G 0-63, dS 64-127, Yoff / Yint in
 // two buffers from 128.  NN = 128: G 0-63, the fp32 state 64-191 (dS is
@@ -168,7 +187,9 @@ __device__ __forceinline__ uint32_t tm_yint(int buf) { return NN == 64 ? 192u + 
 enum {
     BAR_OPS_FULL = 0, BAR_MCAT_FULL, BAR_S_FULL, BAR_G_DONE, BAR_DS_DONE, BAR_Y_DONE0, BAR_Y_DONE1,
     BAR_STAGE_FULL, BAR_Y_STAGED, BAR_Y_FREE, BAR_VEC_FULL0, BAR_VEC_EMPTY0 = BAR_VEC_FULL0 + kVecSlots,
-    BAR_CONV_DONE = BAR_VEC_EMPTY0 + kVecSlots, BAR_STG_FREE, NBARS
+    BAR_CONV_DONE = BAR_VEC_EMPTY0 + kVecSlots, BAR_STG_FREE,
+    BAR_DFULL0, BAR_DFREE0 = BAR_DFULL0 + 2,  // the direct layout's two staging buffers: loaded, read
+    NBARS = BAR_DFREE0 + 2
 };
 
 // TMA descriptors of x [B,L,H*P] and B, C [B,L,G*N] as 3-D tensors
@@ -532,7 +553,15 @@ template <int IO, bool BF16, bool VARLEN, int ZM, int NN = 64, bool CV = false>
 __global__ void __launch_bounds__(CV ? kThreadsConv : kThreads, 1)
 ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMaps tm, int n_units,
                  unsigned int *err, int norm_cs) {
-    using L = Smem<NN, IO, CV>;
+    // dtype of the tiles the operand stage reads: the staging tiles, or with the
+    // conv1d the convolved tiles in POST (in the operand dtype)
+    constexpr int SIO = CV ? (BF16 ? IO_BF16 : IO_F16) : IO;
+    // those tiles hold the operand dtype already: x (unweighted), B and C are
+    // copied chunk by chunk (or at N = 128 read in place), only the decay-weighted x
+    // is converted
+    constexpr bool kRaw = SIO != IO_F32 && ((SIO == IO_BF16) == BF16);
+    constexpr bool DIRECT = NN == 128 && kRaw && !CV;
+    using L = Smem<NN, IO, CV, DIRECT>;
     constexpr bool SEG = NN == 128;
     constexpr bool kAliasY = L::kAliasY;
     static_assert(NN == 64 || NN == 128, "state width 64 or 128");
@@ -541,12 +570,6 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
     static_assert(!kAliasY || ZM == 0, "with y staged in the C tile there is no room for a z tile");
     constexpr int kGCols = 16;      // this thread's columns of each 64-column region (G, Yoff, Yint)
     constexpr int kSCols = NN / 4;  // this thread's state columns
-    // dtype of the tiles the operand stage reads: the staging tiles, or with the
-    // conv1d the convolved tiles in POST (in the operand dtype)
-    constexpr int SIO = CV ? (BF16 ? IO_BF16 : IO_F16) : IO;
-    // those tiles hold the operand dtype already: x (unweighted), B and C are
-    // copied chunk by chunk, only the decay-weighted x is converted
-    constexpr bool kRaw = SIO != IO_F32 && ((SIO == IO_BF16) == BF16);
     extern __shared__ unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t bars[NBARS];
     __shared__ uint32_t tmem_slot;
@@ -577,6 +600,10 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
         }
         tc::mbar_init(bar(BAR_CONV_DONE), kConvWarps);
         tc::mbar_init(bar(BAR_STG_FREE), kConvWarps);
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(bar(BAR_DFULL0 + i), 1);
+            tc::mbar_init(bar(BAR_DFREE0 + i), 1);
+        }
         if constexpr (ZM > 0) tc::mbar_init(sbase + L::NORM + NORM_ZBAR, 1);
         if constexpr (ZM == 2) {
             if (norm_cs > 1)
@@ -595,6 +622,10 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
     }
     // Mcat starts zero: the blocks above the diagonal that no warp writes stay so
     for (int e = tid; e < 16384 / 16; e += blockDim.x) st_shared_v4(sbase + L::MC + 16 * e, 0u, 0u, 0u, 0u);
+    if constexpr (DIRECT) {  // the zero box between the heads' x boxes, both buffers (no copy writes it)
+        for (int e = tid; e < 2 * 8192 / 16; e += blockDim.x)
+            st_shared_v4(sbase + L::STGD + (e >> 9) * DStg::BUF + DStg::DX + 8192 + 16 * (e & 511), 0u, 0u, 0u, 0u);
+    }
     tc::fence_smem_to_async();
     tc::fence_before_sync();
     __syncthreads();
@@ -624,6 +655,47 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                     const uint32_t ph = gk & 1u;
                     const int buf = gk & 1;
                     const int xbuf = L::kXcBufs == 2 ? buf : 0;
+                    if constexpr (DIRECT) {
+                        // x, B and C straight from staging buffer gk % 2 (128-byte swizzle): K-major
+                        // operands step 32 bytes per K = 16 inside a box row, and move to the
+                        // features 64-127 box after four steps; MN-major ones step 16 token rows
+                        const uint32_t sb = sbase + L::STGD + (gk & 1u) * DStg::BUF;
+                        wait(BAR_OPS_FULL, ph);
+                        wait(BAR_DFULL0 + (gk & 1u), (gk >> 1) & 1u);  // (complete: the compute warps saw it)
+                        tc::fence_after_sync();
+#pragma unroll
+                        for (int ks = 0; ks < NN / 16; ++ks)  // G = C B^T, K = n: C's two copies give 128 rows
+                            tc::mma_f16(tmem + TM_G,
+                                        tc::desc_sw128(sb + DStg::DC + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+                                        tc::desc_sw128(sb + DStg::DB + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024),
+                                        ID_KK, ks > 0);
+                        tc::commit(bar(BAR_G_DONE));
+                        wait(BAR_S_FULL, ph);
+                        tc::fence_after_sync();
+#pragma unroll
+                        for (int ks = 0; ks < kQ / 16; ++ks)  // S += Xw^T B onto the decayed state, K = j
+                            tc::mma_f16(tmem + TM_S32, tc::desc(sbase + L::XT + ks * 4096, 2048, 128),
+                                        tc::desc_sw128(sb + DStg::DB + ks * 2048, 8192, 1024), ID_MNMN, 1u);
+#pragma unroll
+                        for (int ks = 0; ks < NN / 16; ++ks)  // Yoff = S C^T, S from TMEM, K = n
+                            tc::mma_f16_ts(tmem + tm_yoff<NN>(buf), tmem + TM_SBF + ks * 8,
+                                           tc::desc_sw128(sb + DStg::DC + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+                                           ID_KK, ks > 0);
+                        tc::commit(bar(BAR_DS_DONE));
+                        wait(BAR_MCAT_FULL, ph);
+                        tc::fence_after_sync();
+                        const uint32_t mc = sbase + L::MC;
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh)  // head hh's x box beside the zero box: its M half of Xcat
+#pragma unroll
+                            for (int ks = 0; ks < kQ / 16; ++ks)
+                                tc::mma_f16(tmem + tm_yint<NN>(buf),
+                                            tc::desc_sw128(sb + DStg::DX + hh * 8192 + ks * 2048, 8192, 1024),
+                                            tc::desc(mc + hh * 8192 + ks * 2048, 1024, 128), ID_MNK, (hh | ks) != 0);
+                        tc::commit(bar(buf ? BAR_Y_DONE1 : BAR_Y_DONE0));
+                        tc::commit(bar(BAR_DFREE0 + (gk & 1u)));  // every product of this buffer issued
+                        continue;
+                    }
                     wait(BAR_OPS_FULL, ph);
                     tc::fence_after_sync();
 #pragma unroll
@@ -767,6 +839,85 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                         if (k > 0) store_y(u, k - 1);
                     }
                     if (u.nch > 0) store_y(u, u.nch - 1);
+                }
+                tc::bulk_wait_all();
+            } else if constexpr (SEG && DIRECT) {
+                // chunk g of this CTA's walk into staging buffer g % 2, two chunks ahead:
+                // buffer g % 2 takes chunk g + 2 once the products of chunk g have read it
+                // (the MMA warp's commit after the intra product)
+                auto load_chunk = [&](const Span &u, int k, uint32_t i) {
+                    const int tok = u.t0 + k * kQ;
+                    const uint32_t sb = sbase + L::STGD + i * DStg::BUF, fb = bar(BAR_DFULL0 + i);
+                    tc::mbar_arrive_expect_tx(fb, 8 * BOX_BYTES);
+#pragma unroll
+                    for (int bx = 0; bx < 2; ++bx) {
+                        tc::tma_load_3d(sb + DStg::DX + bx * 16384, &tm.x, u.h0 * kP + bx * 64, tok, u.b, fb);
+                        tc::tma_load_3d(sb + DStg::DB + bx * 8192, &tm.b, u.g * NN + bx * 64, tok, u.b, fb);
+#pragma unroll
+                        for (int cp = 0; cp < 2; ++cp)  // C twice: rows 64-127 of C B^T's A operand
+                            tc::tma_load_3d(sb + DStg::DC + bx * 16384 + cp * 8192, &tm.c, u.g * NN + bx * 64, tok, u.b,
+                                            fb);
+                    }
+                    if constexpr (ZM > 0) {  // this chunk's z into L2, ahead of its load into the y tile
+#pragma unroll
+                        for (int bx = 0; bx < 2; ++bx) tc::tma_prefetch_3d(&tm.z, u.h0 * kP + bx * 64, tok, u.b);
+                    }
+                };
+                // the load cursor: the next chunk of the walk to stage (lu is the span of lunit)
+                int lunit = blockIdx.x, lk = 0;
+                Span lu{};
+                if (lunit < n_units) lu = unit_span<false, true>(p, dm, lunit);
+                uint32_t gl = 0;  // chunks staged so far
+                auto load_next = [&]() {
+                    while (lunit < n_units && lk >= lu.nch) {
+                        lk = 0;
+                        lunit += gridDim.x;
+                        if (lunit < n_units) lu = unit_span<false, true>(p, dm, lunit);
+                    }
+                    if (lunit >= n_units) return;
+                    load_chunk(lu, lk, gl & 1u);
+                    ++lk;
+                    ++gl;
+                };
+                auto load_z = [&](const Span &u, int k) {
+                    if constexpr (ZM > 0) {
+                        const uint32_t zbar = sbase + L::NORM + NORM_ZBAR;
+                        tc::mbar_arrive_expect_tx(zbar, 2 * BOX_BYTES);
+#pragma unroll
+                        for (int bx = 0; bx < 2; ++bx)
+                            tc::tma_load_3d(sbase + L::YSTAGE + bx * BOX_BYTES, &tm.z, u.h0 * kP + bx * 64,
+                                            u.t0 + k * kQ, u.b, zbar);
+                    }
+                };
+                uint32_t yt = 0;  // y tiles stored so far
+                auto store_y = [&](const Span &u, int k) {
+                    wait(BAR_Y_STAGED, yt & 1u);
+#pragma unroll
+                    for (int bx = 0; bx < 2; ++bx)
+                        tc::tma_store_3d(&tm.y, sbase + L::YSTAGE + bx * BOX_BYTES, u.h0 * kP + bx * 64,
+                                         u.t0 + k * kQ, u.b);
+                    tc::bulk_commit();
+                    tc::bulk_wait_read();
+                    tc::mbar_arrive(bar(BAR_Y_FREE));
+                    ++yt;
+                };
+                load_next();
+                load_next();
+                if ((int)blockIdx.x < n_units) load_z(unit_span<false, true>(p, dm, blockIdx.x), 0);
+                uint32_t gk = 0;
+                for (int unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
+                    const Span u = unit_span<false, true>(p, dm, unit);
+                    const bool more = unit + (int)gridDim.x < n_units;
+                    for (int k = 0; k < u.nch; ++k, ++gk) {
+                        if (k > 0) {
+                            store_y(u, k - 1);
+                            load_z(u, k);  // the next tile the compute warps stage
+                        }
+                        wait(BAR_DFREE0 + (gk & 1u), (gk >> 1) & 1u);  // chunk gk's products have read it
+                        load_next();                                   // chunk gk + 2 into the same buffer
+                    }
+                    store_y(u, u.nch - 1);
+                    if (more) load_z(unit_span<false, true>(p, dm, unit + gridDim.x), 0);
                 }
                 tc::bulk_wait_all();
             } else if constexpr (SEG) {
@@ -1259,7 +1410,8 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                 }
 
                 // ---- A: operands of chunk k into shared memory ----
-                wait(CV ? BAR_CONV_DONE : BAR_STAGE_FULL, ph);  // with the conv1d: once it has run
+                if constexpr (DIRECT) wait(BAR_DFULL0 + (gk & 1u), (gk >> 1) & 1u);
+                else wait(CV ? BAR_CONV_DONE : BAR_STAGE_FULL, ph);  // with the conv1d: once it has run
                 // one Xcat buffer: the previous chunk's intra product has read it
                 if (L::kXcBufs == 1 && gk > 0) wait((gk - 1) & 1 ? BAR_Y_DONE1 : BAR_Y_DONE0, ((gk - 1) >> 1) & 1u);
                 {
@@ -1279,7 +1431,10 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                         const int mgc = h ? 16 + po : po;
                         const uint32_t xsrc = sbase + (CV ? L::POST : L::STG_X);
                         float xv[8];
-                        if constexpr (kRaw) {  // the staged chunk is the operand already
+                        if constexpr (DIRECT) {  // only the weighted copy: the products read x in place
+                            const uint32_t xb = sbase + L::STGD + (gk & 1u) * DStg::BUF + DStg::DX + h * 16384;
+                            tcstage::unpack8(tc::ld_shared_v4(tcstage::swz(xb, jg * 8 + jl, po)), BF16, xv);
+                        } else if constexpr (kRaw) {  // the staged chunk is the operand already
                             const uint4 raw = stage_raw16(xsrc, jg * 8 + jl, c16);
                             st_shared_v4(xc + (jg * 24 + mgc) * 128 + jl * 16, raw.x, raw.y, raw.z, raw.w);
                             tcstage::unpack8(raw, BF16, xv);
@@ -1293,7 +1448,7 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                         store8(sbase + L::XT + (jg * 16 + 8 * h + po) * 128 + jl * 16, xs, BF16);
                     }
 #pragma unroll
-                    for (int it = 0; it < NN / 64; ++it) {
+                    for (int it = 0; it < (DIRECT ? 0 : NN / 64); ++it) {  // (DIRECT: B and C are read in place)
                         const int e = tid + kComputeThreads * it;
                         const int jl = e & 7, ng = (e >> 3) & (NN / 8 - 1), jg = e / NN;
                         const uint32_t bsrc = sbase + (CV ? L::POST_B : L::STG_B);

@@ -38,7 +38,7 @@ def _full(oracle_mod, inp, y, fin, mode, what):
 
 @pytest.mark.parametrize("shape", SHAPES)
 @pytest.mark.parametrize("feat", ["plain", "all"])
-@pytest.mark.parametrize("io,ops", [("f32", "bf16"), ("f32", "f16"), ("bf16", "bf16")])
+@pytest.mark.parametrize("io,ops", [("f32", "bf16"), ("f32", "f16"), ("bf16", "bf16"), ("f16", "f16")])
 def test_fused128(oracle_mod, shape, feat, io, ops):
     B, L, H, P, N, G, Q = shape
     f = dict(D=True, z=True, dt_bias=True, h0=True) if feat == "all" else {}
