@@ -1492,21 +1492,15 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                     wait(BAR_G_DONE, ph);
                     tc::fence_after_sync();
                     const uint32_t mc = sbase + L::MC;
-                    // N = 128: the thread's 16 columns with one wait, and no mask on blocks that
-                    // lie wholly below the diagonal; N = 64 keeps two 8-column loads and the mask
-                    // (fewer registers live beside its register-resident state)
+                    // the thread's 16 columns with one wait, and no mask on blocks that lie wholly
+                    // below the diagonal (at N = 64 two 8-column loads with the mask everywhere
+                    // measured 1.024 ms against 1.012 at the large training shape)
                     float gall[kGCols];
-                    if constexpr (NN == 128) tc::tmem_ld16(tlane + TM_G + col0, gall);
+                    tc::tmem_ld16(tlane + TM_G + col0, gall);
                     const int rows_lo = 32 * (quarter & 1);  // the warp's first row i
 #pragma unroll
                     for (int q = 0; q < kGCols / 8; ++q) {
                         const int j0 = col0 + 8 * q;
-                        if constexpr (NN == 64) {
-                            float g8[8];
-                            tc::tmem_ld8(tlane + TM_G + j0, g8);
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) gall[8 * q + e] = g8[e];
-                        }
                         const float4 c0 = *reinterpret_cast<const float4 *>(&V.cs2[h][j0]);
                         const float4 c1 = *reinterpret_cast<const float4 *>(&V.cs2[h][j0 + 4]);
                         const float4 d0 = *reinterpret_cast<const float4 *>(&V.d[h][j0]);
@@ -1514,7 +1508,7 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                         const float cj[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
                         const float dj[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
                         float m[8];
-                        if (NN == 128 && j0 + 7 < rows_lo) {  // (warp-uniform) wholly below the diagonal
+                        if (j0 + 7 < rows_lo) {  // (warp-uniform) wholly below the diagonal
 #pragma unroll
                             for (int e = 0; e < 8; ++e) m[e] = gall[8 * q + e] * ex2_approx(csi - cj[e]) * dj[e];
                         } else {
