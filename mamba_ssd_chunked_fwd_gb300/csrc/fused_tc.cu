@@ -659,9 +659,13 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                         // x, B and C straight from staging buffer gk % 2 (128-byte swizzle): K-major
                         // operands step 32 bytes per K = 16 inside a box row, and move to the
                         // features 64-127 box after four steps; MN-major ones step 16 token rows
+                        // C B^T needs only the staged tiles, so it goes out as soon as they land (the
+                        // previous chunk's Mcat has released TM_G: this thread waited for it before the
+                        // previous intra product), then Yoff, and dS once the weighted x is in
+                        // (gated prefill 425.5 -> 414.0 us; the same order with copied operands
+                        // measured slower at N = 128 with fp32 tensors and neutral at N = 64)
                         const uint32_t sb = sbase + L::STGD + (gk & 1u) * DStg::BUF;
-                        wait(BAR_OPS_FULL, ph);
-                        wait(BAR_DFULL0 + (gk & 1u), (gk >> 1) & 1u);  // (complete: the compute warps saw it)
+                        wait(BAR_DFULL0 + (gk & 1u), (gk >> 1) & 1u);
                         tc::fence_after_sync();
 #pragma unroll
                         for (int ks = 0; ks < NN / 16; ++ks)  // G = C B^T, K = n: C's two copies give 128 rows
@@ -673,14 +677,16 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                         wait(BAR_S_FULL, ph);
                         tc::fence_after_sync();
 #pragma unroll
-                        for (int ks = 0; ks < kQ / 16; ++ks)  // S += Xw^T B onto the decayed state, K = j
-                            tc::mma_f16(tmem + TM_S32, tc::desc(sbase + L::XT + ks * 4096, 2048, 128),
-                                        tc::desc_sw128(sb + DStg::DB + ks * 2048, 8192, 1024), ID_MNMN, 1u);
-#pragma unroll
                         for (int ks = 0; ks < NN / 16; ++ks)  // Yoff = S C^T, S from TMEM, K = n
                             tc::mma_f16_ts(tmem + tm_yoff<NN>(buf), tmem + TM_SBF + ks * 8,
                                            tc::desc_sw128(sb + DStg::DC + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
                                            ID_KK, ks > 0);
+                        wait(BAR_OPS_FULL, ph);  // the weighted x
+                        tc::fence_after_sync();
+#pragma unroll
+                        for (int ks = 0; ks < kQ / 16; ++ks)  // S += Xw^T B onto the decayed state, K = j
+                            tc::mma_f16(tmem + TM_S32, tc::desc(sbase + L::XT + ks * 4096, 2048, 128),
+                                        tc::desc_sw128(sb + DStg::DB + ks * 2048, 8192, 1024), ID_MNMN, 1u);
                         tc::commit(bar(BAR_DS_DONE));
                         wait(BAR_MCAT_FULL, ph);
                         tc::fence_after_sync();
