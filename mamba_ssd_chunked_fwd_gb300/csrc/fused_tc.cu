@@ -1328,7 +1328,12 @@ ssd_fused_kernel(const __grid_constant__ Params p, const __grid_constant__ TmaMa
                         const int ng = (scol0 >> 3) + q;
                         store8(sbase + L::S + (ng * 16 + (row >> 3)) * 128 + (row & 7) * 16, v, BF16);
                     }
-                    tc::fence_smem_to_async();
+                    // The product that reads this copy (Yoff) is issued only after the next chunk's
+                    // OPS_FULL, which these threads arrive on behind the operand stage's own proxy
+                    // fence, so none is needed here (a fence here as well measured 0.999 ms against
+                    // 0.986 at the large training shape; packed sequences keep it: 1.082 against
+                    // 1.090 ms without)
+                    if constexpr (VARLEN) tc::fence_smem_to_async();
                 }
                 __syncwarp();
             }
