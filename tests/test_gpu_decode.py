@@ -98,6 +98,39 @@ def test_decode_continues_the_gpu_forward(oracle_mod, dtype):
     assert_close(oracle_mod, st.double().cpu().numpy(), fr, mode, f"decode continuation {dtype} final")
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_decode_streaming_kernel_with_many_units_per_cta(oracle_mod, dtype):
+    """[64,512,32,32] with G = 8: 65536 half blocks over at most 912 CTAs, about
+    72 units walked by each CTA with the next unit's loads in flight."""
+    import mamba_ssd_chunked_fwd_gb300 as ssd
+    B, H, P, N, G = 64, 512, 32, 32, 8
+    one, state = _step_inputs(B, H, P, N, G, dtype=dtype, seed=61, feats=True)
+    y, st = _gpu_step(ssd, one, state)
+    yr, sr = _oracle_step(oracle_mod, one, state)
+    assert_close(oracle_mod, st.double().cpu().numpy(), sr, "f32", f"decode many units {dtype} state")
+    assert_close(oracle_mod, y.double().cpu().numpy(), yr, dtype, f"decode many units {dtype} y")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_decode_step_with_an_unaligned_x_takes_the_streaming_kernel(oracle_mod, dtype):
+    """x one element into its buffer (not 16-byte aligned): the streaming kernel
+    reads x element by element; more half blocks (2048) than CTAs."""
+    import mamba_ssd_chunked_fwd_gb300 as ssd
+    one, state = _step_inputs(8, 128, 64, 64, 8, dtype=dtype, seed=12, feats=True)
+    cu = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in one.items()}
+    xb = torch.zeros(one["x"].numel() + 1, dtype=one["x"].dtype, device="cuda")
+    x = xb[1:].view(one["x"].shape)
+    x.copy_(cu["x"])
+    assert x.data_ptr() % 16 != 0
+    st = state.cuda().contiguous()
+    y = ssd.mamba2_ssd_decode(x, cu["dt"], cu["A"], cu["B"], cu["C"], st, dt_softplus=True,
+                              D=cu["D"], z=cu["z"], dt_bias=cu["dt_bias"])
+    torch.cuda.synchronize()
+    yr, sr = _oracle_step(oracle_mod, one, state)
+    assert_close(oracle_mod, st.double().cpu().numpy(), sr, "f32", f"decode unaligned x {dtype} state")
+    assert_close(oracle_mod, y.double().cpu().numpy(), yr, dtype, f"decode unaligned x {dtype} y")
+
+
 def test_decode_step_with_an_unaligned_state_takes_the_scalar_kernel(oracle_mod):
     """A state that is not 16-byte aligned (a view 4 bytes into a buffer)."""
     import mamba_ssd_chunked_fwd_gb300 as ssd
