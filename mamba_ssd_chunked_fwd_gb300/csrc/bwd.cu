@@ -205,12 +205,64 @@ struct ChunkSmem {
     float red[kThreads / 32];
 };
 
+// One cache line into L2 (a hint: no alignment rule, no completion).
+__device__ __forceinline__ void prefetch_line_l2(const void *q) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(q));
+}
+
+// Ask L2 for every operand line of the chunk kernel's CTA (bh, k): its rows of
+// x, dyp, B, C and dt (one row per thread of each quarter of the CTA), its cs
+// and dtp vectors and its state and adjoint blocks.
+template <int IO>
+__device__ __forceinline__ void bwd_chunk_prefetch(const Params &p, const float *dtp, const float *cs,
+                                                   const float *states, const float *adj, const float *dyp, int bh,
+                                                   int k, int tid) {
+    constexpr int kIo = IO == IO_F32 ? 4 : 2;
+    const int P = p.P, N = p.N, Q = p.Q, L = p.L;
+    const int b = bh / p.H, h = bh - b * p.H, g = h / p.hpg;
+    const int i = tid & (kMax - 1), which = tid >> 6;  // 4 groups of 64 rows
+    const int t = k * Q + i;
+    if (i < Q && t < L) {
+        const unsigned char *row;
+        int bytes;
+        if (which == 0) {
+            row = static_cast<const unsigned char *>(p.x) + (((size_t)b * L + t) * p.H + h) * P * kIo;
+            bytes = P * kIo;
+        } else if (which == 1) {
+            row = reinterpret_cast<const unsigned char *>(dyp + (((size_t)b * L + t) * p.H + h) * P);
+            bytes = P * 4;
+            prefetch_line_l2(p.dt + ((size_t)b * L + t) * p.H + h);
+        } else {
+            row = static_cast<const unsigned char *>(which == 2 ? p.Bm : p.Cm) +
+                  (((size_t)b * L + t) * p.G + g) * N * kIo;
+            bytes = N * kIo;
+        }
+        for (int o = 0; o < bytes; o += 128) prefetch_line_l2(row + o);
+        prefetch_line_l2(row + bytes - 1);
+    }
+    const size_t crow = (((size_t)b * p.H + h) * p.nchunks + k) * Q;
+    if (tid == 0) {
+        prefetch_line_l2(cs + crow);
+        prefetch_line_l2(cs + crow + Q - 1);
+        prefetch_line_l2(dtp + crow);
+        prefetch_line_l2(dtp + crow + Q - 1);
+    }
+    // the state and adjoint blocks: P N floats each, contiguous
+    const size_t st = ((((size_t)b * p.nchunks + k) * p.H + h) * P) * N;
+    const int bytes = P * N * 4, lines = (bytes + 127) / 128;
+    for (int l = tid; l < 2 * lines; l += kThreads) {
+        const float *base = (l < lines ? states : adj) + st;
+        const int o = (l < lines ? l : l - lines) * 128;
+        prefetch_line_l2(reinterpret_cast<const unsigned char *>(base) + (o < bytes ? o : bytes - 1));
+    }
+}
+
 template <int IO>
 __global__ void __launch_bounds__(kThreads)
 bwd_chunk_kernel(Params p, const float *__restrict__ dtp, const float *__restrict__ cs,
                  const float *__restrict__ states, const float *__restrict__ adj, const float *__restrict__ dyp,
                  void *dx, float *__restrict__ ddt, float *__restrict__ dBh, float *__restrict__ dCh,
-                 float *__restrict__ partA, float *__restrict__ partD, float *__restrict__ partBias) {
+                 float *__restrict__ partA, float *__restrict__ partD, float *__restrict__ partBias, int wave) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     ChunkSmem &sm = *reinterpret_cast<ChunkSmem *>(smem_raw);
     const int k = blockIdx.y, bh = blockIdx.x;
@@ -222,6 +274,17 @@ bwd_chunk_kernel(Params p, const float *__restrict__ dtp, const float *__restric
     const size_t st_off = ((((size_t)b * p.nchunks + k) * p.H + h) * P) * N;
     const float A = __ldg(p.A + h);
     const float Dh = p.D ? __ldg(p.D + h) : 0.f;
+
+    // One CTA fills an SM, so the CTA that follows it there would start by
+    // waiting on the memory with nothing to overlap.  CTAs start in linear
+    // order (blockIdx.x fastest), one wave (`wave` CTAs) apart on the SMs, so
+    // this one asks L2 for the operands of the CTA a wave after it.
+    {
+        const long long nxt = (long long)k * gridDim.x + bh + wave;
+        if (wave > 0 && nxt < (long long)gridDim.x * gridDim.y)
+            bwd_chunk_prefetch<IO>(p, dtp, cs, states, adj, dyp, (int)(nxt % gridDim.x), (int)(nxt / gridDim.x),
+                                   tid);
+    }
 
     // (1) operands, every global load issued before the shared-memory stores.
     //     Outside (Q, P, N) and past L: 0, and d = 0 (cs keeps its last value).
@@ -572,27 +635,33 @@ cudaError_t launch_bwd(const Params &p, int io, const BwdBuffers &w, cudaStream_
         p, w.cs, w.dfinal, w.adj, w.dh0);
     const int smem = (int)sizeof(ChunkSmem);
     cudaError_t e;
+    int dev = 0, wave = 0;  // CTAs resident at once: one per SM
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&wave, cudaDevAttrMultiProcessorCount, dev) !=
+                                                  cudaSuccess) {
+        (void)cudaGetLastError();
+        wave = 0;  // no prefetch
+    }
     switch (io) {
         case IO_F32:
             if ((e = cudaFuncSetAttribute(bwd_chunk_kernel<IO_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           smem)) != cudaSuccess)
                 return e;
             bwd_chunk_kernel<IO_F32><<<grid, kThreads, smem, s>>>(p, w.dtp, w.cs, w.states, w.adj, dyp, w.dx,
-                                                                  w.ddt, w.dBh, w.dCh, w.partA, w.partD, w.partBias);
+                                                                  w.ddt, w.dBh, w.dCh, w.partA, w.partD, w.partBias, wave);
             break;
         case IO_F16:
             if ((e = cudaFuncSetAttribute(bwd_chunk_kernel<IO_F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           smem)) != cudaSuccess)
                 return e;
             bwd_chunk_kernel<IO_F16><<<grid, kThreads, smem, s>>>(p, w.dtp, w.cs, w.states, w.adj, dyp, w.dx,
-                                                                  w.ddt, w.dBh, w.dCh, w.partA, w.partD, w.partBias);
+                                                                  w.ddt, w.dBh, w.dCh, w.partA, w.partD, w.partBias, wave);
             break;
         case IO_BF16:
             if ((e = cudaFuncSetAttribute(bwd_chunk_kernel<IO_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           smem)) != cudaSuccess)
                 return e;
             bwd_chunk_kernel<IO_BF16><<<grid, kThreads, smem, s>>>(p, w.dtp, w.cs, w.states, w.adj, dyp, w.dx,
-                                                                   w.ddt, w.dBh, w.dCh, w.partA, w.partD, w.partBias);
+                                                                   w.ddt, w.dBh, w.dCh, w.partA, w.partD, w.partBias, wave);
             break;
     }
     const size_t gtotal = (size_t)p.B * p.L * p.G * p.N / 4;
